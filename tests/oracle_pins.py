@@ -1,0 +1,247 @@
+"""Pins of the fp64 oracle to things other than itself.
+
+Each ``pin_*`` takes an :class:`oracle.Oracle` and raises ``AssertionError``
+when the oracle disagrees with a closed form, a hand-worked golden file, a
+brute-force loop, a numpy textbook attention or an invariant.  The tests run
+them on the real oracle (all must pass) and on deliberately broken copies of
+its C source (at least one must fail for each), so that a dropped term, a
+wrong sign, index or transposed operand in the oracle cannot go unnoticed.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from pa_testutil import (caches_from_tokens, read_golden, random_case, textbook_decode,
+                         token_views)
+
+FP16, BF16 = 0, 1
+TORCH_DT = {FP16: torch.float16, BF16: torch.bfloat16}
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    err = float(np.max(np.abs(a - b) / (1.0 + np.abs(b)))) if a.size else 0.0
+    assert err <= tol, f"{what}: max scaled error {err:.3e} > {tol:.1e}"
+
+
+def pin_textbook_gqa(orc):
+    """Special case = textbook: the oracle equals numpy softmax(scale q K^T) V
+    (GQA groups, random physical placement, ragged lengths), both dtypes."""
+    for dt in (FP16, BF16):
+        q, kc, vc, bt, lens = random_case(11 + dt, S=3, H=4, KH=2, D=16, BS=4, lens=[1, 7, 13],
+                                          dtype=TORCH_DT[dt])
+        ref = textbook_decode(q, kc, vc, bt, lens, 0.3)
+        got = orc.decode(q, kc, vc, bt, lens, 0.3, dt)
+        _close(got, ref, 1e-12, "textbook")
+
+
+def pin_bruteforce_tiny(orc):
+    """Brute force with pure-Python loops and flat offsets computed from the
+    caches' shapes (np.ravel_multi_index), math.exp softmax."""
+    for KH in (1, 2):
+        S, H, D, BS = 2, 2, 8, 2
+        q, kc, vc, bt, lens = random_case(5 + KH, S=S, H=H, KH=KH, D=D, BS=BS, lens=[5, 3])
+        qf = q.to(torch.float64).numpy().ravel()
+        kf = kc.to(torch.float64).numpy().ravel()
+        vf = vc.to(torch.float64).numpy().ravel()
+        scale = float(np.float32(0.7))
+        ref = np.zeros((S, H, D))
+        for s in range(S):
+            for h in range(H):
+                kh = h // (H // KH)
+                z = []
+                for t in range(int(lens[s])):
+                    b = int(bt[s, t // BS])
+                    acc = 0.0
+                    for d in range(D):
+                        ki = np.ravel_multi_index((b, kh, d // 8, t % BS, d % 8), kc.shape)
+                        acc += qf[np.ravel_multi_index((s, h, d), q.shape)] * kf[ki]
+                    z.append(scale * acc)
+                mx = max(z)
+                e = [math.exp(v - mx) for v in z]
+                tot = sum(e)
+                for d in range(D):
+                    num = 0.0
+                    for t in range(int(lens[s])):
+                        b = int(bt[s, t // BS])
+                        num += e[t] * vf[np.ravel_multi_index((b, kh, d, t % BS), vc.shape)]
+                    ref[s, h, d] = num / tot
+        got = orc.decode(q, kc, vc, bt, lens, scale, FP16)
+        _close(got, ref, 1e-13, "brute force")
+
+
+def pin_golden_two_token(orc):
+    """Hand-worked two-token case (tests/golden/two_token_closed_form.txt)."""
+    rows = {r[0]: [float(v) for v in r[1:]] for r in read_golden("two_token_closed_form.txt")}
+    D, BS = 8, 16
+    for dt in (FP16, BF16):
+        tdt = TORCH_DT[dt]
+        q = torch.tensor(rows["q"]).view(1, 1, D).to(tdt)
+        k_tok = torch.zeros((1, BS, 1, D))
+        v_tok = torch.zeros((1, BS, 1, D))
+        k_tok[0, 0, 0], k_tok[0, 1, 0] = torch.tensor(rows["k0"]), torch.tensor(rows["k1"])
+        v_tok[0, 0, 0], v_tok[0, 1, 0] = torch.tensor(rows["v0"]), torch.tensor(rows["v1"])
+        kc, vc = caches_from_tokens(k_tok.to(tdt), v_tok.to(tdt))
+        bt = torch.zeros((1, 1), dtype=torch.int32)
+        lens = torch.tensor([2], dtype=torch.int32)
+        w0, w1 = rows["w"]
+        ref = w0 * np.array(rows["v0"]) + w1 * np.array(rows["v1"])
+        got = orc.decode(q, kc, vc, bt, lens, rows["scale"][0], dt)
+        _close(got[0, 0], ref, 1e-15, "two-token closed form")
+
+
+def pin_golden_layout(orc):
+    """Hand-derived flat offsets (tests/golden/paged_layout_offsets.txt).  A
+    bump at one flat offset must show up at exactly the (b, kh, d, o) the
+    fixture names: with partition_size 1 every partition is one token, so the
+    per-partition max score (K) or partition output (V) locates it."""
+    nb, KH, D, BS = 3, 2, 16, 4
+    table = [2, 0, 1]                     # logical block j -> physical block table[j]
+    L = nb * BS
+    bt = torch.tensor([table], dtype=torch.int32)
+    lens = torch.tensor([L], dtype=torch.int32)
+    scale = 0.25
+    for row in read_golden("paged_layout_offsets.txt"):
+        cache, b, kh, d, o, off = row[0], *[int(v) for v in row[1:]]
+        t_star = table.index(b) * BS + o   # logical token that lives at (b, o)
+        kc = torch.zeros((nb, KH, D // 8, BS, 8), dtype=torch.float16)
+        vc = torch.zeros((nb, KH, D, BS), dtype=torch.float16)
+        q = torch.zeros((1, KH, D), dtype=torch.float16)
+        if cache == "key":
+            kc.view(-1)[off] = 4.0
+            q[0, kh, d] = 1.0
+            m, l, o_p = orc.partitions(q, kc, vc, bt, lens, scale, FP16, 1)
+            want = np.zeros((KH, L))
+            want[kh, t_star] = 4.0 * scale
+            _close(m[0], want, 0.0, f"K layout {row}")
+        else:
+            vc.view(-1)[off] = 4.0
+            m, l, o_p = orc.partitions(q, kc, vc, bt, lens, scale, FP16, 1)
+            want = np.zeros((KH, L, D))
+            want[kh, t_star, d] = 4.0
+            _close(o_p[0], want, 0.0, f"V layout {row}")
+
+
+def pin_seq_len_one(orc):
+    """seq_len = 1: the single weight is exactly 1, so out == V of that token, bitwise."""
+    q, kc, vc, bt, lens = random_case(21, S=3, H=4, KH=2, D=16, BS=4, lens=[1, 1, 1], MB=3)
+    got = orc.decode(q, kc, vc, bt, lens, 0.125, FP16)
+    _, v_tok = token_views(kc, vc)
+    for s in range(3):
+        for h in range(4):
+            want = v_tok[int(bt[s, 0]), 0, h // 2].to(torch.float64).numpy()
+            assert np.array_equal(got[s, h], want), "seq_len 1 must return V exactly"
+
+
+def pin_uniform_weights(orc):
+    """Identical keys, q = 0 or scale = 0 make every weight 1/L: out = mean of V."""
+    q, kc, vc, bt, lens = random_case(31, S=2, H=2, KH=2, D=16, BS=4, lens=[9, 6])
+    k_tok, v_tok = token_views(kc, vc)
+    k_same = k_tok.clone()
+    k_same[:] = k_tok[0, 0]
+    kc_same, _ = caches_from_tokens(k_same, v_tok)
+    from pa_testutil import gather_sequence
+    for variant in ("same_keys", "q_zero", "scale_zero"):
+        qq, kk, sc = q, kc, 0.5
+        if variant == "same_keys":
+            kk = kc_same
+        elif variant == "q_zero":
+            qq = torch.zeros_like(q)
+        else:
+            sc = 0.0
+        got = orc.decode(qq, kk, vc, bt, lens, sc, FP16)
+        for s in range(2):
+            _, V = gather_sequence(kc, vc, bt, s, int(lens[s]))
+            _close(got[s], V.mean(axis=0), 1e-13, variant)
+
+
+def pin_shift_invariance(orc):
+    """Adding delta to K[.., 0] of every token shifts every score of a query with
+    q[0] = 1 by scale*delta; softmax is shift invariant, so out is unchanged.
+    (Small-integer K[.., 0] keeps the shifted values exact in fp16.)"""
+    q, kc, vc, bt, lens = random_case(41, S=2, H=2, KH=1, D=16, BS=4, lens=[11, 5])
+    q[:, :, 0] = 1.0
+    k_tok, v_tok = token_views(kc, vc)
+    g = torch.Generator().manual_seed(2)
+    k1 = k_tok.clone()
+    k1[..., 0] = torch.randint(-4, 5, k1[..., 0].shape, generator=g).to(k1.dtype)
+    k2 = k1.clone()
+    k2[..., 0] = k1[..., 0] + 3
+    kc1, vc1 = caches_from_tokens(k1, v_tok)
+    kc2, _ = caches_from_tokens(k2, v_tok)
+    a = orc.decode(q, kc1, vc1, bt, lens, 0.5, FP16)
+    b = orc.decode(q, kc2, vc1, bt, lens, 0.5, FP16)
+    _close(a, b, 1e-13, "softmax shift invariance")
+    c = orc.decode(q, torch.zeros_like(kc1), vc1, bt, lens, 0.5, FP16)
+    assert np.max(np.abs(a - c)) > 1e-3, "output must depend on K"
+
+
+def pin_permutation_invariance(orc):
+    """Moving physical blocks (and rewriting the table) changes nothing, bitwise."""
+    q, kc, vc, bt, lens = random_case(51, S=3, H=4, KH=2, D=16, BS=4, lens=[13, 4, 9],
+                                      num_blocks=20, MB=4)
+    perm = torch.randperm(20, generator=torch.Generator().manual_seed(9))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(20)
+    kc2, vc2 = kc[perm].contiguous(), vc[perm].contiguous()  # new block i holds old perm[i]
+    bt2 = inv[bt.long()].to(torch.int32)
+    a = orc.decode(q, kc, vc, bt, lens, 0.4, FP16)
+    b = orc.decode(q, kc2, vc2, bt2, lens, 0.4, FP16)
+    assert np.array_equal(a, b), "physical placement must not matter"
+
+
+def pin_partition_invariance(orc):
+    """combine(partitions(P)) equals the unpartitioned result for any P (the
+    phase-2 identity), and unused partitions hold the sentinels (-inf, 0)."""
+    q, kc, vc, bt, lens = random_case(61, S=3, H=4, KH=2, D=16, BS=4, lens=[37, 1, 16], MB=10)
+    ref = orc.decode(q, kc, vc, bt, lens, 0.35, FP16)
+    for P in (1, 4, 8, 7, 16, 64):
+        m, l, o = orc.partitions(q, kc, vc, bt, lens, 0.35, FP16, P)
+        out = orc.combine(m, l, o, lens, P)
+        _close(out, ref, 1e-12, f"partition size {P}")
+        for s in range(3):
+            np_s = -(-int(lens[s]) // P)
+            assert np.all(np.isneginf(m[s, :, np_s:])) and np.all(l[s, :, np_s:] == 0.0)
+            assert np.all(np.isfinite(m[s, :, :np_s])) and np.all(l[s, :, :np_s] >= 1.0)
+
+
+def pin_empty_sequence(orc):
+    """seq_len = 0 gives zeros (l = 0 -> inverse taken as 0) and all-sentinel partitions."""
+    q, kc, vc, bt, lens = random_case(71, S=2, H=2, KH=2, D=8, BS=4, lens=[0, 5], MB=2)
+    got = orc.decode(q, kc, vc, bt, lens, 0.5, FP16)
+    assert np.all(got[0] == 0.0) and np.any(got[1] != 0.0)
+    m, l, o = orc.partitions(q, kc, vc, bt, lens, 0.5, FP16, 4)
+    assert np.all(np.isneginf(m[0])) and np.all(l[0] == 0.0)
+    assert np.all(orc.combine(m, l, o, lens, 4)[0] == 0.0)
+
+
+def pin_combine_closed_form(orc):
+    """Phase-2 combine on hand-set states: (m, l) = (0, 1) and (-inf, 0) returns
+    o_0 exactly; equal maxima and sums give the plain mean of the o_p;
+    m = (ln 3, 0), l = (1, 1) weighs o_0 : o_1 as 3 : 1."""
+    D = 4
+    lens = np.array([2 * 5], dtype=np.int32)  # P = 5 -> two partitions
+    o = np.zeros((1, 1, 2, D))
+    o[0, 0, 0] = [1.0, -2.0, 0.5, 3.0]
+    o[0, 0, 1] = [5.0, 1.0, -1.0, 0.0]
+    m = np.array([[[0.0, -np.inf]]])
+    l = np.array([[[1.0, 0.0]]])
+    assert np.array_equal(orc.combine(m, l, o, lens, 5)[0, 0], o[0, 0, 0])
+    m = np.array([[[0.7, 0.7]]])
+    l = np.array([[[2.0, 2.0]]])
+    _close(orc.combine(m, l, o, lens, 5)[0, 0], (o[0, 0, 0] + o[0, 0, 1]) / 2, 1e-15, "equal states")
+    m = np.array([[[math.log(3.0), 0.0]]])
+    l = np.array([[[1.0, 1.0]]])
+    _close(orc.combine(m, l, o, lens, 5)[0, 0], 0.75 * o[0, 0, 0] + 0.25 * o[0, 0, 1], 1e-15,
+           "3:1 weights")
+
+
+ALL_PINS = [
+    pin_textbook_gqa, pin_bruteforce_tiny, pin_golden_two_token, pin_golden_layout,
+    pin_seq_len_one, pin_uniform_weights, pin_shift_invariance, pin_permutation_invariance,
+    pin_partition_invariance, pin_empty_sequence, pin_combine_closed_form,
+]

@@ -1,0 +1,110 @@
+"""Helpers shared by the tests: token-major views of the paged caches, a
+numpy textbook attention, golden-file readers and the parity tolerance.
+
+None of this is used by the CUDA library or by the oracle.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+# Elementwise parity bar for fp16/bf16 inputs against the fp64 oracle.
+ATOL = 2e-3
+RTOL = 1e-2
+
+
+def within_tolerance(out, ref, atol=ATOL, rtol=RTOL):
+    out = np.asarray(out, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(out - ref)
+    bound = atol + rtol * np.abs(ref)
+    ok = bool(np.all(err <= bound))
+    worst = float(np.max(err - bound)) if err.size else 0.0
+    return ok, worst
+
+
+def token_views(key_cache: torch.Tensor, value_cache: torch.Tensor):
+    """Token-major views of the pools, [num_blocks, BS, KH, D], obtained by
+    permuting the cache tensors' axes:
+    key_cache [nb, KH, D/x, BS, x] -> [nb, BS, KH, D/x, x] -> [nb, BS, KH, D];
+    value_cache [nb, KH, D, BS] -> [nb, BS, KH, D]."""
+    nb, KH, dx, BS, x = key_cache.shape
+    k_tok = key_cache.permute(0, 3, 1, 2, 4).reshape(nb, BS, KH, dx * x)
+    v_tok = value_cache.permute(0, 3, 1, 2)
+    return k_tok, v_tok
+
+
+def caches_from_tokens(k_tok: torch.Tensor, v_tok: torch.Tensor):
+    """Inverse of :func:`token_views`: build the paged caches from token-major pools."""
+    nb, BS, KH, D = k_tok.shape
+    key_cache = k_tok.reshape(nb, BS, KH, D // 8, 8).permute(0, 2, 3, 1, 4).contiguous()
+    value_cache = v_tok.permute(0, 2, 3, 1).contiguous()
+    return key_cache, value_cache
+
+
+def gather_sequence(key_cache, value_cache, block_tables, s: int, L: int):
+    """K, V of sequence s as [L, KH, D] float64 numpy arrays (torch indexing)."""
+    k_tok, v_tok = token_views(key_cache, value_cache)
+    BS = key_cache.shape[3]
+    t = torch.arange(L)
+    b = block_tables[s].long()[t // BS]
+    o = t % BS
+    return (k_tok[b, o].to(torch.float64).numpy(), v_tok[b, o].to(torch.float64).numpy())
+
+
+def textbook_decode(query, key_cache, value_cache, block_tables, seq_lens, scale):
+    """softmax(scale * q K^T) V per (s, h) with numpy fp64; the kv head of query
+    head h is found by repeating each kv head's K/V G times consecutively."""
+    S, H, D = query.shape
+    KH = key_cache.shape[1]
+    G = H // KH
+    out = np.zeros((S, H, D))
+    q64 = query.to(torch.float64).numpy()
+    sc = float(np.float32(scale))
+    for s in range(S):
+        L = int(seq_lens[s])
+        if L == 0:
+            continue
+        K, V = gather_sequence(key_cache, value_cache, block_tables, s, L)
+        K = np.repeat(K, G, axis=1)  # [L, H, D]
+        V = np.repeat(V, G, axis=1)
+        for h in range(H):
+            z = sc * (K[:, h, :] @ q64[s, h])
+            w = np.exp(z - z.max())
+            w /= w.sum()
+            out[s, h] = w @ V[:, h, :]
+    return out
+
+
+def read_golden(name: str):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+def random_case(seed, S, H, KH, D, BS, lens, dtype=torch.float16, MB=None, num_blocks=None,
+                k_std=1.0):
+    """Small random inputs on the CPU with a random physical placement."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.tensor(lens, dtype=torch.int32)
+    if MB is None:
+        MB = max(1, math.ceil(max(int(v) for v in lens) / BS)) if len(lens) else 1
+    if num_blocks is None:
+        num_blocks = S * MB
+    q = torch.randn((S, H, D), generator=g).to(dtype)
+    kc = (torch.randn((num_blocks, KH, D // 8, BS, 8), generator=g) * k_std).to(dtype)
+    vc = torch.randn((num_blocks, KH, D, BS), generator=g).to(dtype)
+    if num_blocks >= S * MB:
+        bt = torch.randperm(num_blocks, generator=g)[: S * MB].view(S, MB).to(torch.int32)
+    else:
+        bt = torch.stack([torch.randperm(num_blocks, generator=g)[:MB] for _ in range(S)]).to(torch.int32)
+    return q, kc, vc, bt, lens

@@ -1,0 +1,64 @@
+"""CPU tests of the fp64 oracle: every pin on the real oracle, and every
+planted mistake in a copy of its source caught by at least one pin."""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(oracle.default())
+
+
+# (name, text in pa_oracle.c, replacement, count) -- count 0 replaces every occurrence.
+MUTANTS = [
+    ("gqa_modulo", "const int kh = h / (H / KH);", "const int kh = h % KH;", 0),
+    ("slot_shifted", "int o = t % BS;", "int o = (t + 1) % BS;", 1),
+    ("block_table_ignored", "bt[(size_t)s * MB + t / BS]", "bt[(size_t)s * MB + 0]", 1),
+    ("key_read_as_value_layout",
+     "return ((((size_t)b * KH + kh) * (D / x) + d / x) * BS + o) * x + d % x;",
+     "(void)x; return (((size_t)b * KH + kh) * D + d) * BS + o;", 1),
+    ("key_chunk_and_lane_swapped",
+     "return ((((size_t)b * KH + kh) * (D / x) + d / x) * BS + o) * x + d % x;",
+     "return ((((size_t)b * KH + kh) * (D / x) + d % (D / x)) * BS + o) * x + d / (D / x);", 1),
+    ("value_transposed", "return (((size_t)b * KH + kh) * D + d) * BS + o;",
+     "return (((size_t)b * KH + kh) * BS + o) * D + d;", 1),
+    ("scale_dropped", "z[t - t0] = scale * acc;", "z[t - t0] = acc;", 1),
+    ("exp_sign", "z[t] = exp(z[t] - mu);", "z[t] = exp(mu - z[t]);", 1),
+    ("not_normalised", "for (int d = 0; d < D; ++d) o_sh[d] /= den;", "", 1),
+    ("last_token_dropped", "int L = lens[s];\n        double* o_sh",
+     "int L = lens[s] > 1 ? lens[s] - 1 : lens[s];\n        double* o_sh", 1),
+    ("partition_end_short", "start + P < L ? start + P : L", "start + P - 1 < L ? start + P - 1 : L", 1),
+    ("combine_without_l", "exp(m_sh[p] - M) * l_sh[p] / total", "exp(m_sh[p] - M) / total", 1),
+    ("combine_total_without_l", "total += exp(m_sh[p] - M) * l_sh[p];", "total += exp(m_sh[p] - M);", 1),
+    ("sentinel_max_zero", "m[shp] = -INFINITY; l[shp] = 0.0;", "m[shp] = 0.0; l[shp] = 0.0;", 1),
+    ("fp16_exponent_bias", "expo - 25", "expo - 24", 1),
+    ("bf16_shift", "((uint32_t)b) << 16", "((uint32_t)b) << 15", 1),
+    ("empty_sequence_not_zero", "if (L <= 0) continue;\n        if (L > MB * BS) { bad = 1; continue; }\n        double* z",
+     "if (L > MB * BS) { bad = 1; continue; }\n        double* z", 1),
+]
+
+
+def _run_pins(orc):
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError, FloatingPointError) as e:
+            failed.append((pin.__name__, str(e)[:80]))
+    return failed
+
+
+@pytest.mark.parametrize("name,old,new,count", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new, count):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")).read()
+    assert old in src, f"mutation target for {name} not found in the oracle source"
+    mutated = src.replace(old, new) if count == 0 else src.replace(old, new, count)
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    so = oracle.build(force=True, src=str(path), out=str(tmp_path / "libmutant.so"))
+    failed = _run_pins(oracle.Oracle(oracle.load_library(so)))
+    assert failed, f"planted mistake '{name}' passed every pin"
