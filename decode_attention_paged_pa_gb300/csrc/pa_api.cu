@@ -1,0 +1,284 @@
+// pa_api.cu -- C ABI of the paged decode attention library (include/pa_decode.h):
+// argument validation, workspace layout, kernel-family choice and launches.
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include "pa_decode.h"
+#include "pa_launch.h"
+
+namespace pa {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 0 || dev >= 64) {
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+  }
+  if (cache[dev] == 0) {
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct WsLayout {
+  size_t hdr, tickets, m, l, o, total;
+  int pmax;
+};
+
+bool valid_sizes(int S, int H, int KH, int D, int MB, int BS, int P) {
+  if (S < 0 || H <= 0 || KH <= 0 || H % KH != 0 || MB <= 0 || BS <= 0 || P <= 0 || D <= 0) return false;
+  if ((long long)MB * BS > INT_MAX / 2) return false;
+  return true;
+}
+
+bool supported(int D, int BS, int P) {
+  return (D == 64 || D == 128 || D == 256) && (BS == 16 || BS == 32) && P % BS == 0;
+}
+
+bool ws_layout(int S, int H, int KH, int D, int MB, int BS, int P, WsLayout* w) {
+  if (!valid_sizes(S, H, KH, D, MB, BS, P)) return false;
+  const long long pmax = ((long long)MB * BS + P - 1) / P;
+  if (pmax > INT_MAX) return false;
+  w->pmax = (int)pmax;
+  const size_t shp = (size_t)S * H * (size_t)pmax;
+  w->hdr = 0;
+  w->tickets = align_up(kHdrInts * sizeof(int));
+  w->m = align_up(w->tickets + (size_t)S * H * sizeof(int));
+  w->l = align_up(w->m + shp * sizeof(float));
+  w->o = align_up(w->l + shp * sizeof(float));
+  w->total = align_up(w->o + shp * (size_t)D * sizeof(float));
+  return true;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_v2_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                               int head_size, int max_blocks_per_seq, int block_size,
+                                               int partition_size) {
+  WsLayout w;
+  if (!ws_layout(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, block_size,
+                 partition_size, &w))
+    return 0;
+  return w.total;
+}
+
+extern "C" int pa_decode_v2_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                             int max_blocks_per_seq, int block_size, int partition_size,
+                                             size_t offsets[5], int* max_partitions) {
+  WsLayout w;
+  if (!offsets || !ws_layout(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq,
+                             block_size, partition_size, &w))
+    return PA_ERR_INVALID_ARG;
+  offsets[0] = w.m;
+  offsets[1] = w.l;
+  offsets[2] = w.o;
+  offsets[3] = w.hdr;
+  offsets[4] = w.total;
+  if (max_partitions) *max_partitions = w.pmax;
+  return PA_OK;
+}
+
+extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cache,
+                               const void* value_cache, const int32_t* block_tables,
+                               const int32_t* seq_lens, float scale, int num_seqs, int num_heads,
+                               int num_kv_heads, int head_size, int block_size, int partition_size,
+                               int dtype, void* stream, int max_blocks_per_seq, int num_blocks,
+                               void* workspace, size_t workspace_bytes, int variant, int max_ctas,
+                               long long timeout_ns) {
+  const int S = num_seqs, H = num_heads, KH = num_kv_heads, D = head_size, BS = block_size,
+            P = partition_size, MB = max_blocks_per_seq;
+  if (!valid_sizes(S, H, KH, D, MB, BS, P) || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_DTYPE_FP16 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+  if (variant < PA_VARIANT_AUTO || variant > PA_VARIANT_MMA || max_ctas < 0 || timeout_ns < 0)
+    return PA_ERR_INVALID_ARG;
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PA_ERR_INVALID_ARG;
+  if (!supported(D, BS, P)) return PA_ERR_UNSUPPORTED;
+  if (S == 0) return PA_OK;
+  if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(query, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
+      (workspace && !aligned(workspace, 16)))
+    return PA_ERR_INVALID_ARG;
+  WsLayout w;
+  if (!ws_layout(S, H, KH, D, MB, BS, P, &w)) return PA_ERR_INVALID_ARG;
+  if (workspace && workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+
+  const int G = H / KH;
+  if (variant == PA_VARIANT_AUTO) variant = (G <= kSimtMaxGroup) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
+  const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : (G == 1 ? 1 : kSimtMaxGroup);
+  const int hg_per_kv = (G + gt - 1) / gt;
+  const int n_hg = KH * hg_per_kv;
+  const int chunk = S < kMaxSeqsPerLaunch ? S : kMaxSeqsPerLaunch;
+  if ((long long)chunk * w.pmax * n_hg > INT_MAX / 2) return PA_ERR_UNSUPPORTED;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  bool own = false;
+  if (!ws) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), w.total, st) != cudaSuccess) return PA_ERR_CUDA;
+    own = true;
+  }
+  int status = PA_OK;
+  // Error word, work counter and every completion ticket start at zero.
+  if (cudaMemsetAsync(ws, 0, w.m, st) != cudaSuccess) status = PA_ERR_CUDA;
+
+  const size_t esz = 2;
+  for (int s0 = 0; s0 < S && status == PA_OK; s0 += kMaxSeqsPerLaunch) {
+    const int n = (S - s0) < kMaxSeqsPerLaunch ? (S - s0) : kMaxSeqsPerLaunch;
+    if (s0 > 0 && cudaMemsetAsync(ws + sizeof(int) * kHdrWork, 0, sizeof(int), st) != cudaSuccess) {
+      status = PA_ERR_CUDA;
+      break;
+    }
+    KParams prm;
+    std::memset(&prm, 0, sizeof prm);
+    prm.out = static_cast<uint8_t*>(out) + (size_t)s0 * H * D * esz;
+    prm.q = static_cast<const uint8_t*>(query) + (size_t)s0 * H * D * esz;
+    prm.kc = key_cache;
+    prm.vc = value_cache;
+    prm.bt = block_tables + (size_t)s0 * MB;
+    prm.lens = seq_lens + s0;
+    prm.ws_m = reinterpret_cast<float*>(ws + w.m) + (size_t)s0 * H * w.pmax;
+    prm.ws_l = reinterpret_cast<float*>(ws + w.l) + (size_t)s0 * H * w.pmax;
+    prm.ws_o = reinterpret_cast<float*>(ws + w.o) + (size_t)s0 * H * w.pmax * D;
+    prm.hdr = reinterpret_cast<int*>(ws + w.hdr);
+    prm.tickets = reinterpret_cast<int*>(ws + w.tickets) + (size_t)s0 * n_hg;
+    prm.scale_log2 = scale * kLog2e;
+    prm.S = n;
+    prm.H = H;
+    prm.KH = KH;
+    prm.G = G;
+    prm.MB = MB;
+    prm.num_blocks = num_blocks;
+    prm.P = P;
+    prm.Pmax = w.pmax;
+    prm.hg_per_kv = hg_per_kv;
+    prm.n_hg = n_hg;
+    prm.timeout_ns = timeout_ns > 0 ? timeout_ns : (1LL << 31);
+    cudaError_t e;
+    if (variant == PA_VARIANT_MMA)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma_f16(prm, D, BS, max_ctas, st)
+                                 : launch_mma_bf16(prm, D, BS, max_ctas, st);
+    else
+      e = dtype == PA_DTYPE_FP16 ? launch_simt_f16(prm, D, BS, gt, max_ctas, st)
+                                 : launch_simt_bf16(prm, D, BS, gt, max_ctas, st);
+    if (e != cudaSuccess) status = PA_ERR_CUDA;
+  }
+  if (own && cudaFreeAsync(ws, st) != cudaSuccess && status == PA_OK) status = PA_ERR_CUDA;
+  return status;
+}
+
+extern "C" int pa_decode_v2(void* out, const void* query, const void* key_cache, const void* value_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens, float scale,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                            int block_size, int partition_size, int dtype, void* stream,
+                            int max_blocks_per_seq, int num_blocks, void* workspace,
+                            size_t workspace_bytes) {
+  return pa_decode_v2_ex(out, query, key_cache, value_cache, block_tables, seq_lens, scale, num_seqs,
+                         num_heads, num_kv_heads, head_size, block_size, partition_size, dtype, stream,
+                         max_blocks_per_seq, num_blocks, workspace, workspace_bytes, PA_VARIANT_AUTO, 0, 0);
+}
+
+namespace {
+// Staging for the host-I/O entry point, placed after the regular workspace.
+struct HostIoLayout {
+  size_t q, out, bt, lens, total;
+};
+bool host_io_layout(int S, int H, int KH, int D, int MB, int BS, int P, HostIoLayout* h, WsLayout* w) {
+  if (!ws_layout(S, H, KH, D, MB, BS, P, w)) return false;
+  const size_t qbytes = (size_t)S * H * D * 2;
+  h->q = w->total;
+  h->out = align_up(h->q + qbytes);
+  h->bt = align_up(h->out + qbytes);
+  h->lens = align_up(h->bt + (size_t)S * MB * sizeof(int32_t));
+  h->total = align_up(h->lens + (size_t)S * sizeof(int32_t));
+  return true;
+}
+}  // namespace
+
+extern "C" size_t pa_decode_v2_host_io_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                                       int head_size, int max_blocks_per_seq,
+                                                       int block_size, int partition_size) {
+  HostIoLayout h;
+  WsLayout w;
+  if (!host_io_layout(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, block_size,
+                      partition_size, &h, &w))
+    return 0;
+  return h.total;
+}
+
+extern "C" int pa_decode_v2_host_io(void* out_host, const void* query_host, const void* key_cache,
+                                    const void* value_cache, const int32_t* block_tables_host,
+                                    const int32_t* seq_lens_host, float scale, int num_seqs,
+                                    int num_heads, int num_kv_heads, int head_size, int block_size,
+                                    int partition_size, int dtype, void* stream,
+                                    int max_blocks_per_seq, int num_blocks, void* workspace,
+                                    size_t workspace_bytes) {
+  const int S = num_seqs, H = num_heads, D = head_size, MB = max_blocks_per_seq;
+  HostIoLayout h;
+  WsLayout w;
+  if (!host_io_layout(S, H, num_kv_heads, D, MB, block_size, partition_size, &h, &w))
+    return PA_ERR_INVALID_ARG;
+  if (S == 0) return PA_OK;
+  if (!out_host || !query_host || !block_tables_host || !seq_lens_host || !workspace)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < h.total) return PA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t qbytes = (size_t)S * H * D * 2;
+  if (cudaMemcpyAsync(ws + h.q, query_host, qbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(ws + h.bt, block_tables_host, (size_t)S * MB * sizeof(int32_t),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(ws + h.lens, seq_lens_host, (size_t)S * sizeof(int32_t), cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const int status = pa_decode_v2(ws + h.out, ws + h.q, key_cache, value_cache,
+                                  reinterpret_cast<const int32_t*>(ws + h.bt),
+                                  reinterpret_cast<const int32_t*>(ws + h.lens), scale, S, H,
+                                  num_kv_heads, D, block_size, partition_size, dtype, stream, MB,
+                                  num_blocks, ws, w.total);
+  if (status != PA_OK) return status;
+  if (cudaMemcpyAsync(out_host, ws + h.out, qbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+extern "C" int pa_decode_v2_device_status(const void* workspace, void* stream, int* status) {
+  if (!workspace || !status) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+  *status = v;
+  return PA_OK;
+}
+
+extern "C" const char* pa_decode_v2_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_WORKSPACE: return "workspace too small";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_DEVICE_BOUNDS: return "device-side bounds violation (block id or sequence length)";
+    case PA_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,40 @@
+// pa_launch.cuh -- shared-memory sizing and launch of one kernel instance.
+#pragma once
+
+#include "pa_launch.h"
+
+namespace pa {
+
+constexpr uint32_t kSmemBudget = 227u * 1024u;
+
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+// Ring depth: as many K+V stages as fit next to the fixed regions and the
+// largest per-launch prefix array.
+template <class C, int NC>
+struct Sizing {
+  using L1 = Layout<C, NC, 1>;
+  static constexpr uint32_t other = L1::FIXED - L1::RING + 64 * 8 + 16;
+  static constexpr uint32_t pref_max = al16((kMaxSeqsPerLaunch + 1) * 4);
+  static constexpr int NS = cmax(2, cmin(32, (int)((kSmemBudget - other - pref_max) / L1::STAGE)));
+  using LY = Layout<C, NC, NS>;
+  static_assert(LY::bytes(kMaxSeqsPerLaunch) <= kSmemBudget, "shared memory over budget");
+};
+
+template <class C, int NC>
+cudaError_t launch_one(const KParams& prm, int max_ctas, cudaStream_t stream) {
+  using SZ = Sizing<C, NC>;
+  using LY = typename SZ::LY;
+  auto kern = pa_decode_kernel<C, NC, SZ::NS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)LY::bytes(kMaxSeqsPerLaunch));
+  if (e != cudaSuccess) return e;
+  int grid = device_sm_count();
+  if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
+  if (grid < 1) grid = 1;
+  kern<<<grid, LY::THREADS, LY::bytes(prm.S), stream>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

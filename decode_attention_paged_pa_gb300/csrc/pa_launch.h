@@ -1,0 +1,29 @@
+// pa_launch.h -- internal interface between the C ABI (pa_api.cu) and the
+// kernel instantiation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "pa_kernel.cuh"
+
+namespace pa {
+
+// Sequences per launch: the kernel keeps a prefix sum of partitions per
+// sequence in shared memory; longer batches are split into several launches.
+constexpr int kMaxSeqsPerLaunch = 2048;
+
+// Heads per group tile of each kernel family.
+constexpr int kSimtMaxGroup = 2;
+constexpr int kMmaGroup = 8;
+
+// Launch the persistent kernel for one chunk of sequences.  `gt` is the SIMT
+// group tile (1 or 2); ignored by the MMA family.  Returns a cudaError_t.
+cudaError_t launch_simt_f16(const KParams& prm, int D, int BS, int gt, int max_ctas, cudaStream_t st);
+cudaError_t launch_simt_bf16(const KParams& prm, int D, int BS, int gt, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+
+// SM count of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace pa

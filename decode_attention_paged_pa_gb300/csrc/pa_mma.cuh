@@ -1,0 +1,158 @@
+// pa_mma.cuh -- tensor-core consumer for the paged decode kernel, for groups
+// of query heads that share one kv head (GQA).  Per staged block the group's
+// scores and weighted values are two small dense contractions:
+//
+//   S[tokens x heads]  = K[tokens x D] . Q^T[D x heads]       (mma m16n8k16, M = 16 tokens)
+//   O^T[D x heads]    += V^T[D x tokens] . P^T[tokens x heads] (mma m16n8k16, M = 16 dims)
+//
+// with 8 query heads as the N = 8 side of the instruction.  Both cache layouts
+// of the page "paged_attention_v2_triton.py -- Triton PagedAttention V2 for
+// BI-V100" already are the operands ldmatrix wants: a K block [D/8][BS][8]
+// stores 16 bytes (8 dims) of one token contiguously, i.e. one ldmatrix row of
+// K[tokens x dims]; a V block [D][BS] stores 8 tokens of one dim contiguously,
+// i.e. one row of V^T[dims x tokens].  The score fragment is turned into the
+// P^T operand with movmatrix (an in-register 8x8 transpose).
+//
+// Softmax arithmetic is that of the phase-1 kernel `_paged_attn_v2_partition_kernel`
+// (scores in fp32, running max, exp, running sum, rescaled accumulation); the
+// weights enter the second product rounded to the element type.
+#pragma once
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+template <typename T_, int D_, int BS_>
+struct MmaConsumer {
+  using T = T_;
+  static constexpr int D = D_, BS = BS_, GT = 8;
+  static constexpr bool kMma = true;
+  static constexpr int NK = D / 16;    // k-steps of the score product
+  static constexpr int NMT = D / 16;   // 16-dim tiles of the value product
+  static constexpr int NTT = BS / 16;  // 16-token tiles per block
+  static constexpr int SCRATCH_FLOATS = 0;
+
+  uint32_t qb[NK][2];  // Q^T fragments (B operand), packed element pairs
+  float m[2], l[2];    // heads 2*(lane%4) and 2*(lane%4)+1
+  float acc[NMT][4];
+  float scale_log2;
+
+  __device__ __forceinline__ void begin_unit(const T* qs, int nh, float sl2, int lane) {
+    const int n = lane >> 2, kq = (lane & 3) * 2;
+    const uint16_t* q16 = reinterpret_cast<const uint16_t*>(qs);
+#pragma unroll
+    for (int ks = 0; ks < NK; ++ks) {
+      uint32_t lo = 0, hi = 0;
+      if (n < nh) {
+        lo = *reinterpret_cast<const uint32_t*>(q16 + n * D + ks * 16 + kq);
+        hi = *reinterpret_cast<const uint32_t*>(q16 + n * D + ks * 16 + kq + 8);
+      }
+      qb[ks][0] = lo;
+      qb[ks][1] = hi;
+    }
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
+    scale_log2 = sl2;
+  }
+
+  __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane, float*) {
+    const uint32_t kbase = smem_addr(ks), vbase = smem_addr(vs);
+    const int r = lane >> 2;
+    float sc[NTT][4];
+#pragma unroll
+    for (int tt = 0; tt < NTT; ++tt) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) {
+        uint32_t a[4];
+        const int tok = tt * 16 + (lane & 15), chunk = 2 * kk + (lane >> 4);
+        ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
+        Mma<T>::run(c, a, qb[kk][0], qb[kk][1]);
+      }
+      const int t_lo = tt * 16 + r, t_hi = t_lo + 8;
+      sc[tt][0] = t_lo < ntok ? c[0] * scale_log2 : -INFINITY;
+      sc[tt][1] = t_lo < ntok ? c[1] * scale_log2 : -INFINITY;
+      sc[tt][2] = t_hi < ntok ? c[2] * scale_log2 : -INFINITY;
+      sc[tt][3] = t_hi < ntok ? c[3] * scale_log2 : -INFINITY;
+    }
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float bm = fmaxf(sc[0][j], sc[0][j + 2]);
+#pragma unroll
+      for (int tt = 1; tt < NTT; ++tt) bm = fmaxf(bm, fmaxf(sc[tt][j], sc[tt][j + 2]));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+      const float mn = fmaxf(m[j], bm);
+      alpha[j] = exp2f(m[j] - mn);
+      m[j] = mn;
+      float ps = 0.f;
+#pragma unroll
+      for (int tt = 0; tt < NTT; ++tt) {
+        sc[tt][j] = exp2f(sc[tt][j] - mn);
+        sc[tt][j + 2] = exp2f(sc[tt][j + 2] - mn);
+        ps += sc[tt][j] + sc[tt][j + 2];
+      }
+      l[j] = fmaf(l[j], alpha[j], ps);
+    }
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) {
+      acc[mt][0] *= alpha[0];
+      acc[mt][1] *= alpha[1];
+      acc[mt][2] *= alpha[0];
+      acc[mt][3] *= alpha[1];
+    }
+    if (ntok < BS) {
+      // Slots past the sequence end hold arbitrary cache contents; zero them
+      // so that 0 * (NaN or Inf) cannot reach the accumulator.
+      for (int i = lane; i < D * (BS - ntok); i += 32) {
+        const int d = i / (BS - ntok), t = ntok + i % (BS - ntok);
+        reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+#pragma unroll
+    for (int tt = 0; tt < NTT; ++tt) {
+      // P fragment rows = tokens, cols = heads; transpose to the B operand.
+      const uint32_t b0 = movmatrix_trans(F16Traits<T>::pack(sc[tt][0], sc[tt][1]));
+      const uint32_t b1 = movmatrix_trans(F16Traits<T>::pack(sc[tt][2], sc[tt][3]));
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) {
+        uint32_t a[4];
+        const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (lane >> 4);
+        ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
+        Mma<T>::run(acc[mt], a, b0, b1);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void finish(float* acc_out, float* ml, int lane) {
+    const int r = lane >> 2, hq = (lane & 3) * 2;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float ls = l[j];
+      ls += __shfl_xor_sync(0xffffffffu, ls, 4);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+      if (r == 0) {
+        ml[(hq + j) * 2] = m[j];
+        ml[(hq + j) * 2 + 1] = ls;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) {
+      acc_out[hq * D + mt * 16 + r] = acc[mt][0];
+      acc_out[(hq + 1) * D + mt * 16 + r] = acc[mt][1];
+      acc_out[hq * D + mt * 16 + r + 8] = acc[mt][2];
+      acc_out[(hq + 1) * D + mt * 16 + r + 8] = acc[mt][3];
+    }
+  }
+};
+
+}  // namespace pa

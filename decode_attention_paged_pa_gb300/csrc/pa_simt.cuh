@@ -1,0 +1,177 @@
+// pa_simt.cuh -- CUDA-core consumer for the paged decode kernel: one warp
+// turns one staged physical block (K block [D/8][BS][8], V block [D][BS]) into
+// an online-softmax update of its private (m, l, acc) state for GT query heads.
+//
+// Follows the phase-1 kernel `_paged_attn_v2_partition_kernel` of the page
+// "paged_attention_v2_triton.py -- Triton PagedAttention V2 for BI-V100":
+// scores = scale * q . k (fp32), masked tokens -> -inf, block max, exp, running
+// sum and rescaled V accumulation.  Unlike the page, each K/V block is read
+// once for all GT query heads of its kv head, and the accumulator is kept
+// unnormalised per warp (normalised once, when the warps' states are combined).
+#pragma once
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+template <typename T_, int D_, int BS_, int GT_>
+struct SimtConsumer {
+  using T = T_;
+  static constexpr int D = D_, BS = BS_, GT = GT_;
+  static constexpr bool kMma = false;
+  // q.k: each lane takes QKD dims of one token; LPT lanes share a token.
+  static constexpr int QKD = (D >= 128) ? 64 : 32;
+  static constexpr int LPT = D / QKD;
+  static constexpr int TPP = 32 / LPT;        // tokens per pass over the warp
+  static constexpr int NPASS = BS / TPP;
+  static constexpr int QCH = QKD / 8;         // 16-byte K chunks per lane and token
+  // p.V: lane (row r, chunk c) reads the 16-byte chunk c (8 tokens) of V rows
+  // r, r + RPP, ...; consecutive lanes read consecutive 16-byte words.
+  static constexpr int CPR = BS / 8;          // chunks per V row
+  static constexpr int RPP = 32 / CPR;        // rows per warp pass
+  static constexpr int NROW = D / RPP;        // rows per lane
+  static constexpr int SCRATCH_FLOATS = GT * BS;  // per warp: p of the current block
+
+  static_assert(NPASS >= 1 && BS % TPP == 0, "block size must cover whole passes");
+
+  float qf[GT][QKD];
+  float m[GT], l[GT];
+  float acc[GT][NROW];
+
+  // q rows [GT][D] in shared memory; rows >= nh are treated as zero.
+  __device__ __forceinline__ void begin_unit(const T* qs, int nh, float scale_log2, int lane) {
+    const int slice = lane / TPP;
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+#pragma unroll
+      for (int i = 0; i < QCH; ++i) {
+        float f[8];
+        if (g < nh) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(qs + g * D + slice * QKD + i * 8);
+          unpack8<T>(raw, f);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qf[g][i * 8 + e] = f[e] * scale_log2;
+      }
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int r = 0; r < NROW; ++r) acc[g][r] = 0.f;
+    }
+  }
+
+  // One staged block: ks = K block, vs = V block (shared memory), ntok valid
+  // tokens (1..BS).  pw = this warp's scratch (SCRATCH_FLOATS floats).
+  __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane,
+                                        float* pw) {
+    const int tl = lane % TPP, slice = lane / TPP;
+    float sc[NPASS][GT];
+#pragma unroll
+    for (int ps = 0; ps < NPASS; ++ps) {
+      const int t = ps * TPP + tl;
+#pragma unroll
+      for (int g = 0; g < GT; ++g) sc[ps][g] = 0.f;
+#pragma unroll
+      for (int i = 0; i < QCH; ++i) {
+        const int c = slice * QCH + i;
+        const uint4 raw = *reinterpret_cast<const uint4*>(ks + (c * BS + t) * 16);
+        float f[8];
+        unpack8<T>(raw, f);
+#pragma unroll
+        for (int g = 0; g < GT; ++g)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sc[ps][g] = fmaf(qf[g][i * 8 + e], f[e], sc[ps][g]);
+      }
+#pragma unroll
+      for (int g = 0; g < GT; ++g) {
+#pragma unroll
+        for (int off = TPP; off < 32; off <<= 1) sc[ps][g] += __shfl_xor_sync(0xffffffffu, sc[ps][g], off);
+        if (t >= ntok) sc[ps][g] = -INFINITY;
+      }
+    }
+    // Online softmax update (log2 domain: q carries scale * log2(e)).
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+      float bm = sc[0][g];
+#pragma unroll
+      for (int ps = 1; ps < NPASS; ++ps) bm = fmaxf(bm, sc[ps][g]);
+#pragma unroll
+      for (int off = 1; off < TPP; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+      const float mn = fmaxf(m[g], bm);
+      const float alpha = exp2f(m[g] - mn);
+      m[g] = mn;
+      float psum = 0.f;
+#pragma unroll
+      for (int ps = 0; ps < NPASS; ++ps) {
+        const float p = exp2f(sc[ps][g] - mn);
+        sc[ps][g] = p;
+        psum += p;
+      }
+      l[g] = fmaf(l[g], alpha, psum);
+#pragma unroll
+      for (int r = 0; r < NROW; ++r) acc[g][r] *= alpha;
+      if (slice == 0) {
+#pragma unroll
+        for (int ps = 0; ps < NPASS; ++ps) pw[g * BS + ps * TPP + tl] = sc[ps][g];
+      }
+    }
+    if (ntok < BS) {
+      // Slots past the sequence end hold arbitrary cache contents; zero them
+      // so that 0 * (NaN or Inf) cannot reach the accumulator.
+      for (int i = lane; i < D * (BS - ntok); i += 32) {
+        const int d = i / (BS - ntok), t = ntok + i % (BS - ntok);
+        reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+      }
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    const int r0 = lane / CPR, c = lane % CPR;
+    float pv[GT][8];
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+      const float4 a = *reinterpret_cast<const float4*>(pw + g * BS + c * 8);
+      const float4 b = *reinterpret_cast<const float4*>(pw + g * BS + c * 8 + 4);
+      pv[g][0] = a.x; pv[g][1] = a.y; pv[g][2] = a.z; pv[g][3] = a.w;
+      pv[g][4] = b.x; pv[g][5] = b.y; pv[g][6] = b.z; pv[g][7] = b.w;
+    }
+#pragma unroll
+    for (int r = 0; r < NROW; ++r) {
+      const int d = r0 + r * RPP;
+      const uint4 raw = *reinterpret_cast<const uint4*>(vs + (d * BS + c * 8) * 2);
+      float f[8];
+      unpack8<T>(raw, f);
+#pragma unroll
+      for (int g = 0; g < GT; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][r] = fmaf(pv[g][e], f[e], acc[g][r]);
+    }
+    __syncwarp();
+  }
+
+  // Write this warp's state: acc_out [GT][D] (unnormalised), ml [GT][2] = (m, l).
+  __device__ __forceinline__ void finish(float* acc_out, float* ml, int lane) {
+    const int r0 = lane / CPR, c = lane % CPR;
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+      float ls = l[g];
+#pragma unroll
+      for (int off = 1; off < TPP; off <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+#pragma unroll
+      for (int r = 0; r < NROW; ++r) {
+        float v = acc[g][r];
+#pragma unroll
+        for (int off = 1; off < CPR; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (c == 0) acc_out[g * D + r0 + r * RPP] = v;
+      }
+      if (lane == 0) {
+        ml[g * 2] = m[g];
+        ml[g * 2 + 1] = ls;
+      }
+    }
+  }
+};
+
+}  // namespace pa

@@ -1,0 +1,182 @@
+/*
+ * pa_decode.h -- C ABI of a GB300 (sm_103a) single-query paged decode
+ * attention library ("PagedAttention V2": partitioned online softmax followed
+ * by a cross-partition log-sum-exp combine).
+ *
+ * What it computes, per sequence s and query head h (the page
+ * "paged_attention_v2_triton.py -- Triton PagedAttention V2 for BI-V100",
+ * kernels `_paged_attn_v2_partition_kernel` and `_paged_attn_v2_reduce_kernel`
+ * and the module docstring's Phase 2 formula):
+ *
+ *   kv   = h / (num_heads / num_kv_heads)                 (consecutive GQA groups)
+ *   for t < L = seq_lens[s]:  b = block_tables[s, t / block_size], o = t % block_size
+ *       K_t[d] = key_cache  [b, kv, d / x, o, d % x]      x = 16 / sizeof(element) = 8
+ *       V_t[d] = value_cache[b, kv, d, o]
+ *       z_t    = scale * sum_d query[s, h, d] * K_t[d]    (fp32)
+ *   out[s, h, :] = sum_t softmax(z)_t * V_t               rounded to the element type
+ *
+ * computed in partitions of `partition_size` tokens: partition p holds tokens
+ * [p*P, min((p+1)*P, L)) and yields (m_p, l_p, o_p) = (max z, sum e^(z - m_p),
+ * normalised weighted V); the partitions are then combined with
+ * M = max m_p, w_p = e^(m_p - M) l_p / sum_q e^(m_q - M) l_q, out = sum w_p o_p.
+ * A sequence that fits in one partition is written directly (single pass).
+ * L = 0 yields zeros (the "flash_attention.metal" page's forward kernel takes
+ * 1/l as 0 when l = 0).
+ *
+ * Memory: every pointer argument of pa_decode_v2 is a DEVICE pointer on the
+ * current CUDA device; tensors are contiguous row-major.  The caller owns all
+ * buffers.  The library reads query, caches, tables and lengths, and writes
+ * `out` and `workspace` only.  Calls are enqueued on `stream` (a cudaStream_t,
+ * NULL = legacy default stream) and never synchronise; results are ready when
+ * the stream reaches that point.  Concurrent calls must not share a workspace.
+ *
+ * Errors: argument problems are reported by the return value before anything
+ * is enqueued.  Problems only visible on the device (a block id outside
+ * [0, num_blocks), seq_lens[s] outside [0, max_blocks_per_seq*block_size], a
+ * bounded wait that ran out) are recorded in the workspace's error word, read
+ * with pa_decode_v2_device_status(); the kernel never traps and never reads
+ * outside the caches when it records a bad block id.
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of query, caches and output. */
+enum { PA_DTYPE_FP16 = 0, PA_DTYPE_BF16 = 1 };
+
+/* Status codes. */
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, H % KH != 0, ... */
+    PA_ERR_UNSUPPORTED = 2,   /* head_size not 64/128/256, block_size not 16/32,
+                                 partition_size not a positive multiple of block_size */
+    PA_ERR_WORKSPACE = 3,     /* workspace smaller than pa_decode_v2_workspace_bytes() */
+    PA_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, memset, ...) */
+    PA_ERR_DEVICE_BOUNDS = 5, /* device-side: bad block id or sequence length */
+    PA_ERR_TIMEOUT = 6        /* device-side: a bounded wait gave up */
+};
+
+/* Kernel families (pa_decode_v2_ex's `variant`). */
+enum {
+    PA_VARIANT_AUTO = 0,      /* SIMT for groups of 1-2 query heads per kv head, MMA otherwise */
+    PA_VARIANT_SIMT = 1,      /* CUDA-core dot products and warp-shuffle reductions */
+    PA_VARIANT_MMA = 2        /* mma.sync m16n8k16 over the [group x D] . [D x tokens] contraction */
+};
+
+/*
+ * Bytes of device workspace pa_decode_v2 needs for these sizes: a small
+ * header (error word, work counter), one completion ticket per (sequence,
+ * head group), and the phase-1 partition states of the page's launcher:
+ * max_logits [S, H, Pmax] f32, exp_sums [S, H, Pmax] f32 and
+ * tmp_output [S, H, Pmax, head_size] f32, with
+ * Pmax = ceil(max_blocks_per_seq * block_size / partition_size).
+ * Returns 0 for invalid sizes.
+ */
+size_t pa_decode_v2_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                    int max_blocks_per_seq, int block_size, int partition_size);
+
+/*
+ * Byte offsets of the workspace regions (for inspection in tests):
+ * offsets[0] = max_logits (m_p, natural-log units, -inf for unused partitions),
+ * offsets[1] = exp_sums (l_p, 0 for unused partitions),
+ * offsets[2] = tmp_output (o_p, normalised; written only for sequences with
+ *              more than one partition), offsets[3] = header (int32 error word
+ *              at index 0), offsets[4] = total bytes.  *max_partitions = Pmax.
+ * Returns PA_OK or PA_ERR_INVALID_ARG.
+ */
+int pa_decode_v2_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                  int max_blocks_per_seq, int block_size, int partition_size,
+                                  size_t offsets[5], int* max_partitions);
+
+/*
+ * Paged decode attention (see the top of this file).
+ *   out          [num_seqs, num_heads, head_size]                      dtype, written
+ *   query        [num_seqs, num_heads, head_size]                      dtype
+ *   key_cache    [num_blocks, num_kv_heads, head_size/8, block_size, 8] dtype
+ *   value_cache  [num_blocks, num_kv_heads, head_size, block_size]      dtype
+ *   block_tables [num_seqs, max_blocks_per_seq] int32; entries past
+ *                ceil(seq_lens[s]/block_size) are never read
+ *   seq_lens     [num_seqs] int32, each in [0, max_blocks_per_seq*block_size]
+ *   scale        softmax scale applied to q.k (fp32)
+ *   dtype        PA_DTYPE_FP16 or PA_DTYPE_BF16
+ *   stream       cudaStream_t to enqueue on
+ *   max_blocks_per_seq  row stride of block_tables (the page's launcher reads
+ *                it from the tensor's shape; a C ABI has to be told)
+ *   num_blocks   number of physical blocks in each cache (bounds checks)
+ *   workspace    device buffer of >= pa_decode_v2_workspace_bytes() bytes,
+ *                16-byte aligned; NULL makes the call allocate and free one
+ *                stream-ordered (cudaMallocAsync / cudaFreeAsync)
+ * out, query and the caches must be 16-byte aligned; tables 4-byte aligned.
+ */
+int pa_decode_v2(void* out, const void* query, const void* key_cache, const void* value_cache,
+                 const int32_t* block_tables, const int32_t* seq_lens, float scale,
+                 int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                 int block_size, int partition_size, int dtype, void* stream,
+                 int max_blocks_per_seq, int num_blocks, void* workspace, size_t workspace_bytes);
+
+/*
+ * pa_decode_v2 with tuning controls, for tests and measurement.
+ *   variant     PA_VARIANT_*; SIMT handles up to 2 query heads per kv head in
+ *               one pass (larger groups take ceil(G/2) passes), MMA any group
+ *               (8 query heads per pass).
+ *   max_ctas    upper bound on the persistent grid (0 = one CTA per SM).
+ *   timeout_ns  bound on every device-side wait (0 = 2^31 ns).
+ * Results do not depend on variant-independent choices: for a fixed variant
+ * the output is bitwise identical for every max_ctas.
+ */
+int pa_decode_v2_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
+                    const int32_t* block_tables, const int32_t* seq_lens, float scale,
+                    int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                    int block_size, int partition_size, int dtype, void* stream,
+                    int max_blocks_per_seq, int num_blocks, void* workspace, size_t workspace_bytes,
+                    int variant, int max_ctas, long long timeout_ns);
+
+/*
+ * Bytes of device workspace pa_decode_v2_host_io needs: the workspace of
+ * pa_decode_v2 plus device staging for query, out, block_tables and seq_lens.
+ * Returns 0 for invalid sizes.
+ */
+size_t pa_decode_v2_host_io_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                            int head_size, int max_blocks_per_seq, int block_size,
+                                            int partition_size);
+
+/*
+ * pa_decode_v2 for callers that hold the per-step inputs in HOST memory (a
+ * serving loop): query_host, block_tables_host and seq_lens_host are copied
+ * into device staging inside `workspace`, the decode runs on the device-
+ * resident caches (key_cache, value_cache: DEVICE pointers), and the result is
+ * copied back into out_host.  Everything is enqueued on `stream` with
+ * cudaMemcpyAsync; the call returns without synchronising, so the host buffers
+ * must stay alive and untouched until the stream has passed this call (use
+ * page-locked host memory for the copies to be asynchronous).  `workspace`
+ * (DEVICE, 16-byte aligned, >= pa_decode_v2_host_io_workspace_bytes()) is
+ * required.  Sizes, layouts and status codes as for pa_decode_v2.
+ */
+int pa_decode_v2_host_io(void* out_host, const void* query_host, const void* key_cache,
+                         const void* value_cache, const int32_t* block_tables_host,
+                         const int32_t* seq_lens_host, float scale, int num_seqs, int num_heads,
+                         int num_kv_heads, int head_size, int block_size, int partition_size,
+                         int dtype, void* stream, int max_blocks_per_seq, int num_blocks,
+                         void* workspace, size_t workspace_bytes);
+
+/*
+ * Device-side status of the last call that used `workspace`: synchronises
+ * `stream`, copies the error word and stores it in *status (PA_OK if none).
+ * Returns PA_OK, or PA_ERR_CUDA if the copy or the synchronisation failed.
+ */
+int pa_decode_v2_device_status(const void* workspace, void* stream, int* status);
+
+/* Static description of a status code. */
+const char* pa_decode_v2_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

@@ -108,3 +108,32 @@ def random_case(seed, S, H, KH, D, BS, lens, dtype=torch.float16, MB=None, num_b
     else:
         bt = torch.stack([torch.randperm(num_blocks, generator=g)[:MB] for _ in range(S)]).to(torch.int32)
     return q, kc, vc, bt, lens
+
+
+def compact_sequences(inputs: dict, seqs):
+    """Inputs restricted to sequences ``seqs``: the physical blocks they use are
+    copied into a compact pool (CPU) and their tables renumbered.  Plain data
+    movement, so the oracle can check sampled outputs of a full-size batch."""
+    q, kc, vc = inputs["query"], inputs["key_cache"], inputs["value_cache"]
+    bt, lens = inputs["block_tables"], inputs["seq_lens"]
+    BS = kc.shape[3]
+    seqs = [int(s) for s in seqs]
+    lens_cpu = lens.cpu()
+    bt_cpu = bt.cpu()
+    used = []
+    for s in seqs:
+        nb = -(-int(lens_cpu[s]) // BS)
+        used.append(bt_cpu[s, :nb].long())
+    allb = torch.unique(torch.cat(used)) if used else torch.zeros(0, dtype=torch.long)
+    remap = {int(b): i for i, b in enumerate(allb.tolist())}
+    MB = max(1, max((u.numel() for u in used), default=1))
+    bt_sub = torch.zeros((len(seqs), MB), dtype=torch.int32)
+    for i, u in enumerate(used):
+        if u.numel():
+            bt_sub[i, : u.numel()] = torch.tensor([remap[int(b)] for b in u.tolist()], dtype=torch.int32)
+    idx = allb.to(kc.device)
+    kc_sub = kc.index_select(0, idx).cpu() if allb.numel() else kc[:1].cpu()
+    vc_sub = vc.index_select(0, idx).cpu() if allb.numel() else vc[:1].cpu()
+    q_sub = q[torch.tensor(seqs, device=q.device)].cpu()
+    lens_sub = lens_cpu[seqs].clone()
+    return q_sub, kc_sub, vc_sub, bt_sub, lens_sub

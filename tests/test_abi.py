@@ -1,0 +1,104 @@
+"""CPU tests of the C ABI: the library loads, exports every symbol the header
+declares, sizes its workspace as documented and rejects bad arguments before
+it touches the GPU (no compute calls are made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from decode_attention_paged_pa_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa_decode.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(binding.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _align(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("S,H,KH,D,MB,BS,P", [
+    (4, 4, 4, 64, 19, 16, 512),
+    (64, 32, 32, 128, 256, 16, 512),
+    (8, 64, 8, 128, 4096, 32, 512),
+    (3, 6, 2, 256, 7, 16, 32),
+])
+def test_workspace_bytes_and_layout(S, H, KH, D, MB, BS, P):
+    pmax = -(-(MB * BS) // P)
+    hdr = 256
+    tickets = hdr
+    m = _align(tickets + S * H * 4)
+    l = _align(m + S * H * pmax * 4)
+    o = _align(l + S * H * pmax * 4)
+    total = _align(o + S * H * pmax * D * 4)
+    assert binding.workspace_bytes(S, H, KH, D, MB, BS, P) == total
+    offs, pm = binding.workspace_layout(S, H, KH, D, MB, BS, P)
+    assert offs == (m, l, o, 0, total) and pm == pmax
+
+
+def test_workspace_bytes_invalid_sizes_is_zero():
+    assert binding.workspace_bytes(4, 6, 4, 64, 8, 16, 512) == 0   # H % KH != 0
+    assert binding.workspace_bytes(4, 4, 4, 64, 0, 16, 512) == 0   # no blocks per sequence
+    assert binding.workspace_bytes(-1, 4, 4, 64, 8, 16, 512) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced by these calls
+
+
+def call(**kw):
+    a = dict(out=FAKE, query=FAKE, key_cache=FAKE, value_cache=FAKE, block_tables=FAKE,
+             seq_lens=FAKE, scale=0.125, num_seqs=2, num_heads=4, num_kv_heads=2, head_size=128,
+             block_size=16, partition_size=512, dtype=0, stream=None, max_blocks_per_seq=4,
+             num_blocks=8, workspace=FAKE, workspace_bytes=1 << 30)
+    a.update(kw)
+    return binding.lib().pa_decode_v2(
+        a["out"], a["query"], a["key_cache"], a["value_cache"], a["block_tables"], a["seq_lens"],
+        ctypes.c_float(a["scale"]), a["num_seqs"], a["num_heads"], a["num_kv_heads"], a["head_size"],
+        a["block_size"], a["partition_size"], a["dtype"], a["stream"], a["max_blocks_per_seq"],
+        a["num_blocks"], a["workspace"], a["workspace_bytes"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_heads=6, num_kv_heads=4), binding.PA_ERR_INVALID_ARG),
+    (dict(dtype=7), binding.PA_ERR_INVALID_ARG),
+    (dict(head_size=96), binding.PA_ERR_UNSUPPORTED),
+    (dict(block_size=8), binding.PA_ERR_UNSUPPORTED),
+    (dict(partition_size=100), binding.PA_ERR_UNSUPPORTED),
+    (dict(partition_size=0), binding.PA_ERR_INVALID_ARG),
+    (dict(out=None), binding.PA_ERR_INVALID_ARG),
+    (dict(seq_lens=None), binding.PA_ERR_INVALID_ARG),
+    (dict(query=FAKE + 8), binding.PA_ERR_INVALID_ARG),
+    (dict(key_cache=FAKE + 2), binding.PA_ERR_INVALID_ARG),
+    (dict(block_tables=FAKE + 2), binding.PA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), binding.PA_ERR_INVALID_ARG),
+    (dict(max_blocks_per_seq=0), binding.PA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.PA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.PA_ERR_INVALID_ARG),
+    (dict(workspace_bytes=1024), binding.PA_ERR_WORKSPACE),
+    (dict(num_seqs=0), binding.PA_OK),
+])
+def test_rejects_bad_arguments_before_launch(kw, status):
+    assert call(**kw) == status
+
+
+def test_status_strings():
+    for code in range(7):
+        s = binding.status_string(code)
+        assert s and s != "unknown status"
+    assert binding.status_string(99) == "unknown status"
