@@ -59,6 +59,8 @@ def parse_args():
                     help="target CPU time of the oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="use only this many sequences of the workload (smaller case for profiling)")
     return ap.parse_args()
 
 
@@ -268,6 +270,12 @@ def run_native(args, rank, world, local):
         dist.init_process_group("nccl", rank=rank, world_size=world, device_id=dev)
 
     w0 = workloads.WORKLOADS[args.config]
+    if args.seqs > 0:
+        w0 = dataclasses.replace(w0, num_seqs=min(args.seqs, w0.num_seqs),
+                                 num_blocks=min(args.seqs, w0.num_seqs) * w0.max_blocks_per_seq,
+                                 lens=w0.lens if w0.lens_random else w0.lens[:args.seqs],
+                                 forced_lens=tuple((i, v) for i, v in w0.forced_lens if i < args.seqs),
+                                 distinct_tables=False, name=f"{w0.name}[:{args.seqs}]")
     w = dataclasses.replace(w0, seed=w0.seed + 100 * rank)   # each rank: its own replica batch
     inp = workloads.make_inputs(w, device=dev)
     lens = inp["seq_lens"].tolist()
