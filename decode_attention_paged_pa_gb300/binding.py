@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "pa_decode_v2_workspace_layout",
     "pa_decode_v2_host_io",
     "pa_decode_v2_host_io_workspace_bytes",
+    "pa_decode_v2_static_scratch",
     "pa_decode_v2_device_status",
     "pa_decode_v2_status_string",
 )

@@ -166,6 +166,47 @@ int pa_decode_v2_host_io(void* out_host, const void* query_host, const void* key
                          void* workspace, size_t workspace_bytes);
 
 /*
+ * Size of the scratch array behind pa_decode_v2_static_scratch: 32 MiB of
+ * device memory, reserved on every device that loads the library, for as long
+ * as the process lives.
+ */
+#define PA_DECODE_V2_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * pa_decode_v2 for callers that must not allocate device memory at call time.
+ * The pages have no counterpart: this is a deployment aid of this library.
+ *
+ * Who needs it: a process whose device memory is all reserved in advance by
+ * another allocator (so a new cudaMalloc would fail), a latency-critical loop
+ * that cannot risk an allocation call synchronising the device or stalling
+ * other streams, or a deployment that fixes its memory footprint at start-up
+ * and forbids allocation afterwards.  Such callers can use neither a
+ * workspace of their own nor the library's stream-ordered allocation.
+ *
+ * What it does: the same computation as pa_decode_v2 (same arguments, minus
+ * the workspace), with the scratch taken from a fixed array of
+ * PA_DECODE_V2_STATIC_SCRATCH_BYTES inside the library's device memory.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.  The caller
+ * still provides all inputs and `out`.
+ *   - Sizes whose workspace (pa_decode_v2_workspace_bytes) exceeds the array
+ *     are rejected with PA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents; the counters that must start at zero are cleared by each call
+ *     on its stream.  Calls whose execution overlaps on the GPU (different
+ *     streams, or threads without ordering between them) race on the array
+ *     and give undefined results: order them on one stream.
+ * Status codes as for pa_decode_v2.
+ */
+int pa_decode_v2_static_scratch(void* out, const void* query, const void* key_cache,
+                                const void* value_cache, const int32_t* block_tables,
+                                const int32_t* seq_lens, float scale, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_size, int block_size, int partition_size,
+                                int dtype, void* stream, int max_blocks_per_seq, int num_blocks);
+
+/*
  * Device-side status of the last call that used `workspace`: synchronises
  * `stream`, copies the error word and stores it in *status (PA_OK if none).
  * Returns PA_OK, or PA_ERR_CUDA if the copy or the synchronisation failed.
