@@ -32,8 +32,8 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t hdr, tickets, m, l, o, total;
-  int pmax;
+  size_t hdr, tickets, ctickets, m, l, o, cm, cl, co, total;
+  int pmax, cmax;
 };
 
 bool valid_sizes(int S, int H, int KH, int D, int MB, int BS, int P) {
@@ -51,13 +51,19 @@ bool ws_layout(int S, int H, int KH, int D, int MB, int BS, int P, WsLayout* w) 
   const long long pmax = ((long long)MB * BS + P - 1) / P;
   if (pmax > INT_MAX) return false;
   w->pmax = (int)pmax;
+  w->cmax = (int)((pmax + kChunkParts - 1) / kChunkParts);
   const size_t shp = (size_t)S * H * (size_t)pmax;
+  const size_t shc = (size_t)S * H * (size_t)w->cmax;
   w->hdr = 0;
   w->tickets = align_up(kHdrInts * sizeof(int));
-  w->m = align_up(w->tickets + (size_t)S * H * sizeof(int));
+  w->ctickets = align_up(w->tickets + (size_t)S * H * sizeof(int));
+  w->m = align_up(w->ctickets + shc * sizeof(int));
   w->l = align_up(w->m + shp * sizeof(float));
   w->o = align_up(w->l + shp * sizeof(float));
-  w->total = align_up(w->o + shp * (size_t)D * sizeof(float));
+  w->cm = align_up(w->o + shp * (size_t)D * sizeof(float));
+  w->cl = align_up(w->cm + shc * sizeof(float));
+  w->co = align_up(w->cl + shc * sizeof(float));
+  w->total = align_up(w->co + shc * (size_t)D * sizeof(float));
   return true;
 }
 
@@ -121,8 +127,8 @@ extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cac
   if (workspace && workspace_bytes < w.total) return PA_ERR_WORKSPACE;
 
   const int G = H / KH;
-  if (variant == PA_VARIANT_AUTO) variant = (G <= kSimtMaxGroup) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
-  const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : (G == 1 ? 1 : kSimtMaxGroup);
+  if (variant == PA_VARIANT_AUTO) variant = (G == 1) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
+  const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : kSimtGroup;
   const int hg_per_kv = (G + gt - 1) / gt;
   const int n_hg = KH * hg_per_kv;
   const int chunk = S < kMaxSeqsPerLaunch ? S : kMaxSeqsPerLaunch;
@@ -136,7 +142,8 @@ extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cac
     own = true;
   }
   int status = PA_OK;
-  // Error word, work counter and every completion ticket start at zero.
+  // Error word, work counter and every completion ticket (sequence and chunk
+  // level) start at zero.
   if (cudaMemsetAsync(ws, 0, w.m, st) != cudaSuccess) status = PA_ERR_CUDA;
 
   const size_t esz = 2;
@@ -159,6 +166,11 @@ extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cac
     prm.ws_o = reinterpret_cast<float*>(ws + w.o) + (size_t)s0 * H * w.pmax * D;
     prm.hdr = reinterpret_cast<int*>(ws + w.hdr);
     prm.tickets = reinterpret_cast<int*>(ws + w.tickets) + (size_t)s0 * n_hg;
+    prm.ctickets = reinterpret_cast<int*>(ws + w.ctickets) + (size_t)s0 * n_hg * w.cmax;
+    prm.ws_cm = reinterpret_cast<float*>(ws + w.cm) + (size_t)s0 * H * w.cmax;
+    prm.ws_cl = reinterpret_cast<float*>(ws + w.cl) + (size_t)s0 * H * w.cmax;
+    prm.ws_co = reinterpret_cast<float*>(ws + w.co) + (size_t)s0 * H * w.cmax * D;
+    prm.Cmax = w.cmax;
     prm.scale_log2 = scale * kLog2e;
     prm.S = n;
     prm.H = H;
@@ -176,8 +188,8 @@ extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cac
       e = dtype == PA_DTYPE_FP16 ? launch_mma_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma_bf16(prm, D, BS, max_ctas, st);
     else
-      e = dtype == PA_DTYPE_FP16 ? launch_simt_f16(prm, D, BS, gt, max_ctas, st)
-                                 : launch_simt_bf16(prm, D, BS, gt, max_ctas, st);
+      e = dtype == PA_DTYPE_FP16 ? launch_simt_f16(prm, D, BS, max_ctas, st)
+                                 : launch_simt_bf16(prm, D, BS, max_ctas, st);
     if (e != cudaSuccess) status = PA_ERR_CUDA;
   }
   if (own && cudaFreeAsync(ws, st) != cudaSuccess && status == PA_OK) status = PA_ERR_CUDA;

@@ -12,17 +12,30 @@
 //     scheduling balances skewed sequence lengths), publishes each unit's
 //     description and query rows through a 2-slot unit queue, and streams the
 //     unit's physical K and V blocks -- each a contiguous D*BS*2-byte run in
-//     the page's layouts -- into an NSTAGE-deep shared-memory ring with 1-D
-//     bulk async copies completing on mbarriers;
-//   * warps 0..NC-1 (consumers): block j of a unit goes to warp j % NC, which
-//     folds it into its private online-softmax state (SimtConsumer or
-//     MmaConsumer).  At the end of a unit the warps' states are combined in
-//     shared memory into the partition's (m_p, l_p, o_p).
+//     the page's layouts -- into shared memory with 1-D bulk async copies
+//     completing on mbarriers;
+//   * warps 0..NC-1 (consumers): block j of a unit goes to warp j % NC (a
+//     fixed grouping, so results do not depend on scheduling), which folds it
+//     into its private online-softmax state (SimtConsumer or MmaConsumer).
+//     The CTA's g-th block (counted over all its units) lives in ring stage
+//     g % NSTAGE.  Warps run at different speeds, so a fast warp
+//     could reach stage g % NSTAGE while the stage's previous copy (block
+//     g - NSTAGE) is still in flight, and an mbarrier parity wait cannot tell
+//     those two phases apart.  A consumer therefore first waits until the
+//     producer has issued block g (a shared-memory counter): the producer
+//     issues block g only after block g - NSTAGE was consumed, so by then the
+//     stage's previous phase is complete and the parity wait is exact.
+//     At the end of a unit the warps' states are combined in shared memory
+//     into the partition's (m_p, l_p, o_p).
 // Sequences with one partition write the output directly (single pass).  For
 // longer sequences each unit stores its partition state in the workspace and
-// takes a ticket; the CTA that completes a (sequence, head group) performs the
-// phase-2 combine of `_paged_attn_v2_reduce_kernel` (M = max m_p,
-// w_p = e^(m_p - M) l_p / sum, out = sum w_p o_p) for all its partitions.
+// takes a ticket (checked one unit later, off the critical path); the last
+// writer runs the phase-2 combine of `_paged_attn_v2_reduce_kernel`
+// (M = max m_p, w_p = e^(m_p - M) l_p / sum, out = sum w_p o_p).  Up to
+// kChunk = 16 partitions are combined in one step; longer sequences are
+// combined per chunk of 16 partitions by each chunk's last writer, and the
+// chunk states by the last chunk (the combine is associative), so no CTA
+// walks hundreds of partitions alone.
 // Unused partitions get the sentinels (m = -inf, l = 0) of the page.
 #pragma once
 
@@ -40,10 +53,14 @@ struct KParams {
   float* ws_m;   // [S, H, Pmax]
   float* ws_l;   // [S, H, Pmax]
   float* ws_o;   // [S, H, Pmax, D]
+  float* ws_cm;  // [S, H, Cmax]     combined state of each chunk of kChunk partitions
+  float* ws_cl;  // [S, H, Cmax]
+  float* ws_co;  // [S, H, Cmax, D]
   int* hdr;      // kHdrInts ints
-  int* tickets;  // [S, n_hg]
+  int* tickets;  // [S, n_hg]        partitions (or chunks) of a sequence completed
+  int* ctickets; // [S, n_hg, Cmax]  partitions of a chunk completed
   float scale_log2;
-  int S, H, KH, G, MB, num_blocks, P, Pmax;
+  int S, H, KH, G, MB, num_blocks, P, Pmax, Cmax;
   int hg_per_kv;  // ceil(G / GT)
   int n_hg;       // KH * hg_per_kv
   long long timeout_ns;
@@ -76,110 +93,226 @@ struct Layout {
   static constexpr uint32_t OFF_INFO = al16(OFF_SCAN + THREADS * 4);
   static constexpr uint32_t OFF_BAR = al16(OFF_INFO + UQ * sizeof(UnitInfo));
   static constexpr uint32_t OFF_FLAGS = al16(OFF_BAR + (2 * NSTAGE + 2 * UQ) * 8);
-  static constexpr uint32_t OFF_PREF = al16(OFF_FLAGS + 16);
+  static constexpr uint32_t OFF_PREF = al16(OFF_FLAGS + 64);
   static constexpr uint32_t FIXED = OFF_PREF;
   static constexpr uint32_t bytes(int S) { return al16(OFF_PREF + (uint32_t)(S + 1) * 4); }
   static constexpr int OUTS = (C::GT * C::D + NCT - 1) / NCT;  // combine outputs per thread
 };
 
+template <class LY>
+__device__ __forceinline__ uint32_t stage_of(uint32_t g) {
+  return g % LY::NSTAGE;
+}
+template <class LY>
+__device__ __forceinline__ uint32_t phase_of(uint32_t g) {
+  return (g / LY::NSTAGE) & 1u;
+}
+
+// Wait (bounded) until the producer has issued at least `target` blocks.
+__device__ __forceinline__ bool wait_issued(const volatile uint32_t* issued, uint32_t target,
+                                            volatile int* abort_flag, int* err_word,
+                                            long long timeout_ns) {
+  if (*issued >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (*issued >= target) return true;
+    if (*abort_flag) return false;
+    if ((long long)(global_timer_ns() - t0) > timeout_ns) {
+      *abort_flag = 1;
+      atomicCAS(err_word, 0, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// A work unit as the producer sees it.
+struct UnitPlan {
+  int s, p, hg, t0, t1, nb, np, nh, h0, kv;
+};
+
+template <class C>
+__device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pref, int u) {
+  constexpr int BS = C::BS, GT = C::GT;
+  UnitPlan U;
+  const int pair = u / prm.n_hg;
+  U.hg = u - pair * prm.n_hg;
+  int lo = 0, hi = prm.S;  // pref[lo] <= pair < pref[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] <= pair) lo = mid; else hi = mid;
+  }
+  U.s = lo;
+  U.p = pair - pref[lo];
+  U.np = pref[lo + 1] - pref[lo];
+  const int L = min(max(prm.lens[lo], 0), prm.MB * BS);
+  U.t0 = U.p * prm.P;
+  U.t1 = min(U.t0 + prm.P, L);
+  U.nb = (U.t1 - U.t0 + BS - 1) / BS;
+  U.kv = U.hg / prm.hg_per_kv;
+  const int hgk = U.hg - U.kv * prm.hg_per_kv;
+  U.h0 = U.kv * prm.G + hgk * GT;
+  U.nh = min(GT, prm.G - hgk * GT);
+  return U;
+}
+
+// This lane's block-table entry among blocks [c0, c0 + 32) of unit U (0 past
+// the unit's end).  An id outside the pool is recorded and replaced by 0, so
+// nothing is read out of bounds.
+template <class C>
+__device__ __forceinline__ int load_block_id(const KParams& prm, const UnitPlan& U, int c0, int lane) {
+  int b = 0;
+  if (c0 + lane < U.nb) {
+    b = __ldg(prm.bt + (size_t)U.s * prm.MB + U.t0 / C::BS + c0 + lane);
+    if ((unsigned)b >= (unsigned)prm.num_blocks) {
+      atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
+      b = 0;
+    }
+  }
+  return b;
+}
+
 template <class C, class LY>
 __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem, const int* pref,
-                                              UnitInfo* info, volatile int* abort_flag, int lane) {
+                                              UnitInfo* info, volatile int* abort_flag,
+                                              volatile uint32_t* issued, int lane) {
   using T = typename C::T;
-  constexpr int D = C::D, BS = C::BS, GT = C::GT, NS = LY::NSTAGE, UQ = LY::UQ;
+  constexpr int D = C::D, NS = LY::NSTAGE, UQ = LY::UQ;
+  // Blocks issued together, one per lane, as their stages free up.
+  constexpr int BATCH = NS < 8 ? NS : 8;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bar_full = sbase + LY::OFF_BAR, bar_empty = bar_full + NS * 8;
   const uint32_t bar_ufull = bar_empty + NS * 8, bar_uempty = bar_ufull + UQ * 8;
   int* err = prm.hdr + kHdrError;
   const uint64_t pol_stream = l2_policy_evict_first();
   const uint64_t pol_keep = l2_policy_evict_last();
-  const int S = prm.S;
-  const int total = pref[S] * prm.n_hg;
-  const int max_len = prm.MB * BS;
+  const int total = pref[prm.S] * prm.n_hg;
 
-  uint32_t g = 0;   // K/V blocks issued by this CTA
-  uint32_t kq = 0;  // units published
-  int u = 0;
-  if (lane == 0) u = atomicAdd(prm.hdr + kHdrWork, 1);
-  u = __shfl_sync(0xffffffffu, u, 0);
+  uint32_t g = 0;   // blocks whose copies are issued, in order
+  uint32_t kq = 0;  // units published (the end marker included)
   bool ok = true;
-  while (true) {
+  uint32_t batch_hi = 0;  // on abort: upper bound of blocks that may be in flight
+
+  // Publish unit U (or, if !have, the end marker) into the next queue slot:
+  // its description, and a bulk copy of its query rows.
+  auto publish = [&](const UnitPlan& Up, bool have) -> bool {
     const int slot = kq % UQ;
     const uint32_t par = (kq / UQ) & 1u;
-    if (lane == 0) ok = wait_bounded(bar_uempty + 8 * slot, par ^ 1u, abort_flag, err, prm.timeout_ns);
-    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-    if (!ok) break;
-    if (u >= total) {
-      if (lane == 0) {
+    bool okp = true;
+    if (lane == 0) {
+      okp = wait_bounded(bar_uempty + 8 * slot, par ^ 1u, abort_flag, err, prm.timeout_ns);
+      if (okp && !have) {
         info[slot].s = -1;
         mbar_arrive(bar_ufull + 8 * slot);
+      } else if (okp) {
+        UnitInfo& I = info[slot];
+        I.s = Up.s; I.p = Up.p; I.hg = Up.hg; I.t0 = Up.t0; I.t1 = Up.t1; I.nb = Up.nb;
+        I.np = Up.np; I.nh = Up.nh; I.h0 = Up.h0;
+        const uint32_t qbytes = (uint32_t)(Up.nh * D * 2);
+        mbar_arrive_expect_tx(bar_ufull + 8 * slot, qbytes);
+        bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT,
+                      static_cast<const T*>(prm.q) + ((size_t)Up.s * prm.H + Up.h0) * D, qbytes,
+                      bar_ufull + 8 * slot, pol_keep);
       }
-      break;
-    }
-    const int pair = u / prm.n_hg, hg = u - pair * prm.n_hg;
-    int lo = 0, hi = S;  // pref[lo] <= pair < pref[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (pref[mid] <= pair) lo = mid; else hi = mid;
-    }
-    const int s = lo, p = pair - pref[s], np = pref[s + 1] - pref[s];
-    const int L = min(max(prm.lens[s], 0), max_len);
-    const int t0 = p * prm.P, t1 = min(t0 + prm.P, L);
-    const int nb = (t1 - t0 + BS - 1) / BS;
-    const int kv = hg / prm.hg_per_kv, hgk = hg - kv * prm.hg_per_kv;
-    const int h0 = kv * prm.G + hgk * GT;
-    const int nh = min(GT, prm.G - hgk * GT);
-    int u_next = 0;
-    if (lane == 0) {
-      u_next = atomicAdd(prm.hdr + kHdrWork, 1);
-      UnitInfo& I = info[slot];
-      I.s = s; I.p = p; I.hg = hg; I.t0 = t0; I.t1 = t1; I.nb = nb; I.np = np; I.nh = nh; I.h0 = h0;
-      const uint32_t qbytes = (uint32_t)(nh * D * 2);
-      mbar_arrive_expect_tx(bar_ufull + 8 * slot, qbytes);
-      bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT,
-                    static_cast<const T*>(prm.q) + ((size_t)s * prm.H + h0) * D, qbytes,
-                    bar_ufull + 8 * slot, pol_keep);
     }
     ++kq;
-    const int32_t* btrow = prm.bt + (size_t)s * prm.MB + t0 / BS;
-    for (int jb = 0; jb < nb && ok; jb += 32) {
-      const int cnt = min(32, nb - jb);
-      int b = 0;
-      if (lane < cnt) {
-        b = __ldg(btrow + jb + lane);
-        if ((unsigned)b >= (unsigned)prm.num_blocks) {
-          atomicCAS(err, 0, kErrDeviceBounds);
-          b = 0;  // keep the pipeline going on a valid block; the result is flagged
-        }
-      }
-      for (int i = 0; i < cnt; ++i) {
-        const int bi = __shfl_sync(0xffffffffu, b, i);
-        if (lane == 0) {
-          const uint32_t st = g % NS, ph = (g / NS) & 1u;
-          ok = wait_bounded(bar_empty + 8 * st, ph ^ 1u, abort_flag, err, prm.timeout_ns);
-          if (ok) {
+    return __shfl_sync(0xffffffffu, (int)okp, 0) != 0;
+  };
+
+  // The work counter is read two units ahead: while unit k streams, unit k+1
+  // is already planned and published and the index of unit k+2 is in flight,
+  // so neither the atomic nor the block-table loads stall the stream.
+  int u_cur = 0, u_req = 0;
+  if (lane == 0) {
+    u_cur = atomicAdd(prm.hdr + kHdrWork, 1);
+    u_req = atomicAdd(prm.hdr + kHdrWork, 1);
+  }
+  u_cur = __shfl_sync(0xffffffffu, u_cur, 0);
+  bool have = u_cur < total;
+  UnitPlan U{};
+  int bids = 0;  // this lane's block id among the unit's first 32 blocks
+  if (have) {
+    U = plan_unit<C>(prm, pref, u_cur);
+    bids = load_block_id<C>(prm, U, 0, lane);
+  }
+  ok = publish(U, have);
+  while (have && ok) {
+    const int u_nx = __shfl_sync(0xffffffffu, u_req, 0);
+    const bool have_next = u_nx < total;
+    UnitPlan Un{};
+    int bids_next = 0;
+    if (have_next) {
+      Un = plan_unit<C>(prm, pref, u_nx);
+      bids_next = load_block_id<C>(prm, Un, 0, lane);
+      if (lane == 0) u_req = atomicAdd(prm.hdr + kHdrWork, 1);
+    }
+    ok = publish(Un, have_next);
+    if (!ok) break;
+    for (int c0 = 0; c0 < U.nb && ok; c0 += 32) {
+      const int b32 = (c0 == 0) ? bids : load_block_id<C>(prm, U, c0, lane);
+      const int cend = min(c0 + 32, U.nb);
+      for (int jb = c0; jb < cend && ok; jb += BATCH) {
+        const int cnt = min(BATCH, cend - jb);
+        const int bi = __shfl_sync(0xffffffffu, b32, (jb - c0) + (lane < cnt ? lane : 0));
+        // Lanes < cnt issue block g + lane once its stage is free; the
+        // shared `issued` counter follows the prefix of issued blocks.
+        const uint32_t gi = g + lane, st = stage_of<LY>(gi), ph = phase_of<LY>(gi);
+        bool done = lane >= cnt;
+        bool timing = false;
+        uint64_t t_start = 0;
+        while (true) {
+          if (!done && mbar_test_wait(bar_empty + 8 * st, ph ^ 1u)) {
             const uint32_t dst = sbase + st * LY::STAGE;
-            const size_t off = ((size_t)bi * prm.KH + kv) * (size_t)(D * BS);
+            const size_t off = ((size_t)bi * prm.KH + U.kv) * (size_t)(D * C::BS);
             mbar_arrive_expect_tx(bar_full + 8 * st, LY::STAGE);
             bulk_copy_g2s(dst, static_cast<const T*>(prm.kc) + off, LY::KBYTES, bar_full + 8 * st, pol_stream);
             bulk_copy_g2s(dst + LY::KBYTES, static_cast<const T*>(prm.vc) + off, LY::KBYTES,
                           bar_full + 8 * st, pol_stream);
+            done = true;
+          }
+          const unsigned m = __ballot_sync(0xffffffffu, done);
+          const int prefix = (m == 0xffffffffu) ? 32 : (__ffs(~m) - 1);
+          if (lane == 0) *issued = g + (uint32_t)min(prefix, cnt);
+          if (m == 0xffffffffu) break;
+          int stop = 0;
+          if (lane == 0) {
+            if (*abort_flag) {
+              stop = 1;
+            } else {
+              const uint64_t now = global_timer_ns();
+              if (!timing) {
+                timing = true;
+                t_start = now;
+              } else if ((long long)(now - t_start) > prm.timeout_ns) {
+                *abort_flag = 1;
+                atomicCAS(err, 0, kErrTimeout);
+                stop = 1;
+              } else {
+                __nanosleep(32);
+              }
+            }
+          }
+          if (__shfl_sync(0xffffffffu, stop, 0)) {
+            ok = false;
+            batch_hi = g + cnt;
+            break;
           }
         }
-        ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
         if (!ok) break;
-        ++g;
+        g += cnt;
       }
     }
-    if (!ok) break;
-    u = __shfl_sync(0xffffffffu, u_next, 0);
+    U = Un;
+    bids = bids_next;
+    have = have_next;
   }
   if (!ok && lane == 0) {
     // Aborted: let copies that may still be in flight land before the CTA
-    // exits (bounded; the abort flag is ignored here).
-    const long long drain_ns = prm.timeout_ns;
-    for (uint32_t i = (g > (uint32_t)NS ? g - NS : 0u); i < g; ++i) {
-      const uint32_t bar = bar_full + 8 * (i % NS), ph = (i / NS) & 1u;
+    // exits.  Each wait is bounded (100 ms, independent of the caller's
+    // timeout, which may be tiny) and ignores the abort flag.
+    const uint32_t hi = batch_hi > g ? batch_hi : g;
+    const long long drain_ns = 100000000LL;
+    for (uint32_t i = (hi > (uint32_t)NS ? hi - NS : 0u); i < hi; ++i) {
+      const uint32_t bar = bar_full + 8 * stage_of<LY>(i), ph = phase_of<LY>(i);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(bar, ph) && (long long)(global_timer_ns() - t0) < drain_ns) {}
     }
@@ -191,13 +324,170 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   }
 }
 
+// Partitions per combine chunk (kept equal to kChunkParts of the launcher).
+constexpr int kChunk = 16;
+
+// A combine job: the partitions of one (sequence, head group) -- all of them
+// (kind 0, at most kChunk), or chunk c of them (kind 1), whose combined state
+// is then folded with the other chunks' by the last chunk to finish.
+struct RedInfo {
+  int s, hg, h0, nh, np, kind, c, cnt;
+};
+static_assert(sizeof(RedInfo) <= 48, "combine job must fit in the shared flag area");
+
+__device__ __forceinline__ int* ticket_of(const KParams& prm, const RedInfo& R) {
+  const size_t sg = (size_t)R.s * prm.n_hg + R.hg;
+  return R.kind == 0 ? prm.tickets + sg : prm.ctickets + sg * prm.Cmax + R.c;
+}
+
+// Thread 0: decide whether the pending ticket made this CTA the last writer of
+// its partition group; if so, reset the ticket for the next call, acquire the
+// other CTAs' partition states, and publish the combine job.
+__device__ __forceinline__ void settle_ticket(const KParams& prm, bool& pend, int pend_t,
+                                              const RedInfo& pinfo, volatile int* red_go, RedInfo* red) {
+  const bool last = pend && (pend_t == pinfo.cnt - 1);
+  if (last) {
+    *ticket_of(prm, pinfo) = 0;
+    fence_acq_rel_gpu();
+    *red = pinfo;
+  }
+  *red_go = last ? 1 : 0;
+  pend = false;
+}
+
+// Log-sum-exp combine of `count` states (m, l, o) of the heads of R, all
+// consumer threads: per head M = max m_i and total = sum e^(m_i - M) l_i (one
+// warp per head), then o = sum_i (e^(m_i - M) l_i / total) o_i with the
+// weights staged in shared memory in chunks of RCH (the page's Phase 2
+// formula).  State i of head h is m[(s*H + h)*stride + first + i] and
+// o[((s*H + h)*stride + first + i)*D + ...].  TO_OUT writes o, rounded, to
+// the output; otherwise (M, total, o) becomes chunk state `dst_c`.
+template <class C, class LY, bool TO_OUT>
+__device__ __forceinline__ void combine_states(const KParams& prm, const RedInfo& R, const float* sm,
+                                               const float* sl, const float* so, int stride, int first,
+                                               int count, int dst_c, float* rw, float* rstat, int ctid,
+                                               int warp, int lane) {
+  using T = typename C::T;
+  constexpr int D = C::D, GT = C::GT, NC = LY::NC, NCT = LY::NCT, RCH = LY::RCH;
+  constexpr int D4 = D / 4, OUT4 = (GT * D4 + NCT - 1) / NCT;
+  const int H = prm.H;
+  for (int gh = warp; gh < R.nh; gh += NC) {
+    const size_t base = ((size_t)R.s * H + R.h0 + gh) * stride + first;
+    float M = -INFINITY;
+    for (int i = lane; i < count; i += 32) M = fmaxf(M, __ldcg(sm + base + i));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float tot = 0.f;
+    for (int i = lane; i < count; i += 32)
+      tot = fmaf(exp2f((__ldcg(sm + base + i) - M) * kLog2e), __ldcg(sl + base + i), tot);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    if (lane == 0) {
+      rstat[gh * 2] = M;
+      rstat[gh * 2 + 1] = tot;
+    }
+  }
+  float4 acc[OUT4];
+#pragma unroll
+  for (int o = 0; o < OUT4; ++o) acc[o] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < count; c0 += RCH) {
+    const int cn = min(RCH, count - c0);
+    named_barrier_sync(1, NCT);
+    for (int i = ctid; i < R.nh * RCH; i += NCT) {
+      const int gh = i / RCH, pp = i - gh * RCH;
+      if (pp < cn) {
+        const size_t e = ((size_t)R.s * H + R.h0 + gh) * stride + first + c0 + pp;
+        rw[i] = exp2f((__ldcg(sm + e) - rstat[gh * 2]) * kLog2e) * __ldcg(sl + e) / rstat[gh * 2 + 1];
+      }
+    }
+    named_barrier_sync(1, NCT);
+#pragma unroll
+    for (int o = 0; o < OUT4; ++o) {
+      const int idx = ctid + o * NCT;
+      if (idx >= GT * D4) break;
+      const int gh = idx / D4, d4 = idx - gh * D4;
+      if (gh >= R.nh) continue;
+      const float4* src = reinterpret_cast<const float4*>(
+                              so + (((size_t)R.s * H + R.h0 + gh) * stride + first + c0) * D) + d4;
+      float4 a = acc[o], b = make_float4(0.f, 0.f, 0.f, 0.f);
+      int pp = 0;
+#pragma unroll 4
+      for (; pp + 1 < cn; pp += 2) {
+        const float w0 = rw[gh * RCH + pp], w1 = rw[gh * RCH + pp + 1];
+        const float4 v0 = __ldcg(src + (size_t)pp * D4), v1 = __ldcg(src + (size_t)(pp + 1) * D4);
+        a.x = fmaf(w0, v0.x, a.x); a.y = fmaf(w0, v0.y, a.y); a.z = fmaf(w0, v0.z, a.z); a.w = fmaf(w0, v0.w, a.w);
+        b.x = fmaf(w1, v1.x, b.x); b.y = fmaf(w1, v1.y, b.y); b.z = fmaf(w1, v1.z, b.z); b.w = fmaf(w1, v1.w, b.w);
+      }
+      if (pp < cn) {
+        const float w0 = rw[gh * RCH + pp];
+        const float4 v0 = __ldcg(src + (size_t)pp * D4);
+        a.x = fmaf(w0, v0.x, a.x); a.y = fmaf(w0, v0.y, a.y); a.z = fmaf(w0, v0.z, a.z); a.w = fmaf(w0, v0.w, a.w);
+      }
+      acc[o] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    }
+  }
+#pragma unroll
+  for (int o = 0; o < OUT4; ++o) {
+    const int idx = ctid + o * NCT;
+    if (idx >= GT * D4) break;
+    const int gh = idx / D4, d4 = idx - gh * D4;
+    if (gh >= R.nh) continue;
+    const size_t sh = (size_t)R.s * H + R.h0 + gh;
+    if constexpr (TO_OUT) {
+      uint2 v;
+      v.x = F16Traits<T>::pack(acc[o].x, acc[o].y);
+      v.y = F16Traits<T>::pack(acc[o].z, acc[o].w);
+      *reinterpret_cast<uint2*>(static_cast<T*>(prm.out) + sh * D + d4 * 4) = v;
+    } else {
+      reinterpret_cast<float4*>(prm.ws_co + (sh * prm.Cmax + dst_c) * D)[d4] = acc[o];
+      if (d4 == 0) {
+        prm.ws_cm[sh * prm.Cmax + dst_c] = rstat[gh * 2];
+        prm.ws_cl[sh * prm.Cmax + dst_c] = rstat[gh * 2 + 1];
+      }
+    }
+  }
+}
+
+// Run the combine job R (all consumer threads).  A chunk job writes the
+// chunk's state, then takes the sequence-level ticket; the last chunk folds
+// all chunk states into the output.
+template <class C, class LY>
+__device__ __forceinline__ void run_combine(const KParams& prm, const RedInfo R, float* rw, float* rstat,
+                                            volatile int* red2, int ctid, int warp, int lane) {
+  constexpr int NCT = LY::NCT;
+  if (R.kind == 0) {
+    combine_states<C, LY, true>(prm, R, prm.ws_m, prm.ws_l, prm.ws_o, prm.Pmax, 0, R.np, 0, rw, rstat,
+                                ctid, warp, lane);
+    return;
+  }
+  combine_states<C, LY, false>(prm, R, prm.ws_m, prm.ws_l, prm.ws_o, prm.Pmax, R.c * kChunk, R.cnt, R.c,
+                               rw, rstat, ctid, warp, lane);
+  const int nchunks = (R.np + kChunk - 1) / kChunk;
+  named_barrier_sync(1, NCT);
+  if (ctid == 0) {
+    int* tk = prm.tickets + (size_t)R.s * prm.n_hg + R.hg;
+    const int t = atomic_add_release_gpu(tk, 1);
+    const bool last = (t == nchunks - 1);
+    if (last) {
+      *tk = 0;
+      fence_acq_rel_gpu();
+    }
+    *red2 = last ? 1 : 0;
+  }
+  named_barrier_sync(1, NCT);
+  if (*red2)
+    combine_states<C, LY, true>(prm, R, prm.ws_cm, prm.ws_cl, prm.ws_co, prm.Cmax, 0, nchunks, 0, rw,
+                                rstat, ctid, warp, lane);
+}
+
 template <class C, class LY>
 __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem, const int* pref,
                                               const UnitInfo* info, volatile int* abort_flag,
-                                              int* last_flag, int warp, int lane) {
+                                              const volatile uint32_t* issued, volatile int* red_go,
+                                              volatile int* red2, RedInfo* red, int warp, int lane) {
   using T = typename C::T;
   constexpr int D = C::D, BS = C::BS, GT = C::GT, NC = LY::NC, NCT = LY::NCT, NS = LY::NSTAGE,
-                UQ = LY::UQ, RCH = LY::RCH, OUTS = LY::OUTS;
+                UQ = LY::UQ, OUTS = LY::OUTS;
   const int ctid = warp * 32 + lane;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bar_full = sbase + LY::OFF_BAR, bar_empty = bar_full + NS * 8;
@@ -231,13 +521,28 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
 
   C cons;
   uint32_t g = 0, k = 0;
+  // Thread 0 takes a ticket after each multi-partition unit and checks it at
+  // the next epilogue (or at exit), so the atomic's latency is off the
+  // critical path.  If it was the last partition of its (sequence, head
+  // group), the CTA then combines all of them.
+  bool pend = false;
+  int pend_t = 0;
+  RedInfo pinfo{};
   while (true) {
     const int slot = k % UQ;
     const uint32_t par = (k / UQ) & 1u;
     const bool okw = wait_bounded(bar_ufull + 8 * slot, par, abort_flag, err, prm.timeout_ns);
     const UnitInfo I = info[slot];
     const bool stop = named_barrier_or(1, NCT, !okw || I.s < 0 || *abort_flag != 0);
-    if (stop) break;
+    if (stop) {
+      const bool aborted = named_barrier_or(1, NCT, *abort_flag != 0);
+      if (!aborted) {
+        if (ctid == 0) settle_ticket(prm, pend, pend_t, pinfo, red_go, red);
+        named_barrier_sync(1, NCT);
+        if (*red_go) run_combine<C, LY>(prm, *red, rw, rstat, red2, ctid, warp, lane);
+      }
+      break;
+    }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
                     prm.scale_log2, lane);
     __syncwarp();
@@ -245,8 +550,9 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     ++k;
 
     for (int j = warp; j < I.nb; j += NC) {
-      const uint32_t gj = g + j, st = gj % NS, ph = (gj / NS) & 1u;
-      bool okb = wait_bounded(bar_full + 8 * st, ph, abort_flag, err, prm.timeout_ns);
+      const uint32_t gj = g + j, st = stage_of<LY>(gj), ph = phase_of<LY>(gj);
+      bool okb = wait_issued(issued, gj + 1, abort_flag, err, prm.timeout_ns) &&
+                 wait_bounded(bar_full + 8 * st, ph, abort_flag, err, prm.timeout_ns);
       okb = __all_sync(0xffffffffu, okb);
       const int ntok = min(BS, I.t1 - I.t0 - j * BS);
       if (okb) cons.block(smem + st * LY::STAGE, smem + st * LY::STAGE + LY::KBYTES, ntok, lane, scr);
@@ -258,6 +564,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     // Combine the NC warp states into the partition's (m_p, l_p, o_p).
     cons.finish(epi_acc + warp * GT * D, epi_ml + warp * GT * 2, lane);
     named_barrier_sync(1, NCT);
+    if (ctid == 0) settle_ticket(prm, pend, pend_t, pinfo, red_go, red);
     const bool single = (I.np == 1);
 #pragma unroll
     for (int o = 0; o < OUTS; ++o) {
@@ -288,89 +595,38 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
         prm.ws_l[sh * Pmax + I.p] = den;
       }
     }
-    if (!single) {
-      __threadfence();
-      named_barrier_sync(1, NCT);
-      if (ctid == 0) {
-        int* ticket = prm.tickets + (size_t)I.s * prm.n_hg + I.hg;
-        const int t = atomicAdd(ticket, 1);
-        const int last = (t == I.np - 1);
-        if (last) *ticket = 0;
-        *last_flag = last;
-      }
-      named_barrier_sync(1, NCT);
-      if (*last_flag) {
-        __threadfence();
-        // Phase 2 for this (sequence, head group): per head M and 1/total
-        // (warp per head), then the weighted sum of the o_p in chunks.
-        for (int gh = warp; gh < I.nh; gh += NC) {
-          const size_t base = ((size_t)I.s * H + I.h0 + gh) * Pmax;
-          float M = -INFINITY;
-          for (int p = lane; p < I.np; p += 32) M = fmaxf(M, __ldcg(prm.ws_m + base + p));
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-          float tot = 0.f;
-          for (int p = lane; p < I.np; p += 32)
-            tot = fmaf(exp2f((__ldcg(prm.ws_m + base + p) - M) * kLog2e), __ldcg(prm.ws_l + base + p), tot);
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-          if (lane == 0) {
-            rstat[gh * 2] = M;
-            rstat[gh * 2 + 1] = 1.f / tot;
-          }
+    // The barrier orders every consumer thread's partition stores before
+    // thread 0's release-add on the ticket (release is cumulative).
+    named_barrier_sync(1, NCT);
+    if (ctid == 0) {
+      pend = !single;
+      if (pend) {
+        pinfo.s = I.s; pinfo.hg = I.hg; pinfo.h0 = I.h0; pinfo.nh = I.nh; pinfo.np = I.np;
+        if (I.np <= kChunk) {
+          pinfo.kind = 0; pinfo.c = 0; pinfo.cnt = I.np;
+        } else {
+          pinfo.kind = 1; pinfo.c = I.p / kChunk; pinfo.cnt = min(kChunk, I.np - pinfo.c * kChunk);
         }
-        float racc[OUTS];
-#pragma unroll
-        for (int o = 0; o < OUTS; ++o) racc[o] = 0.f;
-        for (int c0 = 0; c0 < I.np; c0 += RCH) {
-          const int cn = min(RCH, I.np - c0);
-          named_barrier_sync(1, NCT);
-          for (int i = ctid; i < I.nh * RCH; i += NCT) {
-            const int gh = i / RCH, pp = i - gh * RCH;
-            if (pp < cn) {
-              const size_t e = ((size_t)I.s * H + I.h0 + gh) * Pmax + c0 + pp;
-              rw[i] = exp2f((__ldcg(prm.ws_m + e) - rstat[gh * 2]) * kLog2e) * __ldcg(prm.ws_l + e) *
-                      rstat[gh * 2 + 1];
-            }
-          }
-          named_barrier_sync(1, NCT);
-#pragma unroll
-          for (int o = 0; o < OUTS; ++o) {
-            const int idx = ctid + o * NCT;
-            if (idx >= GT * D) break;
-            const int gh = idx / D, d = idx - gh * D;
-            if (gh >= I.nh) continue;
-            const float* src = prm.ws_o + (((size_t)I.s * H + I.h0 + gh) * Pmax + c0) * D + d;
-            float a = racc[o];
-#pragma unroll 4
-            for (int pp = 0; pp < cn; ++pp) a = fmaf(rw[gh * RCH + pp], __ldcg(src + (size_t)pp * D), a);
-            racc[o] = a;
-          }
-        }
-#pragma unroll
-        for (int o = 0; o < OUTS; ++o) {
-          const int idx = ctid + o * NCT;
-          if (idx >= GT * D) break;
-          const int gh = idx / D, d = idx - gh * D;
-          if (gh >= I.nh) continue;
-          out[((size_t)I.s * H + I.h0 + gh) * D + d] = F16Traits<T>::from_float(racc[o]);
-        }
+        pend_t = atomic_add_release_gpu(ticket_of(prm, pinfo), 1);
       }
     }
-    named_barrier_sync(1, NCT);
+    if (*red_go) run_combine<C, LY>(prm, *red, rw, rstat, red2, ctid, warp, lane);
   }
 }
 
-template <class C, int NC, int NSTAGE>
-__global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, 1)
+template <class C, int NC, int NSTAGE, int CTAS_PER_SM>
+__global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     pa_decode_kernel(const __grid_constant__ KParams prm) {
   using LY = Layout<C, NC, NSTAGE>;
-  constexpr int NS = NSTAGE, UQ = LY::UQ;
+  constexpr int NS = LY::NSTAGE, UQ = LY::UQ;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS);
-  int* last_flag = reinterpret_cast<int*>(smem + LY::OFF_FLAGS + 4);
+  volatile int* red_go = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 4);
+  volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(smem + LY::OFF_FLAGS + 8);
+  volatile int* red2 = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 12);
+  RedInfo* red = reinterpret_cast<RedInfo*>(smem + LY::OFF_FLAGS + 16);
   int* pref = reinterpret_cast<int*>(smem + LY::OFF_PREF);
   int* scan = reinterpret_cast<int*>(smem + LY::OFF_SCAN);
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + LY::OFF_INFO);
@@ -386,6 +642,8 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, 1)
       mbar_init(bar + 8 * (2 * NS + UQ + i), NC);  // unit empty: every consumer warp
     }
     *abort_flag = 0;
+    *issued = 0;
+    *red_go = 0;
     fence_mbarrier_init();
   }
   // pref[s] = number of used partitions before sequence s (lengths clamped to
@@ -423,9 +681,9 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, 1)
   }
   __syncthreads();
   if (warp == NC) {
-    producer_loop<C, LY>(prm, smem, pref, info, abort_flag, lane);
+    producer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, lane);
   } else {
-    consumer_loop<C, LY>(prm, smem, pref, info, abort_flag, last_flag, warp, lane);
+    consumer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, red_go, red2, red, warp, lane);
   }
 }
 

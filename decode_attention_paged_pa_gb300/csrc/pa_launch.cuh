@@ -5,7 +5,18 @@
 
 namespace pa {
 
-constexpr uint32_t kSmemBudget = 227u * 1024u;
+// Consumer warps per CTA and CTAs per SM.
+#ifndef PA_CONSUMER_WARPS
+#define PA_CONSUMER_WARPS 8
+#endif
+#ifndef PA_CTAS_PER_SM
+#define PA_CTAS_PER_SM 1
+#endif
+constexpr int kConsumerWarps = PA_CONSUMER_WARPS;
+constexpr int kCtasPerSm = PA_CTAS_PER_SM;
+
+// Shared memory per CTA: the SM's 228 KB less 1 KB reserved per CTA.
+constexpr uint32_t kSmemBudget = (kCtasPerSm == 1) ? 227u * 1024u : (228u * 1024u / kCtasPerSm - 1024u);
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
@@ -17,7 +28,8 @@ struct Sizing {
   using L1 = Layout<C, NC, 1>;
   static constexpr uint32_t other = L1::FIXED - L1::RING + 64 * 8 + 16;
   static constexpr uint32_t pref_max = al16((kMaxSeqsPerLaunch + 1) * 4);
-  static constexpr int NS = cmax(2, cmin(32, (int)((kSmemBudget - other - pref_max) / L1::STAGE)));
+  static constexpr int NS = cmin(32, (int)((kSmemBudget - other - pref_max) / L1::STAGE));
+  static_assert(NS >= 2, "shared memory holds fewer than two ring stages");
   using LY = Layout<C, NC, NS>;
   static_assert(LY::bytes(kMaxSeqsPerLaunch) <= kSmemBudget, "shared memory over budget");
 };
@@ -26,11 +38,11 @@ template <class C, int NC>
 cudaError_t launch_one(const KParams& prm, int max_ctas, cudaStream_t stream) {
   using SZ = Sizing<C, NC>;
   using LY = typename SZ::LY;
-  auto kern = pa_decode_kernel<C, NC, SZ::NS>;
+  auto kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)LY::bytes(kMaxSeqsPerLaunch));
   if (e != cudaSuccess) return e;
-  int grid = device_sm_count();
+  int grid = device_sm_count() * kCtasPerSm;
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (grid < 1) grid = 1;
   kern<<<grid, LY::THREADS, LY::bytes(prm.S), stream>>>(prm);

@@ -12,14 +12,18 @@ namespace pa {
 // sequence in shared memory; longer batches are split into several launches.
 constexpr int kMaxSeqsPerLaunch = 2048;
 
-// Heads per group tile of each kernel family.
-constexpr int kSimtMaxGroup = 2;
+// Partitions per combine chunk: sequences with more partitions are combined
+// in two levels (chunks of partitions, then the chunk states).
+constexpr int kChunkParts = 16;
+static_assert(kChunkParts == kChunk, "launcher and kernel must agree on the chunk size");
+
+// Query heads per work unit of each kernel family.
+constexpr int kSimtGroup = 1;
 constexpr int kMmaGroup = 8;
 
-// Launch the persistent kernel for one chunk of sequences.  `gt` is the SIMT
-// group tile (1 or 2); ignored by the MMA family.  Returns a cudaError_t.
-cudaError_t launch_simt_f16(const KParams& prm, int D, int BS, int gt, int max_ctas, cudaStream_t st);
-cudaError_t launch_simt_bf16(const KParams& prm, int D, int BS, int gt, int max_ctas, cudaStream_t st);
+// Launch the persistent kernel for one chunk of sequences.  Returns a cudaError_t.
+cudaError_t launch_simt_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_simt_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 

@@ -65,14 +65,18 @@ struct MmaConsumer {
     float sc[NTT][4];
 #pragma unroll
     for (int tt = 0; tt < NTT; ++tt) {
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      // Two accumulators (even / odd k-steps) halve the dependent mma chain.
+      float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
         uint32_t a[4];
         const int tok = tt * 16 + (lane & 15), chunk = 2 * kk + (lane >> 4);
         ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
-        Mma<T>::run(c, a, qb[kk][0], qb[kk][1]);
+        if (kk & 1) Mma<T>::run(c2, a, qb[kk][0], qb[kk][1]);
+        else Mma<T>::run(c, a, qb[kk][0], qb[kk][1]);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] += c2[i];
       const int t_lo = tt * 16 + r, t_hi = t_lo + 8;
       sc[tt][0] = t_lo < ntok ? c[0] * scale_log2 : -INFINITY;
       sc[tt][1] = t_lo < ntok ? c[1] * scale_log2 : -INFINITY;

@@ -72,8 +72,8 @@ struct SimtConsumer {
 #pragma unroll
     for (int ps = 0; ps < NPASS; ++ps) {
       const int t = ps * TPP + tl;
-#pragma unroll
-      for (int g = 0; g < GT; ++g) sc[ps][g] = 0.f;
+      // One partial sum per 16-byte chunk keeps the FMA chains short.
+      float part[QCH][GT];
 #pragma unroll
       for (int i = 0; i < QCH; ++i) {
         const int c = slice * QCH + i;
@@ -81,12 +81,20 @@ struct SimtConsumer {
         float f[8];
         unpack8<T>(raw, f);
 #pragma unroll
-        for (int g = 0; g < GT; ++g)
+        for (int g = 0; g < GT; ++g) {
+          float a = qf[g][i * 8] * f[0];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sc[ps][g] = fmaf(qf[g][i * 8 + e], f[e], sc[ps][g]);
+          for (int e = 1; e < 8; ++e) a = fmaf(qf[g][i * 8 + e], f[e], a);
+          part[i][g] = a;
+        }
       }
 #pragma unroll
       for (int g = 0; g < GT; ++g) {
+#pragma unroll
+        for (int w = QCH / 2; w >= 1; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) part[i][g] += part[i + w][g];
+        sc[ps][g] = part[0][g];
 #pragma unroll
         for (int off = TPP; off < 32; off <<= 1) sc[ps][g] += __shfl_xor_sync(0xffffffffu, sc[ps][g], off);
         if (t >= ntok) sc[ps][g] = -INFINITY;

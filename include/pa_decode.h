@@ -64,18 +64,20 @@ enum {
 
 /* Kernel families (pa_decode_v2_ex's `variant`). */
 enum {
-    PA_VARIANT_AUTO = 0,      /* SIMT for groups of 1-2 query heads per kv head, MMA otherwise */
+    PA_VARIANT_AUTO = 0,      /* SIMT when each kv head serves one query head (MHA), MMA otherwise */
     PA_VARIANT_SIMT = 1,      /* CUDA-core dot products and warp-shuffle reductions */
     PA_VARIANT_MMA = 2        /* mma.sync m16n8k16 over the [group x D] . [D x tokens] contraction */
 };
 
 /*
  * Bytes of device workspace pa_decode_v2 needs for these sizes: a small
- * header (error word, work counter), one completion ticket per (sequence,
- * head group), and the phase-1 partition states of the page's launcher:
- * max_logits [S, H, Pmax] f32, exp_sums [S, H, Pmax] f32 and
- * tmp_output [S, H, Pmax, head_size] f32, with
- * Pmax = ceil(max_blocks_per_seq * block_size / partition_size).
+ * header (error word, work counter), completion tickets per (sequence, head
+ * group) and per chunk of 16 partitions, the phase-1 partition states of the
+ * page's launcher -- max_logits [S, H, Pmax] f32, exp_sums [S, H, Pmax] f32
+ * and tmp_output [S, H, Pmax, head_size] f32, with
+ * Pmax = ceil(max_blocks_per_seq * block_size / partition_size) -- and the
+ * same three arrays for the combined state of each chunk of 16 partitions
+ * (used by sequences with more than 16 partitions).
  * Returns 0 for invalid sizes.
  */
 size_t pa_decode_v2_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_size,
@@ -122,9 +124,9 @@ int pa_decode_v2(void* out, const void* query, const void* key_cache, const void
 
 /*
  * pa_decode_v2 with tuning controls, for tests and measurement.
- *   variant     PA_VARIANT_*; SIMT handles up to 2 query heads per kv head in
- *               one pass (larger groups take ceil(G/2) passes), MMA any group
- *               (8 query heads per pass).
+ *   variant     PA_VARIANT_*; SIMT takes one query head per pass over the
+ *               kv head's blocks (a group of G query heads takes G passes),
+ *               MMA up to 8 query heads per pass.
  *   max_ctas    upper bound on the persistent grid (0 = one CTA per SM).
  *   timeout_ns  bound on every device-side wait (0 = 2^31 ns).
  * Results do not depend on variant-independent choices: for a fixed variant

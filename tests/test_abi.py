@@ -41,12 +41,17 @@ def _align(x):
 ])
 def test_workspace_bytes_and_layout(S, H, KH, D, MB, BS, P):
     pmax = -(-(MB * BS) // P)
+    cmax = -(-pmax // 16)
     hdr = 256
     tickets = hdr
-    m = _align(tickets + S * H * 4)
+    ctickets = _align(tickets + S * H * 4)
+    m = _align(ctickets + S * H * cmax * 4)
     l = _align(m + S * H * pmax * 4)
     o = _align(l + S * H * pmax * 4)
-    total = _align(o + S * H * pmax * D * 4)
+    cm = _align(o + S * H * pmax * D * 4)
+    cl = _align(cm + S * H * cmax * 4)
+    co = _align(cl + S * H * cmax * 4)
+    total = _align(co + S * H * cmax * D * 4)
     assert binding.workspace_bytes(S, H, KH, D, MB, BS, P) == total
     offs, pm = binding.workspace_layout(S, H, KH, D, MB, BS, P)
     assert offs == (m, l, o, 0, total) and pm == pmax

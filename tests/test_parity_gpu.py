@@ -136,6 +136,23 @@ def test_deterministic_across_runs_and_grid_sizes(variant):
         assert torch.equal(out, base), f"max_ctas={ctas}"
 
 
+@pytest.mark.parametrize("variant,KH,G,BS", [(SIMT, 16, 1, 16), (MMA, 16, 1, 16), (MMA, 8, 4, 32),
+                                              (SIMT, 8, 1, 32)])
+def test_repeatable_under_load(variant, KH, G, BS):
+    """A busy batch (head_size 256, short and long sequences, many units per
+    CTA) run 8 times: every output bit must repeat.  Consumer warps run at
+    different speeds; a pipeline race would show up as run-to-run noise."""
+    rng = np.random.default_rng(16)
+    lens = rng.integers(1, 2049, 48).tolist()
+    q, kc, vc, bt, L = random_case(16, S=48, H=KH * G, KH=KH, D=256, BS=BS, lens=lens)
+    base, _ = run_gpu(q, kc, vc, bt, L, 1.0 / 16, 512, variant)
+    ref = oracle.decode(q, kc, vc, bt, L, 1.0 / 16, oracle.DTYPE_FP16)
+    assert within_tolerance(base.double().numpy(), ref)[0]
+    for _ in range(7):
+        out, _ = run_gpu(q, kc, vc, bt, L, 1.0 / 16, 512, variant)
+        assert torch.equal(out, base)
+
+
 @pytest.mark.parametrize("variant", [SIMT, MMA])
 def test_partition_bookkeeping(variant):
     """Workspace after a call: exactly NP_s partitions per (s, h) hold finite
@@ -223,18 +240,21 @@ def test_more_than_1024_partitions():
     check_parity(q, kc, vc, bt, lens, 0.125, 512, what="1172 partitions")
 
 
+@pytest.mark.parametrize("variant", [binding.PA_VARIANT_AUTO, SIMT, MMA], ids=["auto", "simt", "mma"])
 @pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER)
-def test_workload_sampled_parity(name):
-    """Full-size batch, launched as the bench launches it; the outputs of a
-    sample of sequences (shortest, longest and a few random) are checked
-    against the oracle on exactly those sequences."""
+def test_workload_sampled_parity(name, variant):
+    """Full-size batch; AUTO is the launch the bench times, SIMT and MMA force
+    each kernel family.  The outputs of a sample of sequences (shortest,
+    longest and a few random) are checked against the oracle on exactly those
+    sequences, and the whole output is checked to be finite."""
     w = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(w, device="cuda")
-    out = torch.empty_like(inp["query"])
+    out = torch.full_like(inp["query"], float("nan"))
     ws = binding.pa_decode_v2(out, inp["query"], inp["key_cache"], inp["value_cache"],
                               inp["block_tables"], inp["seq_lens"], inp["scale"],
-                              partition_size=w.partition_size)
+                              partition_size=w.partition_size, variant=variant)
     assert binding.device_status(ws) == binding.PA_OK
+    assert torch.isfinite(out.float()).all()
     lens = inp["seq_lens"].cpu()
     rng = np.random.default_rng(w.seed)
     pick = {int(torch.argmin(lens)), int(torch.argmax(lens)),
