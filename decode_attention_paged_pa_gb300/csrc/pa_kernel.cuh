@@ -77,7 +77,7 @@ template <class C, int NC_, int NSTAGE_>
 struct Layout {
   static constexpr int NC = NC_, NSTAGE = NSTAGE_, UQ = 2;
   static constexpr int NCT = NC * 32;          // consumer threads
-  static constexpr int THREADS = NCT + 32;     // + producer warp
+  static constexpr int THREADS = NCT + 64;     // + producer warp + epilogue warp
   static constexpr int RCH = 64;               // partitions per combine chunk
   static constexpr uint32_t KBYTES = C::D * C::BS * 2;
   static constexpr uint32_t STAGE = 2 * KBYTES;
@@ -89,10 +89,13 @@ struct Layout {
   static constexpr uint32_t OFF_SCR = al16(OFF_EPI_ML + NC * C::GT * 2 * 4);
   static constexpr uint32_t OFF_RED = al16(OFF_SCR + NC * C::SCRATCH_FLOATS * 4);
   static constexpr uint32_t OFF_RSTAT = al16(OFF_RED + C::GT * RCH * 4);
-  static constexpr uint32_t OFF_SCAN = al16(OFF_RSTAT + C::GT * 2 * 4);
+  static constexpr uint32_t OFF_EF = al16(OFF_RSTAT + C::GT * 2 * 4);   // NC*GT warp weights + GT sums
+  static constexpr uint32_t OFF_SCAN = al16(OFF_EF + (NC + 1) * C::GT * 4);
   static constexpr uint32_t OFF_INFO = al16(OFF_SCAN + THREADS * 4);
-  static constexpr uint32_t OFF_BAR = al16(OFF_INFO + UQ * sizeof(UnitInfo));
-  static constexpr uint32_t OFF_FLAGS = al16(OFF_BAR + (2 * NSTAGE + 2 * UQ) * 8);
+  static constexpr uint32_t OFF_EPI_INFO = al16(OFF_INFO + UQ * sizeof(UnitInfo));
+  static constexpr uint32_t OFF_BAR = al16(OFF_EPI_INFO + sizeof(UnitInfo));
+  static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 2;
+  static constexpr uint32_t OFF_FLAGS = al16(OFF_BAR + NBAR * 8);
   static constexpr uint32_t OFF_PREF = al16(OFF_FLAGS + 64);
   static constexpr uint32_t FIXED = OFF_PREF;
   static constexpr uint32_t bytes(int S) { return al16(OFF_PREF + (uint32_t)(S + 1) * 4); }
@@ -190,7 +193,6 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   uint32_t g = 0;   // blocks whose copies are issued, in order
   uint32_t kq = 0;  // units published (the end marker included)
   bool ok = true;
-  uint32_t batch_hi = 0;  // on abort: upper bound of blocks that may be in flight
 
   // Publish unit U (or, if !have, the end marker) into the next queue slot:
   // its description, and a bulk copy of its query rows.
@@ -214,8 +216,9 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
                       bar_ufull + 8 * slot, pol_keep);
       }
     }
-    ++kq;
-    return __shfl_sync(0xffffffffu, (int)okp, 0) != 0;
+    okp = __shfl_sync(0xffffffffu, (int)okp, 0) != 0;
+    if (okp) ++kq;
+    return okp;
   };
 
   // The work counter is read two units ahead: while unit k streams, unit k+1
@@ -292,8 +295,14 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
             }
           }
           if (__shfl_sync(0xffffffffu, stop, 0)) {
+            // Aborted: let this batch's issued copies land before leaving.
             ok = false;
-            batch_hi = g + cnt;
+            if (done && lane < cnt) {
+              const uint64_t t0 = global_timer_ns();
+              while (!mbar_try_wait(bar_full + 8 * st, ph) && (long long)(global_timer_ns() - t0) < 100000000LL) {
+              }
+            }
+            __syncwarp();
             break;
           }
         }
@@ -306,10 +315,11 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     have = have_next;
   }
   if (!ok && lane == 0) {
-    // Aborted: let copies that may still be in flight land before the CTA
-    // exits.  Each wait is bounded (100 ms, independent of the caller's
-    // timeout, which may be tiny) and ignores the abort flag.
-    const uint32_t hi = batch_hi > g ? batch_hi : g;
+    // Aborted: let copies that may still be in flight (the last NSTAGE
+    // blocks and the last UQ query rows issued) land before the CTA exits.
+    // Each wait is bounded (100 ms, independent of the caller's timeout,
+    // which may be tiny) and ignores the abort flag.
+    const uint32_t hi = g;
     const long long drain_ns = 100000000LL;
     for (uint32_t i = (hi > (uint32_t)NS ? hi - NS : 0u); i < hi; ++i) {
       const uint32_t bar = bar_full + 8 * stage_of<LY>(i), ph = phase_of<LY>(i);
@@ -333,45 +343,42 @@ constexpr int kChunk = 16;
 struct RedInfo {
   int s, hg, h0, nh, np, kind, c, cnt;
 };
-static_assert(sizeof(RedInfo) <= 48, "combine job must fit in the shared flag area");
+
+// Lane 0's job, for every lane of the warp.
+__device__ __forceinline__ RedInfo broadcast_job(const RedInfo& J) {
+  RedInfo R;
+  R.s = __shfl_sync(0xffffffffu, J.s, 0);
+  R.hg = __shfl_sync(0xffffffffu, J.hg, 0);
+  R.h0 = __shfl_sync(0xffffffffu, J.h0, 0);
+  R.nh = __shfl_sync(0xffffffffu, J.nh, 0);
+  R.np = __shfl_sync(0xffffffffu, J.np, 0);
+  R.kind = __shfl_sync(0xffffffffu, J.kind, 0);
+  R.c = __shfl_sync(0xffffffffu, J.c, 0);
+  R.cnt = __shfl_sync(0xffffffffu, J.cnt, 0);
+  return R;
+}
 
 __device__ __forceinline__ int* ticket_of(const KParams& prm, const RedInfo& R) {
   const size_t sg = (size_t)R.s * prm.n_hg + R.hg;
   return R.kind == 0 ? prm.tickets + sg : prm.ctickets + sg * prm.Cmax + R.c;
 }
 
-// Thread 0: decide whether the pending ticket made this CTA the last writer of
-// its partition group; if so, reset the ticket for the next call, acquire the
-// other CTAs' partition states, and publish the combine job.
-__device__ __forceinline__ void settle_ticket(const KParams& prm, bool& pend, int pend_t,
-                                              const RedInfo& pinfo, volatile int* red_go, RedInfo* red) {
-  const bool last = pend && (pend_t == pinfo.cnt - 1);
-  if (last) {
-    *ticket_of(prm, pinfo) = 0;
-    fence_acq_rel_gpu();
-    *red = pinfo;
-  }
-  *red_go = last ? 1 : 0;
-  pend = false;
-}
-
-// Log-sum-exp combine of `count` states (m, l, o) of the heads of R, all
-// consumer threads: per head M = max m_i and total = sum e^(m_i - M) l_i (one
-// warp per head), then o = sum_i (e^(m_i - M) l_i / total) o_i with the
-// weights staged in shared memory in chunks of RCH (the page's Phase 2
-// formula).  State i of head h is m[(s*H + h)*stride + first + i] and
-// o[((s*H + h)*stride + first + i)*D + ...].  TO_OUT writes o, rounded, to
-// the output; otherwise (M, total, o) becomes chunk state `dst_c`.
+// Log-sum-exp combine of `count` states (m, l, o) of the heads of R, by one
+// warp: per head M = max m_i and total = sum e^(m_i - M) l_i, then
+// o = sum_i (e^(m_i - M) l_i / total) o_i with the weights staged in shared
+// memory in chunks of RCH (the page's Phase 2 formula).  State i of head h is
+// m[(s*H + h)*stride + first + i] and o[((s*H + h)*stride + first + i)*D + ..].
+// TO_OUT writes o, rounded, to the output; otherwise (M, total, o) becomes
+// chunk state `dst_c`.
 template <class C, class LY, bool TO_OUT>
 __device__ __forceinline__ void combine_states(const KParams& prm, const RedInfo& R, const float* sm,
                                                const float* sl, const float* so, int stride, int first,
-                                               int count, int dst_c, float* rw, float* rstat, int ctid,
-                                               int warp, int lane) {
+                                               int count, int dst_c, float* rw, float* rstat, int lane) {
   using T = typename C::T;
-  constexpr int D = C::D, GT = C::GT, NC = LY::NC, NCT = LY::NCT, RCH = LY::RCH;
-  constexpr int D4 = D / 4, OUT4 = (GT * D4 + NCT - 1) / NCT;
+  constexpr int D = C::D, GT = C::GT, RCH = LY::RCH;
+  constexpr int D4 = D / 4, OUT4 = (GT * D4 + 31) / 32;
   const int H = prm.H;
-  for (int gh = warp; gh < R.nh; gh += NC) {
+  for (int gh = 0; gh < R.nh; ++gh) {
     const size_t base = ((size_t)R.s * H + R.h0 + gh) * stride + first;
     float M = -INFINITY;
     for (int i = lane; i < count; i += 32) M = fmaxf(M, __ldcg(sm + base + i));
@@ -392,18 +399,18 @@ __device__ __forceinline__ void combine_states(const KParams& prm, const RedInfo
   for (int o = 0; o < OUT4; ++o) acc[o] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c0 = 0; c0 < count; c0 += RCH) {
     const int cn = min(RCH, count - c0);
-    named_barrier_sync(1, NCT);
-    for (int i = ctid; i < R.nh * RCH; i += NCT) {
+    __syncwarp();
+    for (int i = lane; i < R.nh * RCH; i += 32) {
       const int gh = i / RCH, pp = i - gh * RCH;
       if (pp < cn) {
         const size_t e = ((size_t)R.s * H + R.h0 + gh) * stride + first + c0 + pp;
         rw[i] = exp2f((__ldcg(sm + e) - rstat[gh * 2]) * kLog2e) * __ldcg(sl + e) / rstat[gh * 2 + 1];
       }
     }
-    named_barrier_sync(1, NCT);
+    __syncwarp();
 #pragma unroll
     for (int o = 0; o < OUT4; ++o) {
-      const int idx = ctid + o * NCT;
+      const int idx = lane + o * 32;
       if (idx >= GT * D4) break;
       const int gh = idx / D4, d4 = idx - gh * D4;
       if (gh >= R.nh) continue;
@@ -428,7 +435,7 @@ __device__ __forceinline__ void combine_states(const KParams& prm, const RedInfo
   }
 #pragma unroll
   for (int o = 0; o < OUT4; ++o) {
-    const int idx = ctid + o * NCT;
+    const int idx = lane + o * 32;
     if (idx >= GT * D4) break;
     const int gh = idx / D4, d4 = idx - gh * D4;
     if (gh >= R.nh) continue;
@@ -446,57 +453,58 @@ __device__ __forceinline__ void combine_states(const KParams& prm, const RedInfo
       }
     }
   }
+  __syncwarp();
 }
 
-// Run the combine job R (all consumer threads).  A chunk job writes the
-// chunk's state, then takes the sequence-level ticket; the last chunk folds
-// all chunk states into the output.
+// Run the combine job R (one warp).  A chunk job writes the chunk's state,
+// then takes the sequence-level ticket; the last chunk folds all chunk states
+// into the output.
 template <class C, class LY>
-__device__ __forceinline__ void run_combine(const KParams& prm, const RedInfo R, float* rw, float* rstat,
-                                            volatile int* red2, int ctid, int warp, int lane) {
-  constexpr int NCT = LY::NCT;
+__device__ __forceinline__ void run_combine(const KParams& prm, const RedInfo& R, float* rw, float* rstat,
+                                            int lane) {
   if (R.kind == 0) {
-    combine_states<C, LY, true>(prm, R, prm.ws_m, prm.ws_l, prm.ws_o, prm.Pmax, 0, R.np, 0, rw, rstat,
-                                ctid, warp, lane);
+    combine_states<C, LY, true>(prm, R, prm.ws_m, prm.ws_l, prm.ws_o, prm.Pmax, 0, R.np, 0, rw, rstat, lane);
     return;
   }
   combine_states<C, LY, false>(prm, R, prm.ws_m, prm.ws_l, prm.ws_o, prm.Pmax, R.c * kChunk, R.cnt, R.c,
-                               rw, rstat, ctid, warp, lane);
+                               rw, rstat, lane);
   const int nchunks = (R.np + kChunk - 1) / kChunk;
-  named_barrier_sync(1, NCT);
-  if (ctid == 0) {
+  int last = 0;
+  if (lane == 0) {
+    // The warp's chunk-state stores (ordered before lane 0 by the __syncwarp
+    // that ends combine_states) are released with the ticket.
     int* tk = prm.tickets + (size_t)R.s * prm.n_hg + R.hg;
     const int t = atomic_add_release_gpu(tk, 1);
-    const bool last = (t == nchunks - 1);
+    last = (t == nchunks - 1);
     if (last) {
       *tk = 0;
       fence_acq_rel_gpu();
     }
-    *red2 = last ? 1 : 0;
   }
-  named_barrier_sync(1, NCT);
-  if (*red2)
+  if (__shfl_sync(0xffffffffu, last, 0))
     combine_states<C, LY, true>(prm, R, prm.ws_cm, prm.ws_cl, prm.ws_co, prm.Cmax, 0, nchunks, 0, rw,
-                                rstat, ctid, warp, lane);
+                                rstat, lane);
 }
 
+// Consumer warp: stream the blocks of every unit assigned to it and hand its
+// online-softmax state for each unit to the epilogue warp through shared
+// memory.  Consumer warps never wait for each other.
 template <class C, class LY>
 __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem, const int* pref,
                                               const UnitInfo* info, volatile int* abort_flag,
-                                              const volatile uint32_t* issued, volatile int* red_go,
-                                              volatile int* red2, RedInfo* red, int warp, int lane) {
+                                              const volatile uint32_t* issued, int warp, int lane) {
   using T = typename C::T;
   constexpr int D = C::D, BS = C::BS, GT = C::GT, NC = LY::NC, NCT = LY::NCT, NS = LY::NSTAGE,
-                UQ = LY::UQ, OUTS = LY::OUTS;
+                UQ = LY::UQ;
   const int ctid = warp * 32 + lane;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bar_full = sbase + LY::OFF_BAR, bar_empty = bar_full + NS * 8;
   const uint32_t bar_ufull = bar_empty + NS * 8, bar_uempty = bar_ufull + UQ * 8;
+  const uint32_t bar_efull = bar_uempty + UQ * 8, bar_eempty = bar_efull + 8;
   float* epi_acc = reinterpret_cast<float*>(smem + LY::OFF_EPI_ACC);
   float* epi_ml = reinterpret_cast<float*>(smem + LY::OFF_EPI_ML);
+  UnitInfo* epi_info = reinterpret_cast<UnitInfo*>(smem + LY::OFF_EPI_INFO);
   float* scr = reinterpret_cast<float*>(smem + LY::OFF_SCR) + warp * C::SCRATCH_FLOATS;
-  float* rw = reinterpret_cast<float*>(smem + LY::OFF_RED);
-  float* rstat = reinterpret_cast<float*>(smem + LY::OFF_RSTAT);
   int* err = prm.hdr + kHdrError;
   const int S = prm.S, H = prm.H, Pmax = prm.Pmax;
   T* out = static_cast<T*>(prm.out);
@@ -521,33 +529,29 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
 
   C cons;
   uint32_t g = 0, k = 0;
-  // Thread 0 takes a ticket after each multi-partition unit and checks it at
-  // the next epilogue (or at exit), so the atomic's latency is off the
-  // critical path.  If it was the last partition of its (sequence, head
-  // group), the CTA then combines all of them.
-  bool pend = false;
-  int pend_t = 0;
-  RedInfo pinfo{};
   while (true) {
     const int slot = k % UQ;
     const uint32_t par = (k / UQ) & 1u;
-    const bool okw = wait_bounded(bar_ufull + 8 * slot, par, abort_flag, err, prm.timeout_ns);
+    const bool okw = __all_sync(0xffffffffu, wait_bounded(bar_ufull + 8 * slot, par, abort_flag, err,
+                                                          prm.timeout_ns));
     const UnitInfo I = info[slot];
-    const bool stop = named_barrier_or(1, NCT, !okw || I.s < 0 || *abort_flag != 0);
-    if (stop) {
-      const bool aborted = named_barrier_or(1, NCT, *abort_flag != 0);
-      if (!aborted) {
-        if (ctid == 0) settle_ticket(prm, pend, pend_t, pinfo, red_go, red);
-        named_barrier_sync(1, NCT);
-        if (*red_go) run_combine<C, LY>(prm, *red, rw, rstat, red2, ctid, warp, lane);
-      }
+    if (!okw) break;
+    if (I.s < 0) {
+      // End of work: pass the end marker on to the epilogue warp, once it has
+      // taken the previous hand-over (the k-th hand-over waits for the
+      // (k-1)-th to be consumed).
+      if (!__all_sync(0xffffffffu, wait_bounded(bar_eempty, (k & 1u) ^ 1u, abort_flag, err,
+                                                prm.timeout_ns)))
+        break;
+      if (warp == 0 && lane == 0) epi_info->s = -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_efull);
       break;
     }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
                     prm.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_uempty + 8 * slot);
-    ++k;
 
     for (int j = warp; j < I.nb; j += NC) {
       const uint32_t gj = g + j, st = stage_of<LY>(gj), ph = phase_of<LY>(gj);
@@ -561,44 +565,105 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     }
     g += I.nb;
 
-    // Combine the NC warp states into the partition's (m_p, l_p, o_p).
+    // Hand this warp's state for unit k to the epilogue warp, once it has
+    // taken unit k-1's.
+    if (!__all_sync(0xffffffffu, wait_bounded(bar_eempty, (k & 1u) ^ 1u, abort_flag, err,
+                                              prm.timeout_ns)))
+      break;
+    ++k;
     cons.finish(epi_acc + warp * GT * D, epi_ml + warp * GT * 2, lane);
-    named_barrier_sync(1, NCT);
-    if (ctid == 0) settle_ticket(prm, pend, pend_t, pinfo, red_go, red);
-    const bool single = (I.np == 1);
-#pragma unroll
-    for (int o = 0; o < OUTS; ++o) {
-      const int idx = ctid + o * NCT;
-      if (idx >= GT * D) break;
-      const int gh = idx / D, d = idx - gh * D;
-      if (gh >= I.nh) continue;
+    if (warp == 0 && lane == 0) *epi_info = I;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_efull);
+  }
+}
+
+// Epilogue warp: for every unit, merge the consumer warps' states into the
+// partition's (m_p, l_p, o_p) (or the output, for a single-partition
+// sequence), take the completion ticket (checked one unit later, off the
+// critical path) and run the combine jobs that fall to this CTA.
+template <class C, class LY>
+__device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem, volatile int* abort_flag,
+                                              int lane) {
+  using T = typename C::T;
+  constexpr int D = C::D, GT = C::GT, NC = LY::NC, NS = LY::NSTAGE, UQ = LY::UQ;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar_efull = sbase + LY::OFF_BAR + (2 * NS + 2 * UQ) * 8, bar_eempty = bar_efull + 8;
+  const float* epi_acc = reinterpret_cast<const float*>(smem + LY::OFF_EPI_ACC);
+  const float* epi_ml = reinterpret_cast<const float*>(smem + LY::OFF_EPI_ML);
+  const UnitInfo* epi_info = reinterpret_cast<const UnitInfo*>(smem + LY::OFF_EPI_INFO);
+  float* rw = reinterpret_cast<float*>(smem + LY::OFF_RED);
+  float* rstat = reinterpret_cast<float*>(smem + LY::OFF_RSTAT);
+  float* ef = reinterpret_cast<float*>(smem + LY::OFF_EF);  // [NC][GT] weights, then [GT] sums
+  int* err = prm.hdr + kHdrError;
+  const int H = prm.H, Pmax = prm.Pmax;
+  T* out = static_cast<T*>(prm.out);
+
+  // Lane 0 only: a ticket taken and not yet checked, and its job.
+  bool pend = false;
+  int pend_t = 0;
+  RedInfo pinfo{};
+  for (uint32_t k = 0;; ++k) {
+    const bool ok = __all_sync(0xffffffffu, wait_bounded(bar_efull, k & 1u, abort_flag, err,
+                                                         prm.timeout_ns));
+    if (!ok) return;  // aborted: the results are abandoned
+    const UnitInfo I = *epi_info;
+    if (I.s < 0) {
+      // End of work: settle the last ticket.
+      int last = 0;
+      if (lane == 0 && pend && pend_t == pinfo.cnt - 1) {
+        last = 1;
+        *ticket_of(prm, pinfo) = 0;
+        fence_acq_rel_gpu();
+      }
+      const RedInfo R = broadcast_job(pinfo);  // pinfo is kept by lane 0 only
+      if (__shfl_sync(0xffffffffu, last, 0)) run_combine<C, LY>(prm, R, rw, rstat, lane);
+      return;
+    }
+    // Per head: M = max over warps, each warp's weight 2^(m_w - M), and the sum l.
+    for (int i = lane; i < GT; i += 32) {
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NC; ++w) M = fmaxf(M, epi_ml[(w * GT + gh) * 2]);
-      float num = 0.f, den = 0.f;
+      for (int w = 0; w < NC; ++w) M = fmaxf(M, epi_ml[(w * GT + i) * 2]);
+      float den = 0.f;
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
-        const float f = exp2f(epi_ml[(w * GT + gh) * 2] - M);
-        num = fmaf(f, epi_acc[(w * GT + gh) * D + d], num);
-        den = fmaf(f, epi_ml[(w * GT + gh) * 2 + 1], den);
+        const float f = exp2f(epi_ml[(w * GT + i) * 2] - M);
+        ef[w * GT + i] = f;
+        den = fmaf(f, epi_ml[(w * GT + i) * 2 + 1], den);
       }
-      const float val = num / den;
-      const int h = I.h0 + gh;
-      const size_t sh = (size_t)I.s * H + h;
-      if (single) {
-        out[sh * D + d] = F16Traits<T>::from_float(val);
-      } else {
-        prm.ws_o[(sh * Pmax + I.p) * D + d] = val;
-      }
+      ef[NC * GT + i] = den;
+      rstat[i * 2] = M;
+    }
+    __syncwarp();
+    const bool single = (I.np == 1);
+    for (int idx = lane; idx < I.nh * D; idx += 32) {
+      const int gh = idx / D, d = idx - gh * D;
+      float num = 0.f;
+#pragma unroll
+      for (int w = 0; w < NC; ++w) num = fmaf(ef[w * GT + gh], epi_acc[(w * GT + gh) * D + d], num);
+      const float val = num / ef[NC * GT + gh];
+      const size_t sh = (size_t)I.s * H + I.h0 + gh;
+      if (single) out[sh * D + d] = F16Traits<T>::from_float(val);
+      else prm.ws_o[(sh * Pmax + I.p) * D + d] = val;
       if (d == 0) {
-        prm.ws_m[sh * Pmax + I.p] = M * kLn2;
-        prm.ws_l[sh * Pmax + I.p] = den;
+        prm.ws_m[sh * Pmax + I.p] = rstat[gh * 2] * kLn2;
+        prm.ws_l[sh * Pmax + I.p] = ef[NC * GT + gh];
       }
     }
-    // The barrier orders every consumer thread's partition stores before
-    // thread 0's release-add on the ticket (release is cumulative).
-    named_barrier_sync(1, NCT);
-    if (ctid == 0) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_eempty);  // the hand-over slot may be refilled
+
+    // Settle the previous ticket; take this unit's (release: the warp's
+    // partition stores above, ordered by __syncwarp, become visible first).
+    int go = 0;
+    RedInfo job = pinfo;
+    if (lane == 0) {
+      if (pend && pend_t == pinfo.cnt - 1) {
+        go = 1;
+        *ticket_of(prm, pinfo) = 0;
+        fence_acq_rel_gpu();
+      }
       pend = !single;
       if (pend) {
         pinfo.s = I.s; pinfo.hg = I.hg; pinfo.h0 = I.h0; pinfo.nh = I.nh; pinfo.np = I.np;
@@ -610,7 +675,8 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
         pend_t = atomic_add_release_gpu(ticket_of(prm, pinfo), 1);
       }
     }
-    if (*red_go) run_combine<C, LY>(prm, *red, rw, rstat, red2, ctid, warp, lane);
+    const RedInfo R = broadcast_job(job);  // pinfo is kept by lane 0 only
+    if (__shfl_sync(0xffffffffu, go, 0)) run_combine<C, LY>(prm, R, rw, rstat, lane);
   }
 }
 
@@ -623,10 +689,7 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS);
-  volatile int* red_go = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 4);
   volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(smem + LY::OFF_FLAGS + 8);
-  volatile int* red2 = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 12);
-  RedInfo* red = reinterpret_cast<RedInfo*>(smem + LY::OFF_FLAGS + 16);
   int* pref = reinterpret_cast<int*>(smem + LY::OFF_PREF);
   int* scan = reinterpret_cast<int*>(smem + LY::OFF_SCAN);
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + LY::OFF_INFO);
@@ -641,9 +704,10 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
       mbar_init(bar + 8 * (2 * NS + i), 1);        // unit full
       mbar_init(bar + 8 * (2 * NS + UQ + i), NC);  // unit empty: every consumer warp
     }
+    mbar_init(bar + 8 * (2 * NS + 2 * UQ), NC);     // hand-over full: every consumer warp
+    mbar_init(bar + 8 * (2 * NS + 2 * UQ + 1), 1);  // hand-over empty: the epilogue warp
     *abort_flag = 0;
     *issued = 0;
-    *red_go = 0;
     fence_mbarrier_init();
   }
   // pref[s] = number of used partitions before sequence s (lengths clamped to
@@ -682,8 +746,10 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
   __syncthreads();
   if (warp == NC) {
     producer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, lane);
+  } else if (warp == NC + 1) {
+    epilogue_loop<C, LY>(prm, smem, abort_flag, lane);
   } else {
-    consumer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, red_go, red2, red, warp, lane);
+    consumer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, warp, lane);
   }
 }
 
