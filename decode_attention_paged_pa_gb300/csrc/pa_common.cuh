@@ -18,6 +18,7 @@ constexpr int kErrTimeout = 6;
 // Workspace header: int32 words.
 constexpr int kHdrError = 0;    // first device-side error code (0 = none)
 constexpr int kHdrWork = 1;     // dynamic work counter (units handed out)
+constexpr int kHdrWhere = 2;    // first timed-out wait: site, CTA, warp, detail (4 ints)
 constexpr int kHdrInts = 64;    // header size in ints (256 bytes)
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -76,19 +77,32 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Record a timed-out wait: kErrTimeout in the error word and, for the first
+// one, where it happened (wait site, CTA, warp, a site-specific detail).
+__device__ __forceinline__ void record_timeout(volatile int* abort_flag, int* err_word, int site,
+                                               int detail) {
+  *abort_flag = 1;
+  atomicCAS(err_word, 0, kErrTimeout);
+  if (atomicCAS(err_word + kHdrWhere, 0, site) == 0) {
+    err_word[kHdrWhere + 1] = blockIdx.x;
+    err_word[kHdrWhere + 2] = threadIdx.x >> 5;
+    err_word[kHdrWhere + 3] = detail;
+  }
+}
+
 // Wait for phase `parity` of an mbarrier with a time bound.  Returns false if
 // the CTA's abort flag is raised or the bound runs out (which raises the flag
-// and records kErrTimeout in the workspace error word).  Never spins forever.
+// and records the timeout).  Never spins forever.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             int* err_word, long long timeout_ns) {
+                                             int* err_word, long long timeout_ns, int site = 1,
+                                             int detail = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if ((long long)(global_timer_ns() - t0) > timeout_ns) {
-      *abort_flag = 1;
-      atomicCAS(err_word, 0, kErrTimeout);
+      record_timeout(abort_flag, err_word, site, detail);
       return false;
     }
   }

@@ -78,7 +78,6 @@ struct Layout {
   static constexpr int NC = NC_, NSTAGE = NSTAGE_, UQ = 2;
   static constexpr int NCT = NC * 32;          // consumer threads
   static constexpr int THREADS = NCT + 64;     // + producer warp + epilogue warp
-  static constexpr int RCH = 64;               // partitions per combine chunk
   static constexpr uint32_t KBYTES = C::D * C::BS * 2;
   static constexpr uint32_t STAGE = 2 * KBYTES;
   static constexpr uint32_t RING = NSTAGE * STAGE;
@@ -87,14 +86,13 @@ struct Layout {
   static constexpr uint32_t OFF_EPI_ACC = al16(OFF_Q + UQ * QSLOT);
   static constexpr uint32_t OFF_EPI_ML = al16(OFF_EPI_ACC + NC * C::GT * C::D * 4);
   static constexpr uint32_t OFF_SCR = al16(OFF_EPI_ML + NC * C::GT * 2 * 4);
-  static constexpr uint32_t OFF_RED = al16(OFF_SCR + NC * C::SCRATCH_FLOATS * 4);
-  static constexpr uint32_t OFF_RSTAT = al16(OFF_RED + C::GT * RCH * 4);
+  static constexpr uint32_t OFF_RSTAT = al16(OFF_SCR + NC * C::SCRATCH_FLOATS * 4);
   static constexpr uint32_t OFF_EF = al16(OFF_RSTAT + C::GT * 2 * 4);   // NC*GT warp weights + GT sums
   static constexpr uint32_t OFF_SCAN = al16(OFF_EF + (NC + 1) * C::GT * 4);
   static constexpr uint32_t OFF_INFO = al16(OFF_SCAN + THREADS * 4);
   static constexpr uint32_t OFF_EPI_INFO = al16(OFF_INFO + UQ * sizeof(UnitInfo));
   static constexpr uint32_t OFF_BAR = al16(OFF_EPI_INFO + sizeof(UnitInfo));
-  static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 2;
+  static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 3;
   static constexpr uint32_t OFF_FLAGS = al16(OFF_BAR + NBAR * 8);
   static constexpr uint32_t OFF_PREF = al16(OFF_FLAGS + 64);
   static constexpr uint32_t FIXED = OFF_PREF;
@@ -111,6 +109,20 @@ __device__ __forceinline__ uint32_t phase_of(uint32_t g) {
   return (g / LY::NSTAGE) & 1u;
 }
 
+// Wait sites recorded by a timeout (workspace header words 2..5).
+enum WaitSite {
+  kSitePublish = 1,     // producer: a unit-queue slot to free up
+  kSiteStage = 2,       // producer: a ring stage to free up
+  kSiteUnit = 3,        // consumer: the next unit's description
+  kSiteIssued = 4,      // consumer: a block to be issued
+  kSiteFull = 5,        // consumer: a block to land
+  kSiteHandover = 6,    // consumer: the hand-over slot to free up
+  kSiteHandEnd = 7,     // consumer: the hand-over slot, for the end marker
+  kSiteServe = 8,       // consumer: the epilogue warp to finish its jobs
+  kSiteEpiFull = 9,     // epilogue: the consumers' states of a unit
+  kSiteJobDone = 10     // epilogue: the helpers of a shared combine job
+};
+
 // Wait (bounded) until the producer has issued at least `target` blocks.
 __device__ __forceinline__ bool wait_issued(const volatile uint32_t* issued, uint32_t target,
                                             volatile int* abort_flag, int* err_word,
@@ -121,8 +133,7 @@ __device__ __forceinline__ bool wait_issued(const volatile uint32_t* issued, uin
     if (*issued >= target) return true;
     if (*abort_flag) return false;
     if ((long long)(global_timer_ns() - t0) > timeout_ns) {
-      *abort_flag = 1;
-      atomicCAS(err_word, 0, kErrTimeout);
+      record_timeout(abort_flag, err_word, kSiteIssued, (int)target);
       return false;
     }
   }
@@ -201,7 +212,8 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     const uint32_t par = (kq / UQ) & 1u;
     bool okp = true;
     if (lane == 0) {
-      okp = wait_bounded(bar_uempty + 8 * slot, par ^ 1u, abort_flag, err, prm.timeout_ns);
+      okp = wait_bounded(bar_uempty + 8 * slot, par ^ 1u, abort_flag, err, prm.timeout_ns, kSitePublish,
+                         (int)kq);
       if (okp && !have) {
         info[slot].s = -1;
         mbar_arrive(bar_ufull + 8 * slot);
@@ -286,8 +298,7 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
                 timing = true;
                 t_start = now;
               } else if ((long long)(now - t_start) > prm.timeout_ns) {
-                *abort_flag = 1;
-                atomicCAS(err, 0, kErrTimeout);
+                record_timeout(abort_flag, err, kSiteStage, (int)g);
                 stop = 1;
               } else {
                 __nanosleep(32);
@@ -337,16 +348,25 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
 // Partitions per combine chunk (kept equal to kChunkParts of the launcher).
 constexpr int kChunk = 16;
 
-// A combine job: the partitions of one (sequence, head group) -- all of them
-// (kind 0, at most kChunk), or chunk c of them (kind 1), whose combined state
-// is then folded with the other chunks' by the last chunk to finish.
-struct RedInfo {
+// A combine job for one (sequence, head group):
+//   kind 0: all np (<= kChunk) partition states -> output;
+//   kind 1: the cnt partition states of chunk c -> chunk state c;
+//   kind 2: the ceil(np / kChunk) chunk states -> output.
+struct Job {
   int s, hg, h0, nh, np, kind, c, cnt;
 };
+static_assert(sizeof(Job) <= 48, "combine job must fit in the shared flag area");
+
+// Jobs that read more float4 values than this are shared with the consumer
+// warps; smaller ones are done by the epilogue warp alone.
+#ifndef PA_SHARE_JOB_LOADS
+#define PA_SHARE_JOB_LOADS 512
+#endif
+constexpr int kShareJobLoads = PA_SHARE_JOB_LOADS;
 
 // Lane 0's job, for every lane of the warp.
-__device__ __forceinline__ RedInfo broadcast_job(const RedInfo& J) {
-  RedInfo R;
+__device__ __forceinline__ Job broadcast_job(const Job& J) {
+  Job R;
   R.s = __shfl_sync(0xffffffffu, J.s, 0);
   R.hg = __shfl_sync(0xffffffffu, J.hg, 0);
   R.h0 = __shfl_sync(0xffffffffu, J.h0, 0);
@@ -358,132 +378,162 @@ __device__ __forceinline__ RedInfo broadcast_job(const RedInfo& J) {
   return R;
 }
 
-__device__ __forceinline__ int* ticket_of(const KParams& prm, const RedInfo& R) {
-  const size_t sg = (size_t)R.s * prm.n_hg + R.hg;
-  return R.kind == 0 ? prm.tickets + sg : prm.ctickets + sg * prm.Cmax + R.c;
+__device__ __forceinline__ int* ticket_of(const KParams& prm, const Job& J) {
+  const size_t sg = (size_t)J.s * prm.n_hg + J.hg;
+  return J.kind == 0 ? prm.tickets + sg : prm.ctickets + sg * prm.Cmax + J.c;
 }
 
-// Log-sum-exp combine of `count` states (m, l, o) of the heads of R, by one
-// warp: per head M = max m_i and total = sum e^(m_i - M) l_i, then
-// o = sum_i (e^(m_i - M) l_i / total) o_i with the weights staged in shared
-// memory in chunks of RCH (the page's Phase 2 formula).  State i of head h is
-// m[(s*H + h)*stride + first + i] and o[((s*H + h)*stride + first + i)*D + ..].
-// TO_OUT writes o, rounded, to the output; otherwise (M, total, o) becomes
-// chunk state `dst_c`.
-template <class C, class LY, bool TO_OUT>
-__device__ __forceinline__ void combine_states(const KParams& prm, const RedInfo& R, const float* sm,
-                                               const float* sl, const float* so, int stride, int first,
-                                               int count, int dst_c, float* rw, float* rstat, int lane) {
+__device__ __forceinline__ int job_count(const Job& J) {
+  return J.kind == 0 ? J.np : (J.kind == 1 ? J.cnt : (J.np + kChunk - 1) / kChunk);
+}
+
+// One participant's share of a combine job: the float4 output columns
+// idx = part*32 + lane (+ nparts*32 ...).  Each lane combines its column over
+// all `count` states on its own (the page's Phase 2 formula): M = max m_i,
+// total = sum e^(m_i - M) l_i, o = sum_i (e^(m_i - M) l_i / total) o_i.
+template <class C>
+__device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, int part, int nparts,
+                                              int lane) {
   using T = typename C::T;
-  constexpr int D = C::D, GT = C::GT, RCH = LY::RCH;
-  constexpr int D4 = D / 4, OUT4 = (GT * D4 + 31) / 32;
-  const int H = prm.H;
-  for (int gh = 0; gh < R.nh; ++gh) {
-    const size_t base = ((size_t)R.s * H + R.h0 + gh) * stride + first;
-    float M = -INFINITY;
-    for (int i = lane; i < count; i += 32) M = fmaxf(M, __ldcg(sm + base + i));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float tot = 0.f;
-    for (int i = lane; i < count; i += 32)
-      tot = fmaf(exp2f((__ldcg(sm + base + i) - M) * kLog2e), __ldcg(sl + base + i), tot);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-    if (lane == 0) {
-      rstat[gh * 2] = M;
-      rstat[gh * 2 + 1] = tot;
-    }
+  constexpr int D = C::D, D4 = D / 4;
+  const float *sm, *sl, *so;
+  int stride, first;
+  if (J.kind == 2) {
+    sm = prm.ws_cm; sl = prm.ws_cl; so = prm.ws_co; stride = prm.Cmax; first = 0;
+  } else {
+    sm = prm.ws_m; sl = prm.ws_l; so = prm.ws_o; stride = prm.Pmax; first = J.kind == 1 ? J.c * kChunk : 0;
   }
-  float4 acc[OUT4];
-#pragma unroll
-  for (int o = 0; o < OUT4; ++o) acc[o] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < count; c0 += RCH) {
-    const int cn = min(RCH, count - c0);
-    __syncwarp();
-    for (int i = lane; i < R.nh * RCH; i += 32) {
-      const int gh = i / RCH, pp = i - gh * RCH;
-      if (pp < cn) {
-        const size_t e = ((size_t)R.s * H + R.h0 + gh) * stride + first + c0 + pp;
-        rw[i] = exp2f((__ldcg(sm + e) - rstat[gh * 2]) * kLog2e) * __ldcg(sl + e) / rstat[gh * 2 + 1];
-      }
-    }
-    __syncwarp();
-#pragma unroll
-    for (int o = 0; o < OUT4; ++o) {
-      const int idx = lane + o * 32;
-      if (idx >= GT * D4) break;
-      const int gh = idx / D4, d4 = idx - gh * D4;
-      if (gh >= R.nh) continue;
-      const float4* src = reinterpret_cast<const float4*>(
-                              so + (((size_t)R.s * H + R.h0 + gh) * stride + first + c0) * D) + d4;
-      float4 a = acc[o], b = make_float4(0.f, 0.f, 0.f, 0.f);
-      int pp = 0;
-#pragma unroll 4
-      for (; pp + 1 < cn; pp += 2) {
-        const float w0 = rw[gh * RCH + pp], w1 = rw[gh * RCH + pp + 1];
-        const float4 v0 = __ldcg(src + (size_t)pp * D4), v1 = __ldcg(src + (size_t)(pp + 1) * D4);
-        a.x = fmaf(w0, v0.x, a.x); a.y = fmaf(w0, v0.y, a.y); a.z = fmaf(w0, v0.z, a.z); a.w = fmaf(w0, v0.w, a.w);
-        b.x = fmaf(w1, v1.x, b.x); b.y = fmaf(w1, v1.y, b.y); b.z = fmaf(w1, v1.z, b.z); b.w = fmaf(w1, v1.w, b.w);
-      }
-      if (pp < cn) {
-        const float w0 = rw[gh * RCH + pp];
-        const float4 v0 = __ldcg(src + (size_t)pp * D4);
-        a.x = fmaf(w0, v0.x, a.x); a.y = fmaf(w0, v0.y, a.y); a.z = fmaf(w0, v0.z, a.z); a.w = fmaf(w0, v0.w, a.w);
-      }
-      acc[o] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-    }
-  }
-#pragma unroll
-  for (int o = 0; o < OUT4; ++o) {
-    const int idx = lane + o * 32;
-    if (idx >= GT * D4) break;
+  const int count = job_count(J);
+  for (int idx = part * 32 + lane; idx < J.nh * D4; idx += nparts * 32) {
     const int gh = idx / D4, d4 = idx - gh * D4;
-    if (gh >= R.nh) continue;
-    const size_t sh = (size_t)R.s * H + R.h0 + gh;
-    if constexpr (TO_OUT) {
-      uint2 v;
-      v.x = F16Traits<T>::pack(acc[o].x, acc[o].y);
-      v.y = F16Traits<T>::pack(acc[o].z, acc[o].w);
-      *reinterpret_cast<uint2*>(static_cast<T*>(prm.out) + sh * D + d4 * 4) = v;
-    } else {
-      reinterpret_cast<float4*>(prm.ws_co + (sh * prm.Cmax + dst_c) * D)[d4] = acc[o];
+    const size_t row = (size_t)J.s * prm.H + J.h0 + gh;
+    const size_t base = row * stride + first;
+    float M = -INFINITY;
+    for (int i = 0; i < count; ++i) M = fmaxf(M, __ldcg(sm + base + i));
+    float tot = 0.f;
+    for (int i = 0; i < count; ++i) tot = fmaf(exp2f((__ldcg(sm + base + i) - M) * kLog2e), __ldcg(sl + base + i), tot);
+    const float inv = 1.f / tot;
+    const float4* src = reinterpret_cast<const float4*>(so + base * D) + d4;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    int i = 0;
+#pragma unroll 4
+    for (; i + 1 < count; i += 2) {
+      const float w0 = exp2f((__ldcg(sm + base + i) - M) * kLog2e) * __ldcg(sl + base + i) * inv;
+      const float w1 = exp2f((__ldcg(sm + base + i + 1) - M) * kLog2e) * __ldcg(sl + base + i + 1) * inv;
+      const float4 v0 = __ldcg(src + (size_t)i * D4), v1 = __ldcg(src + (size_t)(i + 1) * D4);
+      a.x = fmaf(w0, v0.x, a.x); a.y = fmaf(w0, v0.y, a.y); a.z = fmaf(w0, v0.z, a.z); a.w = fmaf(w0, v0.w, a.w);
+      b.x = fmaf(w1, v1.x, b.x); b.y = fmaf(w1, v1.y, b.y); b.z = fmaf(w1, v1.z, b.z); b.w = fmaf(w1, v1.w, b.w);
+    }
+    if (i < count) {
+      const float w0 = exp2f((__ldcg(sm + base + i) - M) * kLog2e) * __ldcg(sl + base + i) * inv;
+      const float4 v0 = __ldcg(src + (size_t)i * D4);
+      a.x = fmaf(w0, v0.x, a.x); a.y = fmaf(w0, v0.y, a.y); a.z = fmaf(w0, v0.z, a.z); a.w = fmaf(w0, v0.w, a.w);
+    }
+    const float4 r = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    if (J.kind == 1) {
+      reinterpret_cast<float4*>(prm.ws_co + (row * prm.Cmax + J.c) * D)[d4] = r;
       if (d4 == 0) {
-        prm.ws_cm[sh * prm.Cmax + dst_c] = rstat[gh * 2];
-        prm.ws_cl[sh * prm.Cmax + dst_c] = rstat[gh * 2 + 1];
+        prm.ws_cm[row * prm.Cmax + J.c] = M;
+        prm.ws_cl[row * prm.Cmax + J.c] = tot;
       }
+    } else {
+      uint2 v;
+      v.x = F16Traits<T>::pack(r.x, r.y);
+      v.y = F16Traits<T>::pack(r.z, r.w);
+      *reinterpret_cast<uint2*>(static_cast<T*>(prm.out) + row * D + d4 * 4) = v;
     }
   }
-  __syncwarp();
 }
 
-// Run the combine job R (one warp).  A chunk job writes the chunk's state,
-// then takes the sequence-level ticket; the last chunk folds all chunk states
-// into the output.
+// Shared state of the job protocol between the epilogue warp (which posts
+// jobs) and the consumer warps (which help with heavy ones at their unit
+// boundaries).
+struct JobChannel {
+  volatile int* posted;    // number of jobs posted for help
+  volatile int* finished;  // set once the epilogue warp posts no more jobs
+  Job* rec;                // the posted job
+  uint32_t bar_done;       // mbarrier: NC + 1 arrivals per job
+};
+
+// A consumer warp's help with the posted job, if there is a new one.
 template <class C, class LY>
-__device__ __forceinline__ void run_combine(const KParams& prm, const RedInfo& R, float* rw, float* rstat,
-                                            int lane) {
-  if (R.kind == 0) {
-    combine_states<C, LY, true>(prm, R, prm.ws_m, prm.ws_l, prm.ws_o, prm.Pmax, 0, R.np, 0, rw, rstat, lane);
-    return;
+__device__ __forceinline__ void help_with_job(const KParams& prm, const JobChannel& ch, int& seen, int warp,
+                                              int lane) {
+  // Lane 0's reading decides for the whole warp.
+  if (__shfl_sync(0xffffffffu, *ch.posted, 0) > seen) {
+    __threadfence_block();
+    const Job J = *ch.rec;
+    combine_share<C>(prm, J, warp, LY::NC + 1, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ch.bar_done);
+    ++seen;
   }
-  combine_states<C, LY, false>(prm, R, prm.ws_m, prm.ws_l, prm.ws_o, prm.Pmax, R.c * kChunk, R.cnt, R.c,
-                               rw, rstat, lane);
-  const int nchunks = (R.np + kChunk - 1) / kChunk;
-  int last = 0;
-  if (lane == 0) {
-    // The warp's chunk-state stores (ordered before lane 0 by the __syncwarp
-    // that ends combine_states) are released with the ticket.
-    int* tk = prm.tickets + (size_t)R.s * prm.n_hg + R.hg;
-    const int t = atomic_add_release_gpu(tk, 1);
-    last = (t == nchunks - 1);
-    if (last) {
-      *tk = 0;
-      fence_acq_rel_gpu();
+}
+
+// Consumer warp: wait (bounded) for the hand-over slot to be free for
+// hand-over k, helping with any combine job posted meanwhile.  (The epilogue
+// warp may be waiting for this warp's help before it can free the slot.)
+template <class C, class LY>
+__device__ __forceinline__ bool wait_handover(const KParams& prm, const JobChannel& ch, int& seen,
+                                              uint32_t bar_eempty, uint32_t k, volatile int* abort_flag,
+                                              int* err, int site, int warp, int lane) {
+  const uint32_t parity = (k & 1u) ^ 1u;
+  if (__all_sync(0xffffffffu, mbar_test_wait(bar_eempty, parity))) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    help_with_job<C, LY>(prm, ch, seen, warp, lane);
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar_eempty, parity))) return true;
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+    if ((long long)(global_timer_ns() - t0) > prm.timeout_ns) {
+      if (lane == 0) record_timeout(abort_flag, err, site, (int)k);
+      return false;
     }
+    __nanosleep(32);
   }
-  if (__shfl_sync(0xffffffffu, last, 0))
-    combine_states<C, LY, true>(prm, R, prm.ws_cm, prm.ws_cl, prm.ws_co, prm.Cmax, 0, nchunks, 0, rw,
-                                rstat, lane);
+}
+
+// Epilogue warp: run job J, sharing it with the consumer warps if it is heavy
+// and they are still around to help.  A chunk job then takes the sequence
+// ticket; the last chunk of the sequence runs the final job.
+template <class C, class LY>
+__device__ __forceinline__ void run_job(const KParams& prm, Job J, const JobChannel& ch, int& nposted,
+                                        volatile int* abort_flag, int* err, int lane) {
+  constexpr int D4 = C::D / 4, NC = LY::NC;
+  while (true) {
+    const bool share = (long long)J.nh * D4 * job_count(J) > kShareJobLoads;
+    if (share) {
+      if (lane == 0) {
+        *ch.rec = J;
+        __threadfence_block();
+        *ch.posted = nposted + 1;
+      }
+      ++nposted;
+      combine_share<C>(prm, J, NC, NC + 1, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ch.bar_done);
+      if (!__all_sync(0xffffffffu, wait_bounded(ch.bar_done, (nposted - 1) & 1, abort_flag, err,
+                                                prm.timeout_ns, kSiteJobDone, nposted)))
+        return;
+    } else {
+      combine_share<C>(prm, J, 0, 1, lane);
+      __syncwarp();
+    }
+    if (J.kind != 1) return;
+    // Chunk written (by all helpers: their arrivals on bar_done were observed
+    // above, so the release below covers their stores too).
+    int last = 0;
+    if (lane == 0) {
+      int* tk = prm.tickets + (size_t)J.s * prm.n_hg + J.hg;
+      const int t = atomic_add_release_gpu(tk, 1);
+      last = (t == (J.np + kChunk - 1) / kChunk - 1);
+      if (last) {
+        *tk = 0;
+        fence_acq_rel_gpu();
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    J.kind = 2;
+  }
 }
 
 // Consumer warp: stream the blocks of every unit assigned to it and hand its
@@ -492,7 +542,8 @@ __device__ __forceinline__ void run_combine(const KParams& prm, const RedInfo& R
 template <class C, class LY>
 __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem, const int* pref,
                                               const UnitInfo* info, volatile int* abort_flag,
-                                              const volatile uint32_t* issued, int warp, int lane) {
+                                              const volatile uint32_t* issued, const JobChannel& ch,
+                                              int warp, int lane) {
   using T = typename C::T;
   constexpr int D = C::D, BS = C::BS, GT = C::GT, NC = LY::NC, NCT = LY::NCT, NS = LY::NSTAGE,
                 UQ = LY::UQ;
@@ -529,23 +580,34 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
 
   C cons;
   uint32_t g = 0, k = 0;
+  int seen = 0;  // combine jobs helped with
   while (true) {
     const int slot = k % UQ;
     const uint32_t par = (k / UQ) & 1u;
     const bool okw = __all_sync(0xffffffffu, wait_bounded(bar_ufull + 8 * slot, par, abort_flag, err,
-                                                          prm.timeout_ns));
+                                                          prm.timeout_ns, kSiteUnit, (int)k));
     const UnitInfo I = info[slot];
     if (!okw) break;
     if (I.s < 0) {
       // End of work: pass the end marker on to the epilogue warp, once it has
       // taken the previous hand-over (the k-th hand-over waits for the
-      // (k-1)-th to be consumed).
-      if (!__all_sync(0xffffffffu, wait_bounded(bar_eempty, (k & 1u) ^ 1u, abort_flag, err,
-                                                prm.timeout_ns)))
+      // (k-1)-th to be consumed), then help with combine jobs until the
+      // epilogue warp has run its last one.
+      if (!wait_handover<C, LY>(prm, ch, seen, bar_eempty, k, abort_flag, err, kSiteHandEnd, warp, lane))
         break;
       if (warp == 0 && lane == 0) epi_info->s = -1;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_efull);
+      const uint64_t t0 = global_timer_ns();
+      while (true) {
+        help_with_job<C, LY>(prm, ch, seen, warp, lane);
+        if (__any_sync(0xffffffffu, *ch.finished != 0 || *abort_flag != 0)) break;
+        if ((long long)(global_timer_ns() - t0) > prm.timeout_ns) {
+          if (lane == 0) record_timeout(abort_flag, err, kSiteServe, seen);
+          break;
+        }
+        __nanosleep(64);
+      }
       break;
     }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
@@ -556,7 +618,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     for (int j = warp; j < I.nb; j += NC) {
       const uint32_t gj = g + j, st = stage_of<LY>(gj), ph = phase_of<LY>(gj);
       bool okb = wait_issued(issued, gj + 1, abort_flag, err, prm.timeout_ns) &&
-                 wait_bounded(bar_full + 8 * st, ph, abort_flag, err, prm.timeout_ns);
+                 wait_bounded(bar_full + 8 * st, ph, abort_flag, err, prm.timeout_ns, kSiteFull, (int)gj);
       okb = __all_sync(0xffffffffu, okb);
       const int ntok = min(BS, I.t1 - I.t0 - j * BS);
       if (okb) cons.block(smem + st * LY::STAGE, smem + st * LY::STAGE + LY::KBYTES, ntok, lane, scr);
@@ -566,9 +628,8 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     g += I.nb;
 
     // Hand this warp's state for unit k to the epilogue warp, once it has
-    // taken unit k-1's.
-    if (!__all_sync(0xffffffffu, wait_bounded(bar_eempty, (k & 1u) ^ 1u, abort_flag, err,
-                                              prm.timeout_ns)))
+    // taken unit k-1's (helping with combine jobs meanwhile).
+    if (!wait_handover<C, LY>(prm, ch, seen, bar_eempty, k, abort_flag, err, kSiteHandover, warp, lane))
       break;
     ++k;
     cons.finish(epi_acc + warp * GT * D, epi_ml + warp * GT * 2, lane);
@@ -584,7 +645,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
 // critical path) and run the combine jobs that fall to this CTA.
 template <class C, class LY>
 __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem, volatile int* abort_flag,
-                                              int lane) {
+                                              const JobChannel& ch, int lane) {
   using T = typename C::T;
   constexpr int D = C::D, GT = C::GT, NC = LY::NC, NS = LY::NSTAGE, UQ = LY::UQ;
   const uint32_t sbase = smem_addr(smem);
@@ -592,7 +653,6 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
   const float* epi_acc = reinterpret_cast<const float*>(smem + LY::OFF_EPI_ACC);
   const float* epi_ml = reinterpret_cast<const float*>(smem + LY::OFF_EPI_ML);
   const UnitInfo* epi_info = reinterpret_cast<const UnitInfo*>(smem + LY::OFF_EPI_INFO);
-  float* rw = reinterpret_cast<float*>(smem + LY::OFF_RED);
   float* rstat = reinterpret_cast<float*>(smem + LY::OFF_RSTAT);
   float* ef = reinterpret_cast<float*>(smem + LY::OFF_EF);  // [NC][GT] weights, then [GT] sums
   int* err = prm.hdr + kHdrError;
@@ -602,22 +662,24 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
   // Lane 0 only: a ticket taken and not yet checked, and its job.
   bool pend = false;
   int pend_t = 0;
-  RedInfo pinfo{};
+  Job pinfo{};
+  int nposted = 0;
   for (uint32_t k = 0;; ++k) {
     const bool ok = __all_sync(0xffffffffu, wait_bounded(bar_efull, k & 1u, abort_flag, err,
-                                                         prm.timeout_ns));
+                                                         prm.timeout_ns, kSiteEpiFull, (int)k));
     if (!ok) return;  // aborted: the results are abandoned
     const UnitInfo I = *epi_info;
     if (I.s < 0) {
-      // End of work: settle the last ticket.
+      // End of work: settle the last ticket, then release the helpers.
       int last = 0;
       if (lane == 0 && pend && pend_t == pinfo.cnt - 1) {
         last = 1;
         *ticket_of(prm, pinfo) = 0;
         fence_acq_rel_gpu();
       }
-      const RedInfo R = broadcast_job(pinfo);  // pinfo is kept by lane 0 only
-      if (__shfl_sync(0xffffffffu, last, 0)) run_combine<C, LY>(prm, R, rw, rstat, lane);
+      const Job R = broadcast_job(pinfo);  // pinfo is kept by lane 0 only
+      if (__shfl_sync(0xffffffffu, last, 0)) run_job<C, LY>(prm, R, ch, nposted, abort_flag, err, lane);
+      if (lane == 0) *ch.finished = 1;
       return;
     }
     // Per head: M = max over warps, each warp's weight 2^(m_w - M), and the sum l.
@@ -637,16 +699,29 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
     }
     __syncwarp();
     const bool single = (I.np == 1);
-    for (int idx = lane; idx < I.nh * D; idx += 32) {
-      const int gh = idx / D, d = idx - gh * D;
-      float num = 0.f;
+    constexpr int D4 = D / 4;
+    for (int idx = lane; idx < I.nh * D4; idx += 32) {
+      const int gh = idx / D4, d4 = idx - gh * D4;
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int w = 0; w < NC; ++w) num = fmaf(ef[w * GT + gh], epi_acc[(w * GT + gh) * D + d], num);
-      const float val = num / ef[NC * GT + gh];
+      for (int w = 0; w < NC; ++w) {
+        const float f = ef[w * GT + gh];
+        const float4 v = reinterpret_cast<const float4*>(epi_acc + (w * GT + gh) * D)[d4];
+        num.x = fmaf(f, v.x, num.x); num.y = fmaf(f, v.y, num.y);
+        num.z = fmaf(f, v.z, num.z); num.w = fmaf(f, v.w, num.w);
+      }
+      const float inv = 1.f / ef[NC * GT + gh];
+      const float4 val = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
       const size_t sh = (size_t)I.s * H + I.h0 + gh;
-      if (single) out[sh * D + d] = F16Traits<T>::from_float(val);
-      else prm.ws_o[(sh * Pmax + I.p) * D + d] = val;
-      if (d == 0) {
+      if (single) {
+        uint2 v;
+        v.x = F16Traits<T>::pack(val.x, val.y);
+        v.y = F16Traits<T>::pack(val.z, val.w);
+        *reinterpret_cast<uint2*>(out + sh * D + d4 * 4) = v;
+      } else {
+        reinterpret_cast<float4*>(prm.ws_o + (sh * Pmax + I.p) * D)[d4] = val;
+      }
+      if (d4 == 0) {
         prm.ws_m[sh * Pmax + I.p] = rstat[gh * 2] * kLn2;
         prm.ws_l[sh * Pmax + I.p] = ef[NC * GT + gh];
       }
@@ -657,7 +732,7 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
     // Settle the previous ticket; take this unit's (release: the warp's
     // partition stores above, ordered by __syncwarp, become visible first).
     int go = 0;
-    RedInfo job = pinfo;
+    Job job = pinfo;
     if (lane == 0) {
       if (pend && pend_t == pinfo.cnt - 1) {
         go = 1;
@@ -675,8 +750,8 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
         pend_t = atomic_add_release_gpu(ticket_of(prm, pinfo), 1);
       }
     }
-    const RedInfo R = broadcast_job(job);  // pinfo is kept by lane 0 only
-    if (__shfl_sync(0xffffffffu, go, 0)) run_combine<C, LY>(prm, R, rw, rstat, lane);
+    const Job R = broadcast_job(job);  // pinfo is kept by lane 0 only
+    if (__shfl_sync(0xffffffffu, go, 0)) run_job<C, LY>(prm, R, ch, nposted, abort_flag, err, lane);
   }
 }
 
@@ -690,6 +765,11 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
   const uint32_t sbase = smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS);
   volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(smem + LY::OFF_FLAGS + 8);
+  JobChannel ch;
+  ch.posted = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 4);
+  ch.finished = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 12);
+  ch.rec = reinterpret_cast<Job*>(smem + LY::OFF_FLAGS + 16);
+  ch.bar_done = sbase + LY::OFF_BAR + 8 * (2 * NS + 2 * UQ + 2);
   int* pref = reinterpret_cast<int*>(smem + LY::OFF_PREF);
   int* scan = reinterpret_cast<int*>(smem + LY::OFF_SCAN);
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + LY::OFF_INFO);
@@ -706,8 +786,11 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     }
     mbar_init(bar + 8 * (2 * NS + 2 * UQ), NC);     // hand-over full: every consumer warp
     mbar_init(bar + 8 * (2 * NS + 2 * UQ + 1), 1);  // hand-over empty: the epilogue warp
+    mbar_init(bar + 8 * (2 * NS + 2 * UQ + 2), NC + 1);  // shared combine job done: all helpers
     *abort_flag = 0;
     *issued = 0;
+    *ch.posted = 0;
+    *ch.finished = 0;
     fence_mbarrier_init();
   }
   // pref[s] = number of used partitions before sequence s (lengths clamped to
@@ -747,9 +830,9 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
   if (warp == NC) {
     producer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, lane);
   } else if (warp == NC + 1) {
-    epilogue_loop<C, LY>(prm, smem, abort_flag, lane);
+    epilogue_loop<C, LY>(prm, smem, abort_flag, ch, lane);
   } else {
-    consumer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, warp, lane);
+    consumer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, ch, warp, lane);
   }
 }
 

@@ -77,6 +77,17 @@ def test_partition_size_invariance(P, variant):
     check_parity(q, kc, vc, bt, L, 0.09, P, variant, f"P={P}")
 
 
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+def test_long_sequences_two_level_combine(dt):
+    """Sequences of 63-94 partitions with 8 query heads per kv head and
+    head_size 256: combined per chunk of 16 partitions, then across chunks;
+    both steps are large enough to be shared between the warps of a CTA."""
+    lens = [1500, 700, 33, 1009]
+    q, kc, vc, bt, L = random_case(78, S=4, H=16, KH=2, D=256, BS=16, lens=lens, dtype=dt)
+    check_parity(q, kc, vc, bt, L, 1.0 / 16, 16, MMA, "two-level combine")
+    check_parity(q, kc, vc, bt, L, 1.0 / 16, 16, SIMT, "two-level combine, SIMT")
+
+
 @pytest.mark.parametrize("variant,G,BS", [(SIMT, 1, 16), (SIMT, 2, 32), (MMA, 4, 16), (MMA, 8, 32)])
 def test_needle_bitexact(variant, G, BS):
     """q = 8 e_0, K[t*][0] = 200 and K[t][0] = 0 elsewhere: the weight of t* is
