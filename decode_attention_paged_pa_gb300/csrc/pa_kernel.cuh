@@ -91,7 +91,8 @@ struct Layout {
   static constexpr uint32_t OFF_SCAN = al16(OFF_EF + (NC + 1) * C::GT * 4);
   static constexpr uint32_t OFF_INFO = al16(OFF_SCAN + THREADS * 4);
   static constexpr uint32_t OFF_EPI_INFO = al16(OFF_INFO + UQ * sizeof(UnitInfo));
-  static constexpr uint32_t OFF_BAR = al16(OFF_EPI_INFO + sizeof(UnitInfo));
+  static constexpr uint32_t OFF_JOBQ = al16(OFF_EPI_INFO + sizeof(UnitInfo));   // 16 combine jobs
+  static constexpr uint32_t OFF_BAR = al16(OFF_JOBQ + 16 * 32);
   static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 3;
   static constexpr uint32_t OFF_FLAGS = al16(OFF_BAR + NBAR * 8);
   static constexpr uint32_t OFF_PREF = al16(OFF_FLAGS + 64);
@@ -395,7 +396,7 @@ template <class C>
 __device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, int part, int nparts,
                                               int lane) {
   using T = typename C::T;
-  constexpr int D = C::D, D4 = D / 4;
+  constexpr int D = C::D, D4 = D / 4, G8 = 8;
   const float *sm, *sl, *so;
   int stride, first;
   if (J.kind == 2) {
@@ -408,28 +409,44 @@ __device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, 
     const int gh = idx / D4, d4 = idx - gh * D4;
     const size_t row = (size_t)J.s * prm.H + J.h0 + gh;
     const size_t base = row * stride + first;
-    float M = -INFINITY;
-    for (int i = 0; i < count; ++i) M = fmaxf(M, __ldcg(sm + base + i));
-    float tot = 0.f;
-    for (int i = 0; i < count; ++i) tot = fmaf(exp2f((__ldcg(sm + base + i) - M) * kLog2e), __ldcg(sl + base + i), tot);
-    const float inv = 1.f / tot;
     const float4* src = reinterpret_cast<const float4*>(so + base * D) + d4;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-    int i = 0;
-#pragma unroll 4
-    for (; i + 1 < count; i += 2) {
-      const float w0 = exp2f((__ldcg(sm + base + i) - M) * kLog2e) * __ldcg(sl + base + i) * inv;
-      const float w1 = exp2f((__ldcg(sm + base + i + 1) - M) * kLog2e) * __ldcg(sl + base + i + 1) * inv;
-      const float4 v0 = __ldcg(src + (size_t)i * D4), v1 = __ldcg(src + (size_t)(i + 1) * D4);
-      a.x = fmaf(w0, v0.x, a.x); a.y = fmaf(w0, v0.y, a.y); a.z = fmaf(w0, v0.z, a.z); a.w = fmaf(w0, v0.w, a.w);
-      b.x = fmaf(w1, v1.x, b.x); b.y = fmaf(w1, v1.y, b.y); b.z = fmaf(w1, v1.z, b.z); b.w = fmaf(w1, v1.w, b.w);
+    // One pass in groups of 8 states, all loads of a group in flight at once,
+    // with the running maximum rescaling the running sums.
+    float M = -INFINITY, tot = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < count; i0 += G8) {
+      float mv[G8], lv[G8];
+      float4 ov[G8];
+#pragma unroll
+      for (int j = 0; j < G8; ++j) {
+        if (i0 + j < count) {
+          mv[j] = __ldcg(sm + base + i0 + j);
+          lv[j] = __ldcg(sl + base + i0 + j);
+          ov[j] = __ldcg(src + (size_t)(i0 + j) * D4);
+        } else {
+          mv[j] = -INFINITY;
+          lv[j] = 0.f;
+          ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float gm = mv[0];
+#pragma unroll
+      for (int j = 1; j < G8; ++j) gm = fmaxf(gm, mv[j]);
+      const float Mn = fmaxf(M, gm);
+      const float sc = exp2f((M - Mn) * kLog2e);
+      tot *= sc;
+      acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+#pragma unroll
+      for (int j = 0; j < G8; ++j) {
+        const float w = exp2f((mv[j] - Mn) * kLog2e) * lv[j];
+        tot += w;
+        acc.x = fmaf(w, ov[j].x, acc.x); acc.y = fmaf(w, ov[j].y, acc.y);
+        acc.z = fmaf(w, ov[j].z, acc.z); acc.w = fmaf(w, ov[j].w, acc.w);
+      }
+      M = Mn;
     }
-    if (i < count) {
-      const float w0 = exp2f((__ldcg(sm + base + i) - M) * kLog2e) * __ldcg(sl + base + i) * inv;
-      const float4 v0 = __ldcg(src + (size_t)i * D4);
-      a.x = fmaf(w0, v0.x, a.x); a.y = fmaf(w0, v0.y, a.y); a.z = fmaf(w0, v0.z, a.z); a.w = fmaf(w0, v0.w, a.w);
-    }
-    const float4 r = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    const float inv = 1.f / tot;
+    const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     if (J.kind == 1) {
       reinterpret_cast<float4*>(prm.ws_co + (row * prm.Cmax + J.c) * D)[d4] = r;
       if (d4 == 0) {
@@ -492,35 +509,35 @@ __device__ __forceinline__ bool wait_handover(const KParams& prm, const JobChann
   }
 }
 
-// Epilogue warp: run job J, sharing it with the consumer warps if it is heavy
-// and they are still around to help.  A chunk job then takes the sequence
-// ticket; the last chunk of the sequence runs the final job.
+// Epilogue warp's combine-job engine.  Jobs are queued; a heavy job is posted
+// for the consumer warps, who take their shares at their next unit boundary,
+// while the epilogue warp takes its own share and goes back to merging
+// hand-overs.  Completion is polled; a completed chunk job (kind 1) then takes
+// the sequence ticket, and the last chunk's final job (kind 2) is started.
+// All members are warp-uniform; jobs live in a shared-memory ring.
 template <class C, class LY>
-__device__ __forceinline__ void run_job(const KParams& prm, Job J, const JobChannel& ch, int& nposted,
-                                        volatile int* abort_flag, int* err, int lane) {
-  constexpr int D4 = C::D / 4, NC = LY::NC;
-  while (true) {
-    const bool share = (long long)J.nh * D4 * job_count(J) > kShareJobLoads;
-    if (share) {
-      if (lane == 0) {
-        *ch.rec = J;
-        __threadfence_block();
-        *ch.posted = nposted + 1;
-      }
-      ++nposted;
-      combine_share<C>(prm, J, NC, NC + 1, lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ch.bar_done);
-      if (!__all_sync(0xffffffffu, wait_bounded(ch.bar_done, (nposted - 1) & 1, abort_flag, err,
-                                                prm.timeout_ns, kSiteJobDone, nposted)))
-        return;
-    } else {
-      combine_share<C>(prm, J, 0, 1, lane);
-      __syncwarp();
-    }
-    if (J.kind != 1) return;
-    // Chunk written (by all helpers: their arrivals on bar_done were observed
-    // above, so the release below covers their stores too).
+struct JobEngine {
+  static constexpr int JQ = 16;
+  const KParams& prm;
+  const JobChannel& ch;
+  Job* q;               // JQ slots
+  volatile int* abort_flag;
+  int* err;
+  int lane;
+  int head = 0, tail = 0, nposted = 0;
+  bool outstanding = false;
+  Job cur{};
+
+  __device__ __forceinline__ JobEngine(const KParams& p, const JobChannel& c, Job* qq, volatile int* ab,
+                                       int* e, int l)
+      : prm(p), ch(c), q(qq), abort_flag(ab), err(e), lane(l) {}
+
+  __device__ __forceinline__ bool heavy(const Job& J) const {
+    return (long long)J.nh * (C::D / 4) * job_count(J) > kShareJobLoads;
+  }
+
+  // Sequence-level ticket after a chunk job; true if it completed the sequence.
+  __device__ __forceinline__ bool chunk_done(const Job& J) {
     int last = 0;
     if (lane == 0) {
       int* tk = prm.tickets + (size_t)J.s * prm.n_hg + J.hg;
@@ -531,10 +548,74 @@ __device__ __forceinline__ void run_job(const KParams& prm, Job J, const JobChan
         fence_acq_rel_gpu();
       }
     }
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    J.kind = 2;
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
   }
-}
+
+  // Start J: post it (heavy, no job outstanding) or run it alone.
+  __device__ __forceinline__ void launch(Job J) {
+    while (true) {
+      if (heavy(J)) {
+        if (lane == 0) {
+          *ch.rec = J;
+          __threadfence_block();
+          *ch.posted = nposted + 1;
+        }
+        ++nposted;
+        combine_share<C>(prm, J, LY::NC, LY::NC + 1, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ch.bar_done);
+        outstanding = true;
+        cur = J;
+        return;
+      }
+      combine_share<C>(prm, J, 0, 1, lane);
+      __syncwarp();
+      if (J.kind != 1 || !chunk_done(J)) return;
+      J.kind = 2;
+    }
+  }
+
+  __device__ __forceinline__ void push(const Job& J) {
+    if (tail - head >= JQ) drain();  // never expected; keeps the ring bounded
+    if (lane == 0) q[tail % JQ] = J;
+    __syncwarp();
+    ++tail;
+  }
+
+  // Make progress without blocking (block = false) or until idle (block = true,
+  // each wait bounded).  Returns false once the CTA is aborting.
+  __device__ __forceinline__ bool poll(bool block) {
+    while (true) {
+      if (outstanding) {
+        const uint32_t par = (uint32_t)(nposted - 1) & 1u;
+        bool done = __all_sync(0xffffffffu, mbar_test_wait(ch.bar_done, par));
+        if (!done && block)
+          done = __all_sync(0xffffffffu, wait_bounded(ch.bar_done, par, abort_flag, err, prm.timeout_ns,
+                                                      kSiteJobDone, nposted));
+        if (!done) return !block && __all_sync(0xffffffffu, *abort_flag == 0);
+        outstanding = false;
+        // The helpers' arrivals were observed: their stores are ordered
+        // before the release in chunk_done.
+        if (cur.kind == 1 && chunk_done(cur)) {
+          Job J = cur;
+          J.kind = 2;
+          launch(J);
+          continue;
+        }
+      }
+      if (head == tail) return true;
+      const Job J = broadcast_job(q[head % JQ]);
+      ++head;
+      launch(J);
+    }
+  }
+
+  __device__ __forceinline__ bool drain() {
+    while (outstanding || head != tail)
+      if (!poll(true)) return false;
+    return true;
+  }
+};
 
 // Consumer warp: stream the blocks of every unit assigned to it and hand its
 // online-softmax state for each unit to the epilogue warp through shared
@@ -658,27 +739,49 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
   int* err = prm.hdr + kHdrError;
   const int H = prm.H, Pmax = prm.Pmax;
   T* out = static_cast<T*>(prm.out);
+  JobEngine<C, LY> jobs(prm, ch, reinterpret_cast<Job*>(smem + LY::OFF_JOBQ), abort_flag, err, lane);
 
   // Lane 0 only: a ticket taken and not yet checked, and its job.
   bool pend = false;
   int pend_t = 0;
   Job pinfo{};
-  int nposted = 0;
+  // Lane 0: if the pending ticket was the last of its group, its job (the
+  // acquire fence orders the other CTAs' partition states before it).
+  auto settle = [&]() -> int {
+    int go = 0;
+    if (lane == 0 && pend && pend_t == pinfo.cnt - 1) {
+      go = 1;
+      *ticket_of(prm, pinfo) = 0;
+      fence_acq_rel_gpu();
+    }
+    pend = false;
+    return __shfl_sync(0xffffffffu, go, 0);
+  };
+
   for (uint32_t k = 0;; ++k) {
-    const bool ok = __all_sync(0xffffffffu, wait_bounded(bar_efull, k & 1u, abort_flag, err,
-                                                         prm.timeout_ns, kSiteEpiFull, (int)k));
-    if (!ok) return;  // aborted: the results are abandoned
+    // Wait for hand-over k, advancing combine jobs meanwhile.
+    bool ok = __all_sync(0xffffffffu, mbar_test_wait(bar_efull, k & 1u));
+    if (!ok) {
+      const uint64_t t0 = global_timer_ns();
+      while (!ok) {
+        if (!jobs.poll(false)) return;
+        ok = __all_sync(0xffffffffu, mbar_test_wait(bar_efull, k & 1u));
+        if (ok) break;
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) return;
+        if ((long long)(global_timer_ns() - t0) > prm.timeout_ns) {
+          if (lane == 0) record_timeout(abort_flag, err, kSiteEpiFull, (int)k);
+          return;
+        }
+        __nanosleep(32);
+      }
+    }
     const UnitInfo I = *epi_info;
     if (I.s < 0) {
-      // End of work: settle the last ticket, then release the helpers.
-      int last = 0;
-      if (lane == 0 && pend && pend_t == pinfo.cnt - 1) {
-        last = 1;
-        *ticket_of(prm, pinfo) = 0;
-        fence_acq_rel_gpu();
-      }
+      // End of work: settle the last ticket, finish every job (the consumer
+      // warps are waiting to help), then release them.
       const Job R = broadcast_job(pinfo);  // pinfo is kept by lane 0 only
-      if (__shfl_sync(0xffffffffu, last, 0)) run_job<C, LY>(prm, R, ch, nposted, abort_flag, err, lane);
+      if (settle()) jobs.push(R);
+      jobs.drain();
       if (lane == 0) *ch.finished = 1;
       return;
     }
@@ -731,14 +834,9 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
 
     // Settle the previous ticket; take this unit's (release: the warp's
     // partition stores above, ordered by __syncwarp, become visible first).
-    int go = 0;
-    Job job = pinfo;
+    const Job R = broadcast_job(pinfo);
+    const int go = settle();
     if (lane == 0) {
-      if (pend && pend_t == pinfo.cnt - 1) {
-        go = 1;
-        *ticket_of(prm, pinfo) = 0;
-        fence_acq_rel_gpu();
-      }
       pend = !single;
       if (pend) {
         pinfo.s = I.s; pinfo.hg = I.hg; pinfo.h0 = I.h0; pinfo.nh = I.nh; pinfo.np = I.np;
@@ -750,8 +848,8 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
         pend_t = atomic_add_release_gpu(ticket_of(prm, pinfo), 1);
       }
     }
-    const Job R = broadcast_job(job);  // pinfo is kept by lane 0 only
-    if (__shfl_sync(0xffffffffu, go, 0)) run_job<C, LY>(prm, R, ch, nposted, abort_flag, err, lane);
+    if (go) jobs.push(R);
+    if (!jobs.poll(false)) return;
   }
 }
 
