@@ -396,7 +396,8 @@ template <class C>
 __device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, int part, int nparts,
                                               int lane) {
   using T = typename C::T;
-  constexpr int D = C::D, D4 = D / 4, G8 = 8;
+  // States per round of loads (fewer where registers are tight).
+  constexpr int D = C::D, D4 = D / 4, G8 = (C::kMma && D >= 256) ? 8 : 16;
   const float *sm, *sl, *so;
   int stride, first;
   if (J.kind == 2) {
