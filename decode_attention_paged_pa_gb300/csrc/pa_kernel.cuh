@@ -91,9 +91,10 @@ struct Layout {
   static constexpr uint32_t OFF_SCAN = al16(OFF_EF + (NC + 1) * C::GT * 4);
   static constexpr uint32_t OFF_INFO = al16(OFF_SCAN + THREADS * 4);
   static constexpr uint32_t OFF_EPI_INFO = al16(OFF_INFO + UQ * sizeof(UnitInfo));
-  static constexpr uint32_t OFF_JOBQ = al16(OFF_EPI_INFO + sizeof(UnitInfo));   // 16 combine jobs
-  static constexpr uint32_t OFF_BAR = al16(OFF_JOBQ + 16 * 32);
-  static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 3;
+  static constexpr uint32_t OFF_JOBQ = al16(OFF_EPI_INFO + sizeof(UnitInfo));   // 16 queued jobs
+  static constexpr uint32_t OFF_JOBREC = al16(OFF_JOBQ + 16 * 32);               // posted-job slots
+  static constexpr uint32_t OFF_BAR = al16(OFF_JOBREC + 8 * 32);
+  static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 2 + 8;
   static constexpr uint32_t OFF_FLAGS = al16(OFF_BAR + NBAR * 8);
   static constexpr uint32_t OFF_PREF = al16(OFF_FLAGS + 64);
   static constexpr uint32_t FIXED = OFF_PREF;
@@ -358,8 +359,9 @@ struct Job {
 };
 static_assert(sizeof(Job) <= 48, "combine job must fit in the shared flag area");
 
-// Jobs that read more float4 values than this are shared with the consumer
-// warps; smaller ones are done by the epilogue warp alone.
+// Jobs that read more float4 values than this (or have more output columns
+// than the epilogue warp has lanes) are shared with the consumer warps;
+// smaller ones are done by the epilogue warp alone.
 #ifndef PA_SHARE_JOB_LOADS
 #define PA_SHARE_JOB_LOADS 512
 #endif
@@ -464,26 +466,30 @@ __device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, 
 }
 
 // Shared state of the job protocol between the epilogue warp (which posts
-// jobs) and the consumer warps (which help with heavy ones at their unit
-// boundaries).
+// jobs) and the consumer warps (which help with heavy ones).  Up to kJobSlots
+// posted jobs can be in flight; job i uses slot i % kJobSlots: its record and
+// an mbarrier that completes when all NC + 1 warps have taken their share.
+constexpr int kJobSlots = 4;
 struct JobChannel {
   volatile int* posted;    // number of jobs posted for help
   volatile int* finished;  // set once the epilogue warp posts no more jobs
-  Job* rec;                // the posted job
-  uint32_t bar_done;       // mbarrier: NC + 1 arrivals per job
+  Job* rec;                // kJobSlots records
+  uint32_t bar_done;       // kJobSlots mbarriers (8 bytes apart)
 };
 
-// A consumer warp's help with the posted job, if there is a new one.
+// A consumer warp's help with every posted job it has not taken yet.
 template <class C, class LY>
 __device__ __forceinline__ void help_with_job(const KParams& prm, const JobChannel& ch, int& seen, int warp,
                                               int lane) {
   // Lane 0's reading decides for the whole warp.
-  if (__shfl_sync(0xffffffffu, *ch.posted, 0) > seen) {
+  const int posted = __shfl_sync(0xffffffffu, *ch.posted, 0);
+  while (seen < posted) {
     __threadfence_block();
-    const Job J = *ch.rec;
+    const int slot = seen % kJobSlots;
+    const Job J = ch.rec[slot];
     combine_share<C>(prm, J, warp, LY::NC + 1, lane);
     __syncwarp();
-    if (lane == 0) mbar_arrive(ch.bar_done);
+    if (lane == 0) mbar_arrive(ch.bar_done + 8 * slot);
     ++seen;
   }
 }
@@ -511,11 +517,12 @@ __device__ __forceinline__ bool wait_handover(const KParams& prm, const JobChann
 }
 
 // Epilogue warp's combine-job engine.  Jobs are queued; a heavy job is posted
-// for the consumer warps, who take their shares at their next unit boundary,
-// while the epilogue warp takes its own share and goes back to merging
-// hand-overs.  Completion is polled; a completed chunk job (kind 1) then takes
-// the sequence ticket, and the last chunk's final job (kind 2) is started.
-// All members are warp-uniform; jobs live in a shared-memory ring.
+// for the consumer warps (up to kJobSlots in flight), who take their shares at
+// their next unit boundary, while the epilogue warp takes its own share and
+// goes back to merging hand-overs.  Completion is polled in posting order; a
+// completed chunk job (kind 1) then takes the sequence ticket, and the last
+// chunk's final job (kind 2) is queued.  All members are warp-uniform; queued
+// jobs live in a shared-memory ring.
 template <class C, class LY>
 struct JobEngine {
   static constexpr int JQ = 16;
@@ -525,16 +532,19 @@ struct JobEngine {
   volatile int* abort_flag;
   int* err;
   int lane;
-  int head = 0, tail = 0, nposted = 0;
-  bool outstanding = false;
-  Job cur{};
+  int head = 0, tail = 0;       // queued jobs
+  int nposted = 0, ndone = 0;   // posted jobs, and those completed (in order)
 
   __device__ __forceinline__ JobEngine(const KParams& p, const JobChannel& c, Job* qq, volatile int* ab,
                                        int* e, int l)
       : prm(p), ch(c), q(qq), abort_flag(ab), err(e), lane(l) {}
 
+  // Shared if it is large, or if the epilogue warp alone would need more than
+  // one output column per lane (columns are combined one after another, each
+  // a round trip to L2).
   __device__ __forceinline__ bool heavy(const Job& J) const {
-    return (long long)J.nh * (C::D / 4) * job_count(J) > kShareJobLoads;
+    const int columns = J.nh * (C::D / 4);
+    return columns > 32 || (long long)columns * job_count(J) > kShareJobLoads;
   }
 
   // Sequence-level ticket after a chunk job; true if it completed the sequence.
@@ -552,23 +562,9 @@ struct JobEngine {
     return __shfl_sync(0xffffffffu, last, 0) != 0;
   }
 
-  // Start J: post it (heavy, no job outstanding) or run it alone.
-  __device__ __forceinline__ void launch(Job J) {
+  // Run J alone, now (and its follow-up).
+  __device__ __forceinline__ void run_alone(Job J) {
     while (true) {
-      if (heavy(J)) {
-        if (lane == 0) {
-          *ch.rec = J;
-          __threadfence_block();
-          *ch.posted = nposted + 1;
-        }
-        ++nposted;
-        combine_share<C>(prm, J, LY::NC, LY::NC + 1, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ch.bar_done);
-        outstanding = true;
-        cur = J;
-        return;
-      }
       combine_share<C>(prm, J, 0, 1, lane);
       __syncwarp();
       if (J.kind != 1 || !chunk_done(J)) return;
@@ -577,42 +573,73 @@ struct JobEngine {
   }
 
   __device__ __forceinline__ void push(const Job& J) {
-    if (tail - head >= JQ) drain();  // never expected; keeps the ring bounded
+    if (tail - head >= JQ) {  // queue full (not expected): no waiting, just do it
+      run_alone(J);
+      return;
+    }
     if (lane == 0) q[tail % JQ] = J;
     __syncwarp();
     ++tail;
+  }
+
+  // Start J: post it (heavy; the caller guarantees a free slot) or run it alone.
+  __device__ __forceinline__ void launch(const Job& J) {
+    {
+      if (heavy(J)) {
+        const int slot = nposted % kJobSlots;
+        if (lane == 0) {
+          ch.rec[slot] = J;
+          __threadfence_block();
+          *ch.posted = nposted + 1;
+        }
+        ++nposted;
+        combine_share<C>(prm, J, LY::NC, LY::NC + 1, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ch.bar_done + 8 * slot);
+        return;
+      }
+      run_alone(J);
+      return;
+    }
   }
 
   // Make progress without blocking (block = false) or until idle (block = true,
   // each wait bounded).  Returns false once the CTA is aborting.
   __device__ __forceinline__ bool poll(bool block) {
     while (true) {
-      if (outstanding) {
-        const uint32_t par = (uint32_t)(nposted - 1) & 1u;
-        bool done = __all_sync(0xffffffffu, mbar_test_wait(ch.bar_done, par));
+      while (ndone < nposted) {
+        const int slot = ndone % kJobSlots;
+        const uint32_t par = (uint32_t)(ndone / kJobSlots) & 1u;
+        const uint32_t bar = ch.bar_done + 8 * slot;
+        bool done = __all_sync(0xffffffffu, mbar_test_wait(bar, par));
         if (!done && block)
-          done = __all_sync(0xffffffffu, wait_bounded(ch.bar_done, par, abort_flag, err, prm.timeout_ns,
-                                                      kSiteJobDone, nposted));
-        if (!done) return !block && __all_sync(0xffffffffu, *abort_flag == 0);
-        outstanding = false;
-        // The helpers' arrivals were observed: their stores are ordered
+          done = __all_sync(0xffffffffu, wait_bounded(bar, par, abort_flag, err, prm.timeout_ns,
+                                                      kSiteJobDone, ndone));
+        if (!done) break;
+        // Every helper's arrival was observed: their stores are ordered
         // before the release in chunk_done.
-        if (cur.kind == 1 && chunk_done(cur)) {
-          Job J = cur;
+        Job J = broadcast_job(ch.rec[slot]);
+        ++ndone;
+        if (J.kind == 1 && chunk_done(J)) {
           J.kind = 2;
-          launch(J);
-          continue;
+          push(J);
         }
       }
-      if (head == tail) return true;
-      const Job J = broadcast_job(q[head % JQ]);
-      ++head;
-      launch(J);
+      if (block && ndone < nposted) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+        continue;  // the bounded wait above gave up: loop re-checks the flag
+      }
+      while (head != tail && nposted - ndone < kJobSlots) {
+        const Job J = broadcast_job(q[head % JQ]);
+        ++head;
+        launch(J);
+      }
+      if (!block || (ndone == nposted && head == tail)) return __all_sync(0xffffffffu, *abort_flag == 0);
     }
   }
 
   __device__ __forceinline__ bool drain() {
-    while (outstanding || head != tail)
+    while (ndone < nposted || head != tail)
       if (!poll(true)) return false;
     return true;
   }
@@ -867,7 +894,7 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
   JobChannel ch;
   ch.posted = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 4);
   ch.finished = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 12);
-  ch.rec = reinterpret_cast<Job*>(smem + LY::OFF_FLAGS + 16);
+  ch.rec = reinterpret_cast<Job*>(smem + LY::OFF_JOBREC);
   ch.bar_done = sbase + LY::OFF_BAR + 8 * (2 * NS + 2 * UQ + 2);
   int* pref = reinterpret_cast<int*>(smem + LY::OFF_PREF);
   int* scan = reinterpret_cast<int*>(smem + LY::OFF_SCAN);
@@ -885,7 +912,8 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     }
     mbar_init(bar + 8 * (2 * NS + 2 * UQ), NC);     // hand-over full: every consumer warp
     mbar_init(bar + 8 * (2 * NS + 2 * UQ + 1), 1);  // hand-over empty: the epilogue warp
-    mbar_init(bar + 8 * (2 * NS + 2 * UQ + 2), NC + 1);  // shared combine job done: all helpers
+    for (int i = 0; i < kJobSlots; ++i)
+      mbar_init(bar + 8 * (2 * NS + 2 * UQ + 2 + i), NC + 1);  // shared combine job done: all helpers
     *abort_flag = 0;
     *issued = 0;
     *ch.posted = 0;
