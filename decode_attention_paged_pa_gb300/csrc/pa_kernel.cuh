@@ -205,6 +205,7 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
 
   uint32_t g = 0;   // blocks whose copies are issued, in order
   uint32_t kq = 0;  // units published (the end marker included)
+  uint32_t reissued = 0;  // after an abort inside a batch: lanes whose block g + lane was issued
   bool ok = true;
 
   // Publish unit U (or, if !have, the end marker) into the next queue slot:
@@ -268,6 +269,10 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
       const int b32 = (c0 == 0) ? bids : load_block_id<C>(prm, U, c0, lane);
       const int cend = min(c0 + 32, U.nb);
       for (int jb = c0; jb < cend && ok; jb += BATCH) {
+        if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) {
+          ok = false;
+          break;
+        }
         const int cnt = min(BATCH, cend - jb);
         const int bi = __shfl_sync(0xffffffffu, b32, (jb - c0) + (lane < cnt ? lane : 0));
         // Lanes < cnt issue block g + lane once its stage is free; the
@@ -315,7 +320,7 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
               while (!mbar_try_wait(bar_full + 8 * st, ph) && (long long)(global_timer_ns() - t0) < 100000000LL) {
               }
             }
-            __syncwarp();
+            reissued = __ballot_sync(0xffffffffu, done && lane < cnt);
             break;
           }
         }
@@ -327,14 +332,18 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     bids = bids_next;
     have = have_next;
   }
-  if (!ok && lane == 0) {
-    // Aborted: let copies that may still be in flight (the last NSTAGE
-    // blocks and the last UQ query rows issued) land before the CTA exits.
-    // Each wait is bounded (100 ms, independent of the caller's timeout,
-    // which may be tiny) and ignores the abort flag.
+  if (lane == 0) {
+    // Let copies that may still be in flight (the last NSTAGE blocks and the
+    // last UQ query rows issued) land before this warp exits, so that the CTA
+    // never ends with a copy outstanding, whatever the consumer warps did.
+    // (Without an abort they have landed already.)  Each wait is bounded
+    // (100 ms, independent of the caller's timeout, which may be tiny) and
+    // ignores the abort flag.
     const uint32_t hi = g;
     const long long drain_ns = 100000000LL;
     for (uint32_t i = (hi > (uint32_t)NS ? hi - NS : 0u); i < hi; ++i) {
+      // A stage taken over by block i + NS of an aborted batch was waited for there.
+      if ((reissued >> (i + NS - hi)) & 1u) continue;
       const uint32_t bar = bar_full + 8 * stage_of<LY>(i), ph = phase_of<LY>(i);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(bar, ph) && (long long)(global_timer_ns() - t0) < drain_ns) {}
@@ -488,6 +497,10 @@ __device__ __forceinline__ void help_with_job(const KParams& prm, const JobChann
     const int slot = seen % kJobSlots;
     const Job J = ch.rec[slot];
     combine_share<C>(prm, J, warp, LY::NC + 1, lane);
+    // A chunk state is read by another CTA once the epilogue warp has retired
+    // this job and released the sequence ticket: every lane's stores must be
+    // visible GPU-wide before this warp counts its share done.
+    if (J.kind == 1) fence_acq_rel_gpu();
     __syncwarp();
     if (lane == 0) mbar_arrive(ch.bar_done + 8 * slot);
     ++seen;
@@ -566,6 +579,7 @@ struct JobEngine {
   __device__ __forceinline__ void run_alone(Job J) {
     while (true) {
       combine_share<C>(prm, J, 0, 1, lane);
+      if (J.kind == 1) fence_acq_rel_gpu();  // every lane's chunk state, before the ticket
       __syncwarp();
       if (J.kind != 1 || !chunk_done(J)) return;
       J.kind = 2;
@@ -594,6 +608,7 @@ struct JobEngine {
         }
         ++nposted;
         combine_share<C>(prm, J, LY::NC, LY::NC + 1, lane);
+        if (J.kind == 1) fence_acq_rel_gpu();  // every lane's chunk state, before the ticket
         __syncwarp();
         if (lane == 0) mbar_arrive(ch.bar_done + 8 * slot);
         return;
@@ -721,6 +736,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
                     prm.scale_log2, lane);
+    fence_proxy_async_smem();  // the query slot is refilled by a bulk copy: same ordering as a stage
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_uempty + 8 * slot);
 
@@ -728,12 +744,21 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
       const uint32_t gj = g + j, st = stage_of<LY>(gj), ph = phase_of<LY>(gj);
       bool okb = wait_issued(issued, gj + 1, abort_flag, err, prm.timeout_ns) &&
                  wait_bounded(bar_full + 8 * st, ph, abort_flag, err, prm.timeout_ns, kSiteFull, (int)gj);
-      okb = __all_sync(0xffffffffu, okb);
+      // A stage whose copy this warp has not seen land is never released:
+      // on a failed wait the warp stops (the producer sees the abort and
+      // waits for its copies before the CTA exits).
+      if (!__all_sync(0xffffffffu, okb)) break;
       const int ntok = min(BS, I.t1 - I.t0 - j * BS);
-      if (okb) cons.block(smem + st * LY::STAGE, smem + st * LY::STAGE + LY::KBYTES, ntok, lane, scr);
+      cons.block(smem + st * LY::STAGE, smem + st * LY::STAGE + LY::KBYTES, ntok, lane, scr);
+      // The stage is refilled by a bulk copy (async proxy) once released:
+      // every lane's reads of it (generic proxy) are ordered before that
+      // write by a proxy fence, or the copy can land under reads still
+      // queued (the last V tile read stale data without it).
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * st);
     }
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
     g += I.nb;
 
     // Hand this warp's state for unit k to the epilogue warp, once it has

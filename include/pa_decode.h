@@ -113,7 +113,9 @@ int pa_decode_v2_workspace_layout(int num_seqs, int num_heads, int num_kv_heads,
  *   num_blocks   number of physical blocks in each cache (bounds checks)
  *   workspace    device buffer of >= pa_decode_v2_workspace_bytes() bytes,
  *                16-byte aligned; NULL makes the call allocate and free one
- *                stream-ordered (cudaMallocAsync / cudaFreeAsync)
+ *                stream-ordered (cudaMallocAsync / cudaFreeAsync).  Its
+ *                contents on entry do not matter: the call writes every byte
+ *                of it that it reads.
  * out, query and the caches must be 16-byte aligned; tables 4-byte aligned.
  */
 int pa_decode_v2(void* out, const void* query, const void* key_cache, const void* value_cache,

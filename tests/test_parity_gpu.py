@@ -251,6 +251,39 @@ def test_more_than_1024_partitions():
     check_parity(q, kc, vc, bt, lens, 0.125, 512, what="1172 partitions")
 
 
+def test_poisoned_workspace_two_level_combine():
+    """The workspace's contents on entry do not matter.  It is filled with 0x7f
+    bytes (3.4e38 as f32) before each of 20 calls on the long-context
+    batch (one sequence of 131072 tokens = 256 partitions, combined in 16
+    chunks of 16, eight heads per group): a partition or chunk state read
+    before this call wrote it shows up as a wrong or non-finite output, or as
+    a difference between calls (as does a ring stage refilled under reads
+    still in flight, which corrupts single accumulator tiles)."""
+    w = workloads.WORKLOADS["long_skew_bf16"]
+    inp = workloads.make_inputs(w, device="cuda")
+    need = binding.workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_size,
+                                   w.max_blocks_per_seq, w.block_size, w.partition_size)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(20):
+        ws.fill_(0x7F)
+        out = torch.full_like(inp["query"], float("nan"))
+        binding.pa_decode_v2(out, inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
+                             inp["seq_lens"], inp["scale"], partition_size=w.partition_size, workspace=ws)
+        assert binding.device_status(ws) == binding.PA_OK
+        assert torch.isfinite(out.float()).all()
+        outs.append(out)
+    for i, o in enumerate(outs[1:], 1):
+        assert torch.equal(o, outs[0]), f"call {i} differs from call 0"
+    seqs = [0, 1]   # 256 and 32 partitions: both combined in two levels
+    sub = compact_sequences(inp, seqs)
+    ref = oracle.decode(*sub, inp["scale"], workloads.DTYPE_CODES[w.dtype])
+    ok, worst = within_tolerance(outs[0][torch.tensor(seqs, device="cuda")].cpu().double().numpy(), ref)
+    assert ok, f"worst excess {worst:.3e}"
+    del inp, outs, ws
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("variant", [binding.PA_VARIANT_AUTO, SIMT, MMA], ids=["auto", "simt", "mma"])
 @pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER)
 def test_workload_sampled_parity(name, variant):
