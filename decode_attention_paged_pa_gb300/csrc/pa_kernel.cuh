@@ -236,14 +236,13 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     return okp;
   };
 
-  // The work counter is read two units ahead: while unit k streams, unit k+1
-  // is already planned and published and the index of unit k+2 is in flight,
-  // so neither the atomic nor the block-table loads stall the stream.
-  int u_cur = 0, u_req = 0;
-  if (lane == 0) {
-    u_cur = atomicAdd(prm.hdr + kHdrWork, 1);
-    u_req = atomicAdd(prm.hdr + kHdrWork, 1);
-  }
+  // The work counter is read one unit ahead: the next unit is claimed when
+  // unit k starts streaming, and planned and published once k's first batch
+  // of copies is issued (the atomic has returned by then).  A CTA thus holds
+  // at most the unit it streams and the next one, which keeps the end of the
+  // work even across CTAs.
+  int u_cur = 0;
+  if (lane == 0) u_cur = atomicAdd(prm.hdr + kHdrWork, 1);
   u_cur = __shfl_sync(0xffffffffu, u_cur, 0);
   bool have = u_cur < total;
   UnitPlan U{};
@@ -254,21 +253,29 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   }
   ok = publish(U, have);
   while (have && ok) {
-    const int u_nx = __shfl_sync(0xffffffffu, u_req, 0);
-    const bool have_next = u_nx < total;
+    int u_req = 0;
+    if (lane == 0) u_req = atomicAdd(prm.hdr + kHdrWork, 1);
+    bool have_next = false, published_next = false;
     UnitPlan Un{};
     int bids_next = 0;
-    if (have_next) {
-      Un = plan_unit<C>(prm, pref, u_nx);
-      bids_next = load_block_id<C>(prm, Un, 0, lane);
-      if (lane == 0) u_req = atomicAdd(prm.hdr + kHdrWork, 1);
-    }
-    ok = publish(Un, have_next);
-    if (!ok) break;
+    auto publish_next = [&]() {
+      const int u_nx = __shfl_sync(0xffffffffu, u_req, 0);
+      have_next = u_nx < total;
+      if (have_next) {
+        Un = plan_unit<C>(prm, pref, u_nx);
+        bids_next = load_block_id<C>(prm, Un, 0, lane);
+      }
+      ok = publish(Un, have_next);
+      published_next = true;
+    };
     for (int c0 = 0; c0 < U.nb && ok; c0 += 32) {
       const int b32 = (c0 == 0) ? bids : load_block_id<C>(prm, U, c0, lane);
       const int cend = min(c0 + 32, U.nb);
       for (int jb = c0; jb < cend && ok; jb += BATCH) {
+        if (jb > 0 && !published_next) {
+          publish_next();
+          if (!ok) break;
+        }
         if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) {
           ok = false;
           break;
@@ -328,6 +335,7 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
         g += cnt;
       }
     }
+    if (ok && !published_next) publish_next();
     U = Un;
     bids = bids_next;
     have = have_next;
