@@ -494,6 +494,17 @@ struct JobChannel {
   uint32_t bar_done;       // kJobSlots mbarriers (8 bytes apart)
 };
 
+#ifndef PA_SETTLE_WHEN_IDLE
+#define PA_SETTLE_WHEN_IDLE 1
+#endif
+constexpr bool kSettleWhenIdle = PA_SETTLE_WHEN_IDLE != 0;
+// Consumer warps of the tensor-core kernel (several heads per unit, so
+// combine jobs are shared) also look for posted jobs before every block.
+#ifndef PA_MMA_HELP_PER_BLOCK
+#define PA_MMA_HELP_PER_BLOCK 1
+#endif
+constexpr bool kMmaHelpPerBlock = PA_MMA_HELP_PER_BLOCK != 0;
+
 // A consumer warp's help with every posted job it has not taken yet.
 template <class C, class LY>
 __device__ __forceinline__ void help_with_job(const KParams& prm, const JobChannel& ch, int& seen, int warp,
@@ -513,6 +524,12 @@ __device__ __forceinline__ void help_with_job(const KParams& prm, const JobChann
     if (lane == 0) mbar_arrive(ch.bar_done + 8 * slot);
     ++seen;
   }
+}
+
+template <class C, class LY>
+__device__ __noinline__ void help_with_job_out_of_line(const KParams& prm, const JobChannel& ch, int& seen,
+                                                       int warp, int lane) {
+  help_with_job<C, LY>(prm, ch, seen, warp, lane);
 }
 
 // Consumer warp: wait (bounded) for the hand-over slot to be free for
@@ -749,6 +766,9 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     if (lane == 0) mbar_arrive(bar_uempty + 8 * slot);
 
     for (int j = warp; j < I.nb; j += NC) {
+      if constexpr (C::kMma && kMmaHelpPerBlock) {
+        if (__shfl_sync(0xffffffffu, *ch.posted, 0) > seen) help_with_job<C, LY>(prm, ch, seen, warp, lane);
+      }
       const uint32_t gj = g + j, st = stage_of<LY>(gj), ph = phase_of<LY>(gj);
       bool okb = wait_issued(issued, gj + 1, abort_flag, err, prm.timeout_ns) &&
                  wait_bounded(bar_full + 8 * st, ph, abort_flag, err, prm.timeout_ns, kSiteFull, (int)gj);
@@ -823,6 +843,12 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
     // Wait for hand-over k, advancing combine jobs meanwhile.
     bool ok = __all_sync(0xffffffffu, mbar_test_wait(bar_efull, k & 1u));
     if (!ok) {
+      // Idle: settle the pending ticket now rather than at the next merge
+      // (its atomic has long returned), so a job it completes starts early.
+      if (kSettleWhenIdle) {
+        const Job R = broadcast_job(pinfo);
+        if (settle()) jobs.push(R);
+      }
       const uint64_t t0 = global_timer_ns();
       while (!ok) {
         if (!jobs.poll(false)) return;

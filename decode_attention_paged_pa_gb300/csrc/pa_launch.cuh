@@ -13,6 +13,14 @@ namespace pa {
 #define PA_CTAS_PER_SM 1
 #endif
 constexpr int kConsumerWarps = PA_CONSUMER_WARPS;
+// The tensor-core kernel's consumer warps: six (eight warps in all) leave
+// each thread up to 255 registers (ten warps cap it at 168 by the SM
+// sub-partitions' register files) and shrink the hand-over buffer, which
+// lengthens the ring.
+#ifndef PA_MMA_CONSUMER_WARPS
+#define PA_MMA_CONSUMER_WARPS 6
+#endif
+constexpr int kMmaConsumerWarps = PA_MMA_CONSUMER_WARPS;
 constexpr int kCtasPerSm = PA_CTAS_PER_SM;
 
 // Shared memory per CTA: the SM's 228 KB less 1 KB reserved per CTA.

@@ -10,7 +10,10 @@ namespace pa {
 
 // Sequences per launch: the kernel keeps a prefix sum of partitions per
 // sequence in shared memory; longer batches are split into several launches.
-constexpr int kMaxSeqsPerLaunch = 2048;
+#ifndef PA_MAX_SEQS_PER_LAUNCH
+#define PA_MAX_SEQS_PER_LAUNCH 1024
+#endif
+constexpr int kMaxSeqsPerLaunch = PA_MAX_SEQS_PER_LAUNCH;
 
 // Partitions per combine chunk: sequences with more partitions are combined
 // in two levels (chunks of partitions, then the chunk states).
