@@ -16,7 +16,12 @@ definition in ``pa_oracle.c``:
                          reaches);
 * :func:`partitions`  -- per-partition (m_p, l_p, o_p), the phase-1 outputs,
                          with the unused-partition sentinels (-inf, 0);
-* :func:`combine`     -- the phase-2 log-sum-exp combine of those states.
+* :func:`combine`     -- the phase-2 log-sum-exp combine of those states;
+* :func:`lse`         -- log-sum-exp of each (sequence, head)'s scaled scores,
+                         the value the forward kernel of the page
+                         "flash_attention.metal -- Flash Attention Metal Shaders"
+                         stores beside its output (max plus log of the sum);
+* :func:`combine_lse` -- the same from phase-1 states (M + log total).
 
 Inputs are the raw 16-bit patterns of fp16 / bf16 tensors (numpy ``uint16``)
 in the page's layouts; the fp32 ``scale`` is widened to double exactly.
@@ -67,6 +72,10 @@ def _declare(lib):
     lib.pa_oracle_partitions.restype = c_int
     lib.pa_oracle_combine.argtypes = [dp, dp, dp, dp, ip] + [c_int] * 5
     lib.pa_oracle_combine.restype = c_int
+    lib.pa_oracle_lse.argtypes = [dp, up, up, ip, ip, c_double] + [c_int] * 8
+    lib.pa_oracle_lse.restype = c_int
+    lib.pa_oracle_combine_lse.argtypes = [dp, dp, dp, ip] + [c_int] * 4
+    lib.pa_oracle_combine_lse.restype = c_int
     lib.pa_oracle_max_threads.argtypes = []
     lib.pa_oracle_max_threads.restype = c_int
     return lib
@@ -190,6 +199,36 @@ class Oracle:
         return out
 
 
+    def lse(self, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+            dtype: int, nthreads: int = 0) -> np.ndarray:
+        """fp64 log-sum-exp of scale * q . K^T over each sequence's tokens; [S, H] (-inf if empty)."""
+        q, kc, vc = _u16(query), _u16(key_cache), _u16(value_cache)
+        bt, lens = _i32(block_tables), _i32(seq_lens)
+        S, H, KH, D, BS, MB = _shapes(q, kc, vc, bt)
+        out = np.zeros((S, H), dtype=np.float64)
+        rc = self.lib.pa_oracle_lse(
+            _ptr(out, ctypes.c_double), _ptr(q, ctypes.c_uint16), _ptr(kc, ctypes.c_uint16),
+            _ptr(bt, ctypes.c_int32), _ptr(lens, ctypes.c_int32), float(np.float32(scale)),
+            S, H, KH, D, BS, MB, dtype, nthreads)
+        if rc != 0:
+            raise ValueError("oracle lse rejected its arguments")
+        return out
+
+    def combine_lse(self, m, l, seq_lens, partition_size: int) -> np.ndarray:
+        """Log-sum-exp from phase-1 states (M + log total); [S, H] float64."""
+        m = np.ascontiguousarray(m, dtype=np.float64)
+        l = np.ascontiguousarray(l, dtype=np.float64)
+        lens = _i32(seq_lens)
+        S, H, Pm = m.shape
+        out = np.zeros((S, H), dtype=np.float64)
+        rc = self.lib.pa_oracle_combine_lse(
+            _ptr(out, ctypes.c_double), _ptr(m, ctypes.c_double), _ptr(l, ctypes.c_double),
+            _ptr(lens, ctypes.c_int32), S, H, int(partition_size), Pm)
+        if rc != 0:
+            raise ValueError("oracle combine_lse rejected its arguments")
+        return out
+
+
 _default = None
 
 
@@ -210,3 +249,11 @@ def partitions(*args, **kwargs):
 
 def combine(*args, **kwargs) -> np.ndarray:
     return default().combine(*args, **kwargs)
+
+
+def lse(*args, **kwargs) -> np.ndarray:
+    return default().lse(*args, **kwargs)
+
+
+def combine_lse(*args, **kwargs) -> np.ndarray:
+    return default().combine_lse(*args, **kwargs)

@@ -232,3 +232,62 @@ int pa_oracle_combine(double* out, const double* m, const double* l, const doubl
     }
     return bad ? -1 : 0;
 }
+
+/* Log-sum-exp of the scaled scores of each (s, h) over its seq_lens[s] tokens,
+ * in natural-log units:  lse = mu + log(sum_t exp(z_t - mu)),  mu = max_t z_t.
+ * This is the value the forward kernel of [FA-MTL] stores beside its output
+ * (its running maximum plus the log of its running sum, "log-sum-exp for
+ * backward pass"); outputs computed over disjoint token sets merge with it.
+ * seq_lens[s] == 0 gives -inf (the running maximum never leaves -inf there).
+ * lse is [S, H].  Returns 0, or -1 on a bad argument or allocation failure. */
+int pa_oracle_lse(double* lse, const uint16_t* q, const uint16_t* kc, const int32_t* bt,
+                  const int32_t* lens, double scale, int S, int H, int KH, int D, int BS, int MB,
+                  int dtype, int nthreads) {
+    if (S < 0 || H <= 0 || KH <= 0 || H % KH || D <= 0 || D % 8 || BS <= 0 || MB < 0)
+        return -1;
+    int bad = 0;
+    if (nthreads <= 0) nthreads = pa_oracle_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : bad)
+    for (long sh = 0; sh < (long)S * H; ++sh) {
+        int s = (int)(sh / H), h = (int)(sh % H);
+        int L = lens[s];
+        lse[sh] = -INFINITY;
+        if (L <= 0) continue;
+        if (L > MB * BS) { bad = 1; continue; }
+        double* z = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!z) { bad = 1; continue; }
+        scores_fp64(z, 0, L, s, h, q, kc, bt, scale, H, KH, D, BS, MB, dtype);
+        double mu = -INFINITY;
+        for (int t = 0; t < L; ++t) if (z[t] > mu) mu = z[t];
+        double sum = 0.0;
+        for (int t = 0; t < L; ++t) sum += exp(z[t] - mu);
+        lse[sh] = mu + log(sum);
+        free(z);
+    }
+    return bad ? -1 : 0;
+}
+
+/* The same log-sum-exp from phase-1 states, by the combine of [PA-V2] (module
+ * docstring): M = max_p m_p, total = sum_p exp(m_p - M) l_p, lse = M + log(total),
+ * over the ceil(L / P) used partitions; L == 0 gives -inf.  lse is [S, H]. */
+int pa_oracle_combine_lse(double* lse, const double* m, const double* l, const int32_t* lens,
+                          int S, int H, int P, int Pmax) {
+    if (S < 0 || H <= 0 || P <= 0 || Pmax < 0) return -1;
+    int bad = 0;
+    for (long sh = 0; sh < (long)S * H; ++sh) {
+        int s = (int)(sh / H);
+        int L = lens[s];
+        lse[sh] = -INFINITY;
+        if (L <= 0) continue;
+        int np = (L + P - 1) / P;
+        if (np > Pmax) { bad = 1; continue; }
+        const double* m_sh = m + (size_t)sh * Pmax;
+        const double* l_sh = l + (size_t)sh * Pmax;
+        double M = -INFINITY;
+        for (int p = 0; p < np; ++p) if (m_sh[p] > M) M = m_sh[p];
+        double total = 0.0;
+        for (int p = 0; p < np; ++p) total += exp(m_sh[p] - M) * l_sh[p];
+        lse[sh] = M + log(total);
+    }
+    return bad ? -1 : 0;
+}

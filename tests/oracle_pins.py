@@ -240,8 +240,73 @@ def pin_combine_closed_form(orc):
            "3:1 weights")
 
 
+def pin_lse_golden_two_token(orc):
+    """Hand-worked log-sum-exp of the two-token case: log(e^0 + e^1) = log(1 + e)
+    (tests/golden/two_token_closed_form.txt)."""
+    rows = {r[0]: [float(v) for v in r[1:]] for r in read_golden("two_token_closed_form.txt")}
+    D, BS = 8, 16
+    for dt in (FP16, BF16):
+        tdt = TORCH_DT[dt]
+        q = torch.tensor(rows["q"]).view(1, 1, D).to(tdt)
+        k_tok = torch.zeros((1, BS, 1, D))
+        k_tok[0, 0, 0], k_tok[0, 1, 0] = torch.tensor(rows["k0"]), torch.tensor(rows["k1"])
+        kc, vc = caches_from_tokens(k_tok.to(tdt), torch.zeros((1, BS, 1, D)).to(tdt))
+        got = orc.lse(q, kc, vc, torch.zeros((1, 1), dtype=torch.int32),
+                      torch.tensor([2], dtype=torch.int32), rows["scale"][0], dt)
+        _close(got[0, 0], rows["lse"][0], 1e-15, "two-token log-sum-exp")
+
+
+def pin_lse_closed_forms(orc):
+    """q = 0 makes every score 0, so lse = log L exactly; a one-token sequence has
+    lse = its one score, scale * q . k (small integers: exact); no tokens give -inf."""
+    q, kc, vc, bt, lens = random_case(81, S=3, H=4, KH=2, D=16, BS=4, lens=[9, 1, 0], MB=3)
+    got = orc.lse(torch.zeros_like(q), kc, vc, bt, lens, 0.5, FP16)
+    assert np.array_equal(got[0], np.full(4, math.log(9.0))), "q = 0 must give log L"
+    assert np.array_equal(got[1], np.zeros(4)) and np.all(np.isneginf(got[2]))
+    g = torch.Generator().manual_seed(3)
+    qi = torch.randint(-3, 4, q.shape, generator=g).to(torch.float16)
+    k_tok, v_tok = token_views(kc, vc)
+    ki = torch.randint(-3, 4, k_tok.shape, generator=g).to(torch.float16)
+    kci, _ = caches_from_tokens(ki, v_tok)
+    got = orc.lse(qi, kci, vc, bt, lens, 0.25, FP16)
+    for h in range(4):
+        k0 = ki[int(bt[1, 0]), 0, h // 2].to(torch.float64)
+        assert got[1, h] == 0.25 * float(qi[1, h].to(torch.float64) @ k0), "one-token lse"
+
+
+def pin_lse_library(orc):
+    """Special case = library routine: scipy.special.logsumexp of the scores
+    scale * K q, K gathered densely by torch indexing (GQA, ragged, both dtypes)."""
+    from scipy.special import logsumexp
+    from pa_testutil import gather_sequence
+    for dt in (FP16, BF16):
+        q, kc, vc, bt, lens = random_case(91 + dt, S=3, H=4, KH=2, D=16, BS=4, lens=[1, 7, 13],
+                                          dtype=TORCH_DT[dt])
+        got = orc.lse(q, kc, vc, bt, lens, 0.3, dt)
+        sc = float(np.float32(0.3))
+        for s in range(3):
+            K, _ = gather_sequence(kc, vc, bt, s, int(lens[s]))
+            for h in range(4):
+                z = sc * (K[:, h // 2, :] @ q[s, h].to(torch.float64).numpy())
+                _close(got[s, h], logsumexp(z), 1e-13, "scipy logsumexp")
+
+
+def pin_lse_partition_identity(orc):
+    """combine_lse(partitions(P)) equals the unpartitioned lse for any P (the
+    phase-2 identity), -inf for an empty sequence."""
+    q, kc, vc, bt, lens = random_case(101, S=3, H=4, KH=2, D=16, BS=4, lens=[37, 0, 16], MB=10)
+    ref = orc.lse(q, kc, vc, bt, lens, 0.35, FP16)
+    assert np.all(np.isneginf(ref[1]))
+    for P in (1, 4, 7, 16, 64):
+        m, l, _ = orc.partitions(q, kc, vc, bt, lens, 0.35, FP16, P)
+        got = orc.combine_lse(m, l, lens, P)
+        assert np.all(np.isneginf(got[1]))
+        _close(got[[0, 2]], ref[[0, 2]], 1e-13, f"partition size {P}")
+
+
 ALL_PINS = [
     pin_textbook_gqa, pin_bruteforce_tiny, pin_golden_two_token, pin_golden_layout,
     pin_seq_len_one, pin_uniform_weights, pin_shift_invariance, pin_permutation_invariance,
     pin_partition_invariance, pin_empty_sequence, pin_combine_closed_form,
+    pin_lse_golden_two_token, pin_lse_closed_forms, pin_lse_library, pin_lse_partition_identity,
 ]

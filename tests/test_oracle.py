@@ -37,6 +37,15 @@ MUTANTS = [
     ("sentinel_max_zero", "m[shp] = -INFINITY; l[shp] = 0.0;", "m[shp] = 0.0; l[shp] = 0.0;", 1),
     ("fp16_exponent_bias", "expo - 25", "expo - 24", 1),
     ("bf16_shift", "((uint32_t)b) << 16", "((uint32_t)b) << 15", 1),
+    ("lse_log2", "lse[sh] = mu + log(sum);", "lse[sh] = mu + log2(sum);", 1),
+    ("lse_max_dropped", "lse[sh] = mu + log(sum);", "lse[sh] = log(sum);", 1),
+    ("lse_exp_without_shift", "sum += exp(z[t] - mu);", "sum += exp(z[t]);", 1),
+    ("combine_lse_without_l", "total += exp(m_sh[p] - M) * l_sh[p];\n        lse[sh]",
+     "total += exp(m_sh[p] - M);\n        lse[sh]", 1),
+    ("combine_lse_last_partition_dropped", "for (int p = 0; p < np; ++p) total += exp(m_sh[p] - M) * l_sh[p];\n        lse[sh]",
+     "for (int p = 0; p + 1 < np; ++p) total += exp(m_sh[p] - M) * l_sh[p];\n        lse[sh]", 1),
+    ("lse_empty_zero", "lse[sh] = -INFINITY;\n        if (L <= 0) continue;\n        if (L > MB * BS)",
+     "lse[sh] = 0.0;\n        if (L <= 0) continue;\n        if (L > MB * BS)", 1),
     ("empty_sequence_not_zero", "if (L <= 0) continue;\n        if (L > MB * BS) { bad = 1; continue; }\n        double* z",
      "if (L > MB * BS) { bad = 1; continue; }\n        double* z", 1),
 ]
