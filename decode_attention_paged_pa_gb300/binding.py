@@ -38,6 +38,7 @@ _DTYPE_CODE = {torch.float16: PA_DTYPE_FP16, torch.bfloat16: PA_DTYPE_BF16}
 EXPORTED_SYMBOLS = (
     "pa_decode_v2",
     "pa_decode_v2_ex",
+    "pa_decode_v2_lse",
     "pa_decode_v2_workspace_bytes",
     "pa_decode_v2_workspace_layout",
     "pa_decode_v2_host_io",
@@ -74,6 +75,8 @@ def _declare(lib):
     lib.pa_decode_v2.restype = ci
     lib.pa_decode_v2_ex.argtypes = base + [ci, ci, cll]
     lib.pa_decode_v2_ex.restype = ci
+    lib.pa_decode_v2_lse.argtypes = [vp, vp] + base[1:]   # out, lse, then pa_decode_v2's from query on
+    lib.pa_decode_v2_lse.restype = ci
     lib.pa_decode_v2_host_io.argtypes = base
     lib.pa_decode_v2_host_io.restype = ci
     lib.pa_decode_v2_host_io_workspace_bytes.argtypes = [ci] * 7
@@ -147,12 +150,16 @@ def _check_tensor(name, t, dtype=None, ndim=None):
 
 def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
                  partition_size: int = 512, workspace: torch.Tensor | None = None, stream=None,
-                 variant: int = PA_VARIANT_AUTO, max_ctas: int = 0, timeout_ns: int = 0):
+                 variant: int = PA_VARIANT_AUTO, max_ctas: int = 0, timeout_ns: int = 0,
+                 lse: torch.Tensor | None = None):
     """Paged decode attention into ``out`` (see include/pa_decode.h).
 
     Shapes: query/out [S, H, D]; key_cache [NB, KH, D/8, BS, 8];
     value_cache [NB, KH, D, BS]; block_tables [S, MB] int32; seq_lens [S] int32.
     ``workspace`` (uint8, >= workspace_bytes(...)) is allocated if omitted.
+    ``lse`` (float32 [S, H], optional) receives each (sequence, head)'s
+    log-sum-exp of the scaled scores (``pa_decode_v2_lse``; the kernel family
+    is then chosen automatically).
     Returns the workspace used."""
     _check_tensor("query", query, ndim=3)
     dt = query.dtype
@@ -176,6 +183,19 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, sca
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
     _check_tensor("workspace", workspace, torch.uint8)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, 2)
+        if tuple(lse.shape) != (S, H):
+            raise ValueError("lse must be [num_seqs, num_heads]")
+        if variant != PA_VARIANT_AUTO or max_ctas or timeout_ns:
+            raise ValueError("lse is returned with the automatic kernel choice and defaults only")
+        st = lib().pa_decode_v2_lse(
+            _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+            _ptr(seq_lens), float(scale), S, H, KH, D, BS, int(partition_size), _DTYPE_CODE[dt],
+            _stream_handle(stream), MB, NB, _ptr(workspace), workspace.numel())
+        if st != PA_OK:
+            raise PaError(st, "pa_decode_v2_lse")
+        return workspace
     st = lib().pa_decode_v2_ex(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         _ptr(seq_lens), float(scale), S, H, KH, D, BS, int(partition_size), _DTYPE_CODE[dt],

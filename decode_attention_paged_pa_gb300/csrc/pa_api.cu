@@ -100,13 +100,14 @@ extern "C" int pa_decode_v2_workspace_layout(int num_seqs, int num_heads, int nu
   return PA_OK;
 }
 
-extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cache,
-                               const void* value_cache, const int32_t* block_tables,
-                               const int32_t* seq_lens, float scale, int num_seqs, int num_heads,
-                               int num_kv_heads, int head_size, int block_size, int partition_size,
-                               int dtype, void* stream, int max_blocks_per_seq, int num_blocks,
-                               void* workspace, size_t workspace_bytes, int variant, int max_ctas,
-                               long long timeout_ns) {
+namespace {
+
+int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
+                const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                float scale, int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                int block_size, int partition_size, int dtype, void* stream, int max_blocks_per_seq,
+                int num_blocks, void* workspace, size_t workspace_bytes, int variant, int max_ctas,
+                long long timeout_ns) {
   const int S = num_seqs, H = num_heads, KH = num_kv_heads, D = head_size, BS = block_size,
             P = partition_size, MB = max_blocks_per_seq;
   if (!valid_sizes(S, H, KH, D, MB, BS, P) || num_blocks <= 0) return PA_ERR_INVALID_ARG;
@@ -120,7 +121,7 @@ extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cac
     return PA_ERR_INVALID_ARG;
   if (!aligned(out, 16) || !aligned(query, 16) || !aligned(key_cache, 16) ||
       !aligned(value_cache, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
-      (workspace && !aligned(workspace, 16)))
+      (workspace && !aligned(workspace, 16)) || (lse && !aligned(lse, 4)))
     return PA_ERR_INVALID_ARG;
   WsLayout w;
   if (!ws_layout(S, H, KH, D, MB, BS, P, &w)) return PA_ERR_INVALID_ARG;
@@ -167,6 +168,7 @@ extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cac
     prm.hdr = reinterpret_cast<int*>(ws + w.hdr);
     prm.tickets = reinterpret_cast<int*>(ws + w.tickets) + (size_t)s0 * n_hg;
     prm.ctickets = reinterpret_cast<int*>(ws + w.ctickets) + (size_t)s0 * n_hg * w.cmax;
+    prm.lse = lse ? lse + (size_t)s0 * H : nullptr;
     prm.ws_cm = reinterpret_cast<float*>(ws + w.cm) + (size_t)s0 * H * w.cmax;
     prm.ws_cl = reinterpret_cast<float*>(ws + w.cl) + (size_t)s0 * H * w.cmax;
     prm.ws_co = reinterpret_cast<float*>(ws + w.co) + (size_t)s0 * H * w.cmax * D;
@@ -194,6 +196,33 @@ extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cac
   }
   if (own && cudaFreeAsync(ws, st) != cudaSuccess && status == PA_OK) status = PA_ERR_CUDA;
   return status;
+}
+
+}  // namespace
+
+extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cache,
+                               const void* value_cache, const int32_t* block_tables,
+                               const int32_t* seq_lens, float scale, int num_seqs, int num_heads,
+                               int num_kv_heads, int head_size, int block_size, int partition_size,
+                               int dtype, void* stream, int max_blocks_per_seq, int num_blocks,
+                               void* workspace, size_t workspace_bytes, int variant, int max_ctas,
+                               long long timeout_ns) {
+  return decode_impl(out, nullptr, query, key_cache, value_cache, block_tables, seq_lens, scale,
+                     num_seqs, num_heads, num_kv_heads, head_size, block_size, partition_size, dtype,
+                     stream, max_blocks_per_seq, num_blocks, workspace, workspace_bytes, variant,
+                     max_ctas, timeout_ns);
+}
+
+extern "C" int pa_decode_v2_lse(void* out, float* lse, const void* query, const void* key_cache,
+                                const void* value_cache, const int32_t* block_tables,
+                                const int32_t* seq_lens, float scale, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_size, int block_size, int partition_size,
+                                int dtype, void* stream, int max_blocks_per_seq, int num_blocks,
+                                void* workspace, size_t workspace_bytes) {
+  return decode_impl(out, lse, query, key_cache, value_cache, block_tables, seq_lens, scale,
+                     num_seqs, num_heads, num_kv_heads, head_size, block_size, partition_size, dtype,
+                     stream, max_blocks_per_seq, num_blocks, workspace, workspace_bytes,
+                     PA_VARIANT_AUTO, 0, 0);
 }
 
 extern "C" int pa_decode_v2(void* out, const void* query, const void* key_cache, const void* value_cache,

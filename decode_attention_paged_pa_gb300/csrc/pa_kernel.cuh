@@ -59,6 +59,7 @@ struct KParams {
   int* hdr;      // kHdrInts ints
   int* tickets;  // [S, n_hg]        partitions (or chunks) of a sequence completed
   int* ctickets; // [S, n_hg, Cmax]  partitions of a chunk completed
+  float* lse;    // [S, H] log-sum-exp of the scaled scores, or null
   float scale_log2;
   int S, H, KH, G, MB, num_blocks, P, Pmax, Cmax;
   int hg_per_kv;  // ceil(G / GT)
@@ -478,6 +479,9 @@ __device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, 
       v.x = F16Traits<T>::pack(r.x, r.y);
       v.y = F16Traits<T>::pack(r.z, r.w);
       *reinterpret_cast<uint2*>(static_cast<T*>(prm.out) + row * D + d4 * 4) = v;
+      // Final combine: the log-sum-exp of all the sequence's scores is
+      // M + log(total) (natural-log units: the partition and chunk maxima are).
+      if (d4 == 0 && prm.lse) prm.lse[row] = M + logf(tot);
     }
   }
 }
@@ -725,6 +729,10 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
       const int s = (int)(i / ((long long)H * (D / 8)));
       if (pref[s + 1] == pref[s]) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
     }
+    if (prm.lse) {  // no scores: the log-sum-exp is log 0
+      for (int i = blockIdx.x * NCT + ctid; i < S * H; i += gridDim.x * NCT)
+        if (pref[i / H + 1] == pref[i / H]) prm.lse[i] = -INFINITY;
+    }
   }
 
   C cons;
@@ -914,6 +922,9 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
       if (d4 == 0) {
         prm.ws_m[sh * Pmax + I.p] = rstat[gh * 2] * kLn2;
         prm.ws_l[sh * Pmax + I.p] = ef[NC * GT + gh];
+        // A single-partition sequence ends here: its log-sum-exp is the
+        // merged maximum (log2 units -> natural) plus the log of the merged sum.
+        if (single && prm.lse) prm.lse[sh] = rstat[gh * 2] * kLn2 + logf(ef[NC * GT + gh]);
       }
     }
     __syncwarp();

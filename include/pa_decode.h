@@ -142,6 +142,32 @@ int pa_decode_v2_ex(void* out, const void* query, const void* key_cache, const v
                     int variant, int max_ctas, long long timeout_ns);
 
 /*
+ * pa_decode_v2 that also returns, per (sequence, head), the log-sum-exp of
+ * the scaled scores:
+ *     lse[s * num_heads + h] = log( sum_t exp(scale * q[s,h] . k_t) )
+ * over the sequence's seq_lens[s] tokens, natural log, fp32; -INFINITY for a
+ * sequence with no tokens.  It is the value the forward kernel of the page
+ * "flash_attention.metal -- Flash Attention Metal Shaders" stores beside its
+ * output (its running maximum plus the log of its running sum, "log-sum-exp
+ * for backward pass"), reached here by the same cross-partition combine as
+ * the output (page "paged_attention_v2_triton.py -- Triton PagedAttention V2
+ * for BI-V100", module docstring: M = max m_p, total = sum exp(m_p - M) l_p,
+ * lse = M + log total).  With it, outputs computed over disjoint token sets
+ * (for example the two halves of a sequence split across calls or devices)
+ * merge exactly: out = sum_i exp(lse_i - LSE) out_i, LSE = log sum_i exp(lse_i).
+ *   lse   DEVICE buffer of num_seqs * num_heads floats, 4-byte aligned, written
+ *         (NULL: behaves as pa_decode_v2).
+ * Every other argument, the ownership and the errors are those of
+ * pa_decode_v2 (the kernel family is chosen as PA_VARIANT_AUTO); a misaligned
+ * lse is PA_ERR_INVALID_ARG.
+ */
+int pa_decode_v2_lse(void* out, float* lse, const void* query, const void* key_cache,
+                     const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                     float scale, int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                     int block_size, int partition_size, int dtype, void* stream,
+                     int max_blocks_per_seq, int num_blocks, void* workspace, size_t workspace_bytes);
+
+/*
  * Bytes of device workspace pa_decode_v2_host_io needs: the workspace of
  * pa_decode_v2 plus device staging for query, out, block_tables and seq_lens.
  * Returns 0 for invalid sizes.

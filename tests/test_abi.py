@@ -102,6 +102,15 @@ def test_rejects_bad_arguments_before_launch(kw, status):
     assert call(**kw) == status
 
 
+def test_lse_entry_rejects_misaligned_lse():
+    lib = binding.lib()
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 2, 4, 2, 128, 16, 512, 0, None, 4, 8,
+            FAKE, 1 << 30)
+    assert lib.pa_decode_v2_lse(FAKE, FAKE + 2, *args) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_v2_lse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 0, 4, 2,
+                                128, 16, 512, 0, None, 4, 8, FAKE, 1 << 30) == binding.PA_OK
+
+
 def test_status_strings():
     for code in range(7):
         s = binding.status_string(code)
