@@ -21,7 +21,10 @@ definition in ``pa_oracle.c``:
                          the value the forward kernel of the page
                          "flash_attention.metal -- Flash Attention Metal Shaders"
                          stores beside its output (max plus log of the sum);
-* :func:`combine_lse` -- the same from phase-1 states (M + log total).
+* :func:`combine_lse` -- the same from phase-1 states (M + log total);
+* :func:`decode_mq`   -- multi-query decode: q_len new tokens per sequence, the
+                         i-th at position L - q_len + i attending causally to
+                         positions 0 .. L - q_len + i (output and log-sum-exp).
 
 Inputs are the raw 16-bit patterns of fp16 / bf16 tensors (numpy ``uint16``)
 in the page's layouts; the fp32 ``scale`` is widened to double exactly.
@@ -76,6 +79,8 @@ def _declare(lib):
     lib.pa_oracle_lse.restype = c_int
     lib.pa_oracle_combine_lse.argtypes = [dp, dp, dp, ip] + [c_int] * 4
     lib.pa_oracle_combine_lse.restype = c_int
+    lib.pa_oracle_decode_mq.argtypes = [dp, dp, up, up, up, ip, ip, c_double] + [c_int] * 9
+    lib.pa_oracle_decode_mq.restype = c_int
     lib.pa_oracle_max_threads.argtypes = []
     lib.pa_oracle_max_threads.restype = c_int
     return lib
@@ -229,6 +234,28 @@ class Oracle:
         return out
 
 
+    def decode_mq(self, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                  dtype: int, nthreads: int = 0):
+        """Multi-query decode; query is [S, q_len, H, D].  Returns (out [S, q_len, H, D],
+        lse [S, q_len, H]) in float64."""
+        q, kc, vc = _u16(query), _u16(key_cache), _u16(value_cache)
+        bt, lens = _i32(block_tables), _i32(seq_lens)
+        S, q_len, H, D = q.shape
+        _, KH, _, BS, _ = kc.shape
+        _shapes(q.reshape(S * q_len, H, D), kc, vc, np.zeros((S * q_len, bt.shape[1]), np.int32))
+        MB = bt.shape[1]
+        out = np.zeros((S, q_len, H, D), dtype=np.float64)
+        lse = np.zeros((S, q_len, H), dtype=np.float64)
+        rc = self.lib.pa_oracle_decode_mq(
+            _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), _ptr(q, ctypes.c_uint16),
+            _ptr(kc, ctypes.c_uint16), _ptr(vc, ctypes.c_uint16), _ptr(bt, ctypes.c_int32),
+            _ptr(lens, ctypes.c_int32), float(np.float32(scale)), S, q_len, H, KH, D, BS, MB, dtype,
+            nthreads)
+        if rc != 0:
+            raise ValueError("oracle decode_mq rejected its arguments")
+        return out, lse
+
+
 _default = None
 
 
@@ -257,3 +284,7 @@ def lse(*args, **kwargs) -> np.ndarray:
 
 def combine_lse(*args, **kwargs) -> np.ndarray:
     return default().combine_lse(*args, **kwargs)
+
+
+def decode_mq(*args, **kwargs):
+    return default().decode_mq(*args, **kwargs)

@@ -291,3 +291,64 @@ int pa_oracle_combine_lse(double* lse, const double* m, const double* l, const i
     }
     return bad ? -1 : 0;
 }
+
+/* Multi-query decode (several new tokens per sequence, e.g. speculative
+ * verification): query[s, i, h, :] for i < q_len is the query of the i-th of
+ * the sequence's last q_len tokens, which sits at position L - q_len + i of its
+ * seq_lens[s] = L cached tokens and attends causally to positions
+ * 0 .. L - q_len + i.  This is the decode of [PA-V2] widened from one query
+ * row (its module docstring: "For decode (BLOCK_M=1), the Q tile is just one
+ * vector") to q_len rows with the causal rule of the prefix-prefill kernel its
+ * gather comes from.  out and lse are [S, q_len, H, D] and [S, q_len, H]; lse
+ * (may be NULL) is as in pa_oracle_lse.  L < q_len is an error (the new
+ * tokens must be in the cache). */
+int pa_oracle_decode_mq(double* out, double* lse, const uint16_t* q, const uint16_t* kc,
+                        const uint16_t* vc, const int32_t* bt, const int32_t* lens, double scale,
+                        int S, int q_len, int H, int KH, int D, int BS, int MB, int dtype,
+                        int nthreads) {
+    if (S < 0 || q_len <= 0 || H <= 0 || KH <= 0 || H % KH || D <= 0 || D % 8 || BS <= 0 || MB < 0)
+        return -1;
+    int bad = 0;
+    if (nthreads <= 0) nthreads = pa_oracle_max_threads();
+    const long rows = (long)S * q_len * H;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : bad)
+    for (long r = 0; r < rows; ++r) {
+        const int h = (int)(r % H);
+        const int i = (int)((r / H) % q_len);
+        const int s = (int)(r / ((long)H * q_len));
+        double* o_r = out + (size_t)r * D;
+        for (int d = 0; d < D; ++d) o_r[d] = 0.0;
+        if (lse) lse[r] = -INFINITY;
+        const int L = lens[s];
+        if (L < q_len || L > MB * BS) { bad = 1; continue; }
+        const int visible = L - q_len + i + 1;          /* positions 0 .. L - q_len + i */
+        double* z = (double*)malloc(sizeof(double) * (size_t)visible);
+        if (!z) { bad = 1; continue; }
+        /* Scores of this query row: its vector is query[s, i, h, :], i.e. row
+         * s * q_len + i of a [S * q_len, H, D] array, against sequence s's keys. */
+        const int kh = h / (H / KH);
+        const uint16_t* qv = q + ((size_t)(s * q_len + i) * H + h) * D;
+        for (int t = 0; t < visible; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += to_double(qv[d], dtype) * to_double(kc[key_index(b, kh, d, o, KH, D, BS)], dtype);
+            z[t] = scale * acc;
+        }
+        double mu = -INFINITY;
+        for (int t = 0; t < visible; ++t) if (z[t] > mu) mu = z[t];
+        double den = 0.0;
+        for (int t = 0; t < visible; ++t) { z[t] = exp(z[t] - mu); den += z[t]; }
+        for (int t = 0; t < visible; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            for (int d = 0; d < D; ++d)
+                o_r[d] += z[t] * to_double(vc[value_index(b, kh, d, o, KH, D, BS)], dtype);
+        }
+        for (int d = 0; d < D; ++d) o_r[d] /= den;
+        if (lse) lse[r] = mu + log(den);
+        free(z);
+    }
+    return bad ? -1 : 0;
+}

@@ -304,9 +304,57 @@ def pin_lse_partition_identity(orc):
         _close(got[[0, 2]], ref[[0, 2]], 1e-13, f"partition size {P}")
 
 
+def _mq_case(seed, S, q_len, H, KH, D, BS, lens, dtype=torch.float16):
+    """Random multi-query inputs: query [S, q_len, H, D] and paged caches."""
+    q, kc, vc, bt, L = random_case(seed, S=S * q_len, H=H, KH=KH, D=D, BS=BS, lens=list(lens) * q_len,
+                                   dtype=dtype)
+    return q.view(S, q_len, H, D).contiguous(), kc, vc, bt[:S].contiguous(), L[:S].contiguous()
+
+
+def pin_mq_textbook_causal(orc):
+    """Special case = textbook: numpy softmax(scale q K^T + causal mask) V and
+    scipy logsumexp of the masked scores, K/V gathered densely by torch
+    indexing; row i of a sequence of L tokens sees positions <= L - q_len + i."""
+    from scipy.special import logsumexp
+    from pa_testutil import gather_sequence
+    q, kc, vc, bt, lens = _mq_case(111, S=2, q_len=3, H=4, KH=2, D=16, BS=4, lens=[5, 11])
+    out, lse = orc.decode_mq(q, kc, vc, bt, lens, 0.3, FP16)
+    sc = float(np.float32(0.3))
+    for s in range(2):
+        L = int(lens[s])
+        K, V = gather_sequence(kc, vc, bt, s, L)
+        for i in range(3):
+            n = L - 3 + i + 1
+            for h in range(4):
+                z = sc * (K[:n, h // 2, :] @ q[s, i, h].to(torch.float64).numpy())
+                w = np.exp(z - z.max())
+                _close(out[s, i, h], (w / w.sum()) @ V[:n, h // 2, :], 1e-13, "causal textbook")
+                _close(lse[s, i, h], logsumexp(z), 1e-13, "causal logsumexp")
+
+
+def pin_mq_uniform_causal_bounds(orc):
+    """q = 0 makes every visible weight equal: row i's output is the plain mean of V
+    over positions 0 .. L - q_len + i and its lse is log of that count, exactly
+    pinning each row's causal bound (L = q_len leaves row 0 one token)."""
+    from pa_testutil import gather_sequence
+    q, kc, vc, bt, lens = _mq_case(121, S=2, q_len=4, H=2, KH=1, D=8, BS=4, lens=[4, 10])
+    out, lse = orc.decode_mq(torch.zeros_like(q), kc, vc, bt, lens, 0.5, FP16)
+    for s in range(2):
+        L = int(lens[s])
+        _, V = gather_sequence(kc, vc, bt, s, L)
+        for i in range(4):
+            n = L - 4 + i + 1
+            for h in range(2):
+                _close(out[s, i, h], V[:n, 0, :].mean(axis=0), 1e-14, f"mean of {n} tokens")
+                assert lse[s, i, h] == math.log(n), "lse of n equal scores is log n"
+    _, V0 = gather_sequence(kc, vc, bt, 0, 1)
+    assert np.array_equal(out[0, 0, 0], V0[0, 0]), "row 0 with L = q_len sees exactly token 0"
+
+
 ALL_PINS = [
     pin_textbook_gqa, pin_bruteforce_tiny, pin_golden_two_token, pin_golden_layout,
     pin_seq_len_one, pin_uniform_weights, pin_shift_invariance, pin_permutation_invariance,
     pin_partition_invariance, pin_empty_sequence, pin_combine_closed_form,
     pin_lse_golden_two_token, pin_lse_closed_forms, pin_lse_library, pin_lse_partition_identity,
+    pin_mq_textbook_causal, pin_mq_uniform_causal_bounds,
 ]

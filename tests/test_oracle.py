@@ -46,6 +46,10 @@ MUTANTS = [
      "for (int p = 0; p + 1 < np; ++p) total += exp(m_sh[p] - M) * l_sh[p];\n        lse[sh]", 1),
     ("lse_empty_zero", "lse[sh] = -INFINITY;\n        if (L <= 0) continue;\n        if (L > MB * BS)",
      "lse[sh] = 0.0;\n        if (L <= 0) continue;\n        if (L > MB * BS)", 1),
+    ("mq_not_causal", "const int visible = L - q_len + i + 1;", "const int visible = L;", 1),
+    ("mq_causal_off_by_one", "const int visible = L - q_len + i + 1;", "const int visible = L - q_len + i;", 1),
+    ("mq_rows_reversed", "const int visible = L - q_len + i + 1;", "const int visible = L - i;", 1),
+    ("mq_first_query_row_only", "q + ((size_t)(s * q_len + i) * H + h) * D", "q + ((size_t)(s * q_len) * H + h) * D", 1),
     ("empty_sequence_not_zero", "if (L <= 0) continue;\n        if (L > MB * BS) { bad = 1; continue; }\n        double* z",
      "if (L > MB * BS) { bad = 1; continue; }\n        double* z", 1),
 ]
