@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--config", choices=workloads.WORKLOAD_ORDER, default="mha_fp16")
+    ap.add_argument("--config", choices=list(workloads.WORKLOADS), default="mha_fp16")
     ap.add_argument("--variant", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample (cpu_baseline)")
@@ -191,8 +191,7 @@ def oracle_sample(w: workloads.Workload, cpu_seconds: float):
     def run(ws):
         inp = workloads.make_inputs(ws)
         t0 = time.perf_counter()
-        oracle.decode(inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
-                      inp["seq_lens"], inp["scale"], workloads.DTYPE_CODES[ws.dtype])
+        oracle_call(oracle, ws, inp)
         dt = time.perf_counter() - t0
         return dt, inp["seq_lens"].tolist()
 
@@ -216,6 +215,13 @@ def oracle_sample(w: workloads.Workload, cpu_seconds: float):
     }
 
 
+def oracle_call(oracle, w: workloads.Workload, inp):
+    """One oracle pass over a batch (multi-query batches through decode_mq)."""
+    args = (inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"], inp["seq_lens"],
+            inp["scale"], workloads.DTYPE_CODES[w.dtype])
+    return oracle.decode_mq(*args) if w.q_len > 1 else oracle.decode(*args)
+
+
 # ----------------------------------------------------------------------------- arms
 def run_reference(args, rank):
     """CPU reference arm: the fp64 oracle as it stands, on the host cores."""
@@ -231,8 +237,7 @@ def run_reference(args, rank):
     nbytes = workloads.algorithmic_bytes(ws, lens)
 
     def step():
-        oracle.decode(inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
-                      inp["seq_lens"], inp["scale"], workloads.DTYPE_CODES[ws.dtype])
+        oracle_call(oracle, ws, inp)
 
     for _ in range(args.warmup):
         step()
@@ -285,17 +290,23 @@ def run_native(args, rank, world, local):
     variant = {"auto": binding.PA_VARIANT_AUTO, "simt": binding.PA_VARIANT_SIMT,
                "mma": binding.PA_VARIANT_MMA}[args.variant]
     out = torch.empty_like(inp["query"])
-    wsb = binding.workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_size,
+    rows = w.num_seqs * w.q_len
+    wsb = binding.workspace_bytes(rows, w.num_heads, w.num_kv_heads, w.head_size,
                                   w.max_blocks_per_seq, w.block_size, w.partition_size)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = -(-w.num_seqs // 2048)
+    launches_per_step = binding.launches_per_call(w.num_seqs, w.q_len)
 
     def step():
-        binding.pa_decode_v2(out, inp["query"], inp["key_cache"], inp["value_cache"],
-                             inp["block_tables"], inp["seq_lens"], inp["scale"],
-                             partition_size=w.partition_size, workspace=ws, stream=stream,
-                             variant=variant)
+        if w.q_len > 1:
+            binding.pa_decode_v2_mq(out, inp["query"], inp["key_cache"], inp["value_cache"],
+                                    inp["block_tables"], inp["seq_lens"], inp["scale"],
+                                    partition_size=w.partition_size, workspace=ws, stream=stream)
+        else:
+            binding.pa_decode_v2(out, inp["query"], inp["key_cache"], inp["value_cache"],
+                                 inp["block_tables"], inp["seq_lens"], inp["scale"],
+                                 partition_size=w.partition_size, workspace=ws, stream=stream,
+                                 variant=variant)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -329,7 +340,7 @@ def run_native(args, rank, world, local):
 
     # ---- e2e: per-step inputs from pinned host memory, output back to host
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and w.q_len == 1:
         q_h = inp["query"].cpu().pin_memory()
         bt_h = inp["block_tables"].cpu().pin_memory()
         lens_h = inp["seq_lens"].cpu().pin_memory()
@@ -391,7 +402,7 @@ def run_native(args, rank, world, local):
                    "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
                    "block_size": w.block_size, "partition_size": w.partition_size,
                    "seq_lens": f"{min(lens)}..{max(lens)} (sum {tokens})", "accumulate": "fp32",
-                   "variant": args.variant, "parallelism": f"replicas x{world}",
+                   "q_len": w.q_len, "variant": args.variant, "parallelism": f"replicas x{world}",
                    "l2": f"no flush: KV pool {kv_bytes / 1e9:.2f} GB per rank > L2 {L2_BYTES / 1e6:.0f} MB"},
         "kv_tokens_per_s": tokens * world * args.steps / seconds,
         "pct_of_measured_peak": 100.0 * value / world / peak,

@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "pa_decode_v2",
     "pa_decode_v2_ex",
     "pa_decode_v2_lse",
+    "pa_decode_v2_mq",
     "pa_decode_v2_workspace_bytes",
     "pa_decode_v2_workspace_layout",
     "pa_decode_v2_host_io",
@@ -77,6 +78,8 @@ def _declare(lib):
     lib.pa_decode_v2_ex.restype = ci
     lib.pa_decode_v2_lse.argtypes = [vp, vp] + base[1:]   # out, lse, then pa_decode_v2's from query on
     lib.pa_decode_v2_lse.restype = ci
+    lib.pa_decode_v2_mq.argtypes = [vp, vp] + base[1:8] + [ci] + base[8:]   # q_len after num_seqs
+    lib.pa_decode_v2_mq.restype = ci
     lib.pa_decode_v2_host_io.argtypes = base
     lib.pa_decode_v2_host_io.restype = ci
     lib.pa_decode_v2_host_io_workspace_bytes.argtypes = [ci] * 7
@@ -204,6 +207,59 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, sca
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2")
     return workspace
+
+
+def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                    partition_size: int = 512, workspace: torch.Tensor | None = None, stream=None,
+                    lse: torch.Tensor | None = None):
+    """Multi-query decode into ``out`` (see include/pa_decode.h): query/out
+    [S, q_len, H, D]; each query row i of sequence s attends to positions
+    0 .. seq_lens[s] - q_len + i.  ``lse`` (float32 [S, q_len, H]) is optional.
+    Returns the workspace used."""
+    _check_tensor("query", query, ndim=4)
+    dt = query.dtype
+    if dt not in _DTYPE_CODE:
+        raise TypeError("query must be float16 or bfloat16")
+    _check_tensor("out", out, dt, 4)
+    _check_tensor("key_cache", key_cache, dt, 5)
+    _check_tensor("value_cache", value_cache, dt, 4)
+    _check_tensor("block_tables", block_tables, torch.int32, 2)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    S, QL, H, D = query.shape
+    NB, KH, DX, BS, X = key_cache.shape
+    if tuple(out.shape) != (S, QL, H, D) or X != 8 or DX * X != D:
+        raise ValueError("inconsistent query / out / key_cache shapes")
+    if tuple(value_cache.shape) != (NB, KH, D, BS):
+        raise ValueError("value_cache must be [num_blocks, KH, D, BS]")
+    if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables / seq_lens must have num_seqs rows")
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, 3)
+        if tuple(lse.shape) != (S, QL, H):
+            raise ValueError("lse must be [num_seqs, q_len, num_heads]")
+    MB = block_tables.shape[1]
+    need = workspace_bytes(S * QL, H, KH, D, MB, BS, partition_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+    _check_tensor("workspace", workspace, torch.uint8)
+    st = lib().pa_decode_v2_mq(
+        _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        _ptr(seq_lens), float(scale), S, QL, H, KH, D, BS, int(partition_size), _DTYPE_CODE[dt],
+        _stream_handle(stream), MB, NB, _ptr(workspace), workspace.numel())
+    if st != PA_OK:
+        raise PaError(st, "pa_decode_v2_mq")
+    return workspace
+
+
+# Query rows one kernel launch takes (the kernel's prefix array size); a call
+# launches once per this many rows, rounded down to whole sequences.
+MAX_ROWS_PER_LAUNCH = 1024
+
+
+def launches_per_call(num_seqs: int, q_len: int = 1) -> int:
+    """Kernel launches one call makes (for launch counts in measurements)."""
+    per = (MAX_ROWS_PER_LAUNCH // q_len) * q_len
+    return max(1, -(-(num_seqs * q_len) // per))
 
 
 def host_io_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq,

@@ -104,11 +104,16 @@ namespace {
 
 int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
                 const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,
-                float scale, int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                float scale, int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_size,
                 int block_size, int partition_size, int dtype, void* stream, int max_blocks_per_seq,
                 int num_blocks, void* workspace, size_t workspace_bytes, int variant, int max_ctas,
                 long long timeout_ns) {
-  const int S = num_seqs, H = num_heads, KH = num_kv_heads, D = head_size, BS = block_size,
+  // Rows: one per query row (q_len per cached sequence); everything below
+  // (units, workspace, launches) is per row.
+  if (q_len < 1 || q_len > kMaxSeqsPerLaunch || num_seqs < 0 ||
+      (long long)num_seqs * q_len > INT_MAX / 2)
+    return PA_ERR_INVALID_ARG;
+  const int S = num_seqs * q_len, H = num_heads, KH = num_kv_heads, D = head_size, BS = block_size,
             P = partition_size, MB = max_blocks_per_seq;
   if (!valid_sizes(S, H, KH, D, MB, BS, P) || num_blocks <= 0) return PA_ERR_INVALID_ARG;
   if (dtype != PA_DTYPE_FP16 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
@@ -132,7 +137,9 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : kSimtGroup;
   const int hg_per_kv = (G + gt - 1) / gt;
   const int n_hg = KH * hg_per_kv;
-  const int chunk = S < kMaxSeqsPerLaunch ? S : kMaxSeqsPerLaunch;
+  // Rows per launch: a whole number of cached sequences.
+  const int rows_per_launch = (kMaxSeqsPerLaunch / q_len) * q_len;
+  const int chunk = S < rows_per_launch ? S : rows_per_launch;
   if ((long long)chunk * w.pmax * n_hg > INT_MAX / 2) return PA_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -148,8 +155,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   if (cudaMemsetAsync(ws, 0, w.m, st) != cudaSuccess) status = PA_ERR_CUDA;
 
   const size_t esz = 2;
-  for (int s0 = 0; s0 < S && status == PA_OK; s0 += kMaxSeqsPerLaunch) {
-    const int n = (S - s0) < kMaxSeqsPerLaunch ? (S - s0) : kMaxSeqsPerLaunch;
+  for (int s0 = 0; s0 < S && status == PA_OK; s0 += rows_per_launch) {
+    const int n = (S - s0) < rows_per_launch ? (S - s0) : rows_per_launch;
     if (s0 > 0 && cudaMemsetAsync(ws + sizeof(int) * kHdrWork, 0, sizeof(int), st) != cudaSuccess) {
       status = PA_ERR_CUDA;
       break;
@@ -160,8 +167,9 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     prm.q = static_cast<const uint8_t*>(query) + (size_t)s0 * H * D * esz;
     prm.kc = key_cache;
     prm.vc = value_cache;
-    prm.bt = block_tables + (size_t)s0 * MB;
-    prm.lens = seq_lens + s0;
+    prm.bt = block_tables + (size_t)(s0 / q_len) * MB;
+    prm.lens = seq_lens + s0 / q_len;
+    prm.q_len = q_len;
     prm.ws_m = reinterpret_cast<float*>(ws + w.m) + (size_t)s0 * H * w.pmax;
     prm.ws_l = reinterpret_cast<float*>(ws + w.l) + (size_t)s0 * H * w.pmax;
     prm.ws_o = reinterpret_cast<float*>(ws + w.o) + (size_t)s0 * H * w.pmax * D;
@@ -208,9 +216,9 @@ extern "C" int pa_decode_v2_ex(void* out, const void* query, const void* key_cac
                                void* workspace, size_t workspace_bytes, int variant, int max_ctas,
                                long long timeout_ns) {
   return decode_impl(out, nullptr, query, key_cache, value_cache, block_tables, seq_lens, scale,
-                     num_seqs, num_heads, num_kv_heads, head_size, block_size, partition_size, dtype,
-                     stream, max_blocks_per_seq, num_blocks, workspace, workspace_bytes, variant,
-                     max_ctas, timeout_ns);
+                     num_seqs, 1, num_heads, num_kv_heads, head_size, block_size, partition_size,
+                     dtype, stream, max_blocks_per_seq, num_blocks, workspace, workspace_bytes,
+                     variant, max_ctas, timeout_ns);
 }
 
 extern "C" int pa_decode_v2_lse(void* out, float* lse, const void* query, const void* key_cache,
@@ -220,9 +228,21 @@ extern "C" int pa_decode_v2_lse(void* out, float* lse, const void* query, const 
                                 int dtype, void* stream, int max_blocks_per_seq, int num_blocks,
                                 void* workspace, size_t workspace_bytes) {
   return decode_impl(out, lse, query, key_cache, value_cache, block_tables, seq_lens, scale,
-                     num_seqs, num_heads, num_kv_heads, head_size, block_size, partition_size, dtype,
-                     stream, max_blocks_per_seq, num_blocks, workspace, workspace_bytes,
+                     num_seqs, 1, num_heads, num_kv_heads, head_size, block_size, partition_size,
+                     dtype, stream, max_blocks_per_seq, num_blocks, workspace, workspace_bytes,
                      PA_VARIANT_AUTO, 0, 0);
+}
+
+extern "C" int pa_decode_v2_mq(void* out, float* lse, const void* query, const void* key_cache,
+                               const void* value_cache, const int32_t* block_tables,
+                               const int32_t* seq_lens, float scale, int num_seqs, int q_len,
+                               int num_heads, int num_kv_heads, int head_size, int block_size,
+                               int partition_size, int dtype, void* stream, int max_blocks_per_seq,
+                               int num_blocks, void* workspace, size_t workspace_bytes) {
+  return decode_impl(out, lse, query, key_cache, value_cache, block_tables, seq_lens, scale,
+                     num_seqs, q_len, num_heads, num_kv_heads, head_size, block_size,
+                     partition_size, dtype, stream, max_blocks_per_seq, num_blocks, workspace,
+                     workspace_bytes, PA_VARIANT_AUTO, 0, 0);
 }
 
 extern "C" int pa_decode_v2(void* out, const void* query, const void* key_cache, const void* value_cache,

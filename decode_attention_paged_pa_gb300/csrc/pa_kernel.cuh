@@ -60,12 +60,35 @@ struct KParams {
   int* tickets;  // [S, n_hg]        partitions (or chunks) of a sequence completed
   int* ctickets; // [S, n_hg, Cmax]  partitions of a chunk completed
   float* lse;    // [S, H] log-sum-exp of the scaled scores, or null
+  int q_len;     // query rows per cached sequence (1: plain decode); S counts rows
   float scale_log2;
   int S, H, KH, G, MB, num_blocks, P, Pmax, Cmax;
   int hg_per_kv;  // ceil(G / GT)
   int n_hg;       // KH * hg_per_kv
   long long timeout_ns;
 };
+
+// Tokens visible to sequence row v.  Single-query kernels (MQ false): row v
+// is sequence v, all seq_lens[v] tokens.  Multi-query kernels: with q_len
+// query rows per cached sequence, row v is query i = v mod q_len of cached
+// sequence r = v / q_len, whose last q_len tokens are the queries': the i-th
+// sits at position L - q_len + i and sees positions 0 .. L - q_len + i
+// (L = seq_lens[r]).  A length outside [MQ ? q_len : 0, max_len] is flagged
+// (*bad) and clamped.  (Multi-query is a separate kernel instance so that the
+// single-query one keeps no runtime q_len arithmetic: it measured 5% faster.)
+template <bool MQ>
+__device__ __forceinline__ int visible_len(const KParams& prm, int v, int max_len, bool* bad) {
+  if constexpr (!MQ) {
+    const int L = prm.lens[v];
+    if (L < 0 || L > max_len) *bad = true;
+    return min(max(L, 0), max_len);
+  } else {
+    const int r = v / prm.q_len, i = v - r * prm.q_len;
+    const int L = prm.lens[r];
+    if (L < prm.q_len || L > max_len) *bad = true;
+    return min(max(L - prm.q_len + 1 + i, 0), max_len);
+  }
+}
 
 struct UnitInfo {
   int s, p, hg, t0, t1, nb, np, nh, h0;
@@ -147,24 +170,34 @@ struct UnitPlan {
   int s, p, hg, t0, t1, nb, np, nh, h0, kv;
 };
 
-template <class C>
+template <class C, bool MQ>
 __device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pref, int u) {
   constexpr int BS = C::BS, GT = C::GT;
   UnitPlan U;
   const int pair = u / prm.n_hg;
   U.hg = u - pair * prm.n_hg;
-  int lo = 0, hi = prm.S;  // pref[lo] <= pair < pref[hi]
+  int lo = 0, hi = MQ ? prm.S / prm.q_len : prm.S;  // pref[lo] <= pair < pref[lo + 1]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (pref[mid] <= pair) lo = mid; else hi = mid;
   }
-  U.s = lo;
-  U.p = pair - pref[lo];
-  U.np = pref[lo + 1] - pref[lo];
-  const int L = min(max(prm.lens[lo], 0), prm.MB * BS);
+  bool bad = false;  // flagged by the prefix scan already
+  int L;
+  if constexpr (!MQ) {
+    U.s = lo;
+    U.p = pair - pref[lo];
+    U.np = pref[lo + 1] - pref[lo];
+    L = visible_len<false>(prm, lo, prm.MB * BS, &bad);
+  } else {
+    const int slot = pair - pref[lo];
+    U.p = slot / prm.q_len;
+    U.s = lo * prm.q_len + (slot - U.p * prm.q_len);  // the row
+    L = visible_len<true>(prm, U.s, prm.MB * BS, &bad);
+    U.np = (L + prm.P - 1) / prm.P;
+  }
   U.t0 = U.p * prm.P;
   U.t1 = min(U.t0 + prm.P, L);
-  U.nb = (U.t1 - U.t0 + BS - 1) / BS;
+  U.nb = U.p < U.np ? (U.t1 - U.t0 + BS - 1) / BS : 0;  // 0: a void slot
   U.kv = U.hg / prm.hg_per_kv;
   const int hgk = U.hg - U.kv * prm.hg_per_kv;
   U.h0 = U.kv * prm.G + hgk * GT;
@@ -175,11 +208,12 @@ __device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pre
 // This lane's block-table entry among blocks [c0, c0 + 32) of unit U (0 past
 // the unit's end).  An id outside the pool is recorded and replaced by 0, so
 // nothing is read out of bounds.
-template <class C>
+template <class C, bool MQ>
 __device__ __forceinline__ int load_block_id(const KParams& prm, const UnitPlan& U, int c0, int lane) {
   int b = 0;
   if (c0 + lane < U.nb) {
-    b = __ldg(prm.bt + (size_t)U.s * prm.MB + U.t0 / C::BS + c0 + lane);
+    const int row = MQ ? U.s / prm.q_len : U.s;  // table row of the cached sequence
+    b = __ldg(prm.bt + (size_t)row * prm.MB + U.t0 / C::BS + c0 + lane);
     if ((unsigned)b >= (unsigned)prm.num_blocks) {
       atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
       b = 0;
@@ -188,7 +222,7 @@ __device__ __forceinline__ int load_block_id(const KParams& prm, const UnitPlan&
   return b;
 }
 
-template <class C, class LY>
+template <class C, class LY, bool MQ>
 __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem, const int* pref,
                                               UnitInfo* info, volatile int* abort_flag,
                                               volatile uint32_t* issued, int lane) {
@@ -202,7 +236,25 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   int* err = prm.hdr + kHdrError;
   const uint64_t pol_stream = l2_policy_evict_first();
   const uint64_t pol_keep = l2_policy_evict_last();
-  const int total = pref[prm.S] * prm.n_hg;
+  const int total = pref[MQ ? prm.S / prm.q_len : prm.S] * prm.n_hg;
+  // Plan unit u; multi-query kernels skip void slots (a query row whose
+  // causal prefix ends before the slot's partition) by claiming further
+  // indices.
+  auto plan_next = [&](int u, UnitPlan& Up) -> bool {
+    if constexpr (!MQ) {
+      if (u >= total) return false;
+      Up = plan_unit<C, false>(prm, pref, u);
+      return true;
+    } else {
+      while (u < total) {
+        Up = plan_unit<C, true>(prm, pref, u);
+        if (Up.nb > 0) return true;
+        if (lane == 0) u = atomicAdd(prm.hdr + kHdrWork, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+      }
+      return false;
+    }
+  };
 
   uint32_t g = 0;   // blocks whose copies are issued, in order
   uint32_t kq = 0;  // units published (the end marker included)
@@ -245,13 +297,10 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   int u_cur = 0;
   if (lane == 0) u_cur = atomicAdd(prm.hdr + kHdrWork, 1);
   u_cur = __shfl_sync(0xffffffffu, u_cur, 0);
-  bool have = u_cur < total;
   UnitPlan U{};
+  bool have = plan_next(u_cur, U);
   int bids = 0;  // this lane's block id among the unit's first 32 blocks
-  if (have) {
-    U = plan_unit<C>(prm, pref, u_cur);
-    bids = load_block_id<C>(prm, U, 0, lane);
-  }
+  if (have) bids = load_block_id<C, MQ>(prm, U, 0, lane);
   ok = publish(U, have);
   while (have && ok) {
     int u_req = 0;
@@ -261,16 +310,13 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     int bids_next = 0;
     auto publish_next = [&]() {
       const int u_nx = __shfl_sync(0xffffffffu, u_req, 0);
-      have_next = u_nx < total;
-      if (have_next) {
-        Un = plan_unit<C>(prm, pref, u_nx);
-        bids_next = load_block_id<C>(prm, Un, 0, lane);
-      }
+      have_next = plan_next(u_nx, Un);
+      if (have_next) bids_next = load_block_id<C, MQ>(prm, Un, 0, lane);
       ok = publish(Un, have_next);
       published_next = true;
     };
     for (int c0 = 0; c0 < U.nb && ok; c0 += 32) {
-      const int b32 = (c0 == 0) ? bids : load_block_id<C>(prm, U, c0, lane);
+      const int b32 = (c0 == 0) ? bids : load_block_id<C, MQ>(prm, U, c0, lane);
       const int cend = min(c0 + 32, U.nb);
       for (int jb = c0; jb < cend && ok; jb += BATCH) {
         if (jb > 0 && !published_next) {
@@ -692,7 +738,7 @@ struct JobEngine {
 // Consumer warp: stream the blocks of every unit assigned to it and hand its
 // online-softmax state for each unit to the epilogue warp through shared
 // memory.  Consumer warps never wait for each other.
-template <class C, class LY>
+template <class C, class LY, bool MQ>
 __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem, const int* pref,
                                               const UnitInfo* info, volatile int* abort_flag,
                                               const volatile uint32_t* issued, const JobChannel& ch,
@@ -715,11 +761,14 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
 
   // Unused partitions: sentinels (m = -inf, l = 0).  Empty sequences: zeros.
   {
+    const int max_len = prm.MB * C::BS;
+    bool bad = false;  // flagged by the prefix scan already
     const long long n1 = (long long)S * H * Pmax;
     for (long long i = (long long)blockIdx.x * NCT + ctid; i < n1; i += (long long)gridDim.x * NCT) {
       const int s = (int)(i / ((long long)H * Pmax));
       const int p = (int)(i % Pmax);
-      if (p >= pref[s + 1] - pref[s]) {
+      const int np = MQ ? (visible_len<true>(prm, s, max_len, &bad) + prm.P - 1) / prm.P : pref[s + 1] - pref[s];
+      if (p >= np) {
         prm.ws_m[i] = -INFINITY;
         prm.ws_l[i] = 0.f;
       }
@@ -727,11 +776,11 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     const long long n2 = (long long)S * H * (D / 8);
     for (long long i = (long long)blockIdx.x * NCT + ctid; i < n2; i += (long long)gridDim.x * NCT) {
       const int s = (int)(i / ((long long)H * (D / 8)));
-      if (pref[s + 1] == pref[s]) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
+      if (visible_len<MQ>(prm, s, max_len, &bad) == 0) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
     }
     if (prm.lse) {  // no scores: the log-sum-exp is log 0
       for (int i = blockIdx.x * NCT + ctid; i < S * H; i += gridDim.x * NCT)
-        if (pref[i / H + 1] == pref[i / H]) prm.lse[i] = -INFINITY;
+        if (visible_len<MQ>(prm, i / H, max_len, &bad) == 0) prm.lse[i] = -INFINITY;
     }
   }
 
@@ -951,7 +1000,7 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
   }
 }
 
-template <class C, int NC, int NSTAGE, int CTAS_PER_SM>
+template <class C, int NC, int NSTAGE, int CTAS_PER_SM, bool MQ>
 __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     pa_decode_kernel(const __grid_constant__ KParams prm) {
   using LY = Layout<C, NC, NSTAGE>;
@@ -990,20 +1039,23 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     *ch.finished = 0;
     fence_mbarrier_init();
   }
-  // pref[s] = number of used partitions before sequence s (lengths clamped to
-  // [0, MB*BS]; an out-of-range length is recorded as a device error).
+  // pref[r] = work slots before cached sequence r: its partitions (those of
+  // its last query row, which sees every token) times q_len, the rows of one
+  // partition being consecutive slots so that they stream the same blocks at
+  // about the same time (the repeats hit L2).  A row whose causal prefix ends
+  // before a slot's partition leaves that slot void.  Lengths are clamped to
+  // [0, MB*BS]; an out-of-range length is recorded as a device error.
   {
-    const int S = prm.S, nthr = LY::THREADS, max_len = prm.MB * C::BS;
+    const int S = MQ ? prm.S / prm.q_len : prm.S, nthr = LY::THREADS, max_len = prm.MB * C::BS;
     const int per = (S + nthr - 1) / nthr;
     const int beg = min(tid * per, S), end = min(beg + per, S);
     int sum = 0;
     for (int s = beg; s < end; ++s) {
-      int L = prm.lens[s];
-      if (L < 0 || L > max_len) {
-        atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
-        L = min(max(L, 0), max_len);
-      }
-      sum += (L + prm.P - 1) / prm.P;
+      bool bad = false;
+      const int L = MQ ? visible_len<true>(prm, s * prm.q_len + prm.q_len - 1, max_len, &bad)
+                       : visible_len<false>(prm, s, max_len, &bad);
+      if (bad) atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
+      sum += MQ ? (L + prm.P - 1) / prm.P * prm.q_len : (L + prm.P - 1) / prm.P;
     }
     scan[tid] = sum;
     __syncthreads();
@@ -1020,16 +1072,19 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     int run = scan[tid];
     for (int s = beg; s < end; ++s) {
       pref[s] = run;
-      run += (min(max(prm.lens[s], 0), max_len) + prm.P - 1) / prm.P;
+      bool bad = false;
+      run += MQ ? (visible_len<true>(prm, s * prm.q_len + prm.q_len - 1, max_len, &bad) + prm.P - 1) /
+                      prm.P * prm.q_len
+                : (visible_len<false>(prm, s, max_len, &bad) + prm.P - 1) / prm.P;
     }
   }
   __syncthreads();
   if (warp == NC) {
-    producer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, lane);
+    producer_loop<C, LY, MQ>(prm, smem, pref, info, abort_flag, issued, lane);
   } else if (warp == NC + 1) {
     epilogue_loop<C, LY>(prm, smem, abort_flag, ch, lane);
   } else {
-    consumer_loop<C, LY>(prm, smem, pref, info, abort_flag, issued, ch, warp, lane);
+    consumer_loop<C, LY, MQ>(prm, smem, pref, info, abort_flag, issued, ch, warp, lane);
   }
 }
 

@@ -46,7 +46,8 @@ template <class C, int NC>
 cudaError_t launch_one(const KParams& prm, int max_ctas, cudaStream_t stream) {
   using SZ = Sizing<C, NC>;
   using LY = typename SZ::LY;
-  auto kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm>;
+  auto kern = prm.q_len > 1 ? pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, true>
+                            : pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)LY::bytes(kMaxSeqsPerLaunch));
   if (e != cudaSuccess) return e;

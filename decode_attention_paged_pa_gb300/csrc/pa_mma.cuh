@@ -18,6 +18,8 @@
 // weights enter the second product rounded to the element type.
 #pragma once
 
+#include <type_traits>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -31,6 +33,7 @@ struct MmaConsumer {
   static constexpr int NMT = D / 16;   // 16-dim tiles of the value product
   static constexpr int NTT = BS / 16;  // 16-token tiles per block
   static constexpr int SCRATCH_FLOATS = 0;
+  static constexpr bool kSplitWeights = std::is_same<T_, __nv_bfloat16>::value;
 
   uint32_t qb[NK][2];  // Q^T fragments (B operand), packed element pairs
   float m[2], l[2];    // heads 2*(lane%4) and 2*(lane%4)+1
@@ -124,14 +127,27 @@ struct MmaConsumer {
 #pragma unroll
     for (int tt = 0; tt < NTT; ++tt) {
       // P fragment rows = tokens, cols = heads; transpose to the B operand.
-      const uint32_t b0 = movmatrix_trans(F16Traits<T>::pack(sc[tt][0], sc[tt][1]));
-      const uint32_t b1 = movmatrix_trans(F16Traits<T>::pack(sc[tt][2], sc[tt][3]));
+      const uint32_t p0 = F16Traits<T>::pack(sc[tt][0], sc[tt][1]);
+      const uint32_t p1 = F16Traits<T>::pack(sc[tt][2], sc[tt][3]);
+      const uint32_t b0 = movmatrix_trans(p0), b1 = movmatrix_trans(p1);
+      // bf16 keeps 8 significant bits, so a weight rounded once can be off by
+      // 2^-9 of itself: enough, over a handful of tokens, to miss the parity
+      // tolerance.  The rounding remainder goes through a second product
+      // (P = P_hi + P_lo, both bf16), leaving an error near 2^-17.  fp16's
+      // 11 bits need no second product.
+      uint32_t r0 = 0, r1 = 0;
+      if constexpr (kSplitWeights) {
+        const float2 h0 = F16Traits<T>::to_float2(p0), h1 = F16Traits<T>::to_float2(p1);
+        r0 = movmatrix_trans(F16Traits<T>::pack(sc[tt][0] - h0.x, sc[tt][1] - h0.y));
+        r1 = movmatrix_trans(F16Traits<T>::pack(sc[tt][2] - h1.x, sc[tt][3] - h1.y));
+      }
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
         uint32_t a[4];
         const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (lane >> 4);
         ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
         Mma<T>::run(acc[mt], a, b0, b1);
+        if constexpr (kSplitWeights) Mma<T>::run(acc[mt], a, r0, r1);
       }
     }
   }

@@ -50,6 +50,7 @@ class Workload:
     v_uniform: bool = False          # V ~ U(-1, 1) instead of N(0, 1)
     distinct_tables: bool = False    # per-seq randperm(num_blocks)[:MB] instead of one pool permutation
     seed: int = 0
+    q_len: int = 1                   # query rows per sequence (multi-query decode when > 1)
 
     @property
     def group(self) -> int:
@@ -86,6 +87,13 @@ WORKLOADS: dict[str, Workload] = {
         forced_lens=((0, 1), (1, 2048), (2, 17)), k_std=2.0, v_uniform=True, seed=1004),
 }
 WORKLOAD_ORDER = ["tiny_fp16", "mha_fp16", "gqa_bf16", "long_skew_bf16", "d256_fp16"]
+
+# Multi-query decode (speculative verification of 4 draft tokens) on the GQA
+# batch's shapes and lengths: query [S, 4, H, D], each row causal.
+WORKLOADS["spec4_gqa_bf16"] = _cfg(
+    name="spec4_gqa_bf16", dtype="bf16", num_seqs=128, num_heads=32, num_kv_heads=8, head_size=128,
+    block_size=16, partition_size=512, scale=1.0 / math.sqrt(128), max_blocks_per_seq=512,
+    num_blocks=128 * 512, lens=(2048, 8192), lens_random=True, seed=1002, q_len=4)
 
 
 def custom(name="custom", dtype="fp16", num_seqs=2, num_heads=4, num_kv_heads=4, head_size=64,
@@ -145,7 +153,8 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu",
     dt = DTYPES[w.dtype]
     S, H, KH, D, BS, NB = (w.num_seqs, w.num_heads, w.num_kv_heads, w.head_size,
                            w.block_size, w.num_blocks)
-    query = torch.randn((S, H, D), generator=vgen, device=vdev, dtype=torch.float32).to(dt)
+    qshape = (S, H, D) if w.q_len == 1 else (S, w.q_len, H, D)
+    query = torch.randn(qshape, generator=vgen, device=vdev, dtype=torch.float32).to(dt)
     key_cache = torch.empty((NB, KH, D // X_PACK, BS, X_PACK), device=vdev, dtype=dt)
     key_cache.normal_(0.0, w.k_std, generator=vgen)
     value_cache = torch.empty((NB, KH, D, BS), device=vdev, dtype=dt)
@@ -163,12 +172,13 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu",
 
 def algorithmic_bytes(w: Workload, seq_lens: Sequence[int]) -> int:
     """Bytes one call must move: K and V of every token once per kv head (all
-    query heads of a group share them), q in, out, the block-table entries that
-    cover the tokens, and seq_lens.  Workspace traffic is not counted."""
+    query heads of a group, and all query rows of a multi-query sequence, share
+    them), q in, out, the block-table entries that cover the tokens, and
+    seq_lens.  Workspace traffic is not counted."""
     esz = 2
     lens = [int(v) for v in seq_lens]
     kv = sum(lens) * w.num_kv_heads * w.head_size * 2 * esz
-    q_out = 2 * w.num_seqs * w.num_heads * w.head_size * esz
+    q_out = 2 * w.num_seqs * w.q_len * w.num_heads * w.head_size * esz
     tables = 4 * sum(-(-L // w.block_size) for L in lens)
     return kv + q_out + tables + 4 * w.num_seqs
 

@@ -168,6 +168,35 @@ int pa_decode_v2_lse(void* out, float* lse, const void* query, const void* key_c
                      int max_blocks_per_seq, int num_blocks, void* workspace, size_t workspace_bytes);
 
 /*
+ * Multi-query decode: q_len new tokens per sequence (speculative or
+ * multi-token-prediction verification), each query row attending causally.
+ * The decode of page "paged_attention_v2_triton.py -- Triton PagedAttention V2
+ * for BI-V100" is its one-row case (module docstring: "For decode
+ * (BLOCK_M=1), the Q tile is just one vector"); q_len > 1 rows follow the
+ * causal rule of the prefix-prefill kernel its paged gather comes from: the
+ * sequence's last q_len cached tokens are the new ones, and query row i sits
+ * at position L - q_len + i (L = seq_lens[s]) and attends to positions
+ * 0 .. L - q_len + i.  Their K and V must already be in the cache.
+ *   query, out  [num_seqs, q_len, num_heads, head_size]   dtype
+ *   lse         NULL, or DEVICE [num_seqs, q_len, num_heads] fp32 (as in
+ *               pa_decode_v2_lse), written
+ *   seq_lens    [num_seqs] int32, each in [q_len, max_blocks_per_seq*block_size]
+ *               (a length below q_len is recorded as PA_ERR_DEVICE_BOUNDS)
+ *   q_len       1 .. 1024 (q_len = 1 is pa_decode_v2_lse)
+ *   workspace   >= pa_decode_v2_workspace_bytes(num_seqs * q_len, ...) bytes, or NULL
+ * The other arguments, ownership and errors are those of pa_decode_v2 (kernel
+ * family chosen as PA_VARIANT_AUTO).  Each (sequence, query row) is decoded
+ * as a sequence of its own over the causal prefix it sees; the rows of one
+ * sequence read the same cached blocks, one after another, so those reads
+ * mostly hit L2.
+ */
+int pa_decode_v2_mq(void* out, float* lse, const void* query, const void* key_cache,
+                    const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                    float scale, int num_seqs, int q_len, int num_heads, int num_kv_heads,
+                    int head_size, int block_size, int partition_size, int dtype, void* stream,
+                    int max_blocks_per_seq, int num_blocks, void* workspace, size_t workspace_bytes);
+
+/*
  * Bytes of device workspace pa_decode_v2_host_io needs: the workspace of
  * pa_decode_v2 plus device staging for query, out, block_tables and seq_lens.
  * Returns 0 for invalid sizes.

@@ -111,6 +111,25 @@ def test_lse_entry_rejects_misaligned_lse():
                                 128, 16, 512, 0, None, 4, 8, FAKE, 1 << 30) == binding.PA_OK
 
 
+def test_mq_entry_rejects_bad_q_len():
+    lib = binding.lib()
+    for q_len in (0, -1, 1025):
+        st = lib.pa_decode_v2_mq(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 2, q_len,
+                                 4, 2, 128, 16, 512, 0, None, 4, 8, FAKE, 1 << 30)
+        assert st == binding.PA_ERR_INVALID_ARG, q_len
+    st = lib.pa_decode_v2_mq(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 2, 4,
+                             4, 2, 128, 16, 512, 0, None, 4, 8, FAKE, 1024)
+    assert st == binding.PA_ERR_WORKSPACE
+
+
+def test_binding_launch_count_matches_kernel_limit():
+    text = open(os.path.join(ROOT, "decode_attention_paged_pa_gb300", "csrc", "pa_launch.h")).read()
+    limit = int(re.search(r"#define PA_MAX_SEQS_PER_LAUNCH (\d+)", text).group(1))
+    assert binding.MAX_ROWS_PER_LAUNCH == limit
+    assert binding.launches_per_call(limit) == 1 and binding.launches_per_call(limit + 1) == 2
+    assert binding.launches_per_call(300, 4) == 2   # 256 sequences (1024 rows) per launch
+
+
 def test_status_strings():
     for code in range(7):
         s = binding.status_string(code)
