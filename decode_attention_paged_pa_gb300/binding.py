@@ -251,15 +251,14 @@ def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, 
     return workspace
 
 
-# Query rows one kernel launch takes (the kernel's prefix array size); a call
-# launches once per this many rows, rounded down to whole sequences.
+# Sequences one kernel launch takes (the kernel's prefix array size); a call
+# launches once per this many sequences, whatever q_len.
 MAX_ROWS_PER_LAUNCH = 1024
 
 
 def launches_per_call(num_seqs: int, q_len: int = 1) -> int:
     """Kernel launches one call makes (for launch counts in measurements)."""
-    per = (MAX_ROWS_PER_LAUNCH // q_len) * q_len
-    return max(1, -(-(num_seqs * q_len) // per))
+    return max(1, -(-num_seqs // MAX_ROWS_PER_LAUNCH))
 
 
 def host_io_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq,

@@ -108,12 +108,12 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
                 int block_size, int partition_size, int dtype, void* stream, int max_blocks_per_seq,
                 int num_blocks, void* workspace, size_t workspace_bytes, int variant, int max_ctas,
                 long long timeout_ns) {
-  // Rows: one per query row (q_len per cached sequence); everything below
-  // (units, workspace, launches) is per row.
-  if (q_len < 1 || q_len > kMaxSeqsPerLaunch || num_seqs < 0 ||
-      (long long)num_seqs * q_len > INT_MAX / 2)
+  // Multi-query: the kernel sees q_len "row heads" per caller head (H below
+  // counts them), q_len * G per kv head, all sharing the kv head's blocks.
+  if (q_len < 1 || q_len > kMaxSeqsPerLaunch || num_heads <= 0 ||
+      (long long)num_heads * q_len > 65536)
     return PA_ERR_INVALID_ARG;
-  const int S = num_seqs * q_len, H = num_heads, KH = num_kv_heads, D = head_size, BS = block_size,
+  const int S = num_seqs, H = num_heads * q_len, KH = num_kv_heads, D = head_size, BS = block_size,
             P = partition_size, MB = max_blocks_per_seq;
   if (!valid_sizes(S, H, KH, D, MB, BS, P) || num_blocks <= 0) return PA_ERR_INVALID_ARG;
   if (dtype != PA_DTYPE_FP16 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
@@ -137,8 +137,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : kSimtGroup;
   const int hg_per_kv = (G + gt - 1) / gt;
   const int n_hg = KH * hg_per_kv;
-  // Rows per launch: a whole number of cached sequences.
-  const int rows_per_launch = (kMaxSeqsPerLaunch / q_len) * q_len;
+  const int rows_per_launch = kMaxSeqsPerLaunch;  // sequences per launch
   const int chunk = S < rows_per_launch ? S : rows_per_launch;
   if ((long long)chunk * w.pmax * n_hg > INT_MAX / 2) return PA_ERR_UNSUPPORTED;
 
@@ -167,9 +166,11 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     prm.q = static_cast<const uint8_t*>(query) + (size_t)s0 * H * D * esz;
     prm.kc = key_cache;
     prm.vc = value_cache;
-    prm.bt = block_tables + (size_t)(s0 / q_len) * MB;
-    prm.lens = seq_lens + s0 / q_len;
+    prm.bt = block_tables + (size_t)s0 * MB;
+    prm.lens = seq_lens + s0;
     prm.q_len = q_len;
+    prm.Hu = num_heads;
+    prm.Gu = num_heads / KH;
     prm.ws_m = reinterpret_cast<float*>(ws + w.m) + (size_t)s0 * H * w.pmax;
     prm.ws_l = reinterpret_cast<float*>(ws + w.l) + (size_t)s0 * H * w.pmax;
     prm.ws_o = reinterpret_cast<float*>(ws + w.o) + (size_t)s0 * H * w.pmax * D;

@@ -60,7 +60,9 @@ struct KParams {
   int* tickets;  // [S, n_hg]        partitions (or chunks) of a sequence completed
   int* ctickets; // [S, n_hg, Cmax]  partitions of a chunk completed
   float* lse;    // [S, H] log-sum-exp of the scaled scores, or null
-  int q_len;     // query rows per cached sequence (1: plain decode); S counts rows
+  int q_len;     // query tokens per sequence (multi-query kernels; 1 otherwise)
+  int Hu, Gu;    // the caller's heads and heads per kv head; H and G below count row
+                 // heads, q_len of them per caller head (H = q_len * Hu, G = q_len * Gu)
   float scale_log2;
   int S, H, KH, G, MB, num_blocks, P, Pmax, Cmax;
   int hg_per_kv;  // ceil(G / GT)
@@ -68,31 +70,50 @@ struct KParams {
   long long timeout_ns;
 };
 
-// Tokens visible to sequence row v.  Single-query kernels (MQ false): row v
-// is sequence v, all seq_lens[v] tokens.  Multi-query kernels: with q_len
-// query rows per cached sequence, row v is query i = v mod q_len of cached
-// sequence r = v / q_len, whose last q_len tokens are the queries': the i-th
-// sits at position L - q_len + i and sees positions 0 .. L - q_len + i
-// (L = seq_lens[r]).  A length outside [MQ ? q_len : 0, max_len] is flagged
-// (*bad) and clamped.  (Multi-query is a separate kernel instance so that the
-// single-query one keeps no runtime q_len arithmetic: it measured 5% faster.)
+// Cached tokens of sequence s, clamped to [0, max_len].  A length outside
+// [MQ ? q_len : 0, max_len] is flagged (*bad): a multi-query sequence holds
+// its q_len new tokens.
 template <bool MQ>
-__device__ __forceinline__ int visible_len(const KParams& prm, int v, int max_len, bool* bad) {
+__device__ __forceinline__ int seq_tokens(const KParams& prm, int s, int max_len, bool* bad) {
+  const int L = prm.lens[s];
+  if (L < (MQ ? prm.q_len : 0) || L > max_len) *bad = true;
+  return min(max(L, 0), max_len);
+}
+
+// Multi-query decode keeps the single-query work decomposition and gives the
+// rows of a unit to (query token, head) pairs: within kv head kv, row head
+// h = kv * G + l (l < G = q_len * Gu) is query token i = l / Gu and caller
+// head kv * Gu + l % Gu.  Every row head streams the same K/V blocks (one
+// load serves q_len * Gu rows); token i sits at position L - q_len + i and
+// sees positions 0 .. L - q_len + i.  (Multi-query kernels are separate
+// instances: carrying q_len through the single-query kernel cost it 5%.)
+template <bool MQ>
+__device__ __forceinline__ size_t out_row(const KParams& prm, int s, int h) {
   if constexpr (!MQ) {
-    const int L = prm.lens[v];
-    if (L < 0 || L > max_len) *bad = true;
-    return min(max(L, 0), max_len);
+    return (size_t)s * prm.H + h;
   } else {
-    const int r = v / prm.q_len, i = v - r * prm.q_len;
-    const int L = prm.lens[r];
-    if (L < prm.q_len || L > max_len) *bad = true;
-    return min(max(L - prm.q_len + 1 + i, 0), max_len);
+    const int kv = h / prm.G, l = h - kv * prm.G, i = l / prm.Gu;
+    return ((size_t)s * prm.q_len + i) * prm.Hu + kv * prm.Gu + (l - i * prm.Gu);
+  }
+}
+// out_row for code shared by both kernel kinds (final writes only).
+__device__ __forceinline__ size_t out_row_rt(const KParams& prm, int s, int h) {
+  return prm.q_len > 1 ? out_row<true>(prm, s, h) : out_row<false>(prm, s, h);
+}
+// Positions [0, limit) that row head h of a sequence of L tokens sees.
+template <bool MQ>
+__device__ __forceinline__ int row_limit(const KParams& prm, int L, int h) {
+  if constexpr (!MQ) {
+    return L;
+  } else {
+    return L - prm.q_len + (h % prm.G) / prm.Gu + 1;
   }
 }
 
 struct UnitInfo {
   int s, p, hg, t0, t1, nb, np, nh, h0;
-  int pad[3];
+  int L;  // the sequence's tokens
+  int pad[2];
 };
 
 constexpr uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -167,7 +188,7 @@ __device__ __forceinline__ bool wait_issued(const volatile uint32_t* issued, uin
 
 // A work unit as the producer sees it.
 struct UnitPlan {
-  int s, p, hg, t0, t1, nb, np, nh, h0, kv;
+  int s, p, hg, t0, t1, nb, np, nh, h0, kv, L;
 };
 
 template <class C, bool MQ>
@@ -176,28 +197,20 @@ __device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pre
   UnitPlan U;
   const int pair = u / prm.n_hg;
   U.hg = u - pair * prm.n_hg;
-  int lo = 0, hi = MQ ? prm.S / prm.q_len : prm.S;  // pref[lo] <= pair < pref[lo + 1]
+  int lo = 0, hi = prm.S;  // pref[lo] <= pair < pref[lo + 1]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (pref[mid] <= pair) lo = mid; else hi = mid;
   }
   bool bad = false;  // flagged by the prefix scan already
-  int L;
-  if constexpr (!MQ) {
-    U.s = lo;
-    U.p = pair - pref[lo];
-    U.np = pref[lo + 1] - pref[lo];
-    L = visible_len<false>(prm, lo, prm.MB * BS, &bad);
-  } else {
-    const int slot = pair - pref[lo];
-    U.p = slot / prm.q_len;
-    U.s = lo * prm.q_len + (slot - U.p * prm.q_len);  // the row
-    L = visible_len<true>(prm, U.s, prm.MB * BS, &bad);
-    U.np = (L + prm.P - 1) / prm.P;
-  }
+  U.s = lo;
+  U.p = pair - pref[lo];
+  U.np = pref[lo + 1] - pref[lo];
+  const int L = seq_tokens<MQ>(prm, lo, prm.MB * BS, &bad);
+  U.L = L;
   U.t0 = U.p * prm.P;
   U.t1 = min(U.t0 + prm.P, L);
-  U.nb = U.p < U.np ? (U.t1 - U.t0 + BS - 1) / BS : 0;  // 0: a void slot
+  U.nb = (U.t1 - U.t0 + BS - 1) / BS;
   U.kv = U.hg / prm.hg_per_kv;
   const int hgk = U.hg - U.kv * prm.hg_per_kv;
   U.h0 = U.kv * prm.G + hgk * GT;
@@ -212,8 +225,7 @@ template <class C, bool MQ>
 __device__ __forceinline__ int load_block_id(const KParams& prm, const UnitPlan& U, int c0, int lane) {
   int b = 0;
   if (c0 + lane < U.nb) {
-    const int row = MQ ? U.s / prm.q_len : U.s;  // table row of the cached sequence
-    b = __ldg(prm.bt + (size_t)row * prm.MB + U.t0 / C::BS + c0 + lane);
+    b = __ldg(prm.bt + (size_t)U.s * prm.MB + U.t0 / C::BS + c0 + lane);
     if ((unsigned)b >= (unsigned)prm.num_blocks) {
       atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
       b = 0;
@@ -236,24 +248,11 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   int* err = prm.hdr + kHdrError;
   const uint64_t pol_stream = l2_policy_evict_first();
   const uint64_t pol_keep = l2_policy_evict_last();
-  const int total = pref[MQ ? prm.S / prm.q_len : prm.S] * prm.n_hg;
-  // Plan unit u; multi-query kernels skip void slots (a query row whose
-  // causal prefix ends before the slot's partition) by claiming further
-  // indices.
+  const int total = pref[prm.S] * prm.n_hg;
   auto plan_next = [&](int u, UnitPlan& Up) -> bool {
-    if constexpr (!MQ) {
-      if (u >= total) return false;
-      Up = plan_unit<C, false>(prm, pref, u);
-      return true;
-    } else {
-      while (u < total) {
-        Up = plan_unit<C, true>(prm, pref, u);
-        if (Up.nb > 0) return true;
-        if (lane == 0) u = atomicAdd(prm.hdr + kHdrWork, 1);
-        u = __shfl_sync(0xffffffffu, u, 0);
-      }
-      return false;
-    }
+    if (u >= total) return false;
+    Up = plan_unit<C, MQ>(prm, pref, u);
+    return true;
   };
 
   uint32_t g = 0;   // blocks whose copies are issued, in order
@@ -276,15 +275,24 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
       } else if (okp) {
         UnitInfo& I = info[slot];
         I.s = Up.s; I.p = Up.p; I.hg = Up.hg; I.t0 = Up.t0; I.t1 = Up.t1; I.nb = Up.nb;
-        I.np = Up.np; I.nh = Up.nh; I.h0 = Up.h0;
+        I.np = Up.np; I.nh = Up.nh; I.h0 = Up.h0; I.L = Up.L;
         const uint32_t qbytes = (uint32_t)(Up.nh * D * 2);
         mbar_arrive_expect_tx(bar_ufull + 8 * slot, qbytes);
-        bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT,
-                      static_cast<const T*>(prm.q) + ((size_t)Up.s * prm.H + Up.h0) * D, qbytes,
-                      bar_ufull + 8 * slot, pol_keep);
+        if constexpr (!MQ)
+          bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT,
+                        static_cast<const T*>(prm.q) + ((size_t)Up.s * prm.H + Up.h0) * D, qbytes,
+                        bar_ufull + 8 * slot, pol_keep);
       }
     }
     okp = __shfl_sync(0xffffffffu, (int)okp, 0) != 0;
+    if constexpr (MQ) {
+      // The row heads of a multi-query unit are scattered over the caller's
+      // [S, q_len, H] rows: one row copy per lane.
+      if (okp && have && lane < Up.nh)
+        bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT + lane * D * 2,
+                      static_cast<const T*>(prm.q) + out_row<true>(prm, Up.s, Up.h0 + lane) * D,
+                      (uint32_t)(D * 2), bar_ufull + 8 * slot, pol_keep);
+    }
     if (okp) ++kq;
     return okp;
   };
@@ -500,19 +508,22 @@ __device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, 
 #pragma unroll
       for (int j = 1; j < G8; ++j) gm = fmaxf(gm, mv[j]);
       const float Mn = fmaxf(M, gm);
-      const float sc = exp2f((M - Mn) * kLog2e);
+      // States a causal row never reached are (-inf, 0): while every state so
+      // far is one, subtract 0 so that they weigh 0 instead of NaN.
+      const float Ms = (Mn == -INFINITY) ? 0.f : Mn;
+      const float sc = exp2f((M - Ms) * kLog2e);
       tot *= sc;
       acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
 #pragma unroll
       for (int j = 0; j < G8; ++j) {
-        const float w = exp2f((mv[j] - Mn) * kLog2e) * lv[j];
+        const float w = exp2f((mv[j] - Ms) * kLog2e) * lv[j];
         tot += w;
         acc.x = fmaf(w, ov[j].x, acc.x); acc.y = fmaf(w, ov[j].y, acc.y);
         acc.z = fmaf(w, ov[j].z, acc.z); acc.w = fmaf(w, ov[j].w, acc.w);
       }
       M = Mn;
     }
-    const float inv = 1.f / tot;
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
     const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     if (J.kind == 1) {
       reinterpret_cast<float4*>(prm.ws_co + (row * prm.Cmax + J.c) * D)[d4] = r;
@@ -524,10 +535,11 @@ __device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, 
       uint2 v;
       v.x = F16Traits<T>::pack(r.x, r.y);
       v.y = F16Traits<T>::pack(r.z, r.w);
-      *reinterpret_cast<uint2*>(static_cast<T*>(prm.out) + row * D + d4 * 4) = v;
+      const size_t orow = out_row_rt(prm, J.s, J.h0 + gh);
+      *reinterpret_cast<uint2*>(static_cast<T*>(prm.out) + orow * D + d4 * 4) = v;
       // Final combine: the log-sum-exp of all the sequence's scores is
       // M + log(total) (natural-log units: the partition and chunk maxima are).
-      if (d4 == 0 && prm.lse) prm.lse[row] = M + logf(tot);
+      if (d4 == 0 && prm.lse) prm.lse[orow] = M + logf(tot);
     }
   }
 }
@@ -759,28 +771,28 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
   const int S = prm.S, H = prm.H, Pmax = prm.Pmax;
   T* out = static_cast<T*>(prm.out);
 
-  // Unused partitions: sentinels (m = -inf, l = 0).  Empty sequences: zeros.
+  // Unused partitions: sentinels (m = -inf, l = 0).  Empty sequences: zeros
+  // (a multi-query sequence is never empty: it holds its new tokens).
   {
-    const int max_len = prm.MB * C::BS;
-    bool bad = false;  // flagged by the prefix scan already
     const long long n1 = (long long)S * H * Pmax;
     for (long long i = (long long)blockIdx.x * NCT + ctid; i < n1; i += (long long)gridDim.x * NCT) {
       const int s = (int)(i / ((long long)H * Pmax));
       const int p = (int)(i % Pmax);
-      const int np = MQ ? (visible_len<true>(prm, s, max_len, &bad) + prm.P - 1) / prm.P : pref[s + 1] - pref[s];
-      if (p >= np) {
+      if (p >= pref[s + 1] - pref[s]) {
         prm.ws_m[i] = -INFINITY;
         prm.ws_l[i] = 0.f;
       }
     }
-    const long long n2 = (long long)S * H * (D / 8);
-    for (long long i = (long long)blockIdx.x * NCT + ctid; i < n2; i += (long long)gridDim.x * NCT) {
-      const int s = (int)(i / ((long long)H * (D / 8)));
-      if (visible_len<MQ>(prm, s, max_len, &bad) == 0) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
-    }
-    if (prm.lse) {  // no scores: the log-sum-exp is log 0
-      for (int i = blockIdx.x * NCT + ctid; i < S * H; i += gridDim.x * NCT)
-        if (visible_len<MQ>(prm, i / H, max_len, &bad) == 0) prm.lse[i] = -INFINITY;
+    if constexpr (!MQ) {
+      const long long n2 = (long long)S * H * (D / 8);
+      for (long long i = (long long)blockIdx.x * NCT + ctid; i < n2; i += (long long)gridDim.x * NCT) {
+        const int s = (int)(i / ((long long)H * (D / 8)));
+        if (pref[s + 1] == pref[s]) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
+      }
+      if (prm.lse) {  // no scores: the log-sum-exp is log 0
+        for (int i = blockIdx.x * NCT + ctid; i < S * H; i += gridDim.x * NCT)
+          if (pref[i / H + 1] == pref[i / H]) prm.lse[i] = -INFINITY;
+      }
     }
   }
 
@@ -818,6 +830,10 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
                     prm.scale_log2, lane);
+    if constexpr (C::kMma) {
+      const int hq = I.h0 + (lane & 3) * 2;  // this lane's two heads of the fragment
+      cons.set_limits(row_limit<MQ>(prm, I.L, hq), row_limit<MQ>(prm, I.L, hq + 1));
+    }
     fence_proxy_async_smem();  // the query slot is refilled by a bulk copy: same ordering as a stage
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_uempty + 8 * slot);
@@ -834,7 +850,8 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
       // waits for its copies before the CTA exits).
       if (!__all_sync(0xffffffffu, okb)) break;
       const int ntok = min(BS, I.t1 - I.t0 - j * BS);
-      cons.block(smem + st * LY::STAGE, smem + st * LY::STAGE + LY::KBYTES, ntok, lane, scr);
+      cons.block(smem + st * LY::STAGE, smem + st * LY::STAGE + LY::KBYTES, ntok, lane, scr,
+                 I.t0 + j * BS);
       // The stage is refilled by a bulk copy (async proxy) once released:
       // every lane's reads of it (generic proxy) are ordered before that
       // write by a proxy fence, or the copy can land under reads still
@@ -935,9 +952,12 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
 #pragma unroll
       for (int w = 0; w < NC; ++w) M = fmaxf(M, epi_ml[(w * GT + i) * 2]);
       float den = 0.f;
+      // A causal row with no position in this partition has M = -inf: its
+      // weights come out 0 (subtracting 0), its state (-inf, 0, 0).
+      const float Ms = (M == -INFINITY) ? 0.f : M;
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
-        const float f = exp2f(epi_ml[(w * GT + i) * 2] - M);
+        const float f = exp2f(epi_ml[(w * GT + i) * 2] - Ms);
         ef[w * GT + i] = f;
         den = fmaf(f, epi_ml[(w * GT + i) * 2 + 1], den);
       }
@@ -957,14 +977,15 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
         num.x = fmaf(f, v.x, num.x); num.y = fmaf(f, v.y, num.y);
         num.z = fmaf(f, v.z, num.z); num.w = fmaf(f, v.w, num.w);
       }
-      const float inv = 1.f / ef[NC * GT + gh];
+      const float den = ef[NC * GT + gh];
+      const float inv = den > 0.f ? 1.f / den : 0.f;
       const float4 val = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
       const size_t sh = (size_t)I.s * H + I.h0 + gh;
       if (single) {
         uint2 v;
         v.x = F16Traits<T>::pack(val.x, val.y);
         v.y = F16Traits<T>::pack(val.z, val.w);
-        *reinterpret_cast<uint2*>(out + sh * D + d4 * 4) = v;
+        *reinterpret_cast<uint2*>(out + out_row_rt(prm, I.s, I.h0 + gh) * D + d4 * 4) = v;
       } else {
         reinterpret_cast<float4*>(prm.ws_o + (sh * Pmax + I.p) * D)[d4] = val;
       }
@@ -973,7 +994,7 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
         prm.ws_l[sh * Pmax + I.p] = ef[NC * GT + gh];
         // A single-partition sequence ends here: its log-sum-exp is the
         // merged maximum (log2 units -> natural) plus the log of the merged sum.
-        if (single && prm.lse) prm.lse[sh] = rstat[gh * 2] * kLn2 + logf(ef[NC * GT + gh]);
+        if (single && prm.lse) prm.lse[out_row_rt(prm, I.s, I.h0 + gh)] = rstat[gh * 2] * kLn2 + logf(ef[NC * GT + gh]);
       }
     }
     __syncwarp();
@@ -1039,23 +1060,18 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     *ch.finished = 0;
     fence_mbarrier_init();
   }
-  // pref[r] = work slots before cached sequence r: its partitions (those of
-  // its last query row, which sees every token) times q_len, the rows of one
-  // partition being consecutive slots so that they stream the same blocks at
-  // about the same time (the repeats hit L2).  A row whose causal prefix ends
-  // before a slot's partition leaves that slot void.  Lengths are clamped to
-  // [0, MB*BS]; an out-of-range length is recorded as a device error.
+  // pref[s] = number of used partitions before sequence s (lengths clamped to
+  // [0, MB*BS]; an out-of-range length is recorded as a device error).
   {
-    const int S = MQ ? prm.S / prm.q_len : prm.S, nthr = LY::THREADS, max_len = prm.MB * C::BS;
+    const int S = prm.S, nthr = LY::THREADS, max_len = prm.MB * C::BS;
     const int per = (S + nthr - 1) / nthr;
     const int beg = min(tid * per, S), end = min(beg + per, S);
     int sum = 0;
     for (int s = beg; s < end; ++s) {
       bool bad = false;
-      const int L = MQ ? visible_len<true>(prm, s * prm.q_len + prm.q_len - 1, max_len, &bad)
-                       : visible_len<false>(prm, s, max_len, &bad);
+      const int L = seq_tokens<MQ>(prm, s, max_len, &bad);
       if (bad) atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
-      sum += MQ ? (L + prm.P - 1) / prm.P * prm.q_len : (L + prm.P - 1) / prm.P;
+      sum += (L + prm.P - 1) / prm.P;
     }
     scan[tid] = sum;
     __syncthreads();
@@ -1073,9 +1089,7 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     for (int s = beg; s < end; ++s) {
       pref[s] = run;
       bool bad = false;
-      run += MQ ? (visible_len<true>(prm, s * prm.q_len + prm.q_len - 1, max_len, &bad) + prm.P - 1) /
-                      prm.P * prm.q_len
-                : (visible_len<false>(prm, s, max_len, &bad) + prm.P - 1) / prm.P;
+      run += (seq_tokens<MQ>(prm, s, max_len, &bad) + prm.P - 1) / prm.P;
     }
   }
   __syncthreads();

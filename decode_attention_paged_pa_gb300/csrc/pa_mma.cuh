@@ -39,6 +39,14 @@ struct MmaConsumer {
   float m[2], l[2];    // heads 2*(lane%4) and 2*(lane%4)+1
   float acc[NMT][4];
   float scale_log2;
+  int lim[2];  // positions [0, lim) the lane's two heads see (causal rows of multi-query decode)
+
+  // Positions each of this lane's two heads (hq, hq + 1) may see; a
+  // single-query unit sees every position of the sequence.
+  __device__ __forceinline__ void set_limits(int lim_hq, int lim_hq1) {
+    lim[0] = lim_hq;
+    lim[1] = lim_hq1;
+  }
 
   __device__ __forceinline__ void begin_unit(const T* qs, int nh, float sl2, int lane) {
     const int n = lane >> 2, kq = (lane & 3) * 2;
@@ -62,7 +70,8 @@ struct MmaConsumer {
     scale_log2 = sl2;
   }
 
-  __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane, float*) {
+  __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane, float*,
+                                        int tok0) {
     const uint32_t kbase = smem_addr(ks), vbase = smem_addr(vs);
     const int r = lane >> 2;
     float sc[NTT][4];
@@ -81,10 +90,10 @@ struct MmaConsumer {
 #pragma unroll
       for (int i = 0; i < 4; ++i) c[i] += c2[i];
       const int t_lo = tt * 16 + r, t_hi = t_lo + 8;
-      sc[tt][0] = t_lo < ntok ? c[0] * scale_log2 : -INFINITY;
-      sc[tt][1] = t_lo < ntok ? c[1] * scale_log2 : -INFINITY;
-      sc[tt][2] = t_hi < ntok ? c[2] * scale_log2 : -INFINITY;
-      sc[tt][3] = t_hi < ntok ? c[3] * scale_log2 : -INFINITY;
+      sc[tt][0] = (t_lo < ntok && tok0 + t_lo < lim[0]) ? c[0] * scale_log2 : -INFINITY;
+      sc[tt][1] = (t_lo < ntok && tok0 + t_lo < lim[1]) ? c[1] * scale_log2 : -INFINITY;
+      sc[tt][2] = (t_hi < ntok && tok0 + t_hi < lim[0]) ? c[2] * scale_log2 : -INFINITY;
+      sc[tt][3] = (t_hi < ntok && tok0 + t_hi < lim[1]) ? c[3] * scale_log2 : -INFINITY;
     }
     float alpha[2];
 #pragma unroll
@@ -96,13 +105,16 @@ struct MmaConsumer {
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
       const float mn = fmaxf(m[j], bm);
-      alpha[j] = exp2f(m[j] - mn);
+      // A causal row that has seen no position yet keeps m = -inf: subtract
+      // 0 instead, so its weights and rescale come out 0, not NaN.
+      const float ms = (mn == -INFINITY) ? 0.f : mn;
+      alpha[j] = exp2f(m[j] - ms);
       m[j] = mn;
       float ps = 0.f;
 #pragma unroll
       for (int tt = 0; tt < NTT; ++tt) {
-        sc[tt][j] = exp2f(sc[tt][j] - mn);
-        sc[tt][j + 2] = exp2f(sc[tt][j + 2] - mn);
+        sc[tt][j] = exp2f(sc[tt][j] - ms);
+        sc[tt][j + 2] = exp2f(sc[tt][j + 2] - ms);
         ps += sc[tt][j] + sc[tt][j + 2];
       }
       l[j] = fmaf(l[j], alpha[j], ps);

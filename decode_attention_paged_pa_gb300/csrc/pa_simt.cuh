@@ -65,8 +65,11 @@ struct SimtConsumer {
 
   // One staged block: ks = K block, vs = V block (shared memory), ntok valid
   // tokens (1..BS).  pw = this warp's scratch (SCRATCH_FLOATS floats).
+  // Causal rows are multi-query only, which runs on the tensor-core consumer.
+  __device__ __forceinline__ void set_limits(int, int) {}
+
   __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane,
-                                        float* pw) {
+                                        float* pw, int /*tok0*/) {
     const int tl = lane % TPP, slice = lane / TPP;
     float sc[NPASS][GT];
 #pragma unroll

@@ -94,6 +94,11 @@ WORKLOADS["spec4_gqa_bf16"] = _cfg(
     name="spec4_gqa_bf16", dtype="bf16", num_seqs=128, num_heads=32, num_kv_heads=8, head_size=128,
     block_size=16, partition_size=512, scale=1.0 / math.sqrt(128), max_blocks_per_seq=512,
     num_blocks=128 * 512, lens=(2048, 8192), lens_random=True, seed=1002, q_len=4)
+# The same on the MHA batch's shapes: 4 row heads per kv head, one unit each.
+WORKLOADS["spec4_mha_fp16"] = _cfg(
+    name="spec4_mha_fp16", dtype="fp16", num_seqs=64, num_heads=32, num_kv_heads=32, head_size=128,
+    block_size=16, partition_size=512, scale=1.0 / math.sqrt(128), max_blocks_per_seq=256,
+    num_blocks=64 * 256, lens=(512, 4096), lens_random=True, seed=1001, q_len=4)
 
 
 def custom(name="custom", dtype="fp16", num_seqs=2, num_heads=4, num_kv_heads=4, head_size=64,

@@ -185,10 +185,10 @@ int pa_decode_v2_lse(void* out, float* lse, const void* query, const void* key_c
  *   q_len       1 .. 1024 (q_len = 1 is pa_decode_v2_lse)
  *   workspace   >= pa_decode_v2_workspace_bytes(num_seqs * q_len, ...) bytes, or NULL
  * The other arguments, ownership and errors are those of pa_decode_v2 (kernel
- * family chosen as PA_VARIANT_AUTO).  Each (sequence, query row) is decoded
- * as a sequence of its own over the causal prefix it sees; the rows of one
- * sequence read the same cached blocks, one after another, so those reads
- * mostly hit L2.
+ * family chosen as PA_VARIANT_AUTO).  The q_len query rows of a sequence share
+ * its K/V loads: each kv head's q_len * (num_heads / num_kv_heads) rows are
+ * the rows of the tensor-core product (eight per work unit), each masked to
+ * the positions it may see.
  */
 int pa_decode_v2_mq(void* out, float* lse, const void* query, const void* key_cache,
                     const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,

@@ -127,7 +127,7 @@ def test_binding_launch_count_matches_kernel_limit():
     limit = int(re.search(r"#define PA_MAX_SEQS_PER_LAUNCH (\d+)", text).group(1))
     assert binding.MAX_ROWS_PER_LAUNCH == limit
     assert binding.launches_per_call(limit) == 1 and binding.launches_per_call(limit + 1) == 2
-    assert binding.launches_per_call(300, 4) == 2   # 256 sequences (1024 rows) per launch
+    assert binding.launches_per_call(300, 4) == 1   # multi-query rows share their sequence's launch
 
 
 def test_status_strings():
