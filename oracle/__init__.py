@@ -24,7 +24,10 @@ definition in ``pa_oracle.c``:
 * :func:`combine_lse` -- the same from phase-1 states (M + log total);
 * :func:`decode_mq`   -- multi-query decode: q_len new tokens per sequence, the
                          i-th at position L - q_len + i attending causally to
-                         positions 0 .. L - q_len + i (output and log-sum-exp).
+                         positions 0 .. L - q_len + i (output and log-sum-exp);
+* :func:`decode_fp8kv` -- decode over an E4M3 (fp8) KV cache with per-tensor
+                         k_scale / v_scale (key layout x = 16), and
+  :func:`e4m3_decode`   the code -> value map it uses.
 
 Inputs are the raw 16-bit patterns of fp16 / bf16 tensors (numpy ``uint16``)
 in the page's layouts; the fp32 ``scale`` is widened to double exactly.
@@ -81,6 +84,11 @@ def _declare(lib):
     lib.pa_oracle_combine_lse.restype = c_int
     lib.pa_oracle_decode_mq.argtypes = [dp, dp, up, up, up, ip, ip, c_double] + [c_int] * 9
     lib.pa_oracle_decode_mq.restype = c_int
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.pa_oracle_e4m3_decode.argtypes = [dp, u8p, c_int]
+    lib.pa_oracle_e4m3_decode.restype = c_int
+    lib.pa_oracle_decode_fp8kv.argtypes = [dp, dp, up, u8p, u8p, ip, ip, c_double, c_double, c_double] + [c_int] * 8
+    lib.pa_oracle_decode_fp8kv.restype = c_int
     lib.pa_oracle_max_threads.argtypes = []
     lib.pa_oracle_max_threads.restype = c_int
     return lib
@@ -119,6 +127,21 @@ def _u16(a) -> np.ndarray:
         a = a.view(np.uint16)
     if a.dtype != np.uint16:
         raise TypeError(f"expected 16-bit float data, got {a.dtype}")
+    return a
+
+
+def _u8(a) -> np.ndarray:
+    """Raw bytes of an fp8 / uint8 array (numpy or torch) as contiguous uint8."""
+    if hasattr(a, "detach"):
+        import torch
+
+        a = a.detach().cpu().contiguous()
+        if a.dtype != torch.uint8:
+            a = a.view(torch.uint8)
+        a = a.numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError(f"expected 8-bit codes, got {a.dtype}")
     return a
 
 
@@ -256,6 +279,39 @@ class Oracle:
         return out, lse
 
 
+    def e4m3_decode(self, codes) -> np.ndarray:
+        """Values of E4M3 codes (uint8 array-like) as float64."""
+        c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+        out = np.zeros(c.shape, dtype=np.float64)
+        rc = self.lib.pa_oracle_e4m3_decode(_ptr(out, ctypes.c_double), _ptr(c, ctypes.c_uint8), c.size)
+        if rc != 0:
+            raise ValueError("oracle e4m3_decode rejected its arguments")
+        return out
+
+    def decode_fp8kv(self, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                     k_scale: float, v_scale: float, qdtype: int, nthreads: int = 0):
+        """Decode over E4M3 caches (uint8 codes: key_cache [NB, KH, D/16, BS, 16], value_cache
+        [NB, KH, D, BS]); returns (out [S, H, D], lse [S, H]) in float64."""
+        q = _u16(query)
+        kc, vc = _u8(key_cache), _u8(value_cache)
+        bt, lens = _i32(block_tables), _i32(seq_lens)
+        S, H, D = q.shape
+        nb, KH, dx, BS, x = kc.shape
+        if x != 16 or dx * x != D or tuple(vc.shape) != (nb, KH, D, BS):
+            raise ValueError("fp8 caches must be [NB, KH, D/16, BS, 16] and [NB, KH, D, BS]")
+        MB = bt.shape[1]
+        out = np.zeros((S, H, D), dtype=np.float64)
+        lse = np.zeros((S, H), dtype=np.float64)
+        rc = self.lib.pa_oracle_decode_fp8kv(
+            _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), _ptr(q, ctypes.c_uint16),
+            _ptr(kc, ctypes.c_uint8), _ptr(vc, ctypes.c_uint8), _ptr(bt, ctypes.c_int32),
+            _ptr(lens, ctypes.c_int32), float(np.float32(scale)), float(np.float32(k_scale)),
+            float(np.float32(v_scale)), S, H, KH, D, BS, MB, qdtype, nthreads)
+        if rc != 0:
+            raise ValueError("oracle decode_fp8kv rejected its arguments")
+        return out, lse
+
+
 _default = None
 
 
@@ -288,3 +344,11 @@ def combine_lse(*args, **kwargs) -> np.ndarray:
 
 def decode_mq(*args, **kwargs):
     return default().decode_mq(*args, **kwargs)
+
+
+def e4m3_decode(*args, **kwargs) -> np.ndarray:
+    return default().e4m3_decode(*args, **kwargs)
+
+
+def decode_fp8kv(*args, **kwargs):
+    return default().decode_fp8kv(*args, **kwargs)

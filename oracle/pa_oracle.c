@@ -352,3 +352,90 @@ int pa_oracle_decode_mq(double* out, double* lse, const uint16_t* q, const uint1
     }
     return bad ? -1 : 0;
 }
+
+/* 8-bit float E4M3 (the "e4m3fn" variant: no infinities) -> double, from the
+ * format's definition: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits;
+ * exponent 0 is subnormal (fraction * 2^-9); exponent 15 with fraction 7 is
+ * NaN; every other code is finite, the largest being 1.75 * 2^8 = 448. */
+static double e4m3_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int expo = (b >> 3) & 0xf;
+    int frac = b & 0x7;
+    double v;
+    if (expo == 15 && frac == 7) {
+        v = NAN;
+    } else if (expo == 0) {
+        v = ldexp((double)frac, -9);                 /* 0.fff * 2^(1-7) */
+    } else {
+        v = ldexp((double)(8 + frac), expo - 10);    /* 1.fff * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+int pa_oracle_e4m3_decode(double* out, const uint8_t* codes, int n) {
+    if (n < 0) return -1;
+    for (int i = 0; i < n; ++i) out[i] = e4m3_to_double(codes[i]);
+    return 0;
+}
+
+/* key_cache[b, kh, d / x, o, d % x] with x = 16 / sizeof(element) = 16 for
+ * one-byte elements (the launcher of [PA-V2] takes x from the cache's last
+ * dimension). */
+static size_t key_index_x16(long b, int kh, int d, int o, int KH, int D, int BS) {
+    const int x = 16;
+    return ((((size_t)b * KH + kh) * (D / x) + d / x) * BS + o) * x + d % x;
+}
+
+/* Decode over an fp8 (E4M3) KV cache with per-tensor scales: the launcher of
+ * [PA-V2] takes kv_cache_dtype, k_scale and v_scale (and ignores them); the
+ * plain reading is that the cached bytes are E4M3 codes and the real keys and
+ * values are k_scale * K and v_scale * V.  query and the result are 16-bit as
+ * before (qdtype); key_cache [NB, KH, D/16, BS, 16] and value_cache
+ * [NB, KH, D, BS] hold the codes.  out [S, H, D], lse [S, H] (may be NULL);
+ * seq_lens[s] == 0 gives zeros and lse -inf. */
+int pa_oracle_decode_fp8kv(double* out, double* lse, const uint16_t* q, const uint8_t* kc,
+                           const uint8_t* vc, const int32_t* bt, const int32_t* lens, double scale,
+                           double k_scale, double v_scale, int S, int H, int KH, int D, int BS,
+                           int MB, int qdtype, int nthreads) {
+    if (S < 0 || H <= 0 || KH <= 0 || H % KH || D <= 0 || D % 16 || BS <= 0 || MB < 0)
+        return -1;
+    int bad = 0;
+    if (nthreads <= 0) nthreads = pa_oracle_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : bad)
+    for (long sh = 0; sh < (long)S * H; ++sh) {
+        int s = (int)(sh / H), h = (int)(sh % H);
+        int L = lens[s];
+        double* o_sh = out + (size_t)sh * D;
+        for (int d = 0; d < D; ++d) o_sh[d] = 0.0;
+        if (lse) lse[sh] = -INFINITY;
+        if (L <= 0) continue;
+        if (L > MB * BS) { bad = 1; continue; }
+        double* z = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!z) { bad = 1; continue; }
+        const int kh = h / (H / KH);
+        const uint16_t* qv = q + (size_t)sh * D;
+        for (int t = 0; t < L; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += to_double(qv[d], qdtype) *
+                       (k_scale * e4m3_to_double(kc[key_index_x16(b, kh, d, o, KH, D, BS)]));
+            z[t] = scale * acc;
+        }
+        double mu = -INFINITY;
+        for (int t = 0; t < L; ++t) if (z[t] > mu) mu = z[t];
+        double den = 0.0;
+        for (int t = 0; t < L; ++t) { z[t] = exp(z[t] - mu); den += z[t]; }
+        for (int t = 0; t < L; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            for (int d = 0; d < D; ++d)
+                o_sh[d] += z[t] * (v_scale * e4m3_to_double(vc[value_index(b, kh, d, o, KH, D, BS)]));
+        }
+        for (int d = 0; d < D; ++d) o_sh[d] /= den;
+        if (lse) lse[sh] = mu + log(den);
+        free(z);
+    }
+    return bad ? -1 : 0;
+}

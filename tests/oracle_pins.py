@@ -351,10 +351,70 @@ def pin_mq_uniform_causal_bounds(orc):
     assert np.array_equal(out[0, 0, 0], V0[0, 0]), "row 0 with L = q_len sees exactly token 0"
 
 
+def pin_e4m3_library(orc):
+    """Special case = library routine: every one of the 256 E4M3 codes decodes
+    to torch.float8_e4m3fn's value (NaN exactly where torch gives NaN)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = orc.e4m3_decode(codes.numpy())
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok]) and np.array_equal(np.signbit(got[ok]), np.signbit(want[ok]))
+
+
+def pin_e4m3_golden(orc):
+    """Hand-derived E4M3 values (tests/golden/e4m3_codes.txt)."""
+    rows = read_golden("e4m3_codes.txt")
+    got = orc.e4m3_decode(np.array([int(r[0], 16) for r in rows], dtype=np.uint8))
+    for (code, value, *_), g in zip(rows, got):
+        v = float(value)
+        assert (math.isnan(g) and math.isnan(v)) or (g == v and math.copysign(1, g) == math.copysign(1, v)), code
+
+
+def pin_fp8kv_textbook(orc):
+    """Special case = textbook: numpy softmax(scale q (k_scale K)^T) (v_scale V)
+    with K and V decoded by torch's float8_e4m3fn and gathered through the block
+    table from token-major views obtained by permuting the caches' axes."""
+    from pa_testutil import fp8_random_case
+    for dt in (FP16, BF16):
+        q, kc, vc, bt, lens = fp8_random_case(131 + dt, S=3, H=4, KH=2, D=32, BS=4, lens=[1, 7, 13],
+                                              qdtype=TORCH_DT[dt])
+        out, lse = orc.decode_fp8kv(q, kc, vc, bt, lens, 0.3, 0.5, 2.0, dt)
+        nb, KH, dx, BS, x = kc.shape
+        k_tok = kc.view(torch.float8_e4m3fn).to(torch.float64).permute(0, 3, 1, 2, 4).reshape(nb, BS, KH, dx * x)
+        v_tok = vc.view(torch.float8_e4m3fn).to(torch.float64).permute(0, 3, 1, 2)
+        sc = float(np.float32(0.3))
+        for s in range(3):
+            L = int(lens[s])
+            t = torch.arange(L)
+            b = bt[s].long()[t // BS]
+            K, V = (0.5 * k_tok[b, t % BS]).numpy(), (2.0 * v_tok[b, t % BS]).numpy()
+            for h in range(4):
+                z = sc * (K[:, h // 2, :] @ q[s, h].to(torch.float64).numpy())
+                w = np.exp(z - z.max())
+                _close(out[s, h], (w / w.sum()) @ V[:, h // 2, :], 1e-13, "fp8 textbook")
+                _close(lse[s, h], z.max() + math.log(w.sum()), 1e-13, "fp8 lse")
+
+
+def pin_fp8kv_scales(orc):
+    """Scales act as multipliers: v_scale 2 doubles the output exactly, and
+    k_scale 2 with scale s equals k_scale 1 with scale 2 s exactly."""
+    from pa_testutil import fp8_random_case
+    q, kc, vc, bt, lens = fp8_random_case(141, S=2, H=2, KH=1, D=32, BS=4, lens=[9, 3])
+    a, la = orc.decode_fp8kv(q, kc, vc, bt, lens, 0.25, 1.0, 1.0, FP16)
+    b, lb = orc.decode_fp8kv(q, kc, vc, bt, lens, 0.25, 1.0, 2.0, FP16)
+    assert np.array_equal(b, 2.0 * a) and np.array_equal(la, lb)
+    c, lc = orc.decode_fp8kv(q, kc, vc, bt, lens, 0.25, 2.0, 1.0, FP16)
+    d, ld = orc.decode_fp8kv(q, kc, vc, bt, lens, 0.5, 1.0, 1.0, FP16)
+    assert np.array_equal(c, d) and np.array_equal(lc, ld)
+    assert np.max(np.abs(c - a)) > 1e-6, "k_scale must matter"
+
+
 ALL_PINS = [
     pin_textbook_gqa, pin_bruteforce_tiny, pin_golden_two_token, pin_golden_layout,
     pin_seq_len_one, pin_uniform_weights, pin_shift_invariance, pin_permutation_invariance,
     pin_partition_invariance, pin_empty_sequence, pin_combine_closed_form,
     pin_lse_golden_two_token, pin_lse_closed_forms, pin_lse_library, pin_lse_partition_identity,
     pin_mq_textbook_causal, pin_mq_uniform_causal_bounds,
+    pin_e4m3_library, pin_e4m3_golden, pin_fp8kv_textbook, pin_fp8kv_scales,
 ]

@@ -137,3 +137,34 @@ def compact_sequences(inputs: dict, seqs):
     q_sub = q[torch.tensor(seqs, device=q.device)].cpu()
     lens_sub = lens_cpu[seqs].clone()
     return q_sub, kc_sub, vc_sub, bt_sub, lens_sub
+
+
+def fp8_caches_from_tokens(k_tok: torch.Tensor, v_tok: torch.Tensor):
+    """E4M3 code caches from token-major uint8 pools [nb, BS, KH, D]: key_cache
+    [nb, KH, D/16, BS, 16] (x = 16 one-byte elements per 16-byte chunk) and
+    value_cache [nb, KH, D, BS], by permuting axes."""
+    nb, BS, KH, D = k_tok.shape
+    key_cache = k_tok.reshape(nb, BS, KH, D // 16, 16).permute(0, 2, 3, 1, 4).contiguous()
+    value_cache = v_tok.permute(0, 2, 3, 1).contiguous()
+    return key_cache, value_cache
+
+
+def fp8_random_case(seed, S, H, KH, D, BS, lens, qdtype=torch.float16, MB=None, num_blocks=None):
+    """Random inputs with E4M3 code caches (values drawn from N(0, 1), rounded to
+    E4M3 by torch; no NaN codes) and a random physical placement."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.tensor(lens, dtype=torch.int32)
+    if MB is None:
+        MB = max(1, math.ceil(max(int(v) for v in lens) / BS)) if len(lens) else 1
+    if num_blocks is None:
+        num_blocks = S * MB
+    q = torch.randn((S, H, D), generator=g).to(qdtype)
+    to_codes = lambda t: t.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    k_tok = to_codes(torch.randn((num_blocks, BS, KH, D), generator=g))
+    v_tok = to_codes(torch.randn((num_blocks, BS, KH, D), generator=g))
+    kc, vc = fp8_caches_from_tokens(k_tok, v_tok)
+    if num_blocks >= S * MB:
+        bt = torch.randperm(num_blocks, generator=g)[: S * MB].view(S, MB).to(torch.int32)
+    else:
+        bt = torch.stack([torch.randperm(num_blocks, generator=g)[:MB] for _ in range(S)]).to(torch.int32)
+    return q, kc, vc, bt, lens

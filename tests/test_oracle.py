@@ -50,6 +50,12 @@ MUTANTS = [
     ("mq_causal_off_by_one", "const int visible = L - q_len + i + 1;", "const int visible = L - q_len + i;", 1),
     ("mq_rows_reversed", "const int visible = L - q_len + i + 1;", "const int visible = L - i;", 1),
     ("mq_first_query_row_only", "q + ((size_t)(s * q_len + i) * H + h) * D", "q + ((size_t)(s * q_len) * H + h) * D", 1),
+    ("e4m3_bias", "ldexp((double)(8 + frac), expo - 10)", "ldexp((double)(8 + frac), expo - 11)", 1),
+    ("e4m3_subnormal_scale", "v = ldexp((double)frac, -9);", "v = ldexp((double)frac, -10);", 1),
+    ("e4m3_no_nan_rule", "if (expo == 15 && frac == 7) {", "if (0) {", 1),
+    ("fp8_k_scale_dropped", "(k_scale * e4m3_to_double(", "(1.0 * e4m3_to_double(", 1),
+    ("fp8_v_scale_dropped", "(v_scale * e4m3_to_double(", "(1.0 * e4m3_to_double(", 1),
+    ("fp8_key_x8", "    const int x = 16;\n    return", "    const int x = 8;\n    return", 1),
     ("empty_sequence_not_zero", "if (L <= 0) continue;\n        if (L > MB * BS) { bad = 1; continue; }\n        double* z",
      "if (L > MB * BS) { bad = 1; continue; }\n        double* z", 1),
 ]
