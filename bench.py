@@ -217,6 +217,10 @@ def oracle_sample(w: workloads.Workload, cpu_seconds: float):
 
 def oracle_call(oracle, w: workloads.Workload, inp):
     """One oracle pass over a batch (multi-query batches through decode_mq)."""
+    if w.kv_dtype == "e4m3":
+        return oracle.decode_fp8kv(inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
+                                   inp["seq_lens"], inp["scale"], w.k_scale, w.v_scale,
+                                   workloads.DTYPE_CODES[w.dtype])
     args = (inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"], inp["seq_lens"],
             inp["scale"], workloads.DTYPE_CODES[w.dtype])
     return oracle.decode_mq(*args) if w.q_len > 1 else oracle.decode(*args)
@@ -286,7 +290,7 @@ def run_native(args, rank, world, local):
     lens = inp["seq_lens"].tolist()
     nbytes = workloads.algorithmic_bytes(w, lens)
     tokens = workloads.kv_tokens(lens)
-    kv_bytes = inp["key_cache"].numel() * 2 * 2
+    kv_bytes = 2 * inp["key_cache"].numel() * inp["key_cache"].element_size()
     variant = {"auto": binding.PA_VARIANT_AUTO, "simt": binding.PA_VARIANT_SIMT,
                "mma": binding.PA_VARIANT_MMA}[args.variant]
     out = torch.empty_like(inp["query"])
@@ -298,7 +302,11 @@ def run_native(args, rank, world, local):
     launches_per_step = binding.launches_per_call(w.num_seqs, w.q_len)
 
     def step():
-        if w.q_len > 1:
+        if w.kv_dtype == "e4m3":
+            binding.pa_decode_v2_fp8(out, inp["query"], inp["key_cache"], inp["value_cache"],
+                                     inp["block_tables"], inp["seq_lens"], inp["scale"], w.k_scale,
+                                     w.v_scale, partition_size=w.partition_size, workspace=ws, stream=stream)
+        elif w.q_len > 1:
             binding.pa_decode_v2_mq(out, inp["query"], inp["key_cache"], inp["value_cache"],
                                     inp["block_tables"], inp["seq_lens"], inp["scale"],
                                     partition_size=w.partition_size, workspace=ws, stream=stream)
@@ -340,7 +348,7 @@ def run_native(args, rank, world, local):
 
     # ---- e2e: per-step inputs from pinned host memory, output back to host
     e2e = None
-    if not args.no_e2e and w.q_len == 1:
+    if not args.no_e2e and w.q_len == 1 and not w.kv_dtype:
         q_h = inp["query"].cpu().pin_memory()
         bt_h = inp["block_tables"].cpu().pin_memory()
         lens_h = inp["seq_lens"].cpu().pin_memory()
@@ -402,7 +410,7 @@ def run_native(args, rank, world, local):
                    "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
                    "block_size": w.block_size, "partition_size": w.partition_size,
                    "seq_lens": f"{min(lens)}..{max(lens)} (sum {tokens})", "accumulate": "fp32",
-                   "q_len": w.q_len, "variant": args.variant, "parallelism": f"replicas x{world}",
+                   "q_len": w.q_len, "kv_dtype": w.kv_dtype or w.dtype, "variant": args.variant, "parallelism": f"replicas x{world}",
                    "l2": f"no flush: KV pool {kv_bytes / 1e9:.2f} GB per rank > L2 {L2_BYTES / 1e6:.0f} MB"},
         "kv_tokens_per_s": tokens * world * args.steps / seconds,
         "pct_of_measured_peak": 100.0 * value / world / peak,

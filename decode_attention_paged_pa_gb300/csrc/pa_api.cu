@@ -107,7 +107,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
                 float scale, int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_size,
                 int block_size, int partition_size, int dtype, void* stream, int max_blocks_per_seq,
                 int num_blocks, void* workspace, size_t workspace_bytes, int variant, int max_ctas,
-                long long timeout_ns) {
+                long long timeout_ns, bool kv_fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
   // Multi-query: the kernel sees q_len "row heads" per caller head (H below
   // counts them), q_len * G per kv head, all sharing the kv head's blocks.
   if (q_len < 1 || q_len > kMaxSeqsPerLaunch || num_heads <= 0 ||
@@ -120,7 +120,11 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   if (variant < PA_VARIANT_AUTO || variant > PA_VARIANT_MMA || max_ctas < 0 || timeout_ns < 0)
     return PA_ERR_INVALID_ARG;
   if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PA_ERR_INVALID_ARG;
+  if (!(k_scale == k_scale) || k_scale == INFINITY || k_scale == -INFINITY || !(v_scale == v_scale) ||
+      v_scale == INFINITY || v_scale == -INFINITY)
+    return PA_ERR_INVALID_ARG;
   if (!supported(D, BS, P)) return PA_ERR_UNSUPPORTED;
+  if (kv_fp8 && variant == PA_VARIANT_SIMT) return PA_ERR_UNSUPPORTED;  // fp8 runs on tensor cores
   if (S == 0) return PA_OK;
   if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens)
     return PA_ERR_INVALID_ARG;
@@ -133,7 +137,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   if (workspace && workspace_bytes < w.total) return PA_ERR_WORKSPACE;
 
   const int G = H / KH;
-  if (variant == PA_VARIANT_AUTO) variant = (G == 1) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
+  if (variant == PA_VARIANT_AUTO) variant = (G == 1 && !kv_fp8) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
   const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : kSimtGroup;
   const int hg_per_kv = (G + gt - 1) / gt;
   const int n_hg = KH * hg_per_kv;
@@ -182,7 +186,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     prm.ws_cl = reinterpret_cast<float*>(ws + w.cl) + (size_t)s0 * H * w.cmax;
     prm.ws_co = reinterpret_cast<float*>(ws + w.co) + (size_t)s0 * H * w.cmax * D;
     prm.Cmax = w.cmax;
-    prm.scale_log2 = scale * kLog2e;
+    prm.scale_log2 = scale * k_scale * kLog2e;
+    prm.v_scale = v_scale;
     prm.S = n;
     prm.H = H;
     prm.KH = KH;
@@ -195,7 +200,10 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     prm.n_hg = n_hg;
     prm.timeout_ns = timeout_ns > 0 ? timeout_ns : (1LL << 31);
     cudaError_t e;
-    if (variant == PA_VARIANT_MMA)
+    if (kv_fp8)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma8_f16(prm, D, BS, max_ctas, st)
+                                 : launch_mma8_bf16(prm, D, BS, max_ctas, st);
+    else if (variant == PA_VARIANT_MMA)
       e = dtype == PA_DTYPE_FP16 ? launch_mma_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma_bf16(prm, D, BS, max_ctas, st);
     else
@@ -232,6 +240,19 @@ extern "C" int pa_decode_v2_lse(void* out, float* lse, const void* query, const 
                      num_seqs, 1, num_heads, num_kv_heads, head_size, block_size, partition_size,
                      dtype, stream, max_blocks_per_seq, num_blocks, workspace, workspace_bytes,
                      PA_VARIANT_AUTO, 0, 0);
+}
+
+extern "C" int pa_decode_v2_fp8(void* out, float* lse, const void* query, const void* key_cache,
+                                const void* value_cache, const int32_t* block_tables,
+                                const int32_t* seq_lens, float scale, float k_scale, float v_scale,
+                                int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                int block_size, int partition_size, int dtype, void* stream,
+                                int max_blocks_per_seq, int num_blocks, void* workspace,
+                                size_t workspace_bytes) {
+  return decode_impl(out, lse, query, key_cache, value_cache, block_tables, seq_lens, scale,
+                     num_seqs, 1, num_heads, num_kv_heads, head_size, block_size, partition_size,
+                     dtype, stream, max_blocks_per_seq, num_blocks, workspace, workspace_bytes,
+                     PA_VARIANT_AUTO, 0, 0, true, k_scale, v_scale);
 }
 
 extern "C" int pa_decode_v2_mq(void* out, float* lse, const void* query, const void* key_cache,

@@ -63,7 +63,8 @@ struct KParams {
   int q_len;     // query tokens per sequence (multi-query kernels; 1 otherwise)
   int Hu, Gu;    // the caller's heads and heads per kv head; H and G below count row
                  // heads, q_len of them per caller head (H = q_len * Hu, G = q_len * Gu)
-  float scale_log2;
+  float scale_log2;   // softmax scale (times k_scale for an fp8 cache) times log2 e
+  float v_scale;      // multiplies every output: 1, or an fp8 cache's v_scale
   int S, H, KH, G, MB, num_blocks, P, Pmax, Cmax;
   int hg_per_kv;  // ceil(G / GT)
   int n_hg;       // KH * hg_per_kv
@@ -123,7 +124,7 @@ struct Layout {
   static constexpr int NC = NC_, NSTAGE = NSTAGE_, UQ = 2;
   static constexpr int NCT = NC * 32;          // consumer threads
   static constexpr int THREADS = NCT + 64;     // + producer warp + epilogue warp
-  static constexpr uint32_t KBYTES = C::D * C::BS * 2;
+  static constexpr uint32_t KBYTES = C::D * C::BS * C::KV_ESZ;  // one block of one kv head
   static constexpr uint32_t STAGE = 2 * KBYTES;
   static constexpr uint32_t RING = NSTAGE * STAGE;
   static constexpr uint32_t QSLOT = C::GT * C::D * 2;
@@ -241,7 +242,10 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   using T = typename C::T;
   constexpr int D = C::D, NS = LY::NSTAGE, UQ = LY::UQ;
   // Blocks issued together, one per lane, as their stages free up.
-  constexpr int BATCH = NS < 8 ? NS : 8;
+#ifndef PA_ISSUE_BATCH
+#define PA_ISSUE_BATCH 8
+#endif
+  constexpr int BATCH = NS < PA_ISSUE_BATCH ? NS : PA_ISSUE_BATCH;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bar_full = sbase + LY::OFF_BAR, bar_empty = bar_full + NS * 8;
   const uint32_t bar_ufull = bar_empty + NS * 8, bar_uempty = bar_ufull + UQ * 8;
@@ -348,8 +352,9 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
             const uint32_t dst = sbase + st * LY::STAGE;
             const size_t off = ((size_t)bi * prm.KH + U.kv) * (size_t)(D * C::BS);
             mbar_arrive_expect_tx(bar_full + 8 * st, LY::STAGE);
-            bulk_copy_g2s(dst, static_cast<const T*>(prm.kc) + off, LY::KBYTES, bar_full + 8 * st, pol_stream);
-            bulk_copy_g2s(dst + LY::KBYTES, static_cast<const T*>(prm.vc) + off, LY::KBYTES,
+            bulk_copy_g2s(dst, static_cast<const uint8_t*>(prm.kc) + off * C::KV_ESZ, LY::KBYTES,
+                          bar_full + 8 * st, pol_stream);
+            bulk_copy_g2s(dst + LY::KBYTES, static_cast<const uint8_t*>(prm.vc) + off * C::KV_ESZ, LY::KBYTES,
                           bar_full + 8 * st, pol_stream);
             done = true;
           }
@@ -978,7 +983,7 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
         num.z = fmaf(f, v.z, num.z); num.w = fmaf(f, v.w, num.w);
       }
       const float den = ef[NC * GT + gh];
-      const float inv = den > 0.f ? 1.f / den : 0.f;
+      const float inv = (den > 0.f ? 1.f / den : 0.f) * prm.v_scale;
       const float4 val = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
       const size_t sh = (size_t)I.s * H + I.h0 + gh;
       if (single) {

@@ -34,9 +34,9 @@ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 template <class C, int NC>
 struct Sizing {
   using L1 = Layout<C, NC, 1>;
-  static constexpr uint32_t other = L1::FIXED - L1::RING + 64 * 8 + 16;
+  static constexpr uint32_t other = L1::FIXED - L1::RING + 128 * 8 + 16;
   static constexpr uint32_t pref_max = al16((kMaxSeqsPerLaunch + 1) * 4);
-  static constexpr int NS = cmin(32, (int)((kSmemBudget - other - pref_max) / L1::STAGE));
+  static constexpr int NS = cmin(64, (int)((kSmemBudget - other - pref_max) / L1::STAGE));
   static_assert(NS >= 2, "shared memory holds fewer than two ring stages");
   using LY = Layout<C, NC, NS>;
   static_assert(LY::bytes(kMaxSeqsPerLaunch) <= kSmemBudget, "shared memory over budget");

@@ -29,6 +29,9 @@ cudaError_t launch_simt_f16(const KParams& prm, int D, int BS, int max_ctas, cud
 cudaError_t launch_simt_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+// The same over an fp8 (E4M3) KV cache, queries and output fp16 / bf16.
+cudaError_t launch_mma8_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 
 // SM count of the current device (cached per device).
 int device_sm_count();

@@ -18,17 +18,24 @@
 // weights enter the second product rounded to the element type.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include <type_traits>
 
 #include "pa_common.cuh"
 
 namespace pa {
 
-template <typename T_, int D_, int BS_>
+// FP8_: the caches hold E4M3 codes (one byte per element, key layout
+// [D/16][BS][16]); operand fragments are then read code pair by code pair and
+// widened to T (every E4M3 value is exact in fp16 and bf16).
+template <typename T_, int D_, int BS_, bool FP8_ = false>
 struct MmaConsumer {
   using T = T_;
   static constexpr int D = D_, BS = BS_, GT = 8;
   static constexpr bool kMma = true;
+  static constexpr bool kFp8 = FP8_;
+  static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
   static constexpr int NK = D / 16;    // k-steps of the score product
   static constexpr int NMT = D / 16;   // 16-dim tiles of the value product
   static constexpr int NTT = BS / 16;  // 16-token tiles per block
@@ -40,6 +47,20 @@ struct MmaConsumer {
   float acc[NMT][4];
   float scale_log2;
   int lim[2];  // positions [0, lim) the lane's two heads see (causal rows of multi-query decode)
+
+  // The two E4M3 codes at shared address addr as a packed pair of T (the
+  // lower code in the lower half, as the fragments want it).
+  __device__ __forceinline__ static uint32_t fp8_pair(uint32_t addr) {
+    uint16_t raw;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(raw) : "r"(addr));
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(raw, __NV_E4M3);
+    if constexpr (std::is_same<T, __half>::value) {
+      return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+      return F16Traits<T>::pack(f.x, f.y);
+    }
+  }
 
   // Positions each of this lane's two heads (hq, hq + 1) may see; a
   // single-query unit sees every position of the sequence.
@@ -82,8 +103,18 @@ struct MmaConsumer {
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
         uint32_t a[4];
-        const int tok = tt * 16 + (lane & 15), chunk = 2 * kk + (lane >> 4);
-        ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
+        if constexpr (kFp8) {
+          // A = K[16 tokens x 16 dims]: rows tt*16 + r (+8), columns (lane%4)*2 (+8);
+          // chunk kk of the key block holds dims 16kk.. of every token in 16 bytes.
+          const uint32_t lo = kbase + (kk * BS + tt * 16 + r) * 16 + (lane & 3) * 2, hi = lo + 8 * 16;
+          a[0] = fp8_pair(lo);
+          a[1] = fp8_pair(hi);
+          a[2] = fp8_pair(lo + 8);
+          a[3] = fp8_pair(hi + 8);
+        } else {
+          const int tok = tt * 16 + (lane & 15), chunk = 2 * kk + (lane >> 4);
+          ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
+        }
         if (kk & 1) Mma<T>::run(c2, a, qb[kk][0], qb[kk][1]);
         else Mma<T>::run(c, a, qb[kk][0], qb[kk][1]);
       }
@@ -131,7 +162,8 @@ struct MmaConsumer {
       // so that 0 * (NaN or Inf) cannot reach the accumulator.
       for (int i = lane; i < D * (BS - ntok); i += 32) {
         const int d = i / (BS - ntok), t = ntok + i % (BS - ntok);
-        reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+        if constexpr (kFp8) reinterpret_cast<uint8_t*>(vs)[d * BS + t] = 0;
+        else reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -156,8 +188,17 @@ struct MmaConsumer {
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
         uint32_t a[4];
-        const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (lane >> 4);
-        ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
+        if constexpr (kFp8) {
+          // A = V[16 dims x 16 tokens]: rows mt*16 + r (+8), columns tt*16 + (lane%4)*2 (+8).
+          const uint32_t lo = vbase + (mt * 16 + r) * BS + tt * 16 + (lane & 3) * 2, hi = lo + 8 * BS;
+          a[0] = fp8_pair(lo);
+          a[1] = fp8_pair(hi);
+          a[2] = fp8_pair(lo + 8);
+          a[3] = fp8_pair(hi + 8);
+        } else {
+          const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (lane >> 4);
+          ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
+        }
         Mma<T>::run(acc[mt], a, b0, b1);
         if constexpr (kSplitWeights) Mma<T>::run(acc[mt], a, r0, r1);
       }

@@ -1,0 +1,19 @@
+// pa_mma8_f16.cu -- instances of the paged decode kernel with the tensor-core
+// (mma.sync) consumer over an fp8 (E4M3) KV cache, queries and output __half.
+#include "pa_launch.cuh"
+#include "pa_mma.cuh"
+
+namespace pa {
+
+template <int D, int BS>
+static cudaError_t go(const KParams& prm, int max_ctas, cudaStream_t st) {
+  return launch_one<MmaConsumer<__half, D, BS, true>, kMmaConsumerWarps>(prm, max_ctas, st);
+}
+
+cudaError_t launch_mma8_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st) {
+  if (D == 64) return BS == 16 ? go<64, 16>(prm, max_ctas, st) : go<64, 32>(prm, max_ctas, st);
+  if (D == 128) return BS == 16 ? go<128, 16>(prm, max_ctas, st) : go<128, 32>(prm, max_ctas, st);
+  return BS == 16 ? go<256, 16>(prm, max_ctas, st) : go<256, 32>(prm, max_ctas, st);
+}
+
+}  // namespace pa

@@ -51,6 +51,9 @@ class Workload:
     distinct_tables: bool = False    # per-seq randperm(num_blocks)[:MB] instead of one pool permutation
     seed: int = 0
     q_len: int = 1                   # query rows per sequence (multi-query decode when > 1)
+    kv_dtype: str = ""               # "e4m3": fp8 caches (codes, key x = 16), else the query's dtype
+    k_scale: float = 1.0             # fp8 caches: real keys / values are k_scale * K, v_scale * V
+    v_scale: float = 1.0
 
     @property
     def group(self) -> int:
@@ -94,6 +97,12 @@ WORKLOADS["spec4_gqa_bf16"] = _cfg(
     name="spec4_gqa_bf16", dtype="bf16", num_seqs=128, num_heads=32, num_kv_heads=8, head_size=128,
     block_size=16, partition_size=512, scale=1.0 / math.sqrt(128), max_blocks_per_seq=512,
     num_blocks=128 * 512, lens=(2048, 8192), lens_random=True, seed=1002, q_len=4)
+# The GQA batch over an fp8 (E4M3) KV cache with per-tensor scales.
+WORKLOADS["gqa_fp8kv_bf16"] = _cfg(
+    name="gqa_fp8kv_bf16", dtype="bf16", num_seqs=128, num_heads=32, num_kv_heads=8, head_size=128,
+    block_size=16, partition_size=512, scale=1.0 / math.sqrt(128), max_blocks_per_seq=512,
+    num_blocks=128 * 512, lens=(2048, 8192), lens_random=True, seed=1002, kv_dtype="e4m3",
+    k_scale=0.5, v_scale=1.5)
 # The same on the MHA batch's shapes: 4 row heads per kv head, one unit each.
 WORKLOADS["spec4_mha_fp16"] = _cfg(
     name="spec4_mha_fp16", dtype="fp16", num_seqs=64, num_heads=32, num_kv_heads=32, head_size=128,
@@ -160,13 +169,21 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu",
                            w.block_size, w.num_blocks)
     qshape = (S, H, D) if w.q_len == 1 else (S, w.q_len, H, D)
     query = torch.randn(qshape, generator=vgen, device=vdev, dtype=torch.float32).to(dt)
-    key_cache = torch.empty((NB, KH, D // X_PACK, BS, X_PACK), device=vdev, dtype=dt)
-    key_cache.normal_(0.0, w.k_std, generator=vgen)
-    value_cache = torch.empty((NB, KH, D, BS), device=vdev, dtype=dt)
-    if w.v_uniform:
-        value_cache.uniform_(-1.0, 1.0, generator=vgen)
+    if w.kv_dtype == "e4m3":
+        # E4M3 codes of N(0, k_std) / N(0, 1) draws (rounded by torch), key x = 16.
+        def codes(shape, std):
+            t = torch.empty(shape, device=vdev, dtype=torch.float32).normal_(0.0, std, generator=vgen)
+            return t.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        key_cache = codes((NB, KH, D // 16, BS, 16), w.k_std)
+        value_cache = codes((NB, KH, D, BS), 1.0)
     else:
-        value_cache.normal_(0.0, 1.0, generator=vgen)
+        key_cache = torch.empty((NB, KH, D // X_PACK, BS, X_PACK), device=vdev, dtype=dt)
+        key_cache.normal_(0.0, w.k_std, generator=vgen)
+        value_cache = torch.empty((NB, KH, D, BS), device=vdev, dtype=dt)
+        if w.v_uniform:
+            value_cache.uniform_(-1.0, 1.0, generator=vgen)
+        else:
+            value_cache.normal_(0.0, 1.0, generator=vgen)
     dev = torch.device(device)
     return {
         "query": query.to(dev), "key_cache": key_cache.to(dev), "value_cache": value_cache.to(dev),
@@ -181,8 +198,9 @@ def algorithmic_bytes(w: Workload, seq_lens: Sequence[int]) -> int:
     them), q in, out, the block-table entries that cover the tokens, and
     seq_lens.  Workspace traffic is not counted."""
     esz = 2
+    kv_esz = 1 if w.kv_dtype == "e4m3" else esz
     lens = [int(v) for v in seq_lens]
-    kv = sum(lens) * w.num_kv_heads * w.head_size * 2 * esz
+    kv = sum(lens) * w.num_kv_heads * w.head_size * 2 * kv_esz
     q_out = 2 * w.num_seqs * w.q_len * w.num_heads * w.head_size * esz
     tables = 4 * sum(-(-L // w.block_size) for L in lens)
     return kv + q_out + tables + 4 * w.num_seqs

@@ -168,6 +168,28 @@ int pa_decode_v2_lse(void* out, float* lse, const void* query, const void* key_c
                      int max_blocks_per_seq, int num_blocks, void* workspace, size_t workspace_bytes);
 
 /*
+ * pa_decode_v2_lse over an fp8 KV cache.  The launcher of page
+ * "paged_attention_v2_triton.py -- Triton PagedAttention V2 for BI-V100" takes
+ * kv_cache_dtype, k_scale and v_scale (and ignores them); here the caches hold
+ * E4M3 codes ("e4m3fn": sign, 4 exponent bits with bias 7, 3 fraction bits,
+ * no infinities, code 0x7f/0xff NaN) and the real keys and values are
+ * k_scale * K and v_scale * V.  With one-byte elements the key layout's x is
+ * 16 (16 bytes per chunk, as the launcher's x_pack = key_cache.shape[-1]):
+ *   key_cache    [num_blocks, num_kv_heads, head_size/16, block_size, 16] uint8
+ *   value_cache  [num_blocks, num_kv_heads, head_size, block_size]        uint8
+ *   query, out   [num_seqs, num_heads, head_size]   dtype (fp16 or bf16)
+ *   k_scale, v_scale   finite fp32 multipliers (PA_ERR_INVALID_ARG otherwise)
+ * Every other argument, the workspace, ownership and errors are those of
+ * pa_decode_v2_lse.  The tensor-core kernel family runs every group size.
+ */
+int pa_decode_v2_fp8(void* out, float* lse, const void* query, const void* key_cache,
+                     const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                     float scale, float k_scale, float v_scale, int num_seqs, int num_heads,
+                     int num_kv_heads, int head_size, int block_size, int partition_size, int dtype,
+                     void* stream, int max_blocks_per_seq, int num_blocks, void* workspace,
+                     size_t workspace_bytes);
+
+/*
  * Multi-query decode: q_len new tokens per sequence (speculative or
  * multi-token-prediction verification), each query row attending causally.
  * The decode of page "paged_attention_v2_triton.py -- Triton PagedAttention V2

@@ -130,6 +130,15 @@ def test_binding_launch_count_matches_kernel_limit():
     assert binding.launches_per_call(300, 4) == 1   # multi-query rows share their sequence's launch
 
 
+def test_fp8_entry_rejects_bad_scales():
+    lib = binding.lib()
+    for ks, vs in ((float("nan"), 1.0), (1.0, float("inf"))):
+        st = lib.pa_decode_v2_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
+                                  ctypes.c_float(ks), ctypes.c_float(vs), 2, 4, 2, 128, 16, 512, 0, None,
+                                  4, 8, FAKE, 1 << 30)
+        assert st == binding.PA_ERR_INVALID_ARG
+
+
 def test_status_strings():
     for code in range(7):
         s = binding.status_string(code)

@@ -1,0 +1,96 @@
+"""GPU parity of decode over an fp8 (E4M3) KV cache (pa_decode_v2_fp8): the
+caches hold E4M3 codes (key layout x = 16), real keys and values are
+k_scale * K and v_scale * V, queries and output fp16 / bf16.  Checked against
+the fp64 oracle's restatement at the benchmark tolerance (every E4M3 value is
+exact in fp16 and bf16, so the arithmetic is that of the 16-bit caches);
+log-sum-exp at the tolerance derived in test_lse_gpu."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_attention_paged_pa_gb300 import binding, workloads
+from pa_testutil import compact_sequences, fp8_random_case, within_tolerance
+from test_lse_gpu import lse_close
+
+pytestmark = pytest.mark.gpu
+
+DT_CODE = {torch.float16: oracle.DTYPE_FP16, torch.bfloat16: oracle.DTYPE_BF16}
+
+
+def run_fp8(q, kc, vc, bt, lens, scale, k_scale, v_scale, P):
+    dev = torch.device("cuda")
+    q, kc, vc, bt, lens = (t.to(dev) for t in (q, kc, vc, bt, lens))
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), device=dev)
+    ws = binding.pa_decode_v2_fp8(out, q, kc, vc, bt, lens, scale, k_scale, v_scale, partition_size=P, lse=lse)
+    assert binding.device_status(ws) == binding.PA_OK
+    return out.cpu(), lse.cpu()
+
+
+CASES = [  # (H, KH, D, BS, qdtype)
+    (4, 4, 128, 16, torch.float16), (8, 2, 128, 16, torch.bfloat16), (16, 2, 128, 32, torch.float16),
+    (8, 2, 64, 16, torch.float16), (8, 2, 64, 32, torch.bfloat16), (4, 2, 256, 16, torch.bfloat16),
+    (8, 8, 256, 32, torch.float16),
+]
+
+
+@pytest.mark.parametrize("H,KH,D,BS,qdtype", CASES,
+                         ids=[f"h{c[0]}kh{c[1]}_d{c[2]}_bs{c[3]}_{'bf16' if c[4] == torch.bfloat16 else 'fp16'}"
+                              for c in CASES])
+def test_fp8kv_matches_oracle(H, KH, D, BS, qdtype):
+    # one token, none, a partial block, block and partition edges, two-level (P = 64)
+    lens = [1, 0, 5, BS, 64, 65, 700, 1500]
+    q, kc, vc, bt, L = fp8_random_case(31 + D + BS + H, S=len(lens), H=H, KH=KH, D=D, BS=BS, lens=lens,
+                                       qdtype=qdtype)
+    out, lse = run_fp8(q, kc, vc, bt, L, 0.09, 0.75, 1.5, 64)
+    ref, ref_lse = oracle.decode_fp8kv(q, kc, vc, bt, L, 0.09, 0.75, 1.5, DT_CODE[qdtype])
+    ok, worst = within_tolerance(out.double().numpy(), ref)
+    assert ok, f"worst excess {worst:.3e}"
+    lse_close(lse.numpy(), ref_lse)
+
+
+def test_fp8kv_scales_act_as_multipliers():
+    """v_scale 2 doubles every output bitwise; k_scale 2 at scale s is scale 2 s."""
+    q, kc, vc, bt, L = fp8_random_case(5, S=4, H=8, KH=2, D=128, BS=16, lens=[30, 513, 1, 2000])
+    a, la = run_fp8(q, kc, vc, bt, L, 0.25, 1.0, 1.0, 512)
+    b, lb = run_fp8(q, kc, vc, bt, L, 0.25, 1.0, 2.0, 512)
+    assert torch.equal(b, 2 * a) and torch.equal(la, lb)
+    c, lc = run_fp8(q, kc, vc, bt, L, 0.25, 2.0, 1.0, 512)
+    d, ld = run_fp8(q, kc, vc, bt, L, 0.5, 1.0, 1.0, 512)
+    assert torch.equal(c, d) and torch.equal(lc, ld)
+
+
+def test_fp8kv_nan_codes_past_the_end_are_ignored():
+    """Cache slots past a sequence's end may hold any code, NaN included."""
+    q, kc, vc, bt, L = fp8_random_case(6, S=2, H=8, KH=2, D=64, BS=16, lens=[20, 7])
+    kc2, vc2 = kc.clone(), vc.clone()
+    for s, n in ((0, 20), (1, 7)):
+        b = int(bt[s, n // 16])
+        kc2[b, :, :, n % 16:, :] = 0x7F
+        vc2[b, :, :, n % 16:] = 0xFF
+    a, _ = run_fp8(q, kc, vc, bt, L, 0.1, 1.0, 1.0, 512)
+    b2, _ = run_fp8(q, kc2, vc2, bt, L, 0.1, 1.0, 1.0, 512)
+    assert torch.isfinite(b2.float()).all() and torch.equal(a, b2)
+
+
+def test_fp8kv_workload_sampled():
+    """The GQA batch over an fp8 cache (k_scale 0.5, v_scale 1.5), sampled sequences."""
+    w = workloads.WORKLOADS["gqa_fp8kv_bf16"]
+    inp = workloads.make_inputs(w, device="cuda")
+    out = torch.full_like(inp["query"], float("nan"))
+    lse = torch.empty(inp["query"].shape[:2], device="cuda")
+    ws = binding.pa_decode_v2_fp8(out, inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
+                                  inp["seq_lens"], inp["scale"], w.k_scale, w.v_scale,
+                                  partition_size=w.partition_size, lse=lse)
+    assert binding.device_status(ws) == binding.PA_OK
+    lens = inp["seq_lens"].cpu()
+    seqs = sorted({int(torch.argmin(lens)), int(torch.argmax(lens)), 3, 64})
+    ref, ref_lse = oracle.decode_fp8kv(*compact_sequences(inp, seqs), inp["scale"], w.k_scale, w.v_scale,
+                                       oracle.DTYPE_BF16)
+    sel = torch.tensor(seqs, device="cuda")
+    ok, worst = within_tolerance(out[sel].cpu().double().numpy(), ref)
+    assert ok, f"worst excess {worst:.3e}"
+    lse_close(lse[sel].cpu().numpy(), ref_lse)
+    del inp, out, ws
+    torch.cuda.empty_cache()
