@@ -14,8 +14,8 @@
 //     unit's physical K and V blocks -- each a contiguous D*BS*2-byte run in
 //     the page's layouts -- into shared memory with 1-D bulk async copies
 //     completing on mbarriers;
-//   * warps 0..NC-1 (consumers): block j of a unit goes to warp j % NC (a
-//     fixed grouping, so results do not depend on scheduling), which folds it
+//   * warps 0..NC-1 (consumers): block j of unit u goes to warp (j + u) % NC
+//     (a fixed grouping, so results do not depend on scheduling), which folds it
 //     into its private online-softmax state (SimtConsumer or MmaConsumer).
 //     The CTA's g-th block (counted over all its units) lives in ring stage
 //     g % NSTAGE.  Warps run at different speeds, so a fast warp
@@ -242,10 +242,8 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   using T = typename C::T;
   constexpr int D = C::D, NS = LY::NSTAGE, UQ = LY::UQ;
   // Blocks issued together, one per lane, as their stages free up.
-#ifndef PA_ISSUE_BATCH
-#define PA_ISSUE_BATCH 8
-#endif
-  constexpr int BATCH = NS < PA_ISSUE_BATCH ? NS : PA_ISSUE_BATCH;
+  static_assert(C::kIssueBatch >= 1 && C::kIssueBatch <= 32, "one block per lane");
+  constexpr int BATCH = NS < C::kIssueBatch ? NS : C::kIssueBatch;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bar_full = sbase + LY::OFF_BAR, bar_empty = bar_full + NS * 8;
   const uint32_t bar_ufull = bar_empty + NS * 8, bar_uempty = bar_ufull + UQ * 8;
@@ -411,7 +409,8 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     const long long drain_ns = 100000000LL;
     for (uint32_t i = (hi > (uint32_t)NS ? hi - NS : 0u); i < hi; ++i) {
       // A stage taken over by block i + NS of an aborted batch was waited for there.
-      if ((reissued >> (i + NS - hi)) & 1u) continue;
+      const uint32_t lane_of_i = i + NS - hi;
+      if (lane_of_i < 32u && ((reissued >> lane_of_i) & 1u)) continue;
       const uint32_t bar = bar_full + 8 * stage_of<LY>(i), ph = phase_of<LY>(i);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(bar, ph) && (long long)(global_timer_ns() - t0) < drain_ns) {}
@@ -843,7 +842,12 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_uempty + 8 * slot);
 
-    for (int j = warp; j < I.nb; j += NC) {
+    // Block j of unit u goes to warp (j + u) % NC: when a unit's block count
+    // is not a multiple of NC, the extra blocks fall on different warps from
+    // unit to unit instead of on warps 0, 1, ... every time.  The grouping
+    // depends only on the unit, never on which CTA runs it.
+    const int u_id = (pref[I.s] + I.p) * prm.n_hg + I.hg;
+    for (int j = (warp + NC - u_id % NC) % NC; j < I.nb; j += NC) {
       if constexpr (C::kMma && kMmaHelpPerBlock) {
         if (__shfl_sync(0xffffffffu, *ch.posted, 0) > seen) help_with_job<C, LY>(prm, ch, seen, warp, lane);
       }

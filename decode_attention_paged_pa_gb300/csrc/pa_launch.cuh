@@ -21,6 +21,13 @@ constexpr int kConsumerWarps = PA_CONSUMER_WARPS;
 #define PA_MMA_CONSUMER_WARPS 6
 #endif
 constexpr int kMmaConsumerWarps = PA_MMA_CONSUMER_WARPS;
+// Over an fp8 KV cache a block carries half the bytes for the same
+// arithmetic, and the consumer warps' latency sets the pace: eight of them
+// where their registers fit under the ten-warp cap (D <= 128), six otherwise.
+template <int D>
+constexpr int mma8_consumer_warps() {
+  return D <= 128 ? 8 : 6;
+}
 constexpr int kCtasPerSm = PA_CTAS_PER_SM;
 
 // Shared memory per CTA: the SM's 228 KB less 1 KB reserved per CTA.

@@ -27,20 +27,35 @@
 namespace pa {
 
 // FP8_: the caches hold E4M3 codes (one byte per element, key layout
-// [D/16][BS][16]); operand fragments are then read code pair by code pair and
-// widened to T (every E4M3 value is exact in fp16 and bf16).
+// [D/16][BS][16]).  Every E4M3 value is exact in fp16, so both products then
+// run as fp16 MMAs whatever T is: K and V codes widen to fp16 in registers
+// (one conversion per code pair), the query is scaled by a power of two into
+// fp16's range (exact for bf16 queries too: bf16 keeps 8 significant bits,
+// fp16 11) with the inverse factor folded into the score scale, and the
+// weights enter the value product rounded once to fp16, as in the fp16 path.
+//
+// The fp8 fragments are read with 4-byte shared loads.  Within a 16-dim
+// k-step, lane quad c holds dims 4c..4c+3 of its token rows (slots k = 2c,
+// 2c+1 and 2c+8, 2c+9; the query fragments use the same assignment), and MMA
+// row i of a 16-token tile holds token kTok(i) below: a lane's value word
+// then covers four consecutive tokens of one dim, and the eight token rows a
+// lane quad reads fall in distinct shared-memory banks.
 template <typename T_, int D_, int BS_, bool FP8_ = false>
 struct MmaConsumer {
   using T = T_;
+  using MT = typename std::conditional<FP8_, __half, T_>::type;  // operand type of the products
   static constexpr int D = D_, BS = BS_, GT = 8;
   static constexpr bool kMma = true;
   static constexpr bool kFp8 = FP8_;
   static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
+  // Blocks the producer warp issues together (one per lane): 2 KB fp8 copies
+  // need more of them in flight than the 4 KB copies of 16-bit caches.
+  static constexpr int kIssueBatch = FP8_ ? 32 : 8;
   static constexpr int NK = D / 16;    // k-steps of the score product
   static constexpr int NMT = D / 16;   // 16-dim tiles of the value product
   static constexpr int NTT = BS / 16;  // 16-token tiles per block
   static constexpr int SCRATCH_FLOATS = 0;
-  static constexpr bool kSplitWeights = std::is_same<T_, __nv_bfloat16>::value;
+  static constexpr bool kSplitWeights = std::is_same<MT, __nv_bfloat16>::value;
 
   uint32_t qb[NK][2];  // Q^T fragments (B operand), packed element pairs
   float m[2], l[2];    // heads 2*(lane%4) and 2*(lane%4)+1
@@ -48,18 +63,25 @@ struct MmaConsumer {
   float scale_log2;
   int lim[2];  // positions [0, lim) the lane's two heads see (causal rows of multi-query decode)
 
-  // The two E4M3 codes at shared address addr as a packed pair of T (the
-  // lower code in the lower half, as the fragments want it).
-  __device__ __forceinline__ static uint32_t fp8_pair(uint32_t addr) {
-    uint16_t raw;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(raw) : "r"(addr));
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(raw, __NV_E4M3);
-    if constexpr (std::is_same<T, __half>::value) {
-      return (uint32_t)h.x | ((uint32_t)h.y << 16);
-    } else {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-      return F16Traits<T>::pack(f.x, f.y);
-    }
+  // fp8 caches: the token (within its 16-token tile) that MMA row i holds.
+  // Rows 2c, 2c+1 and 2c+8, 2c+9 -- the score rows that become the weight
+  // slots of lane quad c -- hold tokens 4c..4c+3, the lower pair on rows
+  // 2c, 2c+1 for c < 2 and on rows 2c+8, 2c+9 for c >= 2.
+  __device__ __forceinline__ static int kTok(int i) {
+    const int c = (i & 7) >> 1;
+    return 4 * c + 2 * ((c >> 1) ^ (i >> 3)) + (i & 1);
+  }
+
+  __device__ __forceinline__ static uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+  }
+
+  // Two E4M3 codes (the low code in bits 0-7) as a packed fp16 pair.
+  __device__ __forceinline__ static uint32_t e4m3x2(uint32_t codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(codes & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
   }
 
   // Positions each of this lane's two heads (hq, hq + 1) may see; a
@@ -72,15 +94,49 @@ struct MmaConsumer {
   __device__ __forceinline__ void begin_unit(const T* qs, int nh, float sl2, int lane) {
     const int n = lane >> 2, kq = (lane & 3) * 2;
     const uint16_t* q16 = reinterpret_cast<const uint16_t*>(qs);
+    if constexpr (kFp8) {
+      // Dims 16ks + 4c .. +3 of head n, scaled by 2^s so that the unit's
+      // largest |q| lies below 2^15 (fp16 tops out near 2^16).
+      float amax = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < NK; ++ks) {
-      uint32_t lo = 0, hi = 0;
-      if (n < nh) {
-        lo = *reinterpret_cast<const uint32_t*>(q16 + n * D + ks * 16 + kq);
-        hi = *reinterpret_cast<const uint32_t*>(q16 + n * D + ks * 16 + kq + 8);
+      for (int ks = 0; ks < NK; ++ks) {
+        if (n < nh) {
+          const uint2 w = *reinterpret_cast<const uint2*>(q16 + n * D + ks * 16 + 2 * kq);
+          const float2 a = F16Traits<T>::to_float2(w.x), b = F16Traits<T>::to_float2(w.y);
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))));
+        }
       }
-      qb[ks][0] = lo;
-      qb[ks][1] = hi;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      // amax < 2^(E - 126) for a normal binary32 with biased exponent E;
+      // zero, subnormal, Inf or NaN leave the query unscaled.
+      const int E = (__float_as_int(amax) >> 23) & 0xff;
+      const int s = (E == 0 || E == 255) ? 0 : max(-110, min(110, 141 - E));
+      const float up = __int_as_float((127 + s) << 23), down = __int_as_float((127 - s) << 23);
+#pragma unroll
+      for (int ks = 0; ks < NK; ++ks) {
+        uint32_t lo = 0, hi = 0;
+        if (n < nh) {
+          const uint2 w = *reinterpret_cast<const uint2*>(q16 + n * D + ks * 16 + 2 * kq);
+          const float2 a = F16Traits<T>::to_float2(w.x), b = F16Traits<T>::to_float2(w.y);
+          lo = F16Traits<__half>::pack(a.x * up, a.y * up);
+          hi = F16Traits<__half>::pack(b.x * up, b.y * up);
+        }
+        qb[ks][0] = lo;
+        qb[ks][1] = hi;
+      }
+      sl2 *= down;
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < NK; ++ks) {
+        uint32_t lo = 0, hi = 0;
+        if (n < nh) {
+          lo = *reinterpret_cast<const uint32_t*>(q16 + n * D + ks * 16 + kq);
+          hi = *reinterpret_cast<const uint32_t*>(q16 + n * D + ks * 16 + kq + 8);
+        }
+        qb[ks][0] = lo;
+        qb[ks][1] = hi;
+      }
     }
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
@@ -93,6 +149,10 @@ struct MmaConsumer {
 
   __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane, float*,
                                         int tok0) {
+    if constexpr (kFp8) {
+      block_fp8(ks, vs, ntok, lane, tok0);
+      return;
+    }
     const uint32_t kbase = smem_addr(ks), vbase = smem_addr(vs);
     const int r = lane >> 2;
     float sc[NTT][4];
@@ -103,18 +163,8 @@ struct MmaConsumer {
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
         uint32_t a[4];
-        if constexpr (kFp8) {
-          // A = K[16 tokens x 16 dims]: rows tt*16 + r (+8), columns (lane%4)*2 (+8);
-          // chunk kk of the key block holds dims 16kk.. of every token in 16 bytes.
-          const uint32_t lo = kbase + (kk * BS + tt * 16 + r) * 16 + (lane & 3) * 2, hi = lo + 8 * 16;
-          a[0] = fp8_pair(lo);
-          a[1] = fp8_pair(hi);
-          a[2] = fp8_pair(lo + 8);
-          a[3] = fp8_pair(hi + 8);
-        } else {
-          const int tok = tt * 16 + (lane & 15), chunk = 2 * kk + (lane >> 4);
-          ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
-        }
+        const int tok = tt * 16 + (lane & 15), chunk = 2 * kk + (lane >> 4);
+        ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
         if (kk & 1) Mma<T>::run(c2, a, qb[kk][0], qb[kk][1]);
         else Mma<T>::run(c, a, qb[kk][0], qb[kk][1]);
       }
@@ -162,8 +212,7 @@ struct MmaConsumer {
       // so that 0 * (NaN or Inf) cannot reach the accumulator.
       for (int i = lane; i < D * (BS - ntok); i += 32) {
         const int d = i / (BS - ntok), t = ntok + i % (BS - ntok);
-        if constexpr (kFp8) reinterpret_cast<uint8_t*>(vs)[d * BS + t] = 0;
-        else reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+        reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -188,19 +237,105 @@ struct MmaConsumer {
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
         uint32_t a[4];
-        if constexpr (kFp8) {
-          // A = V[16 dims x 16 tokens]: rows mt*16 + r (+8), columns tt*16 + (lane%4)*2 (+8).
-          const uint32_t lo = vbase + (mt * 16 + r) * BS + tt * 16 + (lane & 3) * 2, hi = lo + 8 * BS;
-          a[0] = fp8_pair(lo);
-          a[1] = fp8_pair(hi);
-          a[2] = fp8_pair(lo + 8);
-          a[3] = fp8_pair(hi + 8);
-        } else {
-          const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (lane >> 4);
-          ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
-        }
+        const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (lane >> 4);
+        ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
         Mma<T>::run(acc[mt], a, b0, b1);
         if constexpr (kSplitWeights) Mma<T>::run(acc[mt], a, r0, r1);
+      }
+    }
+  }
+
+  // One staged block of E4M3 codes (see the note above the struct).
+  __device__ __forceinline__ void block_fp8(const uint8_t* ks, const uint8_t* vs, int ntok, int lane,
+                                            int tok0) {
+    const uint32_t kbase = smem_addr(ks), vbase = smem_addr(vs);
+    const int r = lane >> 2, c = lane & 3;
+    const int trow_lo = kTok(r), trow_hi = kTok(r + 8);
+    float sc[NTT][4];
+#pragma unroll
+    for (int tt = 0; tt < NTT; ++tt) {
+      // Chunk kk of the key block holds dims 16kk..16kk+15 of every token in 16 bytes.
+      uint32_t wk[NK][2];
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) {
+        wk[kk][0] = lds32(kbase + (kk * BS + tt * 16 + trow_lo) * 16 + c * 4);
+        wk[kk][1] = lds32(kbase + (kk * BS + tt * 16 + trow_hi) * 16 + c * 4);
+      }
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) {
+        const uint32_t a[4] = {e4m3x2(wk[kk][0]), e4m3x2(wk[kk][1]), e4m3x2(wk[kk][0] >> 16),
+                               e4m3x2(wk[kk][1] >> 16)};
+        if (kk & 1) Mma<__half>::run(c1, a, qb[kk][0], qb[kk][1]);
+        else Mma<__half>::run(c0, a, qb[kk][0], qb[kk][1]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c0[i] += c1[i];
+      const int t_lo = tt * 16 + trow_lo, t_hi = tt * 16 + trow_hi;
+      sc[tt][0] = (t_lo < ntok && tok0 + t_lo < lim[0]) ? c0[0] * scale_log2 : -INFINITY;
+      sc[tt][1] = (t_lo < ntok && tok0 + t_lo < lim[1]) ? c0[1] * scale_log2 : -INFINITY;
+      sc[tt][2] = (t_hi < ntok && tok0 + t_hi < lim[0]) ? c0[2] * scale_log2 : -INFINITY;
+      sc[tt][3] = (t_hi < ntok && tok0 + t_hi < lim[1]) ? c0[3] * scale_log2 : -INFINITY;
+    }
+    // Value words (dims mt*16 + r and + 8, tokens tt*16 + 4c .. +3) do not
+    // depend on the weights: read them before the softmax.
+    uint32_t wv[NTT][NMT][2];
+#pragma unroll
+    for (int tt = 0; tt < NTT; ++tt)
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) {
+        wv[tt][mt][0] = lds32(vbase + (mt * 16 + r) * BS + tt * 16 + c * 4);
+        wv[tt][mt][1] = lds32(vbase + (mt * 16 + r + 8) * BS + tt * 16 + c * 4);
+      }
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float bm = fmaxf(sc[0][j], sc[0][j + 2]);
+#pragma unroll
+      for (int tt = 1; tt < NTT; ++tt) bm = fmaxf(bm, fmaxf(sc[tt][j], sc[tt][j + 2]));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+      const float mn = fmaxf(m[j], bm);
+      const float ms = (mn == -INFINITY) ? 0.f : mn;  // a causal row that has seen nothing yet
+      alpha[j] = exp2f(m[j] - ms);
+      m[j] = mn;
+      float ps = 0.f;
+#pragma unroll
+      for (int tt = 0; tt < NTT; ++tt) {
+        sc[tt][j] = exp2f(sc[tt][j] - ms);
+        sc[tt][j + 2] = exp2f(sc[tt][j + 2] - ms);
+        ps += sc[tt][j] + sc[tt][j + 2];
+      }
+      l[j] = fmaf(l[j], alpha[j], ps);
+    }
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) {
+      acc[mt][0] *= alpha[0];
+      acc[mt][1] *= alpha[1];
+      acc[mt][2] *= alpha[0];
+      acc[mt][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int tt = 0; tt < NTT; ++tt) {
+      // Slots past the sequence end hold arbitrary codes (E4M3 has NaNs):
+      // clear those bytes so that 0 * NaN cannot reach the accumulator.
+      const int keep = ntok - (tt * 16 + c * 4);
+      const uint32_t vmask = keep >= 4 ? 0xffffffffu : (keep <= 0 ? 0u : (1u << (8 * keep)) - 1u);
+      const uint32_t p0 = F16Traits<__half>::pack(sc[tt][0], sc[tt][1]);
+      const uint32_t p1 = F16Traits<__half>::pack(sc[tt][2], sc[tt][3]);
+      uint32_t b0 = movmatrix_trans(p0), b1 = movmatrix_trans(p1);
+      // Quads c >= 2 find their tokens 4c, 4c+1 in score rows 2c+8, 2c+9.
+      if (c >= 2) {
+        const uint32_t t = b0;
+        b0 = b1;
+        b1 = t;
+      }
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) {
+        const uint32_t v0 = wv[tt][mt][0] & vmask, v1 = wv[tt][mt][1] & vmask;
+        const uint32_t a[4] = {e4m3x2(v0), e4m3x2(v1), e4m3x2(v0 >> 16), e4m3x2(v1 >> 16)};
+        Mma<__half>::run(acc[mt], a, b0, b1);
       }
     }
   }

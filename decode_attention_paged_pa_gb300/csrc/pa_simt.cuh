@@ -19,6 +19,7 @@ struct SimtConsumer {
   using T = T_;
   static constexpr int D = D_, BS = BS_, GT = GT_;
   static constexpr bool kMma = false;
+  static constexpr int kIssueBatch = 8;  // blocks the producer warp issues together
   static constexpr bool kFp8 = false;
   static constexpr int KV_ESZ = 2;  // bytes per cached element
   // q.k: each lane takes QKD dims of one token; LPT lanes share a token.
