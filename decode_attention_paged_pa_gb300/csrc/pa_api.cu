@@ -42,8 +42,16 @@ bool valid_sizes(int S, int H, int KH, int D, int MB, int BS, int P) {
   return true;
 }
 
+// Shapes every kernel family handles; the tensor-core family also takes head
+// sizes 80, 96, 112 and 8- or 64-token blocks.
+bool base_shape(int D, int BS) {
+  return (D == 64 || D == 128 || D == 256) && (BS == 16 || BS == 32);
+}
+
 bool supported(int D, int BS, int P) {
-  return (D == 64 || D == 128 || D == 256) && (BS == 16 || BS == 32) && P % BS == 0;
+  const bool d_ok = D == 64 || D == 80 || D == 96 || D == 112 || D == 128 || D == 256;
+  const bool bs_ok = BS == 8 || BS == 16 || BS == 32 || BS == 64;
+  return d_ok && bs_ok && P % BS == 0;
 }
 
 bool ws_layout(int S, int H, int KH, int D, int MB, int BS, int P, WsLayout* w) {
@@ -125,6 +133,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     return PA_ERR_INVALID_ARG;
   if (!supported(D, BS, P)) return PA_ERR_UNSUPPORTED;
   if (kv_fp8 && variant == PA_VARIANT_SIMT) return PA_ERR_UNSUPPORTED;  // fp8 runs on tensor cores
+  if (!base_shape(D, BS) && (kv_fp8 || variant == PA_VARIANT_SIMT)) return PA_ERR_UNSUPPORTED;
   if (S == 0) return PA_OK;
   if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens)
     return PA_ERR_INVALID_ARG;
@@ -137,7 +146,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   if (workspace && workspace_bytes < w.total) return PA_ERR_WORKSPACE;
 
   const int G = H / KH;
-  if (variant == PA_VARIANT_AUTO) variant = (G == 1 && !kv_fp8) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
+  if (variant == PA_VARIANT_AUTO)
+    variant = (G == 1 && !kv_fp8 && base_shape(D, BS)) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
   const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : kSimtGroup;
   const int hg_per_kv = (G + gt - 1) / gt;
   const int n_hg = KH * hg_per_kv;
@@ -203,6 +213,15 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     if (kv_fp8)
       e = dtype == PA_DTYPE_FP16 ? launch_mma8_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma8_bf16(prm, D, BS, max_ctas, st);
+    else if (variant == PA_VARIANT_MMA && BS == 8)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma_b8_f16(prm, D, max_ctas, st)
+                                 : launch_mma_b8_bf16(prm, D, max_ctas, st);
+    else if (variant == PA_VARIANT_MMA && BS == 64)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma_b64_f16(prm, D, max_ctas, st)
+                                 : launch_mma_b64_bf16(prm, D, max_ctas, st);
+    else if (variant == PA_VARIANT_MMA && !base_shape(D, BS))
+      e = dtype == PA_DTYPE_FP16 ? launch_mma_xd_f16(prm, D, BS, max_ctas, st)
+                                 : launch_mma_xd_bf16(prm, D, BS, max_ctas, st);
     else if (variant == PA_VARIANT_MMA)
       e = dtype == PA_DTYPE_FP16 ? launch_mma_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma_bf16(prm, D, BS, max_ctas, st);

@@ -29,6 +29,14 @@ cudaError_t launch_simt_f16(const KParams& prm, int D, int BS, int max_ctas, cud
 cudaError_t launch_simt_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+// Tensor-core instances of the other shapes: head sizes 80, 96, 112 (block
+// sizes 16, 32), and 8- or 64-token blocks (head sizes 64, 80, 96, 112, 128, 256).
+cudaError_t launch_mma_xd_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_xd_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_b8_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_b8_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_b64_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_b64_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
 // The same over an fp8 (E4M3) KV cache, queries and output fp16 / bf16.
 cudaError_t launch_mma8_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma8_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);

@@ -48,12 +48,16 @@ struct MmaConsumer {
   static constexpr bool kMma = true;
   static constexpr bool kFp8 = FP8_;
   static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
-  // Blocks the producer warp issues together (one per lane): 2 KB fp8 copies
-  // need more of them in flight than the 4 KB copies of 16-bit caches.
-  static constexpr int kIssueBatch = FP8_ ? 32 : 8;
+  // Blocks the producer warp issues together (one per lane): copies of 2 KB
+  // or less need more of them in flight than the 4 KB ones.
+  static constexpr int kIssueBatch = (KV_ESZ * D * BS <= 2048) ? 32 : 8;
   static constexpr int NK = D / 16;    // k-steps of the score product
   static constexpr int NMT = D / 16;   // 16-dim tiles of the value product
-  static constexpr int NTT = BS / 16;  // 16-token tiles per block
+  // 16-token tiles per block.  An 8-token block fills half of one tile: the
+  // score rows of tokens 8..15 are masked and their value columns are zero.
+  static constexpr int NTT = BS >= 16 ? BS / 16 : 1;
+  static_assert(D % 16 == 0 && (BS == 8 || BS % 16 == 0), "head size a multiple of 16; block 8 or 16k");
+  static_assert(!FP8_ || BS % 16 == 0, "fp8 caches take blocks of 16k tokens");
   static constexpr int SCRATCH_FLOATS = 0;
   static constexpr bool kSplitWeights = std::is_same<MT, __nv_bfloat16>::value;
 
@@ -163,7 +167,8 @@ struct MmaConsumer {
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
         uint32_t a[4];
-        const int tok = tt * 16 + (lane & 15), chunk = 2 * kk + (lane >> 4);
+        // (An 8-token block: rows 8..15 repeat rows 0..7 and are masked below.)
+        const int tok = tt * 16 + (lane & (BS >= 16 ? 15 : 7)), chunk = 2 * kk + (lane >> 4);
         ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
         if (kk & 1) Mma<T>::run(c2, a, qb[kk][0], qb[kk][1]);
         else Mma<T>::run(c, a, qb[kk][0], qb[kk][1]);
@@ -237,8 +242,9 @@ struct MmaConsumer {
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
         uint32_t a[4];
-        const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (lane >> 4);
+        const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
         ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
+        if constexpr (BS < 16) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
         Mma<T>::run(acc[mt], a, b0, b1);
         if constexpr (kSplitWeights) Mma<T>::run(acc[mt], a, r0, r1);
       }

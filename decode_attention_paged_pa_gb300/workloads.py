@@ -103,6 +103,17 @@ WORKLOADS["gqa_fp8kv_bf16"] = _cfg(
     block_size=16, partition_size=512, scale=1.0 / math.sqrt(128), max_blocks_per_seq=512,
     num_blocks=128 * 512, lens=(2048, 8192), lens_random=True, seed=1002, kv_dtype="e4m3",
     k_scale=0.5, v_scale=1.5)
+# Shapes beyond the benchmark definition's (head sizes 80 / 96 / 112, blocks
+# of 8 or 64 tokens): the GQA batch's lengths with head size 112 in 8-token
+# blocks, and the MHA batch's with head size 80 in 64-token blocks.
+WORKLOADS["gqa_d112_bs8_bf16"] = _cfg(
+    name="gqa_d112_bs8_bf16", dtype="bf16", num_seqs=128, num_heads=32, num_kv_heads=8, head_size=112,
+    block_size=8, partition_size=512, scale=1.0 / math.sqrt(112), max_blocks_per_seq=1024,
+    num_blocks=128 * 1024, lens=(2048, 8192), lens_random=True, seed=1005)
+WORKLOADS["mha_d80_bs64_fp16"] = _cfg(
+    name="mha_d80_bs64_fp16", dtype="fp16", num_seqs=64, num_heads=32, num_kv_heads=32, head_size=80,
+    block_size=64, partition_size=512, scale=1.0 / math.sqrt(80), max_blocks_per_seq=64,
+    num_blocks=64 * 64, lens=(512, 4096), lens_random=True, seed=1006)
 # The same on the MHA batch's shapes: 4 row heads per kv head, one unit each.
 WORKLOADS["spec4_mha_fp16"] = _cfg(
     name="spec4_mha_fp16", dtype="fp16", num_seqs=64, num_heads=32, num_kv_heads=32, head_size=128,

@@ -54,8 +54,10 @@ enum { PA_DTYPE_FP16 = 0, PA_DTYPE_BF16 = 1 };
 enum {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, H % KH != 0, ... */
-    PA_ERR_UNSUPPORTED = 2,   /* head_size not 64/128/256, block_size not 16/32,
-                                 partition_size not a positive multiple of block_size */
+    PA_ERR_UNSUPPORTED = 2,   /* head_size not 64/80/96/112/128/256, block_size not
+                                 8/16/32/64, partition_size not a positive multiple of
+                                 block_size; a shape outside the chosen family (see
+                                 pa_decode_v2_ex and pa_decode_v2_fp8) */
     PA_ERR_WORKSPACE = 3,     /* workspace smaller than pa_decode_v2_workspace_bytes() */
     PA_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, memset, ...) */
     PA_ERR_DEVICE_BOUNDS = 5, /* device-side: bad block id or sequence length */
@@ -128,7 +130,10 @@ int pa_decode_v2(void* out, const void* query, const void* key_cache, const void
  * pa_decode_v2 with tuning controls, for tests and measurement.
  *   variant     PA_VARIANT_*; SIMT takes one query head per pass over the
  *               kv head's blocks (a group of G query heads takes G passes),
- *               MMA up to 8 query heads per pass.
+ *               MMA up to 8 query heads per pass.  SIMT handles head sizes
+ *               64/128/256 with blocks of 16 or 32 tokens (other shapes:
+ *               PA_ERR_UNSUPPORTED); MMA every supported shape.  AUTO picks
+ *               SIMT for G = 1 where it applies, MMA otherwise.
  *   max_ctas    upper bound on the persistent grid (0 = one CTA per SM).
  *   timeout_ns  bound on every device-side wait (0 = 2^31 ns).
  * Results do not depend on variant-independent choices: for a fixed variant
@@ -180,7 +185,9 @@ int pa_decode_v2_lse(void* out, float* lse, const void* query, const void* key_c
  *   query, out   [num_seqs, num_heads, head_size]   dtype (fp16 or bf16)
  *   k_scale, v_scale   finite fp32 multipliers (PA_ERR_INVALID_ARG otherwise)
  * Every other argument, the workspace, ownership and errors are those of
- * pa_decode_v2_lse.  The tensor-core kernel family runs every group size.
+ * pa_decode_v2_lse.  The tensor-core kernel family runs every group size;
+ * head_size must be 64, 128 or 256 and block_size 16 or 32
+ * (PA_ERR_UNSUPPORTED otherwise).
  */
 int pa_decode_v2_fp8(void* out, float* lse, const void* query, const void* key_cache,
                      const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,

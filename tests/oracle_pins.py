@@ -37,6 +37,12 @@ def pin_textbook_gqa(orc):
         ref = textbook_decode(q, kc, vc, bt, lens, 0.3)
         got = orc.decode(q, kc, vc, bt, lens, 0.3, dt)
         _close(got, ref, 1e-12, "textbook")
+    # Head size 80 (ten 8-element key chunks) in 8- and 64-token blocks.
+    for BS in (8, 64):
+        q, kc, vc, bt, lens = random_case(17 + BS, S=2, H=4, KH=1, D=80, BS=BS, lens=[9, 130],
+                                          dtype=torch.bfloat16)
+        _close(orc.decode(q, kc, vc, bt, lens, 0.1, BF16), textbook_decode(q, kc, vc, bt, lens, 0.1),
+               1e-12, f"textbook D=80 BS={BS}")
 
 
 def pin_bruteforce_tiny(orc):

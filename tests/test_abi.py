@@ -82,8 +82,11 @@ def call(**kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(num_heads=6, num_kv_heads=4), binding.PA_ERR_INVALID_ARG),
     (dict(dtype=7), binding.PA_ERR_INVALID_ARG),
-    (dict(head_size=96), binding.PA_ERR_UNSUPPORTED),
-    (dict(block_size=8), binding.PA_ERR_UNSUPPORTED),
+    (dict(head_size=72), binding.PA_ERR_UNSUPPORTED),
+    (dict(head_size=100), binding.PA_ERR_UNSUPPORTED),
+    (dict(block_size=4), binding.PA_ERR_UNSUPPORTED),
+    (dict(block_size=24), binding.PA_ERR_UNSUPPORTED),
+    (dict(block_size=64, partition_size=96), binding.PA_ERR_UNSUPPORTED),
     (dict(partition_size=100), binding.PA_ERR_UNSUPPORTED),
     (dict(partition_size=0), binding.PA_ERR_INVALID_ARG),
     (dict(out=None), binding.PA_ERR_INVALID_ARG),
@@ -137,6 +140,26 @@ def test_fp8_entry_rejects_bad_scales():
                                   ctypes.c_float(ks), ctypes.c_float(vs), 2, 4, 2, 128, 16, 512, 0, None,
                                   4, 8, FAKE, 1 << 30)
         assert st == binding.PA_ERR_INVALID_ARG
+
+
+def test_shapes_outside_a_family_are_rejected():
+    """Head sizes 80/96/112 and 8- or 64-token blocks run on the tensor-core
+    family only; fp8 caches take head sizes 64/128/256 and blocks of 16 or 32."""
+    lib = binding.lib()
+
+    def ex(D, BS, variant):
+        return lib.pa_decode_v2_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 0, 4, 2, D, BS,
+                                   512, 0, None, 4, 8, FAKE, 1 << 30, variant, 0, 0)
+
+    for D, BS in ((96, 16), (80, 32), (128, 8), (64, 64)):
+        assert ex(D, BS, binding.PA_VARIANT_SIMT) == binding.PA_ERR_UNSUPPORTED, (D, BS)
+        assert ex(D, BS, binding.PA_VARIANT_MMA) == binding.PA_OK, (D, BS)
+        assert ex(D, BS, binding.PA_VARIANT_AUTO) == binding.PA_OK, (D, BS)
+    for D, BS in ((80, 16), (128, 8), (128, 64)):
+        st = lib.pa_decode_v2_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
+                                  ctypes.c_float(1.0), ctypes.c_float(1.0), 2, 4, 2, D, BS, 512, 0, None,
+                                  4, 8, FAKE, 1 << 30)
+        assert st == binding.PA_ERR_UNSUPPORTED, (D, BS)
 
 
 def test_status_strings():
