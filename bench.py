@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--config", choices=list(workloads.WORKLOADS), default="mha_fp16")
     ap.add_argument("--variant", choices=["auto", "simt", "mma"], default="auto")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="--impl reference: host seconds for all warm-up and timed steps together")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -234,7 +236,10 @@ def run_reference(args, rank):
     import oracle
 
     w = workloads.WORKLOADS[args.config]
-    calib = oracle_sample(w, cpu_seconds=min(2.0, args.cpu_seconds))
+    # Each step is a sample of the workload sized so that all warm-up and
+    # timed steps together take about --ref-seconds of host time.
+    per_step = min(2.0, args.cpu_seconds, args.ref_seconds / max(1, args.steps + args.warmup))
+    calib = oracle_sample(w, cpu_seconds=per_step)
     ws = calib["workload"]
     inp = workloads.make_inputs(ws)
     lens = inp["seq_lens"].tolist()
