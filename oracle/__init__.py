@@ -27,7 +27,8 @@ definition in ``pa_oracle.c``:
                          positions 0 .. L - q_len + i (output and log-sum-exp);
 * :func:`decode_fp8kv` -- decode over an E4M3 (fp8) KV cache with per-tensor
                          k_scale / v_scale (key layout x = 16), and
-  :func:`e4m3_decode`   the code -> value map it uses.
+  :func:`e4m3_decode`   the code -> value map it uses;
+* :func:`decode_fp32` -- decode with fp32 query and caches (key layout x = 4).
 
 Inputs are the raw 16-bit patterns of fp16 / bf16 tensors (numpy ``uint16``)
 in the page's layouts; the fp32 ``scale`` is widened to double exactly.
@@ -89,6 +90,9 @@ def _declare(lib):
     lib.pa_oracle_e4m3_decode.restype = c_int
     lib.pa_oracle_decode_fp8kv.argtypes = [dp, dp, up, u8p, u8p, ip, ip, c_double, c_double, c_double] + [c_int] * 8
     lib.pa_oracle_decode_fp8kv.restype = c_int
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.pa_oracle_decode_fp32.argtypes = [dp, dp, fp, fp, fp, ip, ip, c_double] + [c_int] * 7
+    lib.pa_oracle_decode_fp32.restype = c_int
     lib.pa_oracle_max_threads.argtypes = []
     lib.pa_oracle_max_threads.restype = c_int
     return lib
@@ -165,6 +169,16 @@ def _shapes(query, key_cache, value_cache, block_tables):
         raise ValueError("value_cache must be [num_blocks, KH, D, BS]")
     MB = block_tables.shape[1]
     return S, H, KH, D, BS, MB
+
+
+def _f32(a) -> np.ndarray:
+    """An fp32 array (numpy or torch) as contiguous float32."""
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().contiguous().numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.float32:
+        raise TypeError(f"expected float32 data, got {a.dtype}")
+    return a
 
 
 class Oracle:
@@ -312,6 +326,27 @@ class Oracle:
         return out, lse
 
 
+    def decode_fp32(self, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                        nthreads: int = 0):
+        """Decode with fp32 query and caches (key_cache [NB, KH, D/4, BS, 4], value_cache
+        [NB, KH, D, BS]); returns (out [S, H, D], lse [S, H]) in float64."""
+        q, kc, vc = _f32(query), _f32(key_cache), _f32(value_cache)
+        bt, lens = _i32(block_tables), _i32(seq_lens)
+        S, H, D = q.shape
+        nb, KH, dx, BS, x = kc.shape
+        if x != 4 or dx * x != D or tuple(vc.shape) != (nb, KH, D, BS):
+            raise ValueError("fp32 caches must be [NB, KH, D/4, BS, 4] and [NB, KH, D, BS]")
+        MB = bt.shape[1]
+        out = np.zeros((S, H, D), dtype=np.float64)
+        lse = np.zeros((S, H), dtype=np.float64)
+        rc = self.lib.pa_oracle_decode_fp32(
+            _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), _ptr(q, ctypes.c_float),
+            _ptr(kc, ctypes.c_float), _ptr(vc, ctypes.c_float), _ptr(bt, ctypes.c_int32),
+            _ptr(lens, ctypes.c_int32), float(np.float32(scale)), S, H, KH, D, BS, MB, nthreads)
+        if rc != 0:
+            raise ValueError("oracle decode_fp32 rejected its arguments")
+        return out, lse
+
 _default = None
 
 
@@ -352,3 +387,7 @@ def e4m3_decode(*args, **kwargs) -> np.ndarray:
 
 def decode_fp8kv(*args, **kwargs):
     return default().decode_fp8kv(*args, **kwargs)
+
+
+def decode_fp32(*args, **kwargs):
+    return default().decode_fp32(*args, **kwargs)

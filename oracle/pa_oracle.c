@@ -439,3 +439,61 @@ int pa_oracle_decode_fp8kv(double* out, double* lse, const uint16_t* q, const ui
     }
     return bad ? -1 : 0;
 }
+
+/* key_cache[b, kh, d / x, o, d % x] with x = 16 / sizeof(element) = 4 for
+ * four-byte (fp32) elements ([PA-V2]: the launcher's x = 16 / sizeof(dtype)). */
+static size_t key_index_x4(long b, int kh, int d, int o, int KH, int D, int BS) {
+    const int x = 4;
+    return ((((size_t)b * KH + kh) * (D / x) + d / x) * BS + o) * x + d % x;
+}
+
+/* Decode with fp32 query, caches and result ([PA-V2] takes the element type
+ * from the query's dtype and sizes the key layout's x from it): the plain
+ * definition softmax(scale * q . K^T) . V over all seq_lens[s] tokens, in
+ * fp64 from the fp32 values.  key_cache [NB, KH, D/4, BS, 4], value_cache
+ * [NB, KH, D, BS]; out [S, H, D], lse [S, H] (may be NULL); seq_lens[s] == 0
+ * gives zeros and lse -inf. */
+int pa_oracle_decode_fp32(double* out, double* lse, const float* q, const float* kc, const float* vc,
+                          const int32_t* bt, const int32_t* lens, double scale, int S, int H, int KH,
+                          int D, int BS, int MB, int nthreads) {
+    if (S < 0 || H <= 0 || KH <= 0 || H % KH || D <= 0 || D % 4 || BS <= 0 || MB < 0)
+        return -1;
+    int bad = 0;
+    if (nthreads <= 0) nthreads = pa_oracle_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : bad)
+    for (long sh = 0; sh < (long)S * H; ++sh) {
+        int s = (int)(sh / H), h = (int)(sh % H);
+        int L = lens[s];
+        double* o_sh = out + (size_t)sh * D;
+        for (int d = 0; d < D; ++d) o_sh[d] = 0.0;
+        if (lse) lse[sh] = -INFINITY;
+        if (L <= 0) continue;
+        if (L > MB * BS) { bad = 1; continue; }
+        double* z = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!z) { bad = 1; continue; }
+        const int kh = h / (H / KH);
+        const float* qv = q + (size_t)sh * D;
+        for (int t = 0; t < L; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += (double)qv[d] * (double)kc[key_index_x4(b, kh, d, o, KH, D, BS)];
+            z[t] = scale * acc;
+        }
+        double mu = -INFINITY;
+        for (int t = 0; t < L; ++t) if (z[t] > mu) mu = z[t];
+        double den = 0.0;
+        for (int t = 0; t < L; ++t) { z[t] = exp(z[t] - mu); den += z[t]; }
+        for (int t = 0; t < L; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            for (int d = 0; d < D; ++d)
+                o_sh[d] += z[t] * (double)vc[value_index(b, kh, d, o, KH, D, BS)];
+        }
+        for (int d = 0; d < D; ++d) o_sh[d] /= den;
+        if (lse) lse[sh] = mu + log(den);
+        free(z);
+    }
+    return bad ? -1 : 0;
+}

@@ -416,6 +416,40 @@ def pin_fp8kv_scales(orc):
     assert np.max(np.abs(c - a)) > 1e-6, "k_scale must matter"
 
 
+def pin_fp32_textbook(orc):
+    """Special case = textbook: numpy softmax(scale q K^T) V (and max + log sum
+    of the scores) on fp32 caches whose token-major views come from permuting
+    the axes of the x = 4 layout (GQA, ragged lengths, an empty sequence)."""
+    from pa_testutil import f32_random_case
+    for KH, G in ((2, 2), (1, 4)):
+        q, kc, vc, bt, lens = f32_random_case(151 + G, S=4, H=KH * G, KH=KH, D=24, BS=4, lens=[1, 6, 13, 0])
+        out, lse = orc.decode_fp32(q, kc, vc, bt, lens, 0.3)
+        _close(out, textbook_decode(q, kc, vc, bt, lens, 0.3), 1e-13, "fp32 textbook")
+        k_tok, _ = token_views(kc, vc)
+        for s in range(4):
+            L = int(lens[s])
+            if L == 0:
+                assert np.all(out[s] == 0) and np.all(lse[s] == -np.inf)
+                continue
+            t = torch.arange(L)
+            K = k_tok[bt[s].long()[t // 4], t % 4].to(torch.float64).numpy()
+            for h in range(KH * G):
+                z = float(np.float32(0.3)) * (K[:, h // G, :] @ q[s, h].to(torch.float64).numpy())
+                _close(lse[s, h], z.max() + math.log(np.exp(z - z.max()).sum()), 1e-13, "fp32 lse")
+
+
+def pin_fp32_equals_16bit(orc):
+    """Invariant: fp16 values widened to fp32 (exactly) and stored in the x = 4
+    layout give the 16-bit oracle's result on the x = 8 layout, bitwise."""
+    q, kc, vc, bt, lens = random_case(161, S=3, H=4, KH=2, D=32, BS=4, lens=[5, 11, 2])
+    k_tok, v_tok = token_views(kc, vc)
+    from pa_testutil import f32_caches_from_tokens
+    kc4, vc4 = f32_caches_from_tokens(k_tok.float(), v_tok.float())
+    out, lse = orc.decode_fp32(q.float(), kc4, vc4, bt, lens, 0.3)
+    assert np.array_equal(out, orc.decode(q, kc, vc, bt, lens, 0.3, FP16))
+    assert np.array_equal(lse, orc.lse(q, kc, vc, bt, lens, 0.3, FP16))
+
+
 ALL_PINS = [
     pin_textbook_gqa, pin_bruteforce_tiny, pin_golden_two_token, pin_golden_layout,
     pin_seq_len_one, pin_uniform_weights, pin_shift_invariance, pin_permutation_invariance,
@@ -423,4 +457,5 @@ ALL_PINS = [
     pin_lse_golden_two_token, pin_lse_closed_forms, pin_lse_library, pin_lse_partition_identity,
     pin_mq_textbook_causal, pin_mq_uniform_causal_bounds,
     pin_e4m3_library, pin_e4m3_golden, pin_fp8kv_textbook, pin_fp8kv_scales,
+    pin_fp32_textbook, pin_fp32_equals_16bit,
 ]

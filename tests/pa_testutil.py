@@ -168,3 +168,31 @@ def fp8_random_case(seed, S, H, KH, D, BS, lens, qdtype=torch.float16, MB=None, 
     else:
         bt = torch.stack([torch.randperm(num_blocks, generator=g)[:MB] for _ in range(S)]).to(torch.int32)
     return q, kc, vc, bt, lens
+
+
+def f32_caches_from_tokens(k_tok: torch.Tensor, v_tok: torch.Tensor):
+    """fp32 caches from token-major pools [nb, BS, KH, D]: key_cache
+    [nb, KH, D/4, BS, 4] (x = 4 four-byte elements per 16-byte chunk) and
+    value_cache [nb, KH, D, BS], by permuting axes."""
+    nb, BS, KH, D = k_tok.shape
+    key_cache = k_tok.reshape(nb, BS, KH, D // 4, 4).permute(0, 2, 3, 1, 4).contiguous()
+    value_cache = v_tok.permute(0, 2, 3, 1).contiguous()
+    return key_cache, value_cache
+
+
+def f32_random_case(seed, S, H, KH, D, BS, lens, MB=None, num_blocks=None):
+    """Random fp32 inputs (N(0, 1)) in the x = 4 layout with a random physical placement."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.tensor(lens, dtype=torch.int32)
+    if MB is None:
+        MB = max(1, math.ceil(max(int(v) for v in lens) / BS)) if len(lens) else 1
+    if num_blocks is None:
+        num_blocks = S * MB
+    q = torch.randn((S, H, D), generator=g)
+    kc, vc = f32_caches_from_tokens(torch.randn((num_blocks, BS, KH, D), generator=g),
+                                    torch.randn((num_blocks, BS, KH, D), generator=g))
+    if num_blocks >= S * MB:
+        bt = torch.randperm(num_blocks, generator=g)[: S * MB].view(S, MB).to(torch.int32)
+    else:
+        bt = torch.stack([torch.randperm(num_blocks, generator=g)[:MB] for _ in range(S)]).to(torch.int32)
+    return q, kc, vc, bt, lens

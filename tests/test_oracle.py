@@ -56,6 +56,10 @@ MUTANTS = [
     ("fp8_k_scale_dropped", "(k_scale * e4m3_to_double(", "(1.0 * e4m3_to_double(", 1),
     ("fp8_v_scale_dropped", "(v_scale * e4m3_to_double(", "(1.0 * e4m3_to_double(", 1),
     ("fp8_key_x8", "    const int x = 16;\n    return", "    const int x = 8;\n    return", 1),
+    ("fp32_key_x8", "    const int x = 4;\n    return", "    const int x = 8;\n    return", 1),
+    ("fp32_key_read_as_value", "(double)kc[key_index_x4(b, kh, d, o, KH, D, BS)]",
+     "(double)kc[value_index(b, kh, d, o, KH, D, BS)]", 1),
+    ("fp32_weights_dropped", "o_sh[d] += z[t] * (double)vc[", "o_sh[d] += (double)vc[", 1),
     ("empty_sequence_not_zero", "if (L <= 0) continue;\n        if (L > MB * BS) { bad = 1; continue; }\n        double* z",
      "if (L > MB * BS) { bad = 1; continue; }\n        double* z", 1),
 ]
