@@ -218,11 +218,15 @@ def oracle_sample(w: workloads.Workload, cpu_seconds: float):
 
 
 def oracle_call(oracle, w: workloads.Workload, inp):
-    """One oracle pass over a batch (multi-query batches through decode_mq)."""
+    """One oracle pass over a batch (multi-query batches through decode_mq, fp8
+    caches through decode_fp8kv, fp32 through decode_fp32)."""
     if w.kv_dtype == "e4m3":
         return oracle.decode_fp8kv(inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
                                    inp["seq_lens"], inp["scale"], w.k_scale, w.v_scale,
                                    workloads.DTYPE_CODES[w.dtype])
+    if w.dtype == "fp32":
+        return oracle.decode_fp32(inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
+                                  inp["seq_lens"], inp["scale"])
     args = (inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"], inp["seq_lens"],
             inp["scale"], workloads.DTYPE_CODES[w.dtype])
     return oracle.decode_mq(*args) if w.q_len > 1 else oracle.decode(*args)

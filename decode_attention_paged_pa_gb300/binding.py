@@ -27,12 +27,15 @@ PA_ERR_TIMEOUT = 6
 
 PA_DTYPE_FP16 = 0
 PA_DTYPE_BF16 = 1
+PA_DTYPE_FP32 = 2
 
 PA_VARIANT_AUTO = 0
 PA_VARIANT_SIMT = 1
 PA_VARIANT_MMA = 2
 
 _DTYPE_CODE = {torch.float16: PA_DTYPE_FP16, torch.bfloat16: PA_DTYPE_BF16}
+# pa_decode_v2 and the host-I/O entry point also take fp32 (key layout x = 4).
+_DTYPE_CODE_F32 = {**_DTYPE_CODE, torch.float32: PA_DTYPE_FP32}
 
 # Every symbol the header declares.
 EXPORTED_SYMBOLS = (
@@ -161,8 +164,9 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, sca
                  lse: torch.Tensor | None = None):
     """Paged decode attention into ``out`` (see include/pa_decode.h).
 
-    Shapes: query/out [S, H, D]; key_cache [NB, KH, D/8, BS, 8];
-    value_cache [NB, KH, D, BS]; block_tables [S, MB] int32; seq_lens [S] int32.
+    Shapes: query/out [S, H, D]; key_cache [NB, KH, D/x, BS, x] with
+    x = 16 / element size (8 for fp16/bf16, 4 for fp32); value_cache
+    [NB, KH, D, BS]; block_tables [S, MB] int32; seq_lens [S] int32.
     ``workspace`` (uint8, >= workspace_bytes(...)) is allocated if omitted.
     ``lse`` (float32 [S, H], optional) receives each (sequence, head)'s
     log-sum-exp of the scaled scores (``pa_decode_v2_lse``; the kernel family
@@ -170,8 +174,8 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, sca
     Returns the workspace used."""
     _check_tensor("query", query, ndim=3)
     dt = query.dtype
-    if dt not in _DTYPE_CODE:
-        raise TypeError("query must be float16 or bfloat16")
+    if dt not in _DTYPE_CODE_F32:
+        raise TypeError("query must be float16, bfloat16 or float32")
     _check_tensor("out", out, dt, 3)
     _check_tensor("key_cache", key_cache, dt, 5)
     _check_tensor("value_cache", value_cache, dt, 4)
@@ -179,7 +183,7 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, sca
     _check_tensor("seq_lens", seq_lens, torch.int32, 1)
     S, H, D = query.shape
     NB, KH, DX, BS, X = key_cache.shape
-    if tuple(out.shape) != (S, H, D) or X != 8 or DX * X != D:
+    if tuple(out.shape) != (S, H, D) or X != 16 // query.element_size() or DX * X != D:
         raise ValueError("inconsistent query / out / key_cache shapes")
     if tuple(value_cache.shape) != (NB, KH, D, BS):
         raise ValueError("value_cache must be [num_blocks, KH, D, BS]")
@@ -198,14 +202,14 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, sca
             raise ValueError("lse is returned with the automatic kernel choice and defaults only")
         st = lib().pa_decode_v2_lse(
             _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
-            _ptr(seq_lens), float(scale), S, H, KH, D, BS, int(partition_size), _DTYPE_CODE[dt],
+            _ptr(seq_lens), float(scale), S, H, KH, D, BS, int(partition_size), _DTYPE_CODE_F32[dt],
             _stream_handle(stream), MB, NB, _ptr(workspace), workspace.numel())
         if st != PA_OK:
             raise PaError(st, "pa_decode_v2_lse")
         return workspace
     st = lib().pa_decode_v2_ex(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
-        _ptr(seq_lens), float(scale), S, H, KH, D, BS, int(partition_size), _DTYPE_CODE[dt],
+        _ptr(seq_lens), float(scale), S, H, KH, D, BS, int(partition_size), _DTYPE_CODE_F32[dt],
         _stream_handle(stream), MB, NB, _ptr(workspace), workspace.numel(), int(variant),
         int(max_ctas), int(timeout_ns))
     if st != PA_OK:
@@ -329,8 +333,8 @@ def pa_decode_v2_host_io(out_host, query_host, key_cache, value_cache, block_tab
     _check_tensor("key_cache", key_cache, query_host.dtype, 5)
     _check_tensor("value_cache", value_cache, query_host.dtype, 4)
     _check_tensor("workspace", workspace, torch.uint8)
-    if query_host.dtype not in _DTYPE_CODE or out_host.dtype != query_host.dtype:
-        raise TypeError("query_host / out_host must be float16 or bfloat16")
+    if query_host.dtype not in _DTYPE_CODE_F32 or out_host.dtype != query_host.dtype:
+        raise TypeError("query_host / out_host must be float16, bfloat16 or float32")
     if block_tables_host.dtype != torch.int32 or seq_lens_host.dtype != torch.int32:
         raise TypeError("block_tables_host / seq_lens_host must be int32")
     S, H, D = query_host.shape
@@ -339,7 +343,7 @@ def pa_decode_v2_host_io(out_host, query_host, key_cache, value_cache, block_tab
     st = lib().pa_decode_v2_host_io(
         _ptr(out_host), _ptr(query_host), _ptr(key_cache), _ptr(value_cache),
         _ptr(block_tables_host), _ptr(seq_lens_host), float(scale), S, H, KH, D, BS,
-        int(partition_size), _DTYPE_CODE[query_host.dtype], _stream_handle(stream), MB, NB,
+        int(partition_size), _DTYPE_CODE_F32[query_host.dtype], _stream_handle(stream), MB, NB,
         _ptr(workspace), workspace.numel())
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2_host_io")

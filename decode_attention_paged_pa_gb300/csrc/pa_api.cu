@@ -42,6 +42,8 @@ bool valid_sizes(int S, int H, int KH, int D, int MB, int BS, int P) {
   return true;
 }
 
+size_t elem_bytes(int dtype) { return dtype == PA_DTYPE_FP32 ? 4 : 2; }
+
 // Shapes every kernel family handles; the tensor-core family also takes head
 // sizes 80, 96, 112 and 8- or 64-token blocks.
 bool base_shape(int D, int BS) {
@@ -124,7 +126,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   const int S = num_seqs, H = num_heads * q_len, KH = num_kv_heads, D = head_size, BS = block_size,
             P = partition_size, MB = max_blocks_per_seq;
   if (!valid_sizes(S, H, KH, D, MB, BS, P) || num_blocks <= 0) return PA_ERR_INVALID_ARG;
-  if (dtype != PA_DTYPE_FP16 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_DTYPE_FP16 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP32) return PA_ERR_INVALID_ARG;
   if (variant < PA_VARIANT_AUTO || variant > PA_VARIANT_MMA || max_ctas < 0 || timeout_ns < 0)
     return PA_ERR_INVALID_ARG;
   if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PA_ERR_INVALID_ARG;
@@ -134,6 +136,10 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   if (!supported(D, BS, P)) return PA_ERR_UNSUPPORTED;
   if (kv_fp8 && variant == PA_VARIANT_SIMT) return PA_ERR_UNSUPPORTED;  // fp8 runs on tensor cores
   if (!base_shape(D, BS) && (kv_fp8 || variant == PA_VARIANT_SIMT)) return PA_ERR_UNSUPPORTED;
+  // fp32 runs on the CUDA-core family only (single-query, its shapes).
+  if (dtype == PA_DTYPE_FP32 &&
+      (kv_fp8 || q_len > 1 || variant == PA_VARIANT_MMA || !base_shape(D, BS)))
+    return PA_ERR_UNSUPPORTED;
   if (S == 0) return PA_OK;
   if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens)
     return PA_ERR_INVALID_ARG;
@@ -147,7 +153,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
 
   const int G = H / KH;
   if (variant == PA_VARIANT_AUTO)
-    variant = (G == 1 && !kv_fp8 && base_shape(D, BS)) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
+    variant = ((G == 1 || dtype == PA_DTYPE_FP32) && !kv_fp8 && base_shape(D, BS)) ? PA_VARIANT_SIMT
+                                                                                 : PA_VARIANT_MMA;
   const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : kSimtGroup;
   const int hg_per_kv = (G + gt - 1) / gt;
   const int n_hg = KH * hg_per_kv;
@@ -167,7 +174,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   // level) start at zero.
   if (cudaMemsetAsync(ws, 0, w.m, st) != cudaSuccess) status = PA_ERR_CUDA;
 
-  const size_t esz = 2;
+  const size_t esz = elem_bytes(dtype);
   for (int s0 = 0; s0 < S && status == PA_OK; s0 += rows_per_launch) {
     const int n = (S - s0) < rows_per_launch ? (S - s0) : rows_per_launch;
     if (s0 > 0 && cudaMemsetAsync(ws + sizeof(int) * kHdrWork, 0, sizeof(int), st) != cudaSuccess) {
@@ -225,6 +232,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     else if (variant == PA_VARIANT_MMA)
       e = dtype == PA_DTYPE_FP16 ? launch_mma_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma_bf16(prm, D, BS, max_ctas, st);
+    else if (dtype == PA_DTYPE_FP32)
+      e = launch_simt_f32(prm, D, BS, max_ctas, st);
     else
       e = dtype == PA_DTYPE_FP16 ? launch_simt_f16(prm, D, BS, max_ctas, st)
                                  : launch_simt_bf16(prm, D, BS, max_ctas, st);
@@ -304,7 +313,7 @@ struct HostIoLayout {
 };
 bool host_io_layout(int S, int H, int KH, int D, int MB, int BS, int P, HostIoLayout* h, WsLayout* w) {
   if (!ws_layout(S, H, KH, D, MB, BS, P, w)) return false;
-  const size_t qbytes = (size_t)S * H * D * 2;
+  const size_t qbytes = (size_t)S * H * D * 4;  // room for the widest element type
   h->q = w->total;
   h->out = align_up(h->q + qbytes);
   h->bt = align_up(h->out + qbytes);
@@ -344,7 +353,8 @@ extern "C" int pa_decode_v2_host_io(void* out_host, const void* query_host, cons
   if (workspace_bytes < h.total) return PA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t qbytes = (size_t)S * H * D * 2;
+  if (dtype != PA_DTYPE_FP16 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP32) return PA_ERR_INVALID_ARG;
+  const size_t qbytes = (size_t)S * H * D * elem_bytes(dtype);
   if (cudaMemcpyAsync(ws + h.q, query_host, qbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(ws + h.bt, block_tables_host, (size_t)S * MB * sizeof(int32_t),
                       cudaMemcpyHostToDevice, st) != cudaSuccess ||

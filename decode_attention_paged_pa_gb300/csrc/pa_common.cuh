@@ -184,12 +184,37 @@ template <> struct F16Traits<__nv_bfloat16> {
   __device__ __forceinline__ static __nv_bfloat16 from_float(float f) { return __float2bfloat16_rn(f); }
 };
 
+// Elements of T in one 16-byte chunk (the page's key layout packs x of them).
 template <typename T>
-__device__ __forceinline__ void unpack8(const uint4& raw, float (&f)[8]) {
-  float2 a = F16Traits<T>::to_float2(raw.x), b = F16Traits<T>::to_float2(raw.y);
-  float2 c = F16Traits<T>::to_float2(raw.z), d = F16Traits<T>::to_float2(raw.w);
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+constexpr int elems_per_chunk() {
+  return 16 / (int)sizeof(T);
+}
+
+// One 16-byte chunk of T as floats.
+template <typename T>
+__device__ __forceinline__ void unpack_chunk(const uint4& raw, float (&f)[elems_per_chunk<T>()]) {
+  if constexpr (sizeof(T) == 4) {
+    f[0] = __uint_as_float(raw.x); f[1] = __uint_as_float(raw.y);
+    f[2] = __uint_as_float(raw.z); f[3] = __uint_as_float(raw.w);
+  } else {
+    float2 a = F16Traits<T>::to_float2(raw.x), b = F16Traits<T>::to_float2(raw.y);
+    float2 c = F16Traits<T>::to_float2(raw.z), d = F16Traits<T>::to_float2(raw.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+}
+
+// Four consecutive output elements, rounded to T (round to nearest even).
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, const float4& v) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(dst) = v;
+  } else {
+    uint2 w;
+    w.x = F16Traits<T>::pack(v.x, v.y);
+    w.y = F16Traits<T>::pack(v.z, v.w);
+    *reinterpret_cast<uint2*>(dst) = w;
+  }
 }
 
 // ---------------------------------------------------------------- tensor-core helpers

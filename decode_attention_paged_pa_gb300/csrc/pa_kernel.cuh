@@ -127,7 +127,7 @@ struct Layout {
   static constexpr uint32_t KBYTES = C::D * C::BS * C::KV_ESZ;  // one block of one kv head
   static constexpr uint32_t STAGE = 2 * KBYTES;
   static constexpr uint32_t RING = NSTAGE * STAGE;
-  static constexpr uint32_t QSLOT = C::GT * C::D * 2;
+  static constexpr uint32_t QSLOT = C::GT * C::D * (uint32_t)sizeof(typename C::T);
   static constexpr uint32_t OFF_Q = RING;
   static constexpr uint32_t OFF_EPI_ACC = al16(OFF_Q + UQ * QSLOT);
   static constexpr uint32_t OFF_EPI_ML = al16(OFF_EPI_ACC + NC * C::GT * C::D * 4);
@@ -278,7 +278,7 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
         UnitInfo& I = info[slot];
         I.s = Up.s; I.p = Up.p; I.hg = Up.hg; I.t0 = Up.t0; I.t1 = Up.t1; I.nb = Up.nb;
         I.np = Up.np; I.nh = Up.nh; I.h0 = Up.h0; I.L = Up.L;
-        const uint32_t qbytes = (uint32_t)(Up.nh * D * 2);
+        const uint32_t qbytes = (uint32_t)(Up.nh * D * sizeof(T));
         mbar_arrive_expect_tx(bar_ufull + 8 * slot, qbytes);
         if constexpr (!MQ)
           bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT,
@@ -291,9 +291,9 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
       // The row heads of a multi-query unit are scattered over the caller's
       // [S, q_len, H] rows: one row copy per lane.
       if (okp && have && lane < Up.nh)
-        bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT + lane * D * 2,
+        bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT + lane * D * (uint32_t)sizeof(T),
                       static_cast<const T*>(prm.q) + out_row<true>(prm, Up.s, Up.h0 + lane) * D,
-                      (uint32_t)(D * 2), bar_ufull + 8 * slot, pol_keep);
+                      (uint32_t)(D * sizeof(T)), bar_ufull + 8 * slot, pol_keep);
     }
     if (okp) ++kq;
     return okp;
@@ -536,11 +536,8 @@ __device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, 
         prm.ws_cl[row * prm.Cmax + J.c] = tot;
       }
     } else {
-      uint2 v;
-      v.x = F16Traits<T>::pack(r.x, r.y);
-      v.y = F16Traits<T>::pack(r.z, r.w);
       const size_t orow = out_row_rt(prm, J.s, J.h0 + gh);
-      *reinterpret_cast<uint2*>(static_cast<T*>(prm.out) + orow * D + d4 * 4) = v;
+      store4<T>(static_cast<T*>(prm.out) + orow * D + d4 * 4, r);
       // Final combine: the log-sum-exp of all the sequence's scores is
       // M + log(total) (natural-log units: the partition and chunk maxima are).
       if (d4 == 0 && prm.lse) prm.lse[orow] = M + logf(tot);
@@ -788,9 +785,10 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
       }
     }
     if constexpr (!MQ) {
-      const long long n2 = (long long)S * H * (D / 8);
+      constexpr int D16 = D * (int)sizeof(T) / 16;  // 16-byte words per output row
+      const long long n2 = (long long)S * H * D16;
       for (long long i = (long long)blockIdx.x * NCT + ctid; i < n2; i += (long long)gridDim.x * NCT) {
-        const int s = (int)(i / ((long long)H * (D / 8)));
+        const int s = (int)(i / ((long long)H * D16));
         if (pref[s + 1] == pref[s]) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
       }
       if (prm.lse) {  // no scores: the log-sum-exp is log 0
@@ -991,10 +989,7 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
       const float4 val = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
       const size_t sh = (size_t)I.s * H + I.h0 + gh;
       if (single) {
-        uint2 v;
-        v.x = F16Traits<T>::pack(val.x, val.y);
-        v.y = F16Traits<T>::pack(val.z, val.w);
-        *reinterpret_cast<uint2*>(out + out_row_rt(prm, I.s, I.h0 + gh) * D + d4 * 4) = v;
+        store4<T>(out + out_row_rt(prm, I.s, I.h0 + gh) * D + d4 * 4, val);
       } else {
         reinterpret_cast<float4*>(prm.ws_o + (sh * Pmax + I.p) * D)[d4] = val;
       }

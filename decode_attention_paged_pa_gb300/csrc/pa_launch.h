@@ -27,6 +27,7 @@ constexpr int kMmaGroup = 8;
 // Launch the persistent kernel for one chunk of sequences.  Returns a cudaError_t.
 cudaError_t launch_simt_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_simt_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_simt_f32(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 // Tensor-core instances of the other shapes: head sizes 80, 96, 112 (block

@@ -1,6 +1,7 @@
 // pa_simt.cuh -- CUDA-core consumer for the paged decode kernel: one warp
-// turns one staged physical block (K block [D/8][BS][8], V block [D][BS]) into
-// an online-softmax update of its private (m, l, acc) state for GT query heads.
+// turns one staged physical block (K block [D/x][BS][x] with x = 16 bytes of
+// elements -- 8 for fp16/bf16, 4 for fp32 -- and V block [D][BS]) into an
+// online-softmax update of its private (m, l, acc) state for GT query heads.
 //
 // Follows the phase-1 kernel `_paged_attn_v2_partition_kernel` of the page
 // "paged_attention_v2_triton.py -- Triton PagedAttention V2 for BI-V100":
@@ -21,16 +22,18 @@ struct SimtConsumer {
   static constexpr bool kMma = false;
   static constexpr int kIssueBatch = 8;  // blocks the producer warp issues together
   static constexpr bool kFp8 = false;
-  static constexpr int KV_ESZ = 2;  // bytes per cached element
-  // q.k: each lane takes QKD dims of one token; LPT lanes share a token.
-  static constexpr int QKD = (D >= 128) ? 64 : 32;
+  static constexpr int KV_ESZ = (int)sizeof(T_);  // bytes per cached element
+  static constexpr int EPC = elems_per_chunk<T_>();  // elements per 16-byte chunk
+  // q.k: each lane takes QKD dims of one token; LPT lanes share a token
+  // (32 dims for fp32, whose registers hold half as many per byte).
+  static constexpr int QKD = (D >= 128 && KV_ESZ == 2) ? 64 : 32;
   static constexpr int LPT = D / QKD;
   static constexpr int TPP = 32 / LPT;        // tokens per pass over the warp
   static constexpr int NPASS = BS / TPP;
-  static constexpr int QCH = QKD / 8;         // 16-byte K chunks per lane and token
-  // p.V: lane (row r, chunk c) reads the 16-byte chunk c (8 tokens) of V rows
-  // r, r + RPP, ...; consecutive lanes read consecutive 16-byte words.
-  static constexpr int CPR = BS / 8;          // chunks per V row
+  static constexpr int QCH = QKD / EPC;       // 16-byte K chunks per lane and token
+  // p.V: lane (row r, chunk c) reads the 16-byte chunk c (EPC tokens) of V
+  // rows r, r + RPP, ...; consecutive lanes read consecutive 16-byte words.
+  static constexpr int CPR = BS / EPC;        // chunks per V row
   static constexpr int RPP = 32 / CPR;        // rows per warp pass
   static constexpr int NROW = D / RPP;        // rows per lane
   static constexpr int SCRATCH_FLOATS = GT * BS;  // per warp: p of the current block
@@ -48,16 +51,16 @@ struct SimtConsumer {
     for (int g = 0; g < GT; ++g) {
 #pragma unroll
       for (int i = 0; i < QCH; ++i) {
-        float f[8];
+        float f[EPC];
         if (g < nh) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(qs + g * D + slice * QKD + i * 8);
-          unpack8<T>(raw, f);
+          const uint4 raw = *reinterpret_cast<const uint4*>(qs + g * D + slice * QKD + i * EPC);
+          unpack_chunk<T>(raw, f);
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = 0.f;
+          for (int e = 0; e < EPC; ++e) f[e] = 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qf[g][i * 8 + e] = f[e] * scale_log2;
+        for (int e = 0; e < EPC; ++e) qf[g][i * EPC + e] = f[e] * scale_log2;
       }
       m[g] = -INFINITY;
       l[g] = 0.f;
@@ -84,13 +87,13 @@ struct SimtConsumer {
       for (int i = 0; i < QCH; ++i) {
         const int c = slice * QCH + i;
         const uint4 raw = *reinterpret_cast<const uint4*>(ks + (c * BS + t) * 16);
-        float f[8];
-        unpack8<T>(raw, f);
+        float f[EPC];
+        unpack_chunk<T>(raw, f);
 #pragma unroll
         for (int g = 0; g < GT; ++g) {
-          float a = qf[g][i * 8] * f[0];
+          float a = qf[g][i * EPC] * f[0];
 #pragma unroll
-          for (int e = 1; e < 8; ++e) a = fmaf(qf[g][i * 8 + e], f[e], a);
+          for (int e = 1; e < EPC; ++e) a = fmaf(qf[g][i * EPC + e], f[e], a);
           part[i][g] = a;
         }
       }
@@ -137,30 +140,31 @@ struct SimtConsumer {
       // so that 0 * (NaN or Inf) cannot reach the accumulator.
       for (int i = lane; i < D * (BS - ntok); i += 32) {
         const int d = i / (BS - ntok), t = ntok + i % (BS - ntok);
-        reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+        if constexpr (sizeof(T) == 4) reinterpret_cast<uint32_t*>(vs)[d * BS + t] = 0u;
+        else reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
       }
       fence_proxy_async_smem();
     }
     __syncwarp();
     const int r0 = lane / CPR, c = lane % CPR;
-    float pv[GT][8];
+    float pv[GT][EPC];
 #pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      const float4 a = *reinterpret_cast<const float4*>(pw + g * BS + c * 8);
-      const float4 b = *reinterpret_cast<const float4*>(pw + g * BS + c * 8 + 4);
-      pv[g][0] = a.x; pv[g][1] = a.y; pv[g][2] = a.z; pv[g][3] = a.w;
-      pv[g][4] = b.x; pv[g][5] = b.y; pv[g][6] = b.z; pv[g][7] = b.w;
-    }
+    for (int g = 0; g < GT; ++g)
+#pragma unroll
+      for (int e4 = 0; e4 < EPC; e4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(pw + g * BS + c * EPC + e4);
+        pv[g][e4] = a.x; pv[g][e4 + 1] = a.y; pv[g][e4 + 2] = a.z; pv[g][e4 + 3] = a.w;
+      }
 #pragma unroll
     for (int r = 0; r < NROW; ++r) {
       const int d = r0 + r * RPP;
-      const uint4 raw = *reinterpret_cast<const uint4*>(vs + (d * BS + c * 8) * 2);
-      float f[8];
-      unpack8<T>(raw, f);
+      const uint4 raw = *reinterpret_cast<const uint4*>(vs + (d * BS + c * EPC) * KV_ESZ);
+      float f[EPC];
+      unpack_chunk<T>(raw, f);
 #pragma unroll
       for (int g = 0; g < GT; ++g)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][r] = fmaf(pv[g][e], f[e], acc[g][r]);
+        for (int e = 0; e < EPC; ++e) acc[g][r] = fmaf(pv[g][e], f[e], acc[g][r]);
     }
     __syncwarp();
   }

@@ -8,7 +8,7 @@ CUDA path's tests/bench and the fp64 oracle consume what it makes.
 
 Layouts:
     query        [S, H, D]
-    key_cache    [num_blocks, KH, D/x, BS, x]   x = 16 / sizeof(dtype) = 8
+    key_cache    [num_blocks, KH, D/x, BS, x]   x = 16 / sizeof(dtype): 8 (fp16/bf16), 4 (fp32)
     value_cache  [num_blocks, KH, D, BS]
     block_tables [S, MB] int32
     seq_lens     [S] int32
@@ -23,8 +23,8 @@ import torch
 
 X_PACK = 8  # 16 bytes / sizeof(fp16 or bf16)
 
-DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
-DTYPE_CODES = {"fp16": 0, "bf16": 1}
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp32": torch.float32}
+DTYPE_CODES = {"fp16": 0, "bf16": 1, "fp32": 2}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -114,6 +114,11 @@ WORKLOADS["mha_d80_bs64_fp16"] = _cfg(
     name="mha_d80_bs64_fp16", dtype="fp16", num_seqs=64, num_heads=32, num_kv_heads=32, head_size=80,
     block_size=64, partition_size=512, scale=1.0 / math.sqrt(80), max_blocks_per_seq=64,
     num_blocks=64 * 64, lens=(512, 4096), lens_random=True, seed=1006)
+# The MHA batch in fp32 (query, caches and output; key layout x = 4).
+WORKLOADS["mha_fp32"] = _cfg(
+    name="mha_fp32", dtype="fp32", num_seqs=64, num_heads=32, num_kv_heads=32, head_size=128,
+    block_size=16, partition_size=512, scale=1.0 / math.sqrt(128), max_blocks_per_seq=256,
+    num_blocks=64 * 256, lens=(512, 4096), lens_random=True, seed=1001)
 # The same on the MHA batch's shapes: 4 row heads per kv head, one unit each.
 WORKLOADS["spec4_mha_fp16"] = _cfg(
     name="spec4_mha_fp16", dtype="fp16", num_seqs=64, num_heads=32, num_kv_heads=32, head_size=128,
@@ -188,7 +193,8 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu",
         key_cache = codes((NB, KH, D // 16, BS, 16), w.k_std)
         value_cache = codes((NB, KH, D, BS), 1.0)
     else:
-        key_cache = torch.empty((NB, KH, D // X_PACK, BS, X_PACK), device=vdev, dtype=dt)
+        x = 16 // torch.empty((), dtype=dt).element_size()
+        key_cache = torch.empty((NB, KH, D // x, BS, x), device=vdev, dtype=dt)
         key_cache.normal_(0.0, w.k_std, generator=vgen)
         value_cache = torch.empty((NB, KH, D, BS), device=vdev, dtype=dt)
         if w.v_uniform:
@@ -208,7 +214,7 @@ def algorithmic_bytes(w: Workload, seq_lens: Sequence[int]) -> int:
     query heads of a group, and all query rows of a multi-query sequence, share
     them), q in, out, the block-table entries that cover the tokens, and
     seq_lens.  Workspace traffic is not counted."""
-    esz = 2
+    esz = DTYPES[w.dtype].itemsize
     kv_esz = 1 if w.kv_dtype == "e4m3" else esz
     lens = [int(v) for v in seq_lens]
     kv = sum(lens) * w.num_kv_heads * w.head_size * 2 * kv_esz

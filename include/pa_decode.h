@@ -48,7 +48,7 @@ extern "C" {
 #endif
 
 /* Element types of query, caches and output. */
-enum { PA_DTYPE_FP16 = 0, PA_DTYPE_BF16 = 1 };
+enum { PA_DTYPE_FP16 = 0, PA_DTYPE_BF16 = 1, PA_DTYPE_FP32 = 2 };
 
 /* Status codes. */
 enum {
@@ -102,13 +102,17 @@ int pa_decode_v2_workspace_layout(int num_seqs, int num_heads, int num_kv_heads,
  * Paged decode attention (see the top of this file).
  *   out          [num_seqs, num_heads, head_size]                      dtype, written
  *   query        [num_seqs, num_heads, head_size]                      dtype
- *   key_cache    [num_blocks, num_kv_heads, head_size/8, block_size, 8] dtype
+ *   key_cache    [num_blocks, num_kv_heads, head_size/x, block_size, x] dtype,
+ *                x = 16 / sizeof(element): 8 for fp16/bf16, 4 for fp32
  *   value_cache  [num_blocks, num_kv_heads, head_size, block_size]      dtype
  *   block_tables [num_seqs, max_blocks_per_seq] int32; entries past
  *                ceil(seq_lens[s]/block_size) are never read
  *   seq_lens     [num_seqs] int32, each in [0, max_blocks_per_seq*block_size]
  *   scale        softmax scale applied to q.k (fp32)
- *   dtype        PA_DTYPE_FP16 or PA_DTYPE_BF16
+ *   dtype        PA_DTYPE_FP16, PA_DTYPE_BF16 or PA_DTYPE_FP32 (fp32 runs on the
+ *                CUDA-core family: head size 64/128/256, blocks of 16 or 32
+ *                tokens, one query head per pass; PA_ERR_UNSUPPORTED for the
+ *                tensor-core variant, multi-query decode and fp8 caches)
  *   stream       cudaStream_t to enqueue on
  *   max_blocks_per_seq  row stride of block_tables (the page's launcher reads
  *                it from the tensor's shape; a C ABI has to be told)
@@ -227,8 +231,8 @@ int pa_decode_v2_mq(void* out, float* lse, const void* query, const void* key_ca
 
 /*
  * Bytes of device workspace pa_decode_v2_host_io needs: the workspace of
- * pa_decode_v2 plus device staging for query, out, block_tables and seq_lens.
- * Returns 0 for invalid sizes.
+ * pa_decode_v2 plus device staging for query, out (room for 4-byte elements,
+ * whatever the dtype), block_tables and seq_lens.  Returns 0 for invalid sizes.
  */
 size_t pa_decode_v2_host_io_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
                                             int head_size, int max_blocks_per_seq, int block_size,

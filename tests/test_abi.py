@@ -162,6 +162,35 @@ def test_shapes_outside_a_family_are_rejected():
         assert st == binding.PA_ERR_UNSUPPORTED, (D, BS)
 
 
+def test_fp32_only_on_the_cuda_core_family():
+    """fp32 (dtype 2) runs single-query on the CUDA-core family, its shapes only."""
+    lib = binding.lib()
+
+    def ex(D, BS, variant, dtype=binding.PA_DTYPE_FP32):
+        return lib.pa_decode_v2_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 0, 4, 2, D, BS,
+                                   512, dtype, None, 4, 8, FAKE, 1 << 30, variant, 0, 0)
+
+    assert ex(128, 16, binding.PA_VARIANT_AUTO) == binding.PA_OK
+    assert ex(128, 16, binding.PA_VARIANT_SIMT) == binding.PA_OK
+    assert ex(128, 16, binding.PA_VARIANT_MMA) == binding.PA_ERR_UNSUPPORTED
+    assert ex(96, 16, binding.PA_VARIANT_AUTO) == binding.PA_ERR_UNSUPPORTED
+    assert ex(128, 8, binding.PA_VARIANT_AUTO) == binding.PA_ERR_UNSUPPORTED
+    assert ex(128, 16, binding.PA_VARIANT_AUTO, dtype=3) == binding.PA_ERR_INVALID_ARG
+    st = lib.pa_decode_v2_mq(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 2, 4,
+                             4, 2, 128, 16, 512, binding.PA_DTYPE_FP32, None, 4, 8, FAKE, 1 << 30)
+    assert st == binding.PA_ERR_UNSUPPORTED
+    st = lib.pa_decode_v2_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
+                              ctypes.c_float(1.0), ctypes.c_float(1.0), 2, 4, 2, 128, 16, 512,
+                              binding.PA_DTYPE_FP32, None, 4, 8, FAKE, 1 << 30)
+    assert st == binding.PA_ERR_UNSUPPORTED
+
+
+def test_host_io_staging_has_room_for_fp32():
+    base = binding.workspace_bytes(3, 4, 2, 128, 8, 16, 512)
+    need = binding.host_io_workspace_bytes(3, 4, 2, 128, 8, 16, 512)
+    assert need >= base + 2 * 3 * 4 * 128 * 4 + 3 * 8 * 4 + 3 * 4
+
+
 def test_status_strings():
     for code in range(7):
         s = binding.status_string(code)
