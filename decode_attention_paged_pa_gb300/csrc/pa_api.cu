@@ -155,7 +155,12 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   if (variant == PA_VARIANT_AUTO)
     variant = ((G == 1 || dtype == PA_DTYPE_FP32) && !kv_fp8 && base_shape(D, BS)) ? PA_VARIANT_SIMT
                                                                                  : PA_VARIANT_MMA;
-  const int gt = (variant == PA_VARIANT_MMA) ? kMmaGroup : kSimtGroup;
+  // More than 8 query rows per kv head: the tensor-core instances with two
+  // column tiles (16 rows per unit) read each K/V block once for 16 rows
+  // (head sizes 64 and 128, blocks of 16 or 32 tokens, 16-bit caches).
+  const bool wide = variant == PA_VARIANT_MMA && G > kMmaGroup && !kv_fp8 && D <= 128 &&
+                    base_shape(D, BS);
+  const int gt = (variant == PA_VARIANT_MMA) ? (wide ? kMmaGroupWide : kMmaGroup) : kSimtGroup;
   const int hg_per_kv = (G + gt - 1) / gt;
   const int n_hg = KH * hg_per_kv;
   const int rows_per_launch = kMaxSeqsPerLaunch;  // sequences per launch
@@ -220,6 +225,9 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     if (kv_fp8)
       e = dtype == PA_DTYPE_FP16 ? launch_mma8_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma8_bf16(prm, D, BS, max_ctas, st);
+    else if (wide)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma16_f16(prm, D, BS, max_ctas, st)
+                                 : launch_mma16_bf16(prm, D, BS, max_ctas, st);
     else if (variant == PA_VARIANT_MMA && BS == 8)
       e = dtype == PA_DTYPE_FP16 ? launch_mma_b8_f16(prm, D, max_ctas, st)
                                  : launch_mma_b8_bf16(prm, D, max_ctas, st);

@@ -832,10 +832,8 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
                     prm.scale_log2, lane);
-    if constexpr (C::kMma) {
-      const int hq = I.h0 + (lane & 3) * 2;  // this lane's two heads of the fragment
-      cons.set_limits(row_limit<MQ>(prm, I.L, hq), row_limit<MQ>(prm, I.L, hq + 1));
-    }
+    if constexpr (C::kMma)
+      cons.set_limits([&](int h) { return row_limit<MQ>(prm, I.L, I.h0 + h); }, lane);
     fence_proxy_async_smem();  // the query slot is refilled by a bulk copy: same ordering as a stage
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_uempty + 8 * slot);

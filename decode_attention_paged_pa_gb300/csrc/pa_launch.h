@@ -20,9 +20,11 @@ constexpr int kMaxSeqsPerLaunch = PA_MAX_SEQS_PER_LAUNCH;
 constexpr int kChunkParts = 16;
 static_assert(kChunkParts == kChunk, "launcher and kernel must agree on the chunk size");
 
-// Query heads per work unit of each kernel family.
+// Query heads per work unit of each kernel family (the tensor-core family
+// takes 16, two column tiles, where a kv head has more than 8 query rows).
 constexpr int kSimtGroup = 1;
 constexpr int kMmaGroup = 8;
+constexpr int kMmaGroupWide = 16;
 
 // Launch the persistent kernel for one chunk of sequences.  Returns a cudaError_t.
 cudaError_t launch_simt_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
@@ -30,6 +32,8 @@ cudaError_t launch_simt_bf16(const KParams& prm, int D, int BS, int max_ctas, cu
 cudaError_t launch_simt_f32(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma16_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma16_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 // Tensor-core instances of the other shapes: head sizes 80, 96, 112 (block
 // sizes 16, 32), and 8- or 64-token blocks (head sizes 64, 80, 96, 112, 128, 256).
 cudaError_t launch_mma_xd_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);

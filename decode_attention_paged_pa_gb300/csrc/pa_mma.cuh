@@ -5,7 +5,8 @@
 //   S[tokens x heads]  = K[tokens x D] . Q^T[D x heads]       (mma m16n8k16, M = 16 tokens)
 //   O^T[D x heads]    += V^T[D x tokens] . P^T[tokens x heads] (mma m16n8k16, M = 16 dims)
 //
-// with 8 query heads as the N = 8 side of the instruction.  Both cache layouts
+// with 8 query heads as the N = 8 side of the instruction (NT_ = 2: two such
+// column tiles, 16 heads, share every K and V fragment).  Both cache layouts
 // of the page "paged_attention_v2_triton.py -- Triton PagedAttention V2 for
 // BI-V100" already are the operands ldmatrix wants: a K block [D/8][BS][8]
 // stores 16 bytes (8 dims) of one token contiguously, i.e. one ldmatrix row of
@@ -40,11 +41,13 @@ namespace pa {
 // row i of a 16-token tile holds token kTok(i) below: a lane's value word
 // then covers four consecutive tokens of one dim, and the eight token rows a
 // lane quad reads fall in distinct shared-memory banks.
-template <typename T_, int D_, int BS_, bool FP8_ = false>
+template <typename T_, int D_, int BS_, bool FP8_ = false, int NT_ = 1>
 struct MmaConsumer {
   using T = T_;
   using MT = typename std::conditional<FP8_, __half, T_>::type;  // operand type of the products
-  static constexpr int D = D_, BS = BS_, GT = 8;
+  static constexpr int NT = NT_;  // 8-head column tiles per unit
+  static constexpr int D = D_, BS = BS_, GT = 8 * NT_;
+  static_assert(NT_ == 1 || (NT_ == 2 && !FP8_), "one or two column tiles (one over fp8 caches)");
   static constexpr bool kMma = true;
   static constexpr bool kFp8 = FP8_;
   static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
@@ -61,11 +64,11 @@ struct MmaConsumer {
   static constexpr int SCRATCH_FLOATS = 0;
   static constexpr bool kSplitWeights = std::is_same<MT, __nv_bfloat16>::value;
 
-  uint32_t qb[NK][2];  // Q^T fragments (B operand), packed element pairs
-  float m[2], l[2];    // heads 2*(lane%4) and 2*(lane%4)+1
-  float acc[NMT][4];
+  uint32_t qb[NK][NT][2];  // Q^T fragments (B operand) per column tile, packed element pairs
+  float m[NT][2], l[NT][2];  // heads 8t + 2*(lane%4) and 8t + 2*(lane%4) + 1 of tile t
+  float acc[NMT][NT][4];
   float scale_log2;
-  int lim[2];  // positions [0, lim) the lane's two heads see (causal rows of multi-query decode)
+  int lim[NT][2];  // positions [0, lim) the lane's heads see (causal rows of multi-query decode)
 
   // fp8 caches: the token (within its 16-token tile) that MMA row i holds.
   // Rows 2c, 2c+1 and 2c+8, 2c+9 -- the score rows that become the weight
@@ -88,11 +91,14 @@ struct MmaConsumer {
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
   }
 
-  // Positions each of this lane's two heads (hq, hq + 1) may see; a
-  // single-query unit sees every position of the sequence.
-  __device__ __forceinline__ void set_limits(int lim_hq, int lim_hq1) {
-    lim[0] = lim_hq;
-    lim[1] = lim_hq1;
+  // Positions each of this lane's heads may see: limit_of(h) for head h of
+  // the unit (a single-query unit sees every position of the sequence).
+  template <class F>
+  __device__ __forceinline__ void set_limits(F limit_of, int lane) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) lim[t][j] = limit_of(8 * t + (lane & 3) * 2 + j);
   }
 
   __device__ __forceinline__ void begin_unit(const T* qs, int nh, float sl2, int lane) {
@@ -126,28 +132,36 @@ struct MmaConsumer {
           lo = F16Traits<__half>::pack(a.x * up, a.y * up);
           hi = F16Traits<__half>::pack(b.x * up, b.y * up);
         }
-        qb[ks][0] = lo;
-        qb[ks][1] = hi;
+        qb[ks][0][0] = lo;
+        qb[ks][0][1] = hi;
       }
       sl2 *= down;
     } else {
 #pragma unroll
-      for (int ks = 0; ks < NK; ++ks) {
-        uint32_t lo = 0, hi = 0;
-        if (n < nh) {
-          lo = *reinterpret_cast<const uint32_t*>(q16 + n * D + ks * 16 + kq);
-          hi = *reinterpret_cast<const uint32_t*>(q16 + n * D + ks * 16 + kq + 8);
+      for (int ks = 0; ks < NK; ++ks)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int h = 8 * t + n;
+          uint32_t lo = 0, hi = 0;
+          if (h < nh) {
+            lo = *reinterpret_cast<const uint32_t*>(q16 + h * D + ks * 16 + kq);
+            hi = *reinterpret_cast<const uint32_t*>(q16 + h * D + ks * 16 + kq + 8);
+          }
+          qb[ks][t][0] = lo;
+          qb[ks][t][1] = hi;
         }
-        qb[ks][0] = lo;
-        qb[ks][1] = hi;
-      }
     }
-    m[0] = m[1] = -INFINITY;
-    l[0] = l[1] = 0.f;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      m[t][0] = m[t][1] = -INFINITY;
+      l[t][0] = l[t][1] = 0.f;
+    }
 #pragma unroll
     for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][t][i] = 0.f;
     scale_log2 = sl2;
   }
 
@@ -159,59 +173,74 @@ struct MmaConsumer {
     }
     const uint32_t kbase = smem_addr(ks), vbase = smem_addr(vs);
     const int r = lane >> 2;
-    float sc[NTT][4];
+    float sc[NTT][NT][4];
 #pragma unroll
     for (int tt = 0; tt < NTT; ++tt) {
-      // Two accumulators (even / odd k-steps) halve the dependent mma chain.
-      float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+      // Two accumulators (even / odd k-steps) per column tile halve the
+      // dependent mma chain.
+      float c[NT][4], c2[NT][4];
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[t][i] = c2[t][i] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
         uint32_t a[4];
         // (An 8-token block: rows 8..15 repeat rows 0..7 and are masked below.)
         const int tok = tt * 16 + (lane & (BS >= 16 ? 15 : 7)), chunk = 2 * kk + (lane >> 4);
         ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
-        if (kk & 1) Mma<T>::run(c2, a, qb[kk][0], qb[kk][1]);
-        else Mma<T>::run(c, a, qb[kk][0], qb[kk][1]);
-      }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c[i] += c2[i];
+        for (int t = 0; t < NT; ++t) {
+          if (kk & 1) Mma<T>::run(c2[t], a, qb[kk][t][0], qb[kk][t][1]);
+          else Mma<T>::run(c[t], a, qb[kk][t][0], qb[kk][t][1]);
+        }
+      }
       const int t_lo = tt * 16 + r, t_hi = t_lo + 8;
-      sc[tt][0] = (t_lo < ntok && tok0 + t_lo < lim[0]) ? c[0] * scale_log2 : -INFINITY;
-      sc[tt][1] = (t_lo < ntok && tok0 + t_lo < lim[1]) ? c[1] * scale_log2 : -INFINITY;
-      sc[tt][2] = (t_hi < ntok && tok0 + t_hi < lim[0]) ? c[2] * scale_log2 : -INFINITY;
-      sc[tt][3] = (t_hi < ntok && tok0 + t_hi < lim[1]) ? c[3] * scale_log2 : -INFINITY;
-    }
-    float alpha[2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float bm = fmaxf(sc[0][j], sc[0][j + 2]);
+      for (int t = 0; t < NT; ++t) {
 #pragma unroll
-      for (int tt = 1; tt < NTT; ++tt) bm = fmaxf(bm, fmaxf(sc[tt][j], sc[tt][j + 2]));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-      const float mn = fmaxf(m[j], bm);
-      // A causal row that has seen no position yet keeps m = -inf: subtract
-      // 0 instead, so its weights and rescale come out 0, not NaN.
-      const float ms = (mn == -INFINITY) ? 0.f : mn;
-      alpha[j] = exp2f(m[j] - ms);
-      m[j] = mn;
-      float ps = 0.f;
-#pragma unroll
-      for (int tt = 0; tt < NTT; ++tt) {
-        sc[tt][j] = exp2f(sc[tt][j] - ms);
-        sc[tt][j + 2] = exp2f(sc[tt][j + 2] - ms);
-        ps += sc[tt][j] + sc[tt][j + 2];
+        for (int i = 0; i < 4; ++i) c[t][i] += c2[t][i];
+        sc[tt][t][0] = (t_lo < ntok && tok0 + t_lo < lim[t][0]) ? c[t][0] * scale_log2 : -INFINITY;
+        sc[tt][t][1] = (t_lo < ntok && tok0 + t_lo < lim[t][1]) ? c[t][1] * scale_log2 : -INFINITY;
+        sc[tt][t][2] = (t_hi < ntok && tok0 + t_hi < lim[t][0]) ? c[t][2] * scale_log2 : -INFINITY;
+        sc[tt][t][3] = (t_hi < ntok && tok0 + t_hi < lim[t][1]) ? c[t][3] * scale_log2 : -INFINITY;
       }
-      l[j] = fmaf(l[j], alpha[j], ps);
     }
+    float alpha[NT][2];
 #pragma unroll
-    for (int mt = 0; mt < NMT; ++mt) {
-      acc[mt][0] *= alpha[0];
-      acc[mt][1] *= alpha[1];
-      acc[mt][2] *= alpha[0];
-      acc[mt][3] *= alpha[1];
-    }
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float bm = fmaxf(sc[0][t][j], sc[0][t][j + 2]);
+#pragma unroll
+        for (int tt = 1; tt < NTT; ++tt) bm = fmaxf(bm, fmaxf(sc[tt][t][j], sc[tt][t][j + 2]));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        const float mn = fmaxf(m[t][j], bm);
+        // A causal row that has seen no position yet keeps m = -inf: subtract
+        // 0 instead, so its weights and rescale come out 0, not NaN.
+        const float ms = (mn == -INFINITY) ? 0.f : mn;
+        alpha[t][j] = exp2f(m[t][j] - ms);
+        m[t][j] = mn;
+        float ps = 0.f;
+#pragma unroll
+        for (int tt = 0; tt < NTT; ++tt) {
+          sc[tt][t][j] = exp2f(sc[tt][t][j] - ms);
+          sc[tt][t][j + 2] = exp2f(sc[tt][t][j + 2] - ms);
+          ps += sc[tt][t][j] + sc[tt][t][j + 2];
+        }
+        l[t][j] = fmaf(l[t][j], alpha[t][j], ps);
+      }
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        acc[mt][t][0] *= alpha[t][0];
+        acc[mt][t][1] *= alpha[t][1];
+        acc[mt][t][2] *= alpha[t][0];
+        acc[mt][t][3] *= alpha[t][1];
+      }
     if (ntok < BS) {
       // Slots past the sequence end hold arbitrary cache contents; zero them
       // so that 0 * (NaN or Inf) cannot reach the accumulator.
@@ -225,19 +254,24 @@ struct MmaConsumer {
 #pragma unroll
     for (int tt = 0; tt < NTT; ++tt) {
       // P fragment rows = tokens, cols = heads; transpose to the B operand.
-      const uint32_t p0 = F16Traits<T>::pack(sc[tt][0], sc[tt][1]);
-      const uint32_t p1 = F16Traits<T>::pack(sc[tt][2], sc[tt][3]);
-      const uint32_t b0 = movmatrix_trans(p0), b1 = movmatrix_trans(p1);
       // bf16 keeps 8 significant bits, so a weight rounded once can be off by
       // 2^-9 of itself: enough, over a handful of tokens, to miss the parity
       // tolerance.  The rounding remainder goes through a second product
       // (P = P_hi + P_lo, both bf16), leaving an error near 2^-17.  fp16's
       // 11 bits need no second product.
-      uint32_t r0 = 0, r1 = 0;
-      if constexpr (kSplitWeights) {
-        const float2 h0 = F16Traits<T>::to_float2(p0), h1 = F16Traits<T>::to_float2(p1);
-        r0 = movmatrix_trans(F16Traits<T>::pack(sc[tt][0] - h0.x, sc[tt][1] - h0.y));
-        r1 = movmatrix_trans(F16Traits<T>::pack(sc[tt][2] - h1.x, sc[tt][3] - h1.y));
+      uint32_t b0[NT], b1[NT], r0[NT], r1[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint32_t p0 = F16Traits<T>::pack(sc[tt][t][0], sc[tt][t][1]);
+        const uint32_t p1 = F16Traits<T>::pack(sc[tt][t][2], sc[tt][t][3]);
+        b0[t] = movmatrix_trans(p0);
+        b1[t] = movmatrix_trans(p1);
+        r0[t] = r1[t] = 0u;
+        if constexpr (kSplitWeights) {
+          const float2 h0 = F16Traits<T>::to_float2(p0), h1 = F16Traits<T>::to_float2(p1);
+          r0[t] = movmatrix_trans(F16Traits<T>::pack(sc[tt][t][0] - h0.x, sc[tt][t][1] - h0.y));
+          r1[t] = movmatrix_trans(F16Traits<T>::pack(sc[tt][t][2] - h1.x, sc[tt][t][3] - h1.y));
+        }
       }
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
@@ -245,8 +279,11 @@ struct MmaConsumer {
         const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
         ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
         if constexpr (BS < 16) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
-        Mma<T>::run(acc[mt], a, b0, b1);
-        if constexpr (kSplitWeights) Mma<T>::run(acc[mt], a, r0, r1);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          Mma<T>::run(acc[mt][t], a, b0[t], b1[t]);
+          if constexpr (kSplitWeights) Mma<T>::run(acc[mt][t], a, r0[t], r1[t]);
+        }
       }
     }
   }
@@ -272,16 +309,16 @@ struct MmaConsumer {
       for (int kk = 0; kk < NK; ++kk) {
         const uint32_t a[4] = {e4m3x2(wk[kk][0]), e4m3x2(wk[kk][1]), e4m3x2(wk[kk][0] >> 16),
                                e4m3x2(wk[kk][1] >> 16)};
-        if (kk & 1) Mma<__half>::run(c1, a, qb[kk][0], qb[kk][1]);
-        else Mma<__half>::run(c0, a, qb[kk][0], qb[kk][1]);
+        if (kk & 1) Mma<__half>::run(c1, a, qb[kk][0][0], qb[kk][0][1]);
+        else Mma<__half>::run(c0, a, qb[kk][0][0], qb[kk][0][1]);
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) c0[i] += c1[i];
       const int t_lo = tt * 16 + trow_lo, t_hi = tt * 16 + trow_hi;
-      sc[tt][0] = (t_lo < ntok && tok0 + t_lo < lim[0]) ? c0[0] * scale_log2 : -INFINITY;
-      sc[tt][1] = (t_lo < ntok && tok0 + t_lo < lim[1]) ? c0[1] * scale_log2 : -INFINITY;
-      sc[tt][2] = (t_hi < ntok && tok0 + t_hi < lim[0]) ? c0[2] * scale_log2 : -INFINITY;
-      sc[tt][3] = (t_hi < ntok && tok0 + t_hi < lim[1]) ? c0[3] * scale_log2 : -INFINITY;
+      sc[tt][0] = (t_lo < ntok && tok0 + t_lo < lim[0][0]) ? c0[0] * scale_log2 : -INFINITY;
+      sc[tt][1] = (t_lo < ntok && tok0 + t_lo < lim[0][1]) ? c0[1] * scale_log2 : -INFINITY;
+      sc[tt][2] = (t_hi < ntok && tok0 + t_hi < lim[0][0]) ? c0[2] * scale_log2 : -INFINITY;
+      sc[tt][3] = (t_hi < ntok && tok0 + t_hi < lim[0][1]) ? c0[3] * scale_log2 : -INFINITY;
     }
     // Value words (dims mt*16 + r and + 8, tokens tt*16 + 4c .. +3) do not
     // depend on the weights: read them before the softmax.
@@ -302,10 +339,10 @@ struct MmaConsumer {
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-      const float mn = fmaxf(m[j], bm);
+      const float mn = fmaxf(m[0][j], bm);
       const float ms = (mn == -INFINITY) ? 0.f : mn;  // a causal row that has seen nothing yet
-      alpha[j] = exp2f(m[j] - ms);
-      m[j] = mn;
+      alpha[j] = exp2f(m[0][j] - ms);
+      m[0][j] = mn;
       float ps = 0.f;
 #pragma unroll
       for (int tt = 0; tt < NTT; ++tt) {
@@ -313,14 +350,14 @@ struct MmaConsumer {
         sc[tt][j + 2] = exp2f(sc[tt][j + 2] - ms);
         ps += sc[tt][j] + sc[tt][j + 2];
       }
-      l[j] = fmaf(l[j], alpha[j], ps);
+      l[0][j] = fmaf(l[0][j], alpha[j], ps);
     }
 #pragma unroll
     for (int mt = 0; mt < NMT; ++mt) {
-      acc[mt][0] *= alpha[0];
-      acc[mt][1] *= alpha[1];
-      acc[mt][2] *= alpha[0];
-      acc[mt][3] *= alpha[1];
+      acc[mt][0][0] *= alpha[0];
+      acc[mt][0][1] *= alpha[1];
+      acc[mt][0][2] *= alpha[0];
+      acc[mt][0][3] *= alpha[1];
     }
 #pragma unroll
     for (int tt = 0; tt < NTT; ++tt) {
@@ -341,7 +378,7 @@ struct MmaConsumer {
       for (int mt = 0; mt < NMT; ++mt) {
         const uint32_t v0 = wv[tt][mt][0] & vmask, v1 = wv[tt][mt][1] & vmask;
         const uint32_t a[4] = {e4m3x2(v0), e4m3x2(v1), e4m3x2(v0 >> 16), e4m3x2(v1 >> 16)};
-        Mma<__half>::run(acc[mt], a, b0, b1);
+        Mma<__half>::run(acc[mt][0], a, b0, b1);
       }
     }
   }
@@ -349,23 +386,28 @@ struct MmaConsumer {
   __device__ __forceinline__ void finish(float* acc_out, float* ml, int lane) {
     const int r = lane >> 2, hq = (lane & 3) * 2;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float ls = l[j];
-      ls += __shfl_xor_sync(0xffffffffu, ls, 4);
-      ls += __shfl_xor_sync(0xffffffffu, ls, 8);
-      ls += __shfl_xor_sync(0xffffffffu, ls, 16);
-      if (r == 0) {
-        ml[(hq + j) * 2] = m[j];
-        ml[(hq + j) * 2 + 1] = ls;
-      }
-    }
+    for (int t = 0; t < NT; ++t)
 #pragma unroll
-    for (int mt = 0; mt < NMT; ++mt) {
-      acc_out[hq * D + mt * 16 + r] = acc[mt][0];
-      acc_out[(hq + 1) * D + mt * 16 + r] = acc[mt][1];
-      acc_out[hq * D + mt * 16 + r + 8] = acc[mt][2];
-      acc_out[(hq + 1) * D + mt * 16 + r + 8] = acc[mt][3];
-    }
+      for (int j = 0; j < 2; ++j) {
+        float ls = l[t][j];
+        ls += __shfl_xor_sync(0xffffffffu, ls, 4);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+        if (r == 0) {
+          ml[(8 * t + hq + j) * 2] = m[t][j];
+          ml[(8 * t + hq + j) * 2 + 1] = ls;
+        }
+      }
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float* o = acc_out + (8 * t + hq) * D + mt * 16 + r;
+        o[0] = acc[mt][t][0];
+        o[D] = acc[mt][t][1];
+        o[8] = acc[mt][t][2];
+        o[D + 8] = acc[mt][t][3];
+      }
   }
 };
 

@@ -72,7 +72,8 @@ struct SimtConsumer {
   // One staged block: ks = K block, vs = V block (shared memory), ntok valid
   // tokens (1..BS).  pw = this warp's scratch (SCRATCH_FLOATS floats).
   // Causal rows are multi-query only, which runs on the tensor-core consumer.
-  __device__ __forceinline__ void set_limits(int, int) {}
+  template <class F>
+  __device__ __forceinline__ void set_limits(F, int) {}
 
   __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane,
                                         float* pw, int /*tok0*/) {

@@ -105,3 +105,49 @@ def test_deterministic_new_shapes():
     for _ in range(3):
         b, _ = run(q, kc, vc, bt, L, 0.1, 64)
         assert torch.equal(a, b)
+
+
+WIDE = [(dt, D, BS, G) for dt in (torch.float16, torch.bfloat16) for D in (64, 128, 256)
+        for BS in (16, 32) for G in (9, 16, 24)]
+
+
+@pytest.mark.parametrize("dt,D,BS,G", WIDE, ids=[f"{str(c[0])[6:]}-D{c[1]}-BS{c[2]}-G{c[3]}" for c in WIDE])
+def test_parity_wide_groups(dt, D, BS, G):
+    """More than 8 query heads per kv head: units of 16 heads (two column tiles;
+    head size 256 keeps units of 8), partly filled when G is not a multiple of 16."""
+    P = 64
+    lens = [1, BS + 1, 2 * P - 1, 17 * P + 3]
+    KH = 2
+    q, kc, vc, bt, L = random_case(5000 + D + BS + G, S=len(lens), H=KH * G, KH=KH, D=D, BS=BS,
+                                   lens=lens, dtype=dt)
+    out, lse = run(q, kc, vc, bt, L, 1.0 / math.sqrt(D), P, lse=True)
+    ref = oracle.decode(q, kc, vc, bt, L, 1.0 / math.sqrt(D), DT_CODE[dt])
+    ok, worst = within_tolerance(out.double().numpy(), ref)
+    assert ok, f"worst excess {worst:.3e}"
+    lse_close(lse.numpy(), oracle.lse(q, kc, vc, bt, L, 1.0 / math.sqrt(D), DT_CODE[dt]))
+
+
+@pytest.mark.parametrize("q_len,G", [(4, 4), (3, 4), (2, 8), (5, 4)])
+def test_multi_query_wide_units(q_len, G):
+    """q_len * G row heads per kv head above 8 share 16-row units."""
+    lens = [q_len, 40, 129, 1500]
+    q, kc, vc, bt, L = mq_case(91 + q_len + G, S=len(lens), q_len=q_len, H=2 * G, KH=2, D=128, BS=16,
+                               lens=lens, dtype=torch.bfloat16)
+    out, lse = run_mq(q, kc, vc, bt, L, 0.1, 64)
+    ref, ref_lse = oracle.decode_mq(q, kc, vc, bt, L, 0.1, oracle.DTYPE_BF16)
+    ok, worst = within_tolerance(out.double().numpy(), ref)
+    assert ok, f"worst excess {worst:.3e}"
+    lse_close(lse.numpy(), ref_lse)
+
+
+def test_wide_units_deterministic_across_grid_sizes():
+    q, kc, vc, bt, L = random_case(97, S=4, H=32, KH=2, D=128, BS=16, lens=[5, 300, 2100, 64])
+    dev = torch.device("cuda")
+    outs = []
+    for ctas in (0, 1, 13):
+        out = torch.empty_like(q, device=dev)
+        ws = binding.pa_decode_v2(out, q.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), L.to(dev), 0.1,
+                                  partition_size=64, max_ctas=ctas)
+        assert binding.device_status(ws) == binding.PA_OK
+        outs.append(out.cpu())
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
