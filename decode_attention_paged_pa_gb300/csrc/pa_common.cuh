@@ -1,7 +1,7 @@
 // pa_common.cuh -- device helpers shared by the paged decode attention kernels:
 // inline-PTX wrappers for mbarriers, 1-D bulk async copies (the bulk-copy flavour
 // of the Tensor Memory Accelerator), ldmatrix / movmatrix / mma.sync, bounded
-// waits, and 16-bit float conversions.
+// waits, and element conversions (fp16, bf16, fp32).
 #pragma once
 
 #include <cuda_bf16.h>

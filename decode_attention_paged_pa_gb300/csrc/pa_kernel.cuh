@@ -11,9 +11,9 @@
 //   * warp NC (producer): takes units from a global counter (dynamic
 //     scheduling balances skewed sequence lengths), publishes each unit's
 //     description and query rows through a 2-slot unit queue, and streams the
-//     unit's physical K and V blocks -- each a contiguous D*BS*2-byte run in
-//     the page's layouts -- into shared memory with 1-D bulk async copies
-//     completing on mbarriers;
+//     unit's physical K and V blocks -- each a contiguous D*BS*(element
+//     size)-byte run in the page's layouts -- into shared memory with 1-D
+//     bulk async copies completing on mbarriers;
 //   * warps 0..NC-1 (consumers): block j of unit u goes to warp (j + u) % NC
 //     (a fixed grouping, so results do not depend on scheduling), which folds it
 //     into its private online-softmax state (SimtConsumer or MmaConsumer).
