@@ -450,8 +450,54 @@ def pin_fp32_equals_16bit(orc):
     assert np.array_equal(lse, orc.lse(q, kc, vc, bt, lens, 0.3, FP16))
 
 
+def _tiled_online_forward(q, K, V, scale, tile):
+    """softmax(scale q K^T) V by the tiled online softmax of the forward kernel
+    of the page "flash_attention.metal -- Flash Attention Metal Shaders" (one
+    query row, no causal mask): per key tile, the tile's scores raise the
+    running maximum m, the running sum l and the accumulator are rescaled by
+    e^(m_old - m_new), the tile's weights are added; at the end out = acc / l
+    (0 when l = 0) and the log-sum-exp is m + log l.  fp64 numpy."""
+    m, l = -math.inf, 0.0
+    acc = np.zeros(V.shape[1])
+    for t0 in range(0, K.shape[0], tile):
+        z = scale * (K[t0:t0 + tile] @ q)
+        m_new = max(m, float(z.max()))
+        alpha = math.exp(m - m_new) if m != -math.inf else 0.0
+        w = np.exp(z - m_new)
+        l = l * alpha + float(w.sum())
+        acc = acc * alpha + w @ V[t0:t0 + tile]
+        m = m_new
+    out = acc / l if l > 0 else np.zeros_like(acc)
+    return out, (m + math.log(l) if l > 0 else -math.inf)
+
+
+def pin_flash_tiled_forward(orc):
+    """Special case = a second textbook routine: the tiled online-softmax
+    forward (tiles of 1, 5 and 64 keys) on densely gathered K/V equals the
+    oracle's output and log-sum-exp (GQA, ragged lengths)."""
+    for dt in (FP16, BF16):
+        q, kc, vc, bt, lens = random_case(171 + dt, S=3, H=4, KH=2, D=16, BS=4, lens=[1, 9, 70],
+                                          dtype=TORCH_DT[dt])
+        out = orc.decode(q, kc, vc, bt, lens, 0.3, dt)
+        lse = orc.lse(q, kc, vc, bt, lens, 0.3, dt)
+        k_tok, v_tok = token_views(kc, vc)
+        sc = float(np.float32(0.3))
+        for s in range(3):
+            L = int(lens[s])
+            t = torch.arange(L)
+            b = bt[s].long()[t // 4]
+            K = k_tok[b, t % 4].to(torch.float64).numpy()
+            V = v_tok[b, t % 4].to(torch.float64).numpy()
+            for h in range(4):
+                for tile in (1, 5, 64):
+                    o_ref, lse_ref = _tiled_online_forward(q[s, h].to(torch.float64).numpy(), K[:, h // 2, :],
+                                                           V[:, h // 2, :], sc, tile)
+                    _close(out[s, h], o_ref, 1e-12, f"tiled forward (tile {tile})")
+                    _close(lse[s, h], lse_ref, 1e-12, f"tiled forward lse (tile {tile})")
+
+
 ALL_PINS = [
-    pin_textbook_gqa, pin_bruteforce_tiny, pin_golden_two_token, pin_golden_layout,
+    pin_textbook_gqa, pin_flash_tiled_forward, pin_bruteforce_tiny, pin_golden_two_token, pin_golden_layout,
     pin_seq_len_one, pin_uniform_weights, pin_shift_invariance, pin_permutation_invariance,
     pin_partition_invariance, pin_empty_sequence, pin_combine_closed_form,
     pin_lse_golden_two_token, pin_lse_closed_forms, pin_lse_library, pin_lse_partition_identity,
