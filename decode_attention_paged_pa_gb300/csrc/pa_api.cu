@@ -50,6 +50,13 @@ bool base_shape(int D, int BS) {
   return (D == 64 || D == 128 || D == 256) && (BS == 16 || BS == 32);
 }
 
+// The CUDA-core family's further 16-bit shapes: head sizes 80, 96, 112 with
+// blocks of 16, 32 or 64 tokens, and 64-token blocks at head sizes 64, 128.
+bool simt_extra_shape(int D, int BS) {
+  return ((D == 80 || D == 96 || D == 112) && (BS == 16 || BS == 32 || BS == 64)) ||
+         ((D == 64 || D == 128) && BS == 64);
+}
+
 bool supported(int D, int BS, int P) {
   const bool d_ok = D == 64 || D == 80 || D == 96 || D == 112 || D == 128 || D == 256;
   const bool bs_ok = BS == 8 || BS == 16 || BS == 32 || BS == 64;
@@ -135,7 +142,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     return PA_ERR_INVALID_ARG;
   if (!supported(D, BS, P)) return PA_ERR_UNSUPPORTED;
   if (kv_fp8 && variant == PA_VARIANT_SIMT) return PA_ERR_UNSUPPORTED;  // fp8 runs on tensor cores
-  if (!base_shape(D, BS) && (kv_fp8 || variant == PA_VARIANT_SIMT)) return PA_ERR_UNSUPPORTED;
+  const bool simt_ok = base_shape(D, BS) || (dtype != PA_DTYPE_FP32 && simt_extra_shape(D, BS));
+  if ((!base_shape(D, BS) && kv_fp8) || (variant == PA_VARIANT_SIMT && !simt_ok)) return PA_ERR_UNSUPPORTED;
   // fp32 runs on the CUDA-core family only (single-query, its shapes).
   if (dtype == PA_DTYPE_FP32 &&
       (kv_fp8 || q_len > 1 || variant == PA_VARIANT_MMA || !base_shape(D, BS)))
@@ -153,8 +161,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
 
   const int G = H / KH;
   if (variant == PA_VARIANT_AUTO)
-    variant = ((G == 1 || dtype == PA_DTYPE_FP32) && !kv_fp8 && base_shape(D, BS)) ? PA_VARIANT_SIMT
-                                                                                 : PA_VARIANT_MMA;
+    variant = ((G == 1 || dtype == PA_DTYPE_FP32) && !kv_fp8 && simt_ok) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
   // More than 8 query rows per kv head: the tensor-core instances with two
   // column tiles (16 rows per unit) read each K/V block once for 16 rows
   // (head sizes 64 and 128, blocks of 16 or 32 tokens, 16-bit caches).
@@ -242,6 +249,9 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
                                  : launch_mma_bf16(prm, D, BS, max_ctas, st);
     else if (dtype == PA_DTYPE_FP32)
       e = launch_simt_f32(prm, D, BS, max_ctas, st);
+    else if (!base_shape(D, BS))
+      e = dtype == PA_DTYPE_FP16 ? launch_simtx_f16(prm, D, BS, max_ctas, st)
+                                 : launch_simtx_bf16(prm, D, BS, max_ctas, st);
     else
       e = dtype == PA_DTYPE_FP16 ? launch_simt_f16(prm, D, BS, max_ctas, st)
                                  : launch_simt_bf16(prm, D, BS, max_ctas, st);

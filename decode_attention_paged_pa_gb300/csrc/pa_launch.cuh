@@ -53,8 +53,14 @@ template <class C, int NC>
 cudaError_t launch_one(const KParams& prm, int max_ctas, cudaStream_t stream) {
   using SZ = Sizing<C, NC>;
   using LY = typename SZ::LY;
-  auto kern = prm.q_len > 1 ? pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, true>
-                            : pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, false>;
+  // Multi-query rows run on the tensor-core consumer only (the API routes
+  // them there), so the CUDA-core consumer has no multi-query instance.
+  auto kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, false>;
+  if constexpr (C::kMma) {
+    if (prm.q_len > 1) kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, true>;
+  } else {
+    if (prm.q_len > 1) return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)LY::bytes(kMaxSeqsPerLaunch));
   if (e != cudaSuccess) return e;

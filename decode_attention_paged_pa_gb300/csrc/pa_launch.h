@@ -30,6 +30,10 @@ constexpr int kMmaGroupWide = 16;
 cudaError_t launch_simt_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_simt_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_simt_f32(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+// CUDA-core instances of head sizes 80, 96, 112 (blocks of 16, 32, 64) and of
+// 64-token blocks at head sizes 64, 128 (fp16 / bf16).
+cudaError_t launch_simtx_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_simtx_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma16_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);

@@ -25,8 +25,10 @@ struct SimtConsumer {
   static constexpr int KV_ESZ = (int)sizeof(T_);  // bytes per cached element
   static constexpr int EPC = elems_per_chunk<T_>();  // elements per 16-byte chunk
   // q.k: each lane takes QKD dims of one token; LPT lanes share a token
-  // (32 dims for fp32, whose registers hold half as many per byte).
-  static constexpr int QKD = (D >= 128 && KV_ESZ == 2) ? 64 : 32;
+  // (32 dims for fp32, whose registers hold half as many per byte; half the
+  // head for head sizes 80, 96, 112).
+  static constexpr bool kPow2D = (D & (D - 1)) == 0;
+  static constexpr int QKD = !kPow2D ? D / 2 : (D >= 128 && KV_ESZ == 2) ? 64 : 32;
   static constexpr int LPT = D / QKD;
   static constexpr int TPP = 32 / LPT;        // tokens per pass over the warp
   static constexpr int NPASS = BS / TPP;
@@ -39,6 +41,7 @@ struct SimtConsumer {
   static constexpr int SCRATCH_FLOATS = GT * BS;  // per warp: p of the current block
 
   static_assert(NPASS >= 1 && BS % TPP == 0, "block size must cover whole passes");
+  static_assert(QKD % EPC == 0 && 32 % LPT == 0 && D % RPP == 0, "head size must split over the lanes");
 
   float qf[GT][QKD];
   float m[GT], l[GT];
@@ -100,10 +103,15 @@ struct SimtConsumer {
       }
 #pragma unroll
       for (int g = 0; g < GT; ++g) {
+        if constexpr ((QCH & (QCH - 1)) == 0) {
 #pragma unroll
-        for (int w = QCH / 2; w >= 1; w >>= 1)
+          for (int w = QCH / 2; w >= 1; w >>= 1)
 #pragma unroll
-          for (int i = 0; i < w; ++i) part[i][g] += part[i + w][g];
+            for (int i = 0; i < w; ++i) part[i][g] += part[i + w][g];
+        } else {
+#pragma unroll
+          for (int i = 1; i < QCH; ++i) part[0][g] += part[i][g];
+        }
         sc[ps][g] = part[0][g];
 #pragma unroll
         for (int off = TPP; off < 32; off <<= 1) sc[ps][g] += __shfl_xor_sync(0xffffffffu, sc[ps][g], off);

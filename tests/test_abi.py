@@ -143,15 +143,20 @@ def test_fp8_entry_rejects_bad_scales():
 
 
 def test_shapes_outside_a_family_are_rejected():
-    """Head sizes 80/96/112 and 8- or 64-token blocks run on the tensor-core
-    family only; fp8 caches take head sizes 64/128/256 and blocks of 16 or 32."""
+    """The tensor-core family takes every shape; the CUDA-core family head sizes
+    80/96/112 with 16/32/64-token blocks and 64-token blocks at 64/128 next to
+    its base shapes, never 8-token blocks; fp8 caches take head sizes
+    64/128/256 and blocks of 16 or 32."""
     lib = binding.lib()
 
     def ex(D, BS, variant):
         return lib.pa_decode_v2_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 0, 4, 2, D, BS,
                                    512, 0, None, 4, 8, FAKE, 1 << 30, variant, 0, 0)
 
-    for D, BS in ((96, 16), (80, 32), (128, 8), (64, 64)):
+    for D, BS in ((96, 16), (80, 32), (112, 64), (64, 64), (128, 64)):
+        for variant in (binding.PA_VARIANT_SIMT, binding.PA_VARIANT_MMA, binding.PA_VARIANT_AUTO):
+            assert ex(D, BS, variant) == binding.PA_OK, (D, BS, variant)
+    for D, BS in ((128, 8), (80, 8), (256, 64)):
         assert ex(D, BS, binding.PA_VARIANT_SIMT) == binding.PA_ERR_UNSUPPORTED, (D, BS)
         assert ex(D, BS, binding.PA_VARIANT_MMA) == binding.PA_OK, (D, BS)
         assert ex(D, BS, binding.PA_VARIANT_AUTO) == binding.PA_OK, (D, BS)

@@ -56,6 +56,27 @@ def test_parity_new_shapes(dt, D, BS, G):
     lse_close(lse.numpy(), oracle.lse(q, kc, vc, bt, L, 1.0 / math.sqrt(D), DT_CODE[dt]))
 
 
+SIMT_X = [(dt, D, BS, G, var) for dt in (torch.float16, torch.bfloat16)
+          for D, BS in ((80, 16), (96, 32), (112, 64), (64, 64), (128, 64), (96, 64))
+          for G in (1, 3) for var in (SIMT, MMA)]
+
+
+@pytest.mark.parametrize("dt,D,BS,G,variant", SIMT_X,
+                         ids=[f"{str(c[0])[6:]}-D{c[1]}-BS{c[2]}-G{c[3]}-{'simt' if c[4] == SIMT else 'mma'}"
+                              for c in SIMT_X])
+def test_parity_extra_shapes_both_families(dt, D, BS, G, variant):
+    """Head sizes 80/96/112 and 64-token blocks on the CUDA-core family (head
+    split in halves over lane pairs) and on the tensor cores."""
+    P = 128
+    lens = [1, BS - 1, BS + 1, 2 * P - 1, 17 * P + 3]
+    q, kc, vc, bt, L = random_case(7000 + D + BS + G, S=len(lens), H=2 * G, KH=2, D=D, BS=BS, lens=lens,
+                                   dtype=dt)
+    out, _ = run(q, kc, vc, bt, L, 1.0 / math.sqrt(D), P, variant=variant)
+    ref = oracle.decode(q, kc, vc, bt, L, 1.0 / math.sqrt(D), DT_CODE[dt])
+    ok, worst = within_tolerance(out.double().numpy(), ref)
+    assert ok, f"worst excess {worst:.3e}"
+
+
 @pytest.mark.parametrize("D,BS", [(80, 8), (112, 64), (256, 8), (64, 64)])
 def test_garbage_past_end_new_shapes(D, BS):
     """NaN in every cache slot past each sequence's end (and in unused blocks)
