@@ -274,6 +274,24 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def replica_workload(w: workloads.Workload, rank: int) -> workloads.Workload:
+    """Rank r's own batch: the same shapes and distributions, seed + 100 r
+    (replicas share nothing, so the multi-GPU path has no exchange)."""
+    return dataclasses.replace(w, seed=w.seed + 100 * rank)
+
+
+def aggregate_over_ranks(dist, device, nbytes: float, tokens: float, ms: float):
+    """Whole-job totals of the replicas: bytes and tokens summed over ranks,
+    time the maximum over ranks.  ``dist`` None means one process."""
+    if dist is None:
+        return float(nbytes), float(tokens), float(ms)
+    sums = torch.tensor([float(nbytes), float(tokens)], dtype=torch.float64, device=device)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(sums, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(sums[0].item()), float(sums[1].item()), float(t.item())
+
+
 def run_native(args, rank, world, local):
     from decode_attention_paged_pa_gb300 import binding
 
@@ -294,7 +312,7 @@ def run_native(args, rank, world, local):
                                  lens=w0.lens if w0.lens_random else w0.lens[:args.seqs],
                                  forced_lens=tuple((i, v) for i, v in w0.forced_lens if i < args.seqs),
                                  distinct_tables=False, name=f"{w0.name}[:{args.seqs}]")
-    w = dataclasses.replace(w0, seed=w0.seed + 100 * rank)   # each rank: its own replica batch
+    w = replica_workload(w0, rank)   # each rank: its own replica batch
     inp = workloads.make_inputs(w, device=dev)
     lens = inp["seq_lens"].tolist()
     nbytes = workloads.algorithmic_bytes(w, lens)
@@ -347,13 +365,10 @@ def run_native(args, rank, world, local):
     if dist:
         dist.barrier()
     per_step_ms = [events[k].elapsed_time(events[k + 1]) for k in range(args.steps)]
-    total_ms = events[0].elapsed_time(events[-1])
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    job_bytes, job_tokens, total_ms = aggregate_over_ranks(dist, dev, nbytes, tokens,
+                                                           events[0].elapsed_time(events[-1]))
     seconds = total_ms / 1e3
-    value = nbytes * world * args.steps / seconds / 1e9
+    value = job_bytes * args.steps / seconds / 1e9
 
     # ---- e2e: per-step inputs from pinned host memory, output back to host
     e2e = None
@@ -381,16 +396,12 @@ def run_native(args, rank, world, local):
             step_host()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        _, _, e2e_ms = aggregate_over_ranks(dist, dev, nbytes, tokens, e0.elapsed_time(e1))
         if not torch.equal(out_h, out.cpu()):
             raise SystemExit("bench.py: host-I/O result differs from the device-resident result")
-        e2e = {"value": nbytes * world * args.steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + lens_h.numel() * 4,
-               "d2h_bytes_per_step": out_h.numel() * 2}
+        e2e = {"value": job_bytes * args.steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + lens_h.numel() * 4,
+               "d2h_bytes_per_step": out_h.numel() * out_h.element_size()}
 
     if rank != 0:
         if dist:
@@ -421,7 +432,7 @@ def run_native(args, rank, world, local):
                    "seq_lens": f"{min(lens)}..{max(lens)} (sum {tokens})", "accumulate": "fp32",
                    "q_len": w.q_len, "kv_dtype": w.kv_dtype or w.dtype, "variant": args.variant, "parallelism": f"replicas x{world}",
                    "l2": f"no flush: KV pool {kv_bytes / 1e9:.2f} GB per rank > L2 {L2_BYTES / 1e6:.0f} MB"},
-        "kv_tokens_per_s": tokens * world * args.steps / seconds,
+        "kv_tokens_per_s": job_tokens * args.steps / seconds,
         "pct_of_measured_peak": 100.0 * value / world / peak,
         "pct_of_nominal_8000": 100.0 * value / world / NOMINAL_HBM_GBS,
         "roofline": roofline,
