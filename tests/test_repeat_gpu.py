@@ -79,3 +79,34 @@ def test_repeat_fp32():
     got = repeat(call)
     ref, _ = oracle.decode_fp32(q, kc, vc, bt, L, 0.09)
     assert within_tolerance(got.double().numpy(), ref, 1e-5, 1e-4)[0]
+
+
+def _split_lens(seed):
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(1, 400, (1100,), generator=g).tolist()
+    lens[1023] = lens[1024] = 1300   # multi-partition on both sides of the split
+    lens[-1] = 0
+    return lens
+
+
+def test_fp8_batch_split_across_launches():
+    """More than 1024 sequences over an fp8 cache: split launches, one workspace."""
+    lens = _split_lens(31)
+    q, kc, vc, bt, L = fp8_random_case(6101, S=len(lens), H=8, KH=2, D=64, BS=16, lens=lens, num_blocks=2048)
+    qd, kd, vd, btd, ld = device(q, kc, vc, bt, L)
+    out = torch.full_like(qd, float("nan"))
+    ws = binding.pa_decode_v2_fp8(out, qd, kd, vd, btd, ld, 0.125, 0.75, 1.25, partition_size=256)
+    assert binding.device_status(ws) == binding.PA_OK
+    ref, _ = oracle.decode_fp8kv(q, kc, vc, bt, L, 0.125, 0.75, 1.25, oracle.DTYPE_FP16)
+    assert within_tolerance(out.cpu().double().numpy(), ref)[0]
+
+
+def test_fp32_batch_split_across_launches():
+    lens = _split_lens(32)
+    q, kc, vc, bt, L = f32_random_case(6102, S=len(lens), H=4, KH=4, D=64, BS=16, lens=lens, num_blocks=2048)
+    qd, kd, vd, btd, ld = device(q, kc, vc, bt, L)
+    out = torch.full_like(qd, float("nan"))
+    ws = binding.pa_decode_v2(out, qd, kd, vd, btd, ld, 0.125, partition_size=256)
+    assert binding.device_status(ws) == binding.PA_OK
+    ref, _ = oracle.decode_fp32(q, kc, vc, bt, L, 0.125)
+    assert within_tolerance(out.cpu().double().numpy(), ref, 1e-5, 1e-4)[0]
