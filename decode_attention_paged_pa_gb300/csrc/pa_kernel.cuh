@@ -838,32 +838,49 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_uempty + 8 * slot);
 
-    // Block j of unit u goes to warp (j + u) % NC: when a unit's block count
-    // is not a multiple of NC, the extra blocks fall on different warps from
-    // unit to unit instead of on warps 0, 1, ... every time.  The grouping
-    // depends only on the unit, never on which CTA runs it.
+    // Work item i of unit u goes to warp (i + u) % NC: when a unit's item
+    // count is not a multiple of NC, the extra items fall on different warps
+    // from unit to unit instead of on warps 0, 1, ... every time.  The
+    // grouping depends only on the unit, never on which CTA runs it.  An item
+    // is one block, or for the tensor-core consumer over 8-token blocks two
+    // consecutive blocks (one 16-token tile of the products).
+    constexpr int PB = (C::kMma && BS == 8 && !C::kFp8) ? 2 : 1;
     const int u_id = (pref[I.s] + I.p) * prm.n_hg + I.hg;
-    for (int j = (warp + NC - u_id % NC) % NC; j < I.nb; j += NC) {
+    const int nitem = (I.nb + PB - 1) / PB;
+    for (int it = (warp + NC - u_id % NC) % NC; it < nitem; it += NC) {
       if constexpr (C::kMma && kMmaHelpPerBlock) {
         if (__shfl_sync(0xffffffffu, *ch.posted, 0) > seen) help_with_job<C, LY>(prm, ch, seen, warp, lane);
       }
-      const uint32_t gj = g + j, st = stage_of<LY>(gj), ph = phase_of<LY>(gj);
-      bool okb = wait_issued(issued, gj + 1, abort_flag, err, prm.timeout_ns) &&
-                 wait_bounded(bar_full + 8 * st, ph, abort_flag, err, prm.timeout_ns, kSiteFull, (int)gj);
+      const int j = it * PB, nbi = min(PB, I.nb - j);
+      const uint32_t gj = g + j, st = stage_of<LY>(gj);
+      bool okb = wait_issued(issued, gj + nbi, abort_flag, err, prm.timeout_ns);
+      for (int b = 0; b < nbi && okb; ++b)
+        okb = wait_bounded(bar_full + 8 * stage_of<LY>(gj + b), phase_of<LY>(gj + b), abort_flag, err,
+                           prm.timeout_ns, kSiteFull, (int)(gj + b));
       // A stage whose copy this warp has not seen land is never released:
       // on a failed wait the warp stops (the producer sees the abort and
       // waits for its copies before the CTA exits).
       if (!__all_sync(0xffffffffu, okb)) break;
-      const int ntok = min(BS, I.t1 - I.t0 - j * BS);
-      cons.block(smem + st * LY::STAGE, smem + st * LY::STAGE + LY::KBYTES, ntok, lane, scr,
-                 I.t0 + j * BS);
+      const int ntok = min(nbi * BS, I.t1 - I.t0 - j * BS);
+      uint8_t* sa = smem + st * LY::STAGE;
+      if constexpr (PB == 2) {
+        if (nbi == 2) {
+          uint8_t* sb = smem + stage_of<LY>(gj + 1) * LY::STAGE;
+          cons.block_pair(sa, sa + LY::KBYTES, sb, sb + LY::KBYTES, ntok, lane, I.t0 + j * BS);
+        } else {
+          cons.block(sa, sa + LY::KBYTES, ntok, lane, scr, I.t0 + j * BS);
+        }
+      } else {
+        cons.block(sa, sa + LY::KBYTES, ntok, lane, scr, I.t0 + j * BS);
+      }
       // The stage is refilled by a bulk copy (async proxy) once released:
       // every lane's reads of it (generic proxy) are ordered before that
       // write by a proxy fence, or the copy can land under reads still
       // queued (the last V tile read stale data without it).
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+      if (lane == 0)
+        for (int b = 0; b < nbi; ++b) mbar_arrive(bar_empty + 8 * stage_of<LY>(gj + b));
     }
     if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
     g += I.nb;

@@ -171,7 +171,28 @@ struct MmaConsumer {
       block_fp8(ks, vs, ntok, lane, tok0);
       return;
     }
+    tiles(ks, vs, nullptr, nullptr, ntok, lane, tok0);
+  }
+
+  // Two consecutive 8-token blocks of a unit as one 16-token tile: block A
+  // (tokens 0..7, full) and block B (tokens 8..15, ntok - 8 of them valid).
+  __device__ __forceinline__ void block_pair(const uint8_t* ksA, uint8_t* vsA, const uint8_t* ksB,
+                                             uint8_t* vsB, int ntok, int lane, int tok0) {
+    static_assert(BS == 8 && !kFp8, "pairs are 8-token blocks of 16-bit caches");
+    tiles(ksA, vsA, ksB, vsB, ntok, lane, tok0);
+  }
+
+  // The 16-bit products over the NTT tiles of one block, or over the tile
+  // made of 8-token blocks A and B (ksB == nullptr: B absent, rows 8..15 of
+  // the tile repeat A's and are masked, their value columns are zero).
+  __device__ __forceinline__ void tiles(const uint8_t* ks, uint8_t* vs, const uint8_t* ksB, uint8_t* vsB,
+                                        int ntok, int lane, int tok0) {
     const uint32_t kbase = smem_addr(ks), vbase = smem_addr(vs);
+    const bool has_b = BS < 16 && ksB != nullptr;
+    // 8-token blocks: the K fragment rows 8..15 (lanes 8..15, 24..31) and the
+    // V fragment token columns 8..15 (lanes 16..31) come from block B.
+    const uint32_t krow = (BS < 16 && has_b && (lane & 8)) ? smem_addr(ksB) : kbase;
+    const uint32_t vcol = (BS < 16 && has_b && (lane >> 4)) ? smem_addr(vsB) : vbase;
     const int r = lane >> 2;
     float sc[NTT][NT][4];
 #pragma unroll
@@ -186,9 +207,9 @@ struct MmaConsumer {
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
         uint32_t a[4];
-        // (An 8-token block: rows 8..15 repeat rows 0..7 and are masked below.)
+        // (An 8-token block: rows 8..15 are block B's, or repeat rows 0..7 and are masked below.)
         const int tok = tt * 16 + (lane & (BS >= 16 ? 15 : 7)), chunk = 2 * kk + (lane >> 4);
-        ldmatrix_x4(kbase + (chunk * BS + tok) * 16, a);
+        ldmatrix_x4(krow + (chunk * BS + tok) * 16, a);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (kk & 1) Mma<T>::run(c2[t], a, qb[kk][t][0], qb[kk][t][1]);
@@ -241,12 +262,15 @@ struct MmaConsumer {
         acc[mt][t][2] *= alpha[t][0];
         acc[mt][t][3] *= alpha[t][1];
       }
-    if (ntok < BS) {
-      // Slots past the sequence end hold arbitrary cache contents; zero them
-      // so that 0 * (NaN or Inf) cannot reach the accumulator.
-      for (int i = lane; i < D * (BS - ntok); i += 32) {
-        const int d = i / (BS - ntok), t = ntok + i % (BS - ntok);
-        reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+    // Slots past the sequence end hold arbitrary cache contents; zero them
+    // so that 0 * (NaN or Inf) cannot reach the accumulator (for a pair, in
+    // block B, the one that can be partial).
+    uint8_t* vz = has_b ? vsB : vs;
+    const int nz = has_b ? ntok - 8 : ntok;
+    if (nz < BS) {
+      for (int i = lane; i < D * (BS - nz); i += 32) {
+        const int d = i / (BS - nz), t = nz + i % (BS - nz);
+        reinterpret_cast<uint16_t*>(vz)[d * BS + t] = 0;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -277,8 +301,8 @@ struct MmaConsumer {
       for (int mt = 0; mt < NMT; ++mt) {
         uint32_t a[4];
         const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
-        ldmatrix_x4(vbase + row * (BS * 2) + chunk * 16, a);
-        if constexpr (BS < 16) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
+        ldmatrix_x4(vcol + row * (BS * 2) + chunk * 16, a);
+        if (BS < 16 && !has_b) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           Mma<T>::run(acc[mt][t], a, b0[t], b1[t]);
