@@ -1,7 +1,11 @@
 /*
- * pa_decode.h -- C ABI of a GB300 (sm_103a) single-query paged decode
- * attention library ("PagedAttention V2": partitioned online softmax followed
- * by a cross-partition log-sum-exp combine).
+ * pa_decode.h -- C ABI of a GB300 (sm_103a) paged decode attention library
+ * ("PagedAttention V2": partitioned online softmax followed by a
+ * cross-partition log-sum-exp combine): single-query decode (pa_decode_v2,
+ * pa_decode_v2_ex, pa_decode_v2_lse), multi-query decode (pa_decode_v2_mq),
+ * E4M3 (fp8) caches (pa_decode_v2_fp8), host-resident per-step inputs
+ * (pa_decode_v2_host_io) and a no-allocation variant
+ * (pa_decode_v2_static_scratch).
  *
  * What it computes, per sequence s and query head h (the page
  * "paged_attention_v2_triton.py -- Triton PagedAttention V2 for BI-V100",
@@ -10,7 +14,8 @@
  *
  *   kv   = h / (num_heads / num_kv_heads)                 (consecutive GQA groups)
  *   for t < L = seq_lens[s]:  b = block_tables[s, t / block_size], o = t % block_size
- *       K_t[d] = key_cache  [b, kv, d / x, o, d % x]      x = 16 / sizeof(element) = 8
+ *       K_t[d] = key_cache  [b, kv, d / x, o, d % x]      x = 16 / sizeof(element):
+ *                                                         8 (fp16/bf16), 4 (fp32), 16 (E4M3)
  *       V_t[d] = value_cache[b, kv, d, o]
  *       z_t    = scale * sum_d query[s, h, d] * K_t[d]    (fp32)
  *   out[s, h, :] = sum_t softmax(z)_t * V_t               rounded to the element type
