@@ -125,7 +125,11 @@ struct Layout {
   static constexpr int NCT = NC * 32;          // consumer threads
   static constexpr int THREADS = NCT + 64;     // + producer warp + epilogue warp
   static constexpr uint32_t KBYTES = C::D * C::BS * C::KV_ESZ;  // one block of one kv head
-  static constexpr uint32_t STAGE = 2 * KBYTES;
+  // A stage holds the K block, then the V block in C::kVPieces pieces (with
+  // C::kVPad bytes of padding between them); its copies deliver STAGE_TX bytes.
+  static constexpr uint32_t STAGE = 2 * KBYTES + C::kVPad;
+  static constexpr uint32_t STAGE_TX = 2 * KBYTES;
+  static_assert(C::kVPieces * C::kVPieceBytes == KBYTES, "value pieces cover the block");
   static constexpr uint32_t RING = NSTAGE * STAGE;
   static constexpr uint32_t QSLOT = C::GT * C::D * (uint32_t)sizeof(typename C::T);
   static constexpr uint32_t OFF_Q = RING;
@@ -349,11 +353,14 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
           if (!done && mbar_test_wait(bar_empty + 8 * st, ph ^ 1u)) {
             const uint32_t dst = sbase + st * LY::STAGE;
             const size_t off = ((size_t)bi * prm.KH + U.kv) * (size_t)(D * C::BS);
-            mbar_arrive_expect_tx(bar_full + 8 * st, LY::STAGE);
+            mbar_arrive_expect_tx(bar_full + 8 * st, LY::STAGE_TX);
             bulk_copy_g2s(dst, static_cast<const uint8_t*>(prm.kc) + off * C::KV_ESZ, LY::KBYTES,
                           bar_full + 8 * st, pol_stream);
-            bulk_copy_g2s(dst + LY::KBYTES, static_cast<const uint8_t*>(prm.vc) + off * C::KV_ESZ, LY::KBYTES,
-                          bar_full + 8 * st, pol_stream);
+            const uint8_t* vsrc = static_cast<const uint8_t*>(prm.vc) + off * C::KV_ESZ;
+#pragma unroll
+            for (int pc = 0; pc < C::kVPieces; ++pc)
+              bulk_copy_g2s(dst + LY::KBYTES + pc * (C::kVPieceBytes + 16u), vsrc + pc * C::kVPieceBytes,
+                            C::kVPieceBytes, bar_full + 8 * st, pol_stream);
             done = true;
           }
           const unsigned m = __ballot_sync(0xffffffffu, done);

@@ -25,6 +25,11 @@
 
 #include "pa_common.cuh"
 
+// Pieces a 32-token value block is staged in (see MmaConsumer::kVPieces).
+#ifndef PA_V_PIECES32
+#define PA_V_PIECES32 2
+#endif
+
 namespace pa {
 
 // FP8_: the caches hold E4M3 codes (one byte per element, key layout
@@ -63,6 +68,48 @@ struct MmaConsumer {
   static_assert(!FP8_ || BS % 16 == 0, "fp8 caches take blocks of 16k tokens");
   static constexpr int SCRATCH_FLOATS = 0;
   static constexpr bool kSplitWeights = std::is_same<MT, __nv_bfloat16>::value;
+
+  // Value blocks of 32 tokens.  A dim's row of the page's V layout is then
+  // 64 bytes, so dims d and d + 2 share shared-memory banks, and an ldmatrix
+  // row group of 8 consecutive dims is a 4-way bank conflict.  The block is
+  // staged instead as kVPieces pieces of D / kVPieces dims (one bulk copy
+  // each), piece p placed 16 p bytes past its contiguous position, and the 8
+  // rows of every value fragment matrix take 8 / kVPieces dims from each
+  // piece: 2 pieces leave a 2-way conflict, 4 pieces none.  Every piece is a
+  // copy of its own, and on the long-context batch (32-token blocks, head
+  // size 128) 2 pieces ran fastest: 135 us a call, against 141 us with 4
+  // and 144 us contiguous.  vdim() gives the dim a value-tile row holds: a
+  // fixed permutation of the dims, rotated by kVRot per piece so that
+  // finish()'s stores of the accumulator rows stay spread over the banks
+  // (rotations checked on the CPU for head sizes 64 to 256).  Other block
+  // sizes and fp8 caches stage contiguously.
+  static constexpr int kVPieces = (!FP8_ && BS_ == 32) ? PA_V_PIECES32 : 1;
+  static_assert(kVPieces == 1 || kVPieces == 2 || kVPieces == 4, "1, 2 or 4 value pieces");
+  static constexpr int kVRot = kVPieces == 4 ? 10 : kVPieces == 2 ? 4 : 0;
+  static constexpr int kVDims = D_ / kVPieces;  // dims per piece
+  static constexpr uint32_t kVPieceBytes = (uint32_t)kVDims * BS_ * KV_ESZ;
+  static constexpr uint32_t kVPad = 16u * (kVPieces - 1);  // stage bytes past the contiguous block
+  static_assert(kVPieceBytes % 16 == 0, "pieces are whole 16-byte bulk-copy units");
+
+  // Dim held by row i (0..15) of value tile mt.
+  __device__ __forceinline__ static int vdim(int mt, int i) {
+    if constexpr (kVPieces == 1) {
+      return mt * 16 + i;
+    } else {
+      constexpr int R = 8 / kVPieces;  // rows of a fragment matrix per piece
+      const int h = i >> 3, ri = i & 7, p = ri / R;
+      return p * kVDims + (mt * 2 * R + h * R + ri % R + kVRot * p) % kVDims;
+    }
+  }
+  // Byte offset of dim d's row in a staged value block.
+  __device__ __forceinline__ static uint32_t vrow(int d) {
+    if constexpr (kVPieces == 1) {
+      return (uint32_t)d * BS_ * KV_ESZ;
+    } else {
+      const int p = d / kVDims;
+      return (uint32_t)p * (kVPieceBytes + 16u) + (uint32_t)(d - p * kVDims) * BS_ * KV_ESZ;
+    }
+  }
 
   uint32_t qb[NK][NT][2];  // Q^T fragments (B operand) per column tile, packed element pairs
   float m[NT][2], l[NT][2];  // heads 8t + 2*(lane%4) and 8t + 2*(lane%4) + 1 of tile t
@@ -270,7 +317,7 @@ struct MmaConsumer {
     if (nz < BS) {
       for (int i = lane; i < D * (BS - nz); i += 32) {
         const int d = i / (BS - nz), t = nz + i % (BS - nz);
-        reinterpret_cast<uint16_t*>(vz)[d * BS + t] = 0;
+        *reinterpret_cast<uint16_t*>(vz + vrow(d) + 2 * t) = 0;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -300,8 +347,8 @@ struct MmaConsumer {
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
         uint32_t a[4];
-        const int row = mt * 16 + (lane & 15), chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
-        ldmatrix_x4(vcol + row * (BS * 2) + chunk * 16, a);
+        const int chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
+        ldmatrix_x4(vcol + vrow(vdim(mt, lane & 15)) + chunk * 16, a);
         if (BS < 16 && !has_b) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -426,11 +473,13 @@ struct MmaConsumer {
     for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        float* o = acc_out + (8 * t + hq) * D + mt * 16 + r;
-        o[0] = acc[mt][t][0];
-        o[D] = acc[mt][t][1];
-        o[8] = acc[mt][t][2];
-        o[D + 8] = acc[mt][t][3];
+        // Accumulator rows r and r + 8 of value tile mt hold dims vdim(mt, r), vdim(mt, r + 8).
+        float* o = acc_out + (8 * t + hq) * D;
+        const int d_lo = vdim(mt, r), d_hi = vdim(mt, r + 8);
+        o[d_lo] = acc[mt][t][0];
+        o[D + d_lo] = acc[mt][t][1];
+        o[d_hi] = acc[mt][t][2];
+        o[D + d_hi] = acc[mt][t][3];
       }
   }
 };

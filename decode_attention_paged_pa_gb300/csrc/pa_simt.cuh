@@ -23,6 +23,9 @@ struct SimtConsumer {
   static constexpr int kIssueBatch = 8;  // blocks the producer warp issues together
   static constexpr bool kFp8 = false;
   static constexpr int KV_ESZ = (int)sizeof(T_);  // bytes per cached element
+  // A value block is staged contiguously: one piece, no padding.
+  static constexpr int kVPieces = 1;
+  static constexpr uint32_t kVPieceBytes = (uint32_t)D_ * BS_ * sizeof(T_), kVPad = 0;
   static constexpr int EPC = elems_per_chunk<T_>();  // elements per 16-byte chunk
   // q.k: each lane takes QKD dims of one token; LPT lanes share a token
   // (32 dims for fp32, whose registers hold half as many per byte; half the
