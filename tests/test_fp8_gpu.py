@@ -4,13 +4,12 @@ k_scale * K and v_scale * V, queries and output fp16 / bf16.  Checked against
 the fp64 oracle's restatement at the benchmark tolerance (every E4M3 value is
 exact in fp16 and bf16, so the arithmetic is that of the 16-bit caches);
 log-sum-exp at the tolerance derived in test_lse_gpu."""
-import numpy as np
 import pytest
 import torch
 
 import oracle
-from decode_attention_paged_pa_gb300 import binding, workloads
-from pa_testutil import compact_sequences, fp8_random_case, within_tolerance
+from decode_attention_paged_pa_gb300 import binding
+from pa_testutil import fp8_random_case, within_tolerance
 from test_lse_gpu import lse_close
 
 pytestmark = pytest.mark.gpu
@@ -72,25 +71,3 @@ def test_fp8kv_nan_codes_past_the_end_are_ignored():
     a, _ = run_fp8(q, kc, vc, bt, L, 0.1, 1.0, 1.0, 512)
     b2, _ = run_fp8(q, kc2, vc2, bt, L, 0.1, 1.0, 1.0, 512)
     assert torch.isfinite(b2.float()).all() and torch.equal(a, b2)
-
-
-def test_fp8kv_workload_sampled():
-    """The GQA batch over an fp8 cache (k_scale 0.5, v_scale 1.5), sampled sequences."""
-    w = workloads.WORKLOADS["gqa_fp8kv_bf16"]
-    inp = workloads.make_inputs(w, device="cuda")
-    out = torch.full_like(inp["query"], float("nan"))
-    lse = torch.empty(inp["query"].shape[:2], device="cuda")
-    ws = binding.pa_decode_v2_fp8(out, inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
-                                  inp["seq_lens"], inp["scale"], w.k_scale, w.v_scale,
-                                  partition_size=w.partition_size, lse=lse)
-    assert binding.device_status(ws) == binding.PA_OK
-    lens = inp["seq_lens"].cpu()
-    seqs = sorted({int(torch.argmin(lens)), int(torch.argmax(lens)), 3, 64})
-    ref, ref_lse = oracle.decode_fp8kv(*compact_sequences(inp, seqs), inp["scale"], w.k_scale, w.v_scale,
-                                       oracle.DTYPE_BF16)
-    sel = torch.tensor(seqs, device="cuda")
-    ok, worst = within_tolerance(out[sel].cpu().double().numpy(), ref)
-    assert ok, f"worst excess {worst:.3e}"
-    lse_close(lse[sel].cpu().numpy(), ref_lse)
-    del inp, out, ws
-    torch.cuda.empty_cache()

@@ -13,8 +13,8 @@ import pytest
 import torch
 
 import oracle
-from decode_attention_paged_pa_gb300 import binding, workloads
-from pa_testutil import compact_sequences, random_case, within_tolerance
+from decode_attention_paged_pa_gb300 import binding
+from pa_testutil import random_case, within_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -56,24 +56,6 @@ def test_lse_matches_oracle(H, KH, D, BS, dtype):
     lse_close(lse.numpy(), ref)
     ok, worst = within_tolerance(out.double().numpy(), oracle.decode(q, kc, vc, bt, L, 0.09, DT_CODE[dtype]))
     assert ok, f"output worst excess {worst:.3e}"
-
-
-@pytest.mark.parametrize("name", ["mha_fp16", "long_skew_bf16"])
-def test_lse_workload_sampled(name):
-    """Full-size batch with lse (both kernel families); sampled sequences vs the oracle."""
-    w = workloads.WORKLOADS[name]
-    inp = workloads.make_inputs(w, device="cuda")
-    out = torch.empty_like(inp["query"])
-    lse = torch.empty((w.num_seqs, w.num_heads), device="cuda")
-    ws = binding.pa_decode_v2(out, inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
-                              inp["seq_lens"], inp["scale"], partition_size=w.partition_size, lse=lse)
-    assert binding.device_status(ws) == binding.PA_OK
-    lens = inp["seq_lens"].cpu()
-    seqs = sorted({int(torch.argmin(lens)), int(torch.argmax(lens)), 1})
-    ref = oracle.lse(*compact_sequences(inp, seqs), inp["scale"], workloads.DTYPE_CODES[w.dtype])
-    lse_close(lse[torch.tensor(seqs, device="cuda")].cpu().numpy(), ref)
-    del inp, out, ws
-    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("H,KH", [(4, 4), (8, 2)], ids=["simt", "mma"])

@@ -2,13 +2,12 @@
 sequence, the i-th attending causally to positions 0 .. L - q_len + i, checked
 against the fp64 oracle's direct causal restatement (output at the benchmark
 tolerance, log-sum-exp at the tolerance derived in test_lse_gpu)."""
-import numpy as np
 import pytest
 import torch
 
 import oracle
-from decode_attention_paged_pa_gb300 import binding, workloads
-from pa_testutil import compact_sequences, random_case, within_tolerance
+from decode_attention_paged_pa_gb300 import binding
+from pa_testutil import random_case, within_tolerance
 from test_lse_gpu import lse_close
 
 pytestmark = pytest.mark.gpu
@@ -81,25 +80,3 @@ def test_mq_rows_split_across_launches():
     ok, worst = within_tolerance(out.double().numpy(), ref)
     assert ok, f"worst excess {worst:.3e}"
     lse_close(lse.numpy(), ref_lse)
-
-
-def test_mq_workload_sampled():
-    """The speculative-verification batch (4 rows per sequence, GQA shapes),
-    sampled sequences against the oracle."""
-    w = workloads.WORKLOADS["spec4_gqa_bf16"]
-    inp = workloads.make_inputs(w, device="cuda")
-    out = torch.full_like(inp["query"], float("nan"))
-    lse = torch.empty(inp["query"].shape[:3], device="cuda")
-    ws = binding.pa_decode_v2_mq(out, inp["query"], inp["key_cache"], inp["value_cache"], inp["block_tables"],
-                                 inp["seq_lens"], inp["scale"], partition_size=w.partition_size, lse=lse)
-    assert binding.device_status(ws) == binding.PA_OK
-    assert torch.isfinite(out.float()).all()
-    lens = inp["seq_lens"].cpu()
-    seqs = sorted({int(torch.argmin(lens)), int(torch.argmax(lens)), 5, 77})
-    ref, ref_lse = oracle.decode_mq(*compact_sequences(inp, seqs), inp["scale"], oracle.DTYPE_BF16)
-    sel = torch.tensor(seqs, device="cuda")
-    ok, worst = within_tolerance(out[sel].cpu().double().numpy(), ref)
-    assert ok, f"worst excess {worst:.3e}"
-    lse_close(lse[sel].cpu().numpy(), ref_lse)
-    del inp, out, ws
-    torch.cuda.empty_cache()

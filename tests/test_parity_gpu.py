@@ -298,32 +298,3 @@ def test_poisoned_workspace_two_level_combine():
     assert ok, f"worst excess {worst:.3e}"
     del inp, outs, ws
     torch.cuda.empty_cache()
-
-
-@pytest.mark.parametrize("variant", [binding.PA_VARIANT_AUTO, SIMT, MMA], ids=["auto", "simt", "mma"])
-@pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER)
-def test_workload_sampled_parity(name, variant):
-    """Full-size batch; AUTO is the launch the bench times, SIMT and MMA force
-    each kernel family.  The outputs of a sample of sequences (shortest,
-    longest and a few random) are checked against the oracle on exactly those
-    sequences, and the whole output is checked to be finite."""
-    w = workloads.WORKLOADS[name]
-    inp = workloads.make_inputs(w, device="cuda")
-    out = torch.full_like(inp["query"], float("nan"))
-    ws = binding.pa_decode_v2(out, inp["query"], inp["key_cache"], inp["value_cache"],
-                              inp["block_tables"], inp["seq_lens"], inp["scale"],
-                              partition_size=w.partition_size, variant=variant)
-    assert binding.device_status(ws) == binding.PA_OK
-    assert torch.isfinite(out.float()).all()
-    lens = inp["seq_lens"].cpu()
-    rng = np.random.default_rng(w.seed)
-    pick = {int(torch.argmin(lens)), int(torch.argmax(lens)),
-            *rng.choice(w.num_seqs, size=min(4, w.num_seqs), replace=False).tolist()}
-    seqs = sorted(pick)
-    sub = compact_sequences(inp, seqs)
-    ref = oracle.decode(*sub, inp["scale"], workloads.DTYPE_CODES[w.dtype])
-    got = out[torch.tensor(seqs, device=out.device)].cpu().double().numpy()
-    ok, worst = within_tolerance(got, ref)
-    assert ok, f"{name}: worst excess {worst:.3e}"
-    del inp, out, ws
-    torch.cuda.empty_cache()
