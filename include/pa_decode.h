@@ -288,8 +288,12 @@ int pa_decode_v2_host_io(void* out_host, const void* query_host, const void* key
  *   - Sizes whose workspace (pa_decode_v2_workspace_bytes) exceeds the array
  *     are rejected with PA_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it with the
+ *     id of the device's context; make that first call before any stream
+ *     capture.  If the context is destroyed and recreated (cudaDeviceReset),
+ *     the array is a new one: the next call sees the new context id and looks
+ *     the address up again, so make that call before any capture too.  (The
+ *     array's contents do not survive the reset; nothing relies on them.)
  *   - All calls on a device share the one array, which keeps the last call's
  *     contents; the counters that must start at zero are cleared by each call
  *     on its stream.  Calls whose execution overlaps on the GPU (different
