@@ -259,14 +259,17 @@ def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, 
     return workspace
 
 
-# Sequences one kernel launch takes (the kernel's prefix array size); a call
-# launches once per this many sequences, whatever q_len.
+# Sequences one phase-1 kernel launch takes (the kernel's order and prefix
+# arrays); a call launches phase 1 once per this many sequences, whatever q_len.
 MAX_ROWS_PER_LAUNCH = 1024
 
 
-def launches_per_call(num_seqs: int, q_len: int = 1) -> int:
-    """Kernel launches one call makes (for launch counts in measurements)."""
-    return max(1, -(-num_seqs // MAX_ROWS_PER_LAUNCH))
+def launches_per_call(num_seqs: int, q_len: int = 1, max_partitions: int = 2) -> int:
+    """Kernel launches one call makes (for launch counts in measurements):
+    phase 1 once per MAX_ROWS_PER_LAUNCH sequences, and the phase-2 combine
+    once if a sequence can have more than one partition (``max_partitions`` =
+    ceil(max_blocks_per_seq * block_size / partition_size))."""
+    return max(1, -(-num_seqs // MAX_ROWS_PER_LAUNCH)) + (1 if max_partitions > 1 else 0)
 
 
 def pa_decode_v2_fp8(out, query, key_cache, value_cache, block_tables, seq_lens, scale: float,

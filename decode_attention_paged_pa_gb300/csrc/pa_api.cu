@@ -32,8 +32,8 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t hdr, tickets, ctickets, m, l, o, cm, cl, co, total;
-  int pmax, cmax;
+  size_t hdr, m, l, o, total;
+  int pmax;
 };
 
 bool valid_sizes(int S, int H, int KH, int D, int MB, int BS, int P) {
@@ -68,23 +68,55 @@ bool ws_layout(int S, int H, int KH, int D, int MB, int BS, int P, WsLayout* w) 
   const long long pmax = ((long long)MB * BS + P - 1) / P;
   if (pmax > INT_MAX) return false;
   w->pmax = (int)pmax;
-  w->cmax = (int)((pmax + kChunkParts - 1) / kChunkParts);
   const size_t shp = (size_t)S * H * (size_t)pmax;
-  const size_t shc = (size_t)S * H * (size_t)w->cmax;
   w->hdr = 0;
-  w->tickets = align_up(kHdrInts * sizeof(int));
-  w->ctickets = align_up(w->tickets + (size_t)S * H * sizeof(int));
-  w->m = align_up(w->ctickets + shc * sizeof(int));
+  w->m = align_up(kHdrInts * sizeof(int));
   w->l = align_up(w->m + shp * sizeof(float));
   w->o = align_up(w->l + shp * sizeof(float));
-  w->cm = align_up(w->o + shp * (size_t)D * sizeof(float));
-  w->cl = align_up(w->cm + shc * sizeof(float));
-  w->co = align_up(w->cl + shc * sizeof(float));
-  w->total = align_up(w->co + shc * (size_t)D * sizeof(float));
+  w->total = align_up(w->o + shp * (size_t)D * sizeof(float));
   return true;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library itself).
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of a 16-bit paged value cache for the tensor-core kernels:
+// value_cache [NB, KH, D, BS] as a 3-D tensor [NB*KH][D][BS] with a box of one
+// whole block ([1][D][BS]), stored in shared memory in the swizzle of the
+// rows' width (BS * 2 bytes: 32, 64 or 128).
+bool encode_value_map(KParams* prm, const void* value_cache, int num_blocks, int KH, int D, int BS) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const CUtensorMapSwizzle sw = BS == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                : BS == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_128B;
+  const cuuint32_t unit[3] = {1, 1, 1};
+  const cuuint64_t vdim[3] = {(cuuint64_t)BS, (cuuint64_t)D, (cuuint64_t)num_blocks * (cuuint64_t)KH};
+  const cuuint64_t vstride[2] = {(cuuint64_t)BS * 2, (cuuint64_t)D * BS * 2};
+  const cuuint32_t vbox[3] = {(cuuint32_t)BS, (cuuint32_t)D, 1};
+  return enc(&prm->tmv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(value_cache), vdim, vstride, vbox,
+             unit, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 }  // namespace pa
@@ -128,7 +160,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   // Multi-query: the kernel sees q_len "row heads" per caller head (H below
   // counts them), q_len * G per kv head, all sharing the kv head's blocks.
   if (q_len < 1 || q_len > kMaxSeqsPerLaunch || num_heads <= 0 ||
-      (long long)num_heads * q_len > 65536)
+      (long long)num_heads * q_len > 65535)
     return PA_ERR_INVALID_ARG;
   const int S = num_seqs, H = num_heads * q_len, KH = num_kv_heads, D = head_size, BS = block_size,
             P = partition_size, MB = max_blocks_per_seq;
@@ -173,6 +205,15 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   const int rows_per_launch = kMaxSeqsPerLaunch;  // sequences per launch
   const int chunk = S < rows_per_launch ? S : rows_per_launch;
   if ((long long)chunk * w.pmax * n_hg > INT_MAX / 2) return PA_ERR_UNSUPPORTED;
+  // The tensor-core kernels over 16-bit caches in blocks of 16 tokens or more
+  // stage value blocks by swizzled tensor copies (z coordinates are int32).
+  const bool tma_values = variant == PA_VARIANT_MMA && !kv_fp8 && BS >= 16;
+  KParams maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (tma_values) {
+    if ((long long)num_blocks * KH > INT_MAX) return PA_ERR_UNSUPPORTED;
+    if (!encode_value_map(&maps, value_cache, num_blocks, KH, D, BS)) return PA_ERR_CUDA;
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -182,8 +223,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     own = true;
   }
   int status = PA_OK;
-  // Error word, work counter and every completion ticket (sequence and chunk
-  // level) start at zero.
+  // The header (error word, work counter, timeout record) starts at zero.
   if (cudaMemsetAsync(ws, 0, w.m, st) != cudaSuccess) status = PA_ERR_CUDA;
 
   const size_t esz = elem_bytes(dtype);
@@ -195,6 +235,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     }
     KParams prm;
     std::memset(&prm, 0, sizeof prm);
+    prm.tmv = maps.tmv;
     prm.out = static_cast<uint8_t*>(out) + (size_t)s0 * H * D * esz;
     prm.q = static_cast<const uint8_t*>(query) + (size_t)s0 * H * D * esz;
     prm.kc = key_cache;
@@ -208,13 +249,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     prm.ws_l = reinterpret_cast<float*>(ws + w.l) + (size_t)s0 * H * w.pmax;
     prm.ws_o = reinterpret_cast<float*>(ws + w.o) + (size_t)s0 * H * w.pmax * D;
     prm.hdr = reinterpret_cast<int*>(ws + w.hdr);
-    prm.tickets = reinterpret_cast<int*>(ws + w.tickets) + (size_t)s0 * n_hg;
-    prm.ctickets = reinterpret_cast<int*>(ws + w.ctickets) + (size_t)s0 * n_hg * w.cmax;
     prm.lse = lse ? lse + (size_t)s0 * H : nullptr;
-    prm.ws_cm = reinterpret_cast<float*>(ws + w.cm) + (size_t)s0 * H * w.cmax;
-    prm.ws_cl = reinterpret_cast<float*>(ws + w.cl) + (size_t)s0 * H * w.cmax;
-    prm.ws_co = reinterpret_cast<float*>(ws + w.co) + (size_t)s0 * H * w.cmax * D;
-    prm.Cmax = w.cmax;
     prm.scale_log2 = scale * k_scale * kLog2e;
     prm.v_scale = v_scale;
     prm.S = n;
@@ -256,6 +291,30 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
       e = dtype == PA_DTYPE_FP16 ? launch_simt_f16(prm, D, BS, max_ctas, st)
                                  : launch_simt_bf16(prm, D, BS, max_ctas, st);
     if (e != cudaSuccess) status = PA_ERR_CUDA;
+  }
+  // Phase 2 over the whole batch (no sequence has more than one partition if
+  // the table holds at most P tokens).  Warps per row: enough that a warp
+  // takes at most 8 partitions, up to 8.
+  if (status == PA_OK && w.pmax > 1) {
+    CParams cp;
+    std::memset(&cp, 0, sizeof cp);
+    cp.out = out;
+    cp.lse = lse;
+    cp.ws_m = reinterpret_cast<const float*>(ws + w.m);
+    cp.ws_l = reinterpret_cast<const float*>(ws + w.l);
+    cp.ws_o = reinterpret_cast<const float*>(ws + w.o);
+    cp.lens = seq_lens;
+    cp.S = S;
+    cp.H = H;
+    cp.Pmax = w.pmax;
+    cp.P = P;
+    cp.max_len = MB * BS;
+    cp.wpr = w.pmax > 32 ? 8 : w.pmax > 16 ? 4 : w.pmax > 8 ? 2 : 1;
+    cp.q_len = q_len;
+    cp.Hu = num_heads;
+    cp.Gu = num_heads / KH;
+    cp.G = G;
+    if (launch_combine(cp, (int)esz, dtype == PA_DTYPE_BF16, D, st) != cudaSuccess) status = PA_ERR_CUDA;
   }
   if (own && cudaFreeAsync(ws, st) != cudaSuccess && status == PA_OK) status = PA_ERR_CUDA;
   return status;

@@ -1,0 +1,49 @@
+// pa_combine.cu -- launches of the phase-2 combine kernel (pa_combine.cuh), one
+// instance per output element type and head size.
+#include "pa_combine.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+
+namespace {
+
+template <typename T, int D>
+cudaError_t go(const CParams& prm, cudaStream_t st) {
+  const int rpc = kCombineWarps / prm.wpr;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)prm.S, (unsigned)((prm.H + rpc - 1) / rpc), 1);
+  cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  // A programmatic dependent of the phase-1 launch just before it on the
+  // stream: it may start as soon as every phase-1 CTA has run out of work,
+  // and waits (griddepcontrol.wait) for phase 1 to complete before it reads.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa_combine_kernel<T, D>, prm);
+}
+
+template <typename T>
+cudaError_t by_head_size(const CParams& prm, int D, cudaStream_t st) {
+  switch (D) {
+    case 64: return go<T, 64>(prm, st);
+    case 80: return go<T, 80>(prm, st);
+    case 96: return go<T, 96>(prm, st);
+    case 112: return go<T, 112>(prm, st);
+    case 128: return go<T, 128>(prm, st);
+    case 256: return go<T, 256>(prm, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CParams& prm, int elem_bytes, bool bf16, int D, cudaStream_t st) {
+  if (elem_bytes == 4) return by_head_size<float>(prm, D, st);
+  return bf16 ? by_head_size<__nv_bfloat16>(prm, D, st) : by_head_size<__half>(prm, D, st);
+}
+
+}  // namespace pa

@@ -1,9 +1,10 @@
 // pa_common.cuh -- device helpers shared by the paged decode attention kernels:
-// inline-PTX wrappers for mbarriers, 1-D bulk async copies (the bulk-copy flavour
-// of the Tensor Memory Accelerator), ldmatrix / movmatrix / mma.sync, bounded
-// waits, and element conversions (fp16, bf16, fp32).
+// inline-PTX wrappers for mbarriers, 1-D bulk async copies and 3-D tensor
+// copies (the Tensor Memory Accelerator), ldmatrix / movmatrix / mma.sync,
+// bounded waits, and element conversions (fp16, bf16, fp32).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the type only)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -119,6 +120,20 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+// 3-D tensor copy global -> shared of one box of the tensor map `tmap` (a
+// __grid_constant__ kernel parameter) at element coordinates (x, y, z),
+// completion counted on `bar` in bytes.  `dst` must be 1024-byte aligned (the
+// value tiles use the 32-byte swizzle, whose pattern follows the shared-memory
+// address bits); x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tmap, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // L2 policy for data read once (K/V pages): evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;

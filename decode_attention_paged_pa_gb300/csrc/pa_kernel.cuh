@@ -1,4 +1,5 @@
-// pa_kernel.cuh -- persistent, warp-specialised paged decode attention kernel.
+// pa_kernel.cuh -- persistent, warp-specialised paged decode attention kernel
+// (phase 1).
 //
 // Work unit = (sequence s, partition p, head group hg): the tokens
 // [p*P, min((p+1)*P, L)) of s against GT query heads that share one kv head.
@@ -12,38 +13,50 @@
 //     scheduling balances skewed sequence lengths), publishes each unit's
 //     description and query rows through a 2-slot unit queue, and streams the
 //     unit's physical K and V blocks -- each a contiguous D*BS*(element
-//     size)-byte run in the page's layouts -- into shared memory with 1-D
-//     bulk async copies completing on mbarriers;
-//   * warps 0..NC-1 (consumers): block j of unit u goes to warp (j + u) % NC
-//     (a fixed grouping, so results do not depend on scheduling), which folds it
-//     into its private online-softmax state (SimtConsumer or MmaConsumer).
-//     The CTA's g-th block (counted over all its units) lives in ring stage
-//     g % NSTAGE.  Warps run at different speeds, so a fast warp
-//     could reach stage g % NSTAGE while the stage's previous copy (block
-//     g - NSTAGE) is still in flight, and an mbarrier parity wait cannot tell
-//     those two phases apart.  A consumer therefore first waits until the
-//     producer has issued block g (a shared-memory counter): the producer
-//     issues block g only after block g - NSTAGE was consumed, so by then the
-//     stage's previous phase is complete and the parity wait is exact.
-//     At the end of a unit the warps' states are combined in shared memory
-//     into the partition's (m_p, l_p, o_p).
-// Sequences with one partition write the output directly (single pass).  For
-// longer sequences each unit stores its partition state in the workspace and
-// takes a ticket (checked one unit later, off the critical path); the last
-// writer runs the phase-2 combine of `_paged_attn_v2_reduce_kernel`
-// (M = max m_p, w_p = e^(m_p - M) l_p / sum, out = sum w_p o_p).  Up to
-// kChunk = 16 partitions are combined in one step; longer sequences are
-// combined per chunk of 16 partitions by each chunk's last writer, and the
-// chunk states by the last chunk (the combine is associative), so no CTA
-// walks hundreds of partitions alone.
-// Unused partitions get the sentinels (m = -inf, l = 0) of the page.
+//     size)-byte run in the page's layouts -- into shared memory, completing
+//     on mbarriers: the key block by a 1-D bulk async copy, the value block by
+//     a 1-D bulk copy or (tensor-core consumer over 16-bit caches, C::kTma) a
+//     3-D tensor copy that lays its rows out in the swizzle of their width;
+//   * warps 0..NC-1 (consumers): block j of unit (p, hg) goes to warp
+//     (j + p * n_hg + hg) % NC (a fixed grouping, so results do not depend on
+//     scheduling), which folds it into its private online-softmax state
+//     (SimtConsumer or MmaConsumer).  The CTA's g-th block (counted over all
+//     its units) lives in ring stage g % NSTAGE.  Warps run at different
+//     speeds, so a fast warp could reach stage g % NSTAGE while the stage's
+//     previous copy (block g - NSTAGE) is still in flight, and an mbarrier
+//     parity wait cannot tell those two phases apart.  A consumer therefore
+//     first waits until the producer has issued block g (a shared-memory
+//     counter): the producer issues block g only after block g - NSTAGE was
+//     consumed, so by then the stage's previous phase is complete and the
+//     parity wait is exact.  At the end of a unit each warp hands its state
+//     to the epilogue warp;
+//   * warp NC + 1 (epilogue): merges the consumer warps' states of each unit
+//     into the partition's (m_p, l_p, o_p) in the workspace, or, for a
+//     sequence with one partition, into the output (single pass).
+// Unused partitions get the sentinels (m = -inf, l = 0) of the page.  The
+// cross-partition combine of `_paged_attn_v2_reduce_kernel` is phase 2
+// (pa_combine.cuh), launched as a programmatic dependent of this kernel: each
+// CTA signals it once its producer has run out of units.
 #pragma once
 
 #include "pa_common.cuh"
 
 namespace pa {
 
+// Sequences per launch: the kernel keeps the longest-first order and a prefix
+// sum of partitions per sequence in shared memory; longer batches are split
+// into several launches.
+#ifndef PA_MAX_SEQS_PER_LAUNCH
+#define PA_MAX_SEQS_PER_LAUNCH 1024
+#endif
+constexpr int kMaxSeqsPerLaunch = PA_MAX_SEQS_PER_LAUNCH;
+static_assert(kMaxSeqsPerLaunch <= 65536, "ranks are kept as 16-bit sequence indices");
+
 struct KParams {
+  // Tensor map of the value cache (C::kTma consumers only): [NB * KH][D][BS]
+  // elements, box [1][D][BS], shared-memory rows in the swizzle of their
+  // width (BS * 2 bytes: 32, 64 or 128).
+  CUtensorMap tmv;
   void* out;
   const void* q;
   const void* kc;
@@ -53,19 +66,14 @@ struct KParams {
   float* ws_m;   // [S, H, Pmax]
   float* ws_l;   // [S, H, Pmax]
   float* ws_o;   // [S, H, Pmax, D]
-  float* ws_cm;  // [S, H, Cmax]     combined state of each chunk of kChunk partitions
-  float* ws_cl;  // [S, H, Cmax]
-  float* ws_co;  // [S, H, Cmax, D]
   int* hdr;      // kHdrInts ints
-  int* tickets;  // [S, n_hg]        partitions (or chunks) of a sequence completed
-  int* ctickets; // [S, n_hg, Cmax]  partitions of a chunk completed
   float* lse;    // [S, H] log-sum-exp of the scaled scores, or null
   int q_len;     // query tokens per sequence (multi-query kernels; 1 otherwise)
   int Hu, Gu;    // the caller's heads and heads per kv head; H and G below count row
                  // heads, q_len of them per caller head (H = q_len * Hu, G = q_len * Gu)
   float scale_log2;   // softmax scale (times k_scale for an fp8 cache) times log2 e
   float v_scale;      // multiplies every output: 1, or an fp8 cache's v_scale
-  int S, H, KH, G, MB, num_blocks, P, Pmax, Cmax;
+  int S, H, KH, G, MB, num_blocks, P, Pmax;
   int hg_per_kv;  // ceil(G / GT)
   int n_hg;       // KH * hg_per_kv
   long long timeout_ns;
@@ -124,12 +132,13 @@ struct Layout {
   static constexpr int NC = NC_, NSTAGE = NSTAGE_, UQ = 2;
   static constexpr int NCT = NC * 32;          // consumer threads
   static constexpr int THREADS = NCT + 64;     // + producer warp + epilogue warp
-  static constexpr uint32_t KBYTES = C::D * C::BS * C::KV_ESZ;  // one block of one kv head
-  // A stage holds the K block, then the V block in C::kVPieces pieces (with
-  // C::kVPad bytes of padding between them); its copies deliver STAGE_TX bytes.
-  static constexpr uint32_t STAGE = 2 * KBYTES + C::kVPad;
-  static constexpr uint32_t STAGE_TX = 2 * KBYTES;
-  static_assert(C::kVPieces * C::kVPieceBytes == KBYTES, "value pieces cover the block");
+  // A stage holds one block of one kv head: the K block, then at VOFF the V
+  // block; its copies deliver STAGE_TX bytes.
+  static constexpr uint32_t KBYTES = C::KTILE;
+  static constexpr uint32_t VOFF = C::KREGION;
+  static constexpr uint32_t STAGE = C::STAGE_BYTES;
+  static constexpr uint32_t STAGE_TX = C::STAGE_TX;
+  static_assert(!C::kTma || (STAGE % 1024 == 0 && VOFF % 1024 == 0), "swizzled value blocks 1024-byte aligned");
   static constexpr uint32_t RING = NSTAGE * STAGE;
   static constexpr uint32_t QSLOT = C::GT * C::D * (uint32_t)sizeof(typename C::T);
   static constexpr uint32_t OFF_Q = RING;
@@ -141,15 +150,15 @@ struct Layout {
   static constexpr uint32_t OFF_SCAN = al16(OFF_EF + (NC + 1) * C::GT * 4);
   static constexpr uint32_t OFF_INFO = al16(OFF_SCAN + THREADS * 4);
   static constexpr uint32_t OFF_EPI_INFO = al16(OFF_INFO + UQ * sizeof(UnitInfo));
-  static constexpr uint32_t OFF_JOBQ = al16(OFF_EPI_INFO + sizeof(UnitInfo));   // 16 queued jobs
-  static constexpr uint32_t OFF_JOBREC = al16(OFF_JOBQ + 16 * 32);               // posted-job slots
-  static constexpr uint32_t OFF_BAR = al16(OFF_JOBREC + 8 * 32);
-  static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 2 + 8;
+  static constexpr uint32_t OFF_BAR = al16(OFF_EPI_INFO + sizeof(UnitInfo));
+  static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 2;
   static constexpr uint32_t OFF_FLAGS = al16(OFF_BAR + NBAR * 8);
   static constexpr uint32_t OFF_PREF = al16(OFF_FLAGS + 64);
   static constexpr uint32_t FIXED = OFF_PREF;
-  static constexpr uint32_t bytes(int S) { return al16(OFF_PREF + (uint32_t)(S + 1) * 4); }
-  static constexpr int OUTS = (C::GT * C::D + NCT - 1) / NCT;  // combine outputs per thread
+  // pref: [S + 1] int32 partitions before each rank; then perm: [S] uint16
+  // sequence of each rank (longest first).
+  static constexpr uint32_t perm_off(int S) { return al16(OFF_PREF + (uint32_t)(S + 1) * 4); }
+  static constexpr uint32_t bytes(int S) { return al16(perm_off(S) + (uint32_t)S * 2); }
 };
 
 template <class LY>
@@ -170,9 +179,7 @@ enum WaitSite {
   kSiteFull = 5,        // consumer: a block to land
   kSiteHandover = 6,    // consumer: the hand-over slot to free up
   kSiteHandEnd = 7,     // consumer: the hand-over slot, for the end marker
-  kSiteServe = 8,       // consumer: the epilogue warp to finish its jobs
-  kSiteEpiFull = 9,     // epilogue: the consumers' states of a unit
-  kSiteJobDone = 10     // epilogue: the helpers of a shared combine job
+  kSiteEpiFull = 9      // epilogue: the consumers' states of a unit
 };
 
 // Wait (bounded) until the producer has issued at least `target` blocks.
@@ -196,8 +203,13 @@ struct UnitPlan {
   int s, p, hg, t0, t1, nb, np, nh, h0, kv, L;
 };
 
+// Unit u = (partition pair, head group): pairs are numbered over the
+// sequences in longest-first order (rank r holds sequence perm[r] and
+// partitions pref[r] .. pref[r + 1] - 1), so the sequences with the most
+// partitions, whose combines are the longest chains, start first, and the
+// last units handed out belong to the shortest sequences.
 template <class C, bool MQ>
-__device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pref, int u) {
+__device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pref, const uint16_t* perm, int u) {
   constexpr int BS = C::BS, GT = C::GT;
   UnitPlan U;
   const int pair = u / prm.n_hg;
@@ -207,11 +219,11 @@ __device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pre
     const int mid = (lo + hi) >> 1;
     if (pref[mid] <= pair) lo = mid; else hi = mid;
   }
-  bool bad = false;  // flagged by the prefix scan already
-  U.s = lo;
+  bool bad = false;  // flagged by the prologue already
+  U.s = perm[lo];
   U.p = pair - pref[lo];
   U.np = pref[lo + 1] - pref[lo];
-  const int L = seq_tokens<MQ>(prm, lo, prm.MB * BS, &bad);
+  const int L = seq_tokens<MQ>(prm, U.s, prm.MB * C::BS, &bad);
   U.L = L;
   U.t0 = U.p * prm.P;
   U.t1 = min(U.t0 + prm.P, L);
@@ -241,7 +253,7 @@ __device__ __forceinline__ int load_block_id(const KParams& prm, const UnitPlan&
 
 template <class C, class LY, bool MQ>
 __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem, const int* pref,
-                                              UnitInfo* info, volatile int* abort_flag,
+                                              const uint16_t* perm, UnitInfo* info, volatile int* abort_flag,
                                               volatile uint32_t* issued, int lane) {
   using T = typename C::T;
   constexpr int D = C::D, NS = LY::NSTAGE, UQ = LY::UQ;
@@ -257,10 +269,13 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   const int total = pref[prm.S] * prm.n_hg;
   auto plan_next = [&](int u, UnitPlan& Up) -> bool {
     if (u >= total) return false;
-    Up = plan_unit<C, MQ>(prm, pref, u);
+    Up = plan_unit<C, MQ>(prm, pref, perm, u);
     return true;
   };
 
+  // The prologue kept temporaries in the ring: order those generic-proxy
+  // writes before the copies (async proxy) that will overwrite them.
+  fence_proxy_async_smem();
   uint32_t g = 0;   // blocks whose copies are issued, in order
   uint32_t kq = 0;  // units published (the end marker included)
   uint32_t reissued = 0;  // after an abort inside a batch: lanes whose block g + lane was issued
@@ -307,10 +322,10 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   // unit k starts streaming, and planned and published once k's first batch
   // of copies is issued (the atomic has returned by then).  A CTA thus holds
   // at most the unit it streams and the next one, which keeps the end of the
-  // work even across CTAs.
-  int u_cur = 0;
-  if (lane == 0) u_cur = atomicAdd(prm.hdr + kHdrWork, 1);
-  u_cur = __shfl_sync(0xffffffffu, u_cur, 0);
+  // work even across CTAs.  CTA i's first unit is unit i, without an atomic
+  // (all CTAs start at once, and their first claims would queue on one
+  // word); the counter hands out units gridDim.x, gridDim.x + 1, ...
+  int u_cur = blockIdx.x;
   UnitPlan U{};
   bool have = plan_next(u_cur, U);
   int bids = 0;  // this lane's block id among the unit's first 32 blocks
@@ -318,7 +333,7 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   ok = publish(U, have);
   while (have && ok) {
     int u_req = 0;
-    if (lane == 0) u_req = atomicAdd(prm.hdr + kHdrWork, 1);
+    if (lane == 0) u_req = atomicAdd(prm.hdr + kHdrWork, 1) + (int)gridDim.x;
     bool have_next = false, published_next = false;
     UnitPlan Un{};
     int bids_next = 0;
@@ -352,15 +367,17 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
         while (true) {
           if (!done && mbar_test_wait(bar_empty + 8 * st, ph ^ 1u)) {
             const uint32_t dst = sbase + st * LY::STAGE;
-            const size_t off = ((size_t)bi * prm.KH + U.kv) * (size_t)(D * C::BS);
+            const size_t off = ((size_t)bi * prm.KH + U.kv) * (size_t)(D * C::BS) * C::KV_ESZ;
             mbar_arrive_expect_tx(bar_full + 8 * st, LY::STAGE_TX);
-            bulk_copy_g2s(dst, static_cast<const uint8_t*>(prm.kc) + off * C::KV_ESZ, LY::KBYTES,
-                          bar_full + 8 * st, pol_stream);
-            const uint8_t* vsrc = static_cast<const uint8_t*>(prm.vc) + off * C::KV_ESZ;
-#pragma unroll
-            for (int pc = 0; pc < C::kVPieces; ++pc)
-              bulk_copy_g2s(dst + LY::KBYTES + pc * (C::kVPieceBytes + 16u), vsrc + pc * C::kVPieceBytes,
-                            C::kVPieceBytes, bar_full + 8 * st, pol_stream);
+            bulk_copy_g2s(dst, static_cast<const uint8_t*>(prm.kc) + off, LY::KBYTES, bar_full + 8 * st,
+                          pol_stream);
+            if constexpr (C::kTma) {
+              // The whole value block (x = 0: the 16-byte alignment rule holds).
+              tma_load_3d(dst + LY::VOFF, &prm.tmv, 0, 0, bi * prm.KH + U.kv, bar_full + 8 * st, pol_stream);
+            } else {
+              bulk_copy_g2s(dst + LY::VOFF, static_cast<const uint8_t*>(prm.vc) + off, LY::KBYTES,
+                            bar_full + 8 * st, pol_stream);
+            }
             done = true;
           }
           const unsigned m = __ballot_sync(0xffffffffu, done);
@@ -405,6 +422,9 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     bids = bids_next;
     have = have_next;
   }
+  // No more units for this CTA: phase 2 may be launched once every CTA has
+  // said so (it waits for this grid to complete before it reads anything).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lane == 0) {
     // Let copies that may still be in flight (the last NSTAGE blocks and the
     // last UQ query rows issued) land before this warp exits, so that the CTA
@@ -430,190 +450,14 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   }
 }
 
-// Partitions per combine chunk (kept equal to kChunkParts of the launcher).
-constexpr int kChunk = 16;
-
-// A combine job for one (sequence, head group):
-//   kind 0: all np (<= kChunk) partition states -> output;
-//   kind 1: the cnt partition states of chunk c -> chunk state c;
-//   kind 2: the ceil(np / kChunk) chunk states -> output.
-struct Job {
-  int s, hg, h0, nh, np, kind, c, cnt;
-};
-static_assert(sizeof(Job) <= 48, "combine job must fit in the shared flag area");
-
-// Jobs that read more float4 values than this (or have more output columns
-// than the epilogue warp has lanes) are shared with the consumer warps;
-// smaller ones are done by the epilogue warp alone.
-#ifndef PA_SHARE_JOB_LOADS
-#define PA_SHARE_JOB_LOADS 512
-#endif
-constexpr int kShareJobLoads = PA_SHARE_JOB_LOADS;
-
-// Lane 0's job, for every lane of the warp.
-__device__ __forceinline__ Job broadcast_job(const Job& J) {
-  Job R;
-  R.s = __shfl_sync(0xffffffffu, J.s, 0);
-  R.hg = __shfl_sync(0xffffffffu, J.hg, 0);
-  R.h0 = __shfl_sync(0xffffffffu, J.h0, 0);
-  R.nh = __shfl_sync(0xffffffffu, J.nh, 0);
-  R.np = __shfl_sync(0xffffffffu, J.np, 0);
-  R.kind = __shfl_sync(0xffffffffu, J.kind, 0);
-  R.c = __shfl_sync(0xffffffffu, J.c, 0);
-  R.cnt = __shfl_sync(0xffffffffu, J.cnt, 0);
-  return R;
-}
-
-__device__ __forceinline__ int* ticket_of(const KParams& prm, const Job& J) {
-  const size_t sg = (size_t)J.s * prm.n_hg + J.hg;
-  return J.kind == 0 ? prm.tickets + sg : prm.ctickets + sg * prm.Cmax + J.c;
-}
-
-__device__ __forceinline__ int job_count(const Job& J) {
-  return J.kind == 0 ? J.np : (J.kind == 1 ? J.cnt : (J.np + kChunk - 1) / kChunk);
-}
-
-// One participant's share of a combine job: the float4 output columns
-// idx = part*32 + lane (+ nparts*32 ...).  Each lane combines its column over
-// all `count` states on its own (the page's Phase 2 formula): M = max m_i,
-// total = sum e^(m_i - M) l_i, o = sum_i (e^(m_i - M) l_i / total) o_i.
-template <class C>
-__device__ __forceinline__ void combine_share(const KParams& prm, const Job& J, int part, int nparts,
-                                              int lane) {
-  using T = typename C::T;
-  // States per round of loads (fewer where registers are tight).
-  constexpr int D = C::D, D4 = D / 4, G8 = (C::kMma && D >= 256) ? 8 : 16;
-  const float *sm, *sl, *so;
-  int stride, first;
-  if (J.kind == 2) {
-    sm = prm.ws_cm; sl = prm.ws_cl; so = prm.ws_co; stride = prm.Cmax; first = 0;
-  } else {
-    sm = prm.ws_m; sl = prm.ws_l; so = prm.ws_o; stride = prm.Pmax; first = J.kind == 1 ? J.c * kChunk : 0;
-  }
-  const int count = job_count(J);
-  for (int idx = part * 32 + lane; idx < J.nh * D4; idx += nparts * 32) {
-    const int gh = idx / D4, d4 = idx - gh * D4;
-    const size_t row = (size_t)J.s * prm.H + J.h0 + gh;
-    const size_t base = row * stride + first;
-    const float4* src = reinterpret_cast<const float4*>(so + base * D) + d4;
-    // One pass in groups of 8 states, all loads of a group in flight at once,
-    // with the running maximum rescaling the running sums.
-    float M = -INFINITY, tot = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < count; i0 += G8) {
-      float mv[G8], lv[G8];
-      float4 ov[G8];
-#pragma unroll
-      for (int j = 0; j < G8; ++j) {
-        if (i0 + j < count) {
-          mv[j] = __ldcg(sm + base + i0 + j);
-          lv[j] = __ldcg(sl + base + i0 + j);
-          ov[j] = __ldcg(src + (size_t)(i0 + j) * D4);
-        } else {
-          mv[j] = -INFINITY;
-          lv[j] = 0.f;
-          ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-      float gm = mv[0];
-#pragma unroll
-      for (int j = 1; j < G8; ++j) gm = fmaxf(gm, mv[j]);
-      const float Mn = fmaxf(M, gm);
-      // States a causal row never reached are (-inf, 0): while every state so
-      // far is one, subtract 0 so that they weigh 0 instead of NaN.
-      const float Ms = (Mn == -INFINITY) ? 0.f : Mn;
-      const float sc = exp2f((M - Ms) * kLog2e);
-      tot *= sc;
-      acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
-#pragma unroll
-      for (int j = 0; j < G8; ++j) {
-        const float w = exp2f((mv[j] - Ms) * kLog2e) * lv[j];
-        tot += w;
-        acc.x = fmaf(w, ov[j].x, acc.x); acc.y = fmaf(w, ov[j].y, acc.y);
-        acc.z = fmaf(w, ov[j].z, acc.z); acc.w = fmaf(w, ov[j].w, acc.w);
-      }
-      M = Mn;
-    }
-    const float inv = tot > 0.f ? 1.f / tot : 0.f;
-    const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (J.kind == 1) {
-      reinterpret_cast<float4*>(prm.ws_co + (row * prm.Cmax + J.c) * D)[d4] = r;
-      if (d4 == 0) {
-        prm.ws_cm[row * prm.Cmax + J.c] = M;
-        prm.ws_cl[row * prm.Cmax + J.c] = tot;
-      }
-    } else {
-      const size_t orow = out_row_rt(prm, J.s, J.h0 + gh);
-      store4<T>(static_cast<T*>(prm.out) + orow * D + d4 * 4, r);
-      // Final combine: the log-sum-exp of all the sequence's scores is
-      // M + log(total) (natural-log units: the partition and chunk maxima are).
-      if (d4 == 0 && prm.lse) prm.lse[orow] = M + logf(tot);
-    }
-  }
-}
-
-// Shared state of the job protocol between the epilogue warp (which posts
-// jobs) and the consumer warps (which help with heavy ones).  Up to kJobSlots
-// posted jobs can be in flight; job i uses slot i % kJobSlots: its record and
-// an mbarrier that completes when all NC + 1 warps have taken their share.
-constexpr int kJobSlots = 4;
-struct JobChannel {
-  volatile int* posted;    // number of jobs posted for help
-  volatile int* finished;  // set once the epilogue warp posts no more jobs
-  Job* rec;                // kJobSlots records
-  uint32_t bar_done;       // kJobSlots mbarriers (8 bytes apart)
-};
-
-#ifndef PA_SETTLE_WHEN_IDLE
-#define PA_SETTLE_WHEN_IDLE 1
-#endif
-constexpr bool kSettleWhenIdle = PA_SETTLE_WHEN_IDLE != 0;
-// Consumer warps of the tensor-core kernel (several heads per unit, so
-// combine jobs are shared) also look for posted jobs before every block.
-#ifndef PA_MMA_HELP_PER_BLOCK
-#define PA_MMA_HELP_PER_BLOCK 1
-#endif
-constexpr bool kMmaHelpPerBlock = PA_MMA_HELP_PER_BLOCK != 0;
-
-// A consumer warp's help with every posted job it has not taken yet.
-template <class C, class LY>
-__device__ __forceinline__ void help_with_job(const KParams& prm, const JobChannel& ch, int& seen, int warp,
-                                              int lane) {
-  // Lane 0's reading decides for the whole warp.
-  const int posted = __shfl_sync(0xffffffffu, *ch.posted, 0);
-  while (seen < posted) {
-    __threadfence_block();
-    const int slot = seen % kJobSlots;
-    const Job J = ch.rec[slot];
-    combine_share<C>(prm, J, warp, LY::NC + 1, lane);
-    // A chunk state is read by another CTA once the epilogue warp has retired
-    // this job and released the sequence ticket: every lane's stores must be
-    // visible GPU-wide before this warp counts its share done.
-    if (J.kind == 1) fence_acq_rel_gpu();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(ch.bar_done + 8 * slot);
-    ++seen;
-  }
-}
-
-template <class C, class LY>
-__device__ __noinline__ void help_with_job_out_of_line(const KParams& prm, const JobChannel& ch, int& seen,
-                                                       int warp, int lane) {
-  help_with_job<C, LY>(prm, ch, seen, warp, lane);
-}
-
 // Consumer warp: wait (bounded) for the hand-over slot to be free for
-// hand-over k, helping with any combine job posted meanwhile.  (The epilogue
-// warp may be waiting for this warp's help before it can free the slot.)
-template <class C, class LY>
-__device__ __forceinline__ bool wait_handover(const KParams& prm, const JobChannel& ch, int& seen,
-                                              uint32_t bar_eempty, uint32_t k, volatile int* abort_flag,
-                                              int* err, int site, int warp, int lane) {
+// hand-over k (the epilogue warp has merged hand-over k - 1).
+__device__ __forceinline__ bool wait_handover(const KParams& prm, uint32_t bar_eempty, uint32_t k,
+                                              volatile int* abort_flag, int* err, int site, int lane) {
   const uint32_t parity = (k & 1u) ^ 1u;
   if (__all_sync(0xffffffffu, mbar_test_wait(bar_eempty, parity))) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    help_with_job<C, LY>(prm, ch, seen, warp, lane);
     if (__all_sync(0xffffffffu, mbar_test_wait(bar_eempty, parity))) return true;
     if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
     if ((long long)(global_timer_ns() - t0) > prm.timeout_ns) {
@@ -624,145 +468,13 @@ __device__ __forceinline__ bool wait_handover(const KParams& prm, const JobChann
   }
 }
 
-// Epilogue warp's combine-job engine.  Jobs are queued; a heavy job is posted
-// for the consumer warps (up to kJobSlots in flight), who take their shares at
-// their next unit boundary, while the epilogue warp takes its own share and
-// goes back to merging hand-overs.  Completion is polled in posting order; a
-// completed chunk job (kind 1) then takes the sequence ticket, and the last
-// chunk's final job (kind 2) is queued.  All members are warp-uniform; queued
-// jobs live in a shared-memory ring.
-template <class C, class LY>
-struct JobEngine {
-  static constexpr int JQ = 16;
-  const KParams& prm;
-  const JobChannel& ch;
-  Job* q;               // JQ slots
-  volatile int* abort_flag;
-  int* err;
-  int lane;
-  int head = 0, tail = 0;       // queued jobs
-  int nposted = 0, ndone = 0;   // posted jobs, and those completed (in order)
-
-  __device__ __forceinline__ JobEngine(const KParams& p, const JobChannel& c, Job* qq, volatile int* ab,
-                                       int* e, int l)
-      : prm(p), ch(c), q(qq), abort_flag(ab), err(e), lane(l) {}
-
-  // Shared if it is large, or if the epilogue warp alone would need more than
-  // one output column per lane (columns are combined one after another, each
-  // a round trip to L2).
-  __device__ __forceinline__ bool heavy(const Job& J) const {
-    const int columns = J.nh * (C::D / 4);
-    return columns > 32 || (long long)columns * job_count(J) > kShareJobLoads;
-  }
-
-  // Sequence-level ticket after a chunk job; true if it completed the sequence.
-  __device__ __forceinline__ bool chunk_done(const Job& J) {
-    int last = 0;
-    if (lane == 0) {
-      int* tk = prm.tickets + (size_t)J.s * prm.n_hg + J.hg;
-      const int t = atomic_add_release_gpu(tk, 1);
-      last = (t == (J.np + kChunk - 1) / kChunk - 1);
-      if (last) {
-        *tk = 0;
-        fence_acq_rel_gpu();
-      }
-    }
-    return __shfl_sync(0xffffffffu, last, 0) != 0;
-  }
-
-  // Run J alone, now (and its follow-up).
-  __device__ __forceinline__ void run_alone(Job J) {
-    while (true) {
-      combine_share<C>(prm, J, 0, 1, lane);
-      if (J.kind == 1) fence_acq_rel_gpu();  // every lane's chunk state, before the ticket
-      __syncwarp();
-      if (J.kind != 1 || !chunk_done(J)) return;
-      J.kind = 2;
-    }
-  }
-
-  __device__ __forceinline__ void push(const Job& J) {
-    if (tail - head >= JQ) {  // queue full (not expected): no waiting, just do it
-      run_alone(J);
-      return;
-    }
-    if (lane == 0) q[tail % JQ] = J;
-    __syncwarp();
-    ++tail;
-  }
-
-  // Start J: post it (heavy; the caller guarantees a free slot) or run it alone.
-  __device__ __forceinline__ void launch(const Job& J) {
-    {
-      if (heavy(J)) {
-        const int slot = nposted % kJobSlots;
-        if (lane == 0) {
-          ch.rec[slot] = J;
-          __threadfence_block();
-          *ch.posted = nposted + 1;
-        }
-        ++nposted;
-        combine_share<C>(prm, J, LY::NC, LY::NC + 1, lane);
-        if (J.kind == 1) fence_acq_rel_gpu();  // every lane's chunk state, before the ticket
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ch.bar_done + 8 * slot);
-        return;
-      }
-      run_alone(J);
-      return;
-    }
-  }
-
-  // Make progress without blocking (block = false) or until idle (block = true,
-  // each wait bounded).  Returns false once the CTA is aborting.
-  __device__ __forceinline__ bool poll(bool block) {
-    while (true) {
-      while (ndone < nposted) {
-        const int slot = ndone % kJobSlots;
-        const uint32_t par = (uint32_t)(ndone / kJobSlots) & 1u;
-        const uint32_t bar = ch.bar_done + 8 * slot;
-        bool done = __all_sync(0xffffffffu, mbar_test_wait(bar, par));
-        if (!done && block)
-          done = __all_sync(0xffffffffu, wait_bounded(bar, par, abort_flag, err, prm.timeout_ns,
-                                                      kSiteJobDone, ndone));
-        if (!done) break;
-        // Every helper's arrival was observed: their stores are ordered
-        // before the release in chunk_done.
-        Job J = broadcast_job(ch.rec[slot]);
-        ++ndone;
-        if (J.kind == 1 && chunk_done(J)) {
-          J.kind = 2;
-          push(J);
-        }
-      }
-      if (block && ndone < nposted) {
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
-        continue;  // the bounded wait above gave up: loop re-checks the flag
-      }
-      while (head != tail && nposted - ndone < kJobSlots) {
-        const Job J = broadcast_job(q[head % JQ]);
-        ++head;
-        launch(J);
-      }
-      if (!block || (ndone == nposted && head == tail)) return __all_sync(0xffffffffu, *abort_flag == 0);
-    }
-  }
-
-  __device__ __forceinline__ bool drain() {
-    while (ndone < nposted || head != tail)
-      if (!poll(true)) return false;
-    return true;
-  }
-};
-
 // Consumer warp: stream the blocks of every unit assigned to it and hand its
 // online-softmax state for each unit to the epilogue warp through shared
 // memory.  Consumer warps never wait for each other.
 template <class C, class LY, bool MQ>
-__device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem, const int* pref,
-                                              const UnitInfo* info, volatile int* abort_flag,
-                                              const volatile uint32_t* issued, const JobChannel& ch,
-                                              int warp, int lane) {
+__device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem, const UnitInfo* info,
+                                              volatile int* abort_flag, const volatile uint32_t* issued, int warp,
+                                              int lane) {
   using T = typename C::T;
   constexpr int D = C::D, BS = C::BS, GT = C::GT, NC = LY::NC, NCT = LY::NCT, NS = LY::NSTAGE,
                 UQ = LY::UQ;
@@ -782,11 +494,15 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
   // Unused partitions: sentinels (m = -inf, l = 0).  Empty sequences: zeros
   // (a multi-query sequence is never empty: it holds its new tokens).
   {
+    auto parts_of = [&](int s) {
+      bool bad = false;  // flagged by the prologue already
+      return (seq_tokens<MQ>(prm, s, prm.MB * C::BS, &bad) + prm.P - 1) / prm.P;
+    };
     const long long n1 = (long long)S * H * Pmax;
     for (long long i = (long long)blockIdx.x * NCT + ctid; i < n1; i += (long long)gridDim.x * NCT) {
       const int s = (int)(i / ((long long)H * Pmax));
       const int p = (int)(i % Pmax);
-      if (p >= pref[s + 1] - pref[s]) {
+      if (p >= parts_of(s)) {
         prm.ws_m[i] = -INFINITY;
         prm.ws_l[i] = 0.f;
       }
@@ -796,18 +512,17 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
       const long long n2 = (long long)S * H * D16;
       for (long long i = (long long)blockIdx.x * NCT + ctid; i < n2; i += (long long)gridDim.x * NCT) {
         const int s = (int)(i / ((long long)H * D16));
-        if (pref[s + 1] == pref[s]) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
+        if (parts_of(s) == 0) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
       }
       if (prm.lse) {  // no scores: the log-sum-exp is log 0
         for (int i = blockIdx.x * NCT + ctid; i < S * H; i += gridDim.x * NCT)
-          if (pref[i / H + 1] == pref[i / H]) prm.lse[i] = -INFINITY;
+          if (parts_of(i / H) == 0) prm.lse[i] = -INFINITY;
       }
     }
   }
 
   C cons;
   uint32_t g = 0, k = 0;
-  int seen = 0;  // combine jobs helped with
   while (true) {
     const int slot = k % UQ;
     const uint32_t par = (k / UQ) & 1u;
@@ -818,23 +533,11 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     if (I.s < 0) {
       // End of work: pass the end marker on to the epilogue warp, once it has
       // taken the previous hand-over (the k-th hand-over waits for the
-      // (k-1)-th to be consumed), then help with combine jobs until the
-      // epilogue warp has run its last one.
-      if (!wait_handover<C, LY>(prm, ch, seen, bar_eempty, k, abort_flag, err, kSiteHandEnd, warp, lane))
-        break;
+      // (k-1)-th to be consumed).
+      if (!wait_handover(prm, bar_eempty, k, abort_flag, err, kSiteHandEnd, lane)) break;
       if (warp == 0 && lane == 0) epi_info->s = -1;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_efull);
-      const uint64_t t0 = global_timer_ns();
-      while (true) {
-        help_with_job<C, LY>(prm, ch, seen, warp, lane);
-        if (__any_sync(0xffffffffu, *ch.finished != 0 || *abort_flag != 0)) break;
-        if ((long long)(global_timer_ns() - t0) > prm.timeout_ns) {
-          if (lane == 0) record_timeout(abort_flag, err, kSiteServe, seen);
-          break;
-        }
-        __nanosleep(64);
-      }
       break;
     }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
@@ -845,19 +548,18 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_uempty + 8 * slot);
 
-    // Work item i of unit u goes to warp (i + u) % NC: when a unit's item
-    // count is not a multiple of NC, the extra items fall on different warps
-    // from unit to unit instead of on warps 0, 1, ... every time.  The
-    // grouping depends only on the unit, never on which CTA runs it.  An item
-    // is one block, or for the tensor-core consumer over 8-token blocks two
+    // Work item i of unit (p, hg) goes to warp (i + p * n_hg + hg) % NC: when
+    // a unit's item count is not a multiple of NC, the extra items fall on
+    // different warps from unit to unit instead of on warps 0, 1, ... every
+    // time.  The grouping depends only on the partition and head group, never
+    // on which CTA runs the unit or on the other sequences of the batch, so a
+    // sequence's output is bitwise the same in any batch.  An item is one
+    // block, or for the tensor-core consumer over 8-token blocks two
     // consecutive blocks (one 16-token tile of the products).
     constexpr int PB = (C::kMma && BS == 8 && !C::kFp8) ? 2 : 1;
-    const int u_id = (pref[I.s] + I.p) * prm.n_hg + I.hg;
+    const int u_id = I.p * prm.n_hg + I.hg;
     const int nitem = (I.nb + PB - 1) / PB;
     for (int it = (warp + NC - u_id % NC) % NC; it < nitem; it += NC) {
-      if constexpr (C::kMma && kMmaHelpPerBlock) {
-        if (__shfl_sync(0xffffffffu, *ch.posted, 0) > seen) help_with_job<C, LY>(prm, ch, seen, warp, lane);
-      }
       const int j = it * PB, nbi = min(PB, I.nb - j);
       const uint32_t gj = g + j, st = stage_of<LY>(gj);
       bool okb = wait_issued(issued, gj + nbi, abort_flag, err, prm.timeout_ns);
@@ -873,12 +575,12 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
       if constexpr (PB == 2) {
         if (nbi == 2) {
           uint8_t* sb = smem + stage_of<LY>(gj + 1) * LY::STAGE;
-          cons.block_pair(sa, sa + LY::KBYTES, sb, sb + LY::KBYTES, ntok, lane, I.t0 + j * BS);
+          cons.block_pair(sa, sa + LY::VOFF, sb, sb + LY::VOFF, ntok, lane, I.t0 + j * BS);
         } else {
-          cons.block(sa, sa + LY::KBYTES, ntok, lane, scr, I.t0 + j * BS);
+          cons.block(sa, sa + LY::VOFF, ntok, lane, scr, I.t0 + j * BS);
         }
       } else {
-        cons.block(sa, sa + LY::KBYTES, ntok, lane, scr, I.t0 + j * BS);
+        cons.block(sa, sa + LY::VOFF, ntok, lane, scr, I.t0 + j * BS);
       }
       // The stage is refilled by a bulk copy (async proxy) once released:
       // every lane's reads of it (generic proxy) are ordered before that
@@ -893,9 +595,8 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     g += I.nb;
 
     // Hand this warp's state for unit k to the epilogue warp, once it has
-    // taken unit k-1's (helping with combine jobs meanwhile).
-    if (!wait_handover<C, LY>(prm, ch, seen, bar_eempty, k, abort_flag, err, kSiteHandover, warp, lane))
-      break;
+    // taken unit k-1's.
+    if (!wait_handover(prm, bar_eempty, k, abort_flag, err, kSiteHandover, lane)) break;
     ++k;
     cons.finish(epi_acc + warp * GT * D, epi_ml + warp * GT * 2, lane);
     if (warp == 0 && lane == 0) *epi_info = I;
@@ -905,12 +606,11 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
 }
 
 // Epilogue warp: for every unit, merge the consumer warps' states into the
-// partition's (m_p, l_p, o_p) (or the output, for a single-partition
-// sequence), take the completion ticket (checked one unit later, off the
-// critical path) and run the combine jobs that fall to this CTA.
+// partition's (m_p, l_p, o_p) in the workspace, or, for a sequence with one
+// partition, into the output and its log-sum-exp (single pass).
 template <class C, class LY>
 __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem, volatile int* abort_flag,
-                                              const JobChannel& ch, int lane) {
+                                              int lane) {
   using T = typename C::T;
   constexpr int D = C::D, GT = C::GT, NC = LY::NC, NS = LY::NSTAGE, UQ = LY::UQ;
   const uint32_t sbase = smem_addr(smem);
@@ -923,38 +623,13 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
   int* err = prm.hdr + kHdrError;
   const int H = prm.H, Pmax = prm.Pmax;
   T* out = static_cast<T*>(prm.out);
-  JobEngine<C, LY> jobs(prm, ch, reinterpret_cast<Job*>(smem + LY::OFF_JOBQ), abort_flag, err, lane);
-
-  // Lane 0 only: a ticket taken and not yet checked, and its job.
-  bool pend = false;
-  int pend_t = 0;
-  Job pinfo{};
-  // Lane 0: if the pending ticket was the last of its group, its job (the
-  // acquire fence orders the other CTAs' partition states before it).
-  auto settle = [&]() -> int {
-    int go = 0;
-    if (lane == 0 && pend && pend_t == pinfo.cnt - 1) {
-      go = 1;
-      *ticket_of(prm, pinfo) = 0;
-      fence_acq_rel_gpu();
-    }
-    pend = false;
-    return __shfl_sync(0xffffffffu, go, 0);
-  };
 
   for (uint32_t k = 0;; ++k) {
-    // Wait for hand-over k, advancing combine jobs meanwhile.
+    // Wait (bounded) for hand-over k.
     bool ok = __all_sync(0xffffffffu, mbar_test_wait(bar_efull, k & 1u));
     if (!ok) {
-      // Idle: settle the pending ticket now rather than at the next merge
-      // (its atomic has long returned), so a job it completes starts early.
-      if (kSettleWhenIdle) {
-        const Job R = broadcast_job(pinfo);
-        if (settle()) jobs.push(R);
-      }
       const uint64_t t0 = global_timer_ns();
       while (!ok) {
-        if (!jobs.poll(false)) return;
         ok = __all_sync(0xffffffffu, mbar_test_wait(bar_efull, k & 1u));
         if (ok) break;
         if (__any_sync(0xffffffffu, *abort_flag != 0)) return;
@@ -966,15 +641,7 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
       }
     }
     const UnitInfo I = *epi_info;
-    if (I.s < 0) {
-      // End of work: settle the last ticket, finish every job (the consumer
-      // warps are waiting to help), then release them.
-      const Job R = broadcast_job(pinfo);  // pinfo is kept by lane 0 only
-      if (settle()) jobs.push(R);
-      jobs.drain();
-      if (lane == 0) *ch.finished = 1;
-      return;
-    }
+    if (I.s < 0) return;  // end of work
     // Per head: M = max over warps, each warp's weight 2^(m_w - M), and the sum l.
     for (int i = lane; i < GT; i += 32) {
       float M = -INFINITY;
@@ -1025,25 +692,6 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_eempty);  // the hand-over slot may be refilled
-
-    // Settle the previous ticket; take this unit's (release: the warp's
-    // partition stores above, ordered by __syncwarp, become visible first).
-    const Job R = broadcast_job(pinfo);
-    const int go = settle();
-    if (lane == 0) {
-      pend = !single;
-      if (pend) {
-        pinfo.s = I.s; pinfo.hg = I.hg; pinfo.h0 = I.h0; pinfo.nh = I.nh; pinfo.np = I.np;
-        if (I.np <= kChunk) {
-          pinfo.kind = 0; pinfo.c = 0; pinfo.cnt = I.np;
-        } else {
-          pinfo.kind = 1; pinfo.c = I.p / kChunk; pinfo.cnt = min(kChunk, I.np - pinfo.c * kChunk);
-        }
-        pend_t = atomic_add_release_gpu(ticket_of(prm, pinfo), 1);
-      }
-    }
-    if (go) jobs.push(R);
-    if (!jobs.poll(false)) return;
   }
 }
 
@@ -1057,12 +705,8 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
   const uint32_t sbase = smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS);
   volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(smem + LY::OFF_FLAGS + 8);
-  JobChannel ch;
-  ch.posted = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 4);
-  ch.finished = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS + 12);
-  ch.rec = reinterpret_cast<Job*>(smem + LY::OFF_JOBREC);
-  ch.bar_done = sbase + LY::OFF_BAR + 8 * (2 * NS + 2 * UQ + 2);
   int* pref = reinterpret_cast<int*>(smem + LY::OFF_PREF);
+  uint16_t* perm = reinterpret_cast<uint16_t*>(smem + LY::perm_off(prm.S));
   int* scan = reinterpret_cast<int*>(smem + LY::OFF_SCAN);
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + LY::OFF_INFO);
 
@@ -1078,53 +722,112 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     }
     mbar_init(bar + 8 * (2 * NS + 2 * UQ), NC);     // hand-over full: every consumer warp
     mbar_init(bar + 8 * (2 * NS + 2 * UQ + 1), 1);  // hand-over empty: the epilogue warp
-    for (int i = 0; i < kJobSlots; ++i)
-      mbar_init(bar + 8 * (2 * NS + 2 * UQ + 2 + i), NC + 1);  // shared combine job done: all helpers
     *abort_flag = 0;
     *issued = 0;
-    *ch.posted = 0;
-    *ch.finished = 0;
     fence_mbarrier_init();
   }
-  // pref[s] = number of used partitions before sequence s (lengths clamped to
-  // [0, MB*BS]; an out-of-range length is recorded as a device error).
+  // Longest-first order.  Every CTA computes the same order from the lengths:
+  // perm[r] = the sequence of rank r, sequences sorted by partition count,
+  // most first (counts of 127 or more as equals), ties in batch order (a
+  // stable counting sort); pref[r] = partitions of ranks before r.  Lengths
+  // are clamped to [0, MB*BS]; an out-of-range length is recorded as a device
+  // error.  Temporaries live in the ring, unused until the producer starts.
   {
+    constexpr int NW = LY::THREADS / 32;
+    constexpr int NBK = 128;  // sort buckets
+    static_assert(LY::THREADS % 32 == 0 && NW <= 32, "whole warps, at most 32");
+    static_assert(LY::RING >= (NBK + kMaxSeqsPerLaunch) * 4, "sort temporaries fit in the ring");
     const int S = prm.S, nthr = LY::THREADS, max_len = prm.MB * C::BS;
-    const int per = (S + nthr - 1) / nthr;
-    const int beg = min(tid * per, S), end = min(beg + per, S);
-    int sum = 0;
-    for (int s = beg; s < end; ++s) {
+    int* bucket = reinterpret_cast<int*>(smem);       // [NBK] counts, then next free rank
+    int* parts = reinterpret_cast<int*>(smem) + NBK;  // [S] partitions per sequence
+    for (int i = tid; i < NBK; i += nthr) bucket[i] = 0;
+    __syncthreads();
+    for (int s = tid; s < S; s += nthr) {
       bool bad = false;
       const int L = seq_tokens<MQ>(prm, s, max_len, &bad);
       if (bad) atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
-      sum += (L + prm.P - 1) / prm.P;
+      const int np = (L + prm.P - 1) / prm.P;
+      parts[s] = np;
+      atomicAdd(&bucket[NBK - 1 - min(np, NBK - 1)], 1);
     }
-    scan[tid] = sum;
     __syncthreads();
-    if (tid == 0) {
-      int run = 0;
-      for (int i = 0; i < nthr; ++i) {
-        const int v = scan[i];
-        scan[i] = run;
-        run += v;
+    if (warp == 0) {
+      constexpr int PER = NBK / 32;  // buckets per lane: exclusive scan of the counts
+      int v[PER], tot = 0;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        v[j] = bucket[lane * PER + j];
+        tot += v[j];
       }
-      pref[S] = run;
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      int start = incl - tot;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        bucket[lane * PER + j] = start;
+        start += v[j];
+      }
+      __syncwarp();
+      // 32 sequences at a time, in batch order: lanes with the same bucket
+      // take consecutive ranks in lane order.
+      for (int c0 = 0; c0 < S; c0 += 32) {
+        const int s = c0 + lane;
+        const int key = s < S ? NBK - 1 - min(parts[s], NBK - 1) : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const int before = __popc(peers & ((1u << lane) - 1u));
+        const int base = s < S ? bucket[key] : 0;
+        __syncwarp();
+        if (s < S) {
+          perm[base + before] = (uint16_t)s;
+          if (before == 0) bucket[key] = base + __popc(peers);
+        }
+        __syncwarp();
+      }
     }
     __syncthreads();
-    int run = scan[tid];
-    for (int s = beg; s < end; ++s) {
-      pref[s] = run;
-      bool bad = false;
-      run += (seq_tokens<MQ>(prm, s, max_len, &bad) + prm.P - 1) / prm.P;
+    // pref over ranks: thread t sums a contiguous range of ranks; an exclusive
+    // scan of those sums (within each warp, then over the warp totals).
+    const int per = (S + nthr - 1) / nthr;
+    const int beg = min(tid * per, S), end = min(beg + per, S);
+    int sum = 0;
+    for (int r = beg; r < end; ++r) sum += parts[perm[r]];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int t = lane < NW ? scan[lane] : 0;
+      int ti = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, ti, o);
+        if (lane >= o) ti += n;
+      }
+      if (lane < NW) scan[NW + lane] = ti - t;  // warp starts
+      if (lane == NW - 1) pref[S] = ti;
+    }
+    __syncthreads();
+    int run = scan[NW + warp] + incl - sum;
+    for (int r = beg; r < end; ++r) {
+      pref[r] = run;
+      run += parts[perm[r]];
     }
   }
   __syncthreads();
   if (warp == NC) {
-    producer_loop<C, LY, MQ>(prm, smem, pref, info, abort_flag, issued, lane);
+    producer_loop<C, LY, MQ>(prm, smem, pref, perm, info, abort_flag, issued, lane);
   } else if (warp == NC + 1) {
-    epilogue_loop<C, LY>(prm, smem, abort_flag, ch, lane);
+    epilogue_loop<C, LY>(prm, smem, abort_flag, lane);
   } else {
-    consumer_loop<C, LY, MQ>(prm, smem, pref, info, abort_flag, issued, ch, warp, lane);
+    consumer_loop<C, LY, MQ>(prm, smem, info, abort_flag, issued, warp, lane);
   }
 }
 

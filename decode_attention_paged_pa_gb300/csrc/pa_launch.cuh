@@ -1,6 +1,8 @@
 // pa_launch.cuh -- shared-memory sizing and launch of one kernel instance.
 #pragma once
 
+#include <atomic>
+
 #include "pa_launch.h"
 
 namespace pa {
@@ -37,16 +39,20 @@ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 // Ring depth: as many K+V stages as fit next to the fixed regions and the
-// largest per-launch prefix array.
+// largest per-launch order and prefix arrays.  Each stage beyond the first
+// adds its bytes and two 8-byte mbarriers (both multiples of 16, so no
+// alignment in the layout moves).
 template <class C, int NC>
 struct Sizing {
   using L1 = Layout<C, NC, 1>;
-  static constexpr uint32_t other = L1::FIXED - L1::RING + 128 * 8 + 16;
-  static constexpr uint32_t pref_max = al16((kMaxSeqsPerLaunch + 1) * 4);
-  static constexpr int NS = cmin(64, (int)((kSmemBudget - other - pref_max) / L1::STAGE));
+  static_assert(L1::STAGE % 16 == 0, "stages are whole 16-byte units");
+  static constexpr uint32_t base = L1::bytes(kMaxSeqsPerLaunch);
+  static_assert(base <= kSmemBudget, "shared memory over budget");
+  static constexpr int NS = cmin(64, 1 + (int)((kSmemBudget - base) / (L1::STAGE + 16)));
   static_assert(NS >= 2, "shared memory holds fewer than two ring stages");
   using LY = Layout<C, NC, NS>;
   static_assert(LY::bytes(kMaxSeqsPerLaunch) <= kSmemBudget, "shared memory over budget");
+  static_assert(NS == 64 || Layout<C, NC, NS + 1>::bytes(kMaxSeqsPerLaunch) > kSmemBudget, "ring as deep as fits");
 };
 
 template <class C, int NC>
@@ -61,9 +67,18 @@ cudaError_t launch_one(const KParams& prm, int max_ctas, cudaStream_t stream) {
   } else {
     if (prm.q_len > 1) return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)LY::bytes(kMaxSeqsPerLaunch));
+  // The shared-memory opt-in is set once per kernel instance and device.
+  static std::atomic<uint64_t> opted_in[2] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const int mq = prm.q_len > 1 ? 1 : 0;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (!bit || !(opted_in[mq].load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes(kMaxSeqsPerLaunch));
+    if (e != cudaSuccess) return e;
+    opted_in[mq].fetch_or(bit, std::memory_order_acq_rel);
+  }
   int grid = device_sm_count() * kCtasPerSm;
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (grid < 1) grid = 1;

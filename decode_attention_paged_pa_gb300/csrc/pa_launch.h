@@ -4,21 +4,10 @@
 
 #include <cuda_runtime.h>
 
+#include "pa_combine.cuh"
 #include "pa_kernel.cuh"
 
 namespace pa {
-
-// Sequences per launch: the kernel keeps a prefix sum of partitions per
-// sequence in shared memory; longer batches are split into several launches.
-#ifndef PA_MAX_SEQS_PER_LAUNCH
-#define PA_MAX_SEQS_PER_LAUNCH 1024
-#endif
-constexpr int kMaxSeqsPerLaunch = PA_MAX_SEQS_PER_LAUNCH;
-
-// Partitions per combine chunk: sequences with more partitions are combined
-// in two levels (chunks of partitions, then the chunk states).
-constexpr int kChunkParts = 16;
-static_assert(kChunkParts == kChunk, "launcher and kernel must agree on the chunk size");
 
 // Query heads per work unit of each kernel family (the tensor-core family
 // takes 16, two column tiles, where a kv head has more than 8 query rows).
@@ -49,6 +38,10 @@ cudaError_t launch_mma_b64_bf16(const KParams& prm, int D, int max_ctas, cudaStr
 // The same over an fp8 (E4M3) KV cache, queries and output fp16 / bf16.
 cudaError_t launch_mma8_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma8_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+
+// Phase 2: the cross-partition combine of every multi-partition row, launched
+// as a programmatic dependent of the phase-1 launch before it on `st`.
+cudaError_t launch_combine(const CParams& prm, int elem_bytes, bool bf16, int D, cudaStream_t st);
 
 // SM count of the current device (cached per device).
 int device_sm_count();

@@ -17,6 +17,18 @@
 // Softmax arithmetic is that of the phase-1 kernel `_paged_attn_v2_partition_kernel`
 // (scores in fp32, running max, exp, running sum, rescaled accumulation); the
 // weights enter the second product rounded to the element type.
+//
+// Staging.  A ring stage holds one physical block of one kv head: the key
+// block [D/8][BS][8] by a 1-D bulk copy (it is contiguous), and, with 16-bit
+// caches in blocks of 16 tokens or more (kTma), the value block [D][BS] by a
+// 3-D tensor copy (the value cache viewed as [blocks * kv heads][D][BS]) that
+// stores its rows of R = 2 BS bytes in the R-byte swizzle: the 16-byte chunk
+// index of a row (address bits 4..) is XORed with address bits 7.. .  Without
+// it, the rows an ldmatrix reads (8 consecutive dims, one 16-byte chunk each)
+// are R bytes apart and fall in 8 R / 128 distinct bank groups only (a 2-, 4-
+// or 8-way conflict for R = 32, 64, 128); with it they fall in 8 (checked on
+// the CPU for every head size).  fp8 caches and 8-token blocks are staged by
+// 1-D bulk copies of the contiguous value block.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -25,12 +37,9 @@
 
 #include "pa_common.cuh"
 
-// Pieces a 32-token value block is staged in (see MmaConsumer::kVPieces).
-#ifndef PA_V_PIECES32
-#define PA_V_PIECES32 2
-#endif
-
 namespace pa {
+
+constexpr uint32_t al1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 
 // FP8_: the caches hold E4M3 codes (one byte per element, key layout
 // [D/16][BS][16]).  Every E4M3 value is exact in fp16, so both products then
@@ -51,11 +60,19 @@ struct MmaConsumer {
   using T = T_;
   using MT = typename std::conditional<FP8_, __half, T_>::type;  // operand type of the products
   static constexpr int NT = NT_;  // 8-head column tiles per unit
+  // kTma: the value block is staged by a swizzled tensor copy.
+  static constexpr bool kTma = !FP8_ && BS_ >= 16;
   static constexpr int D = D_, BS = BS_, GT = 8 * NT_;
   static_assert(NT_ == 1 || (NT_ == 2 && !FP8_), "one or two column tiles (one over fp8 caches)");
   static constexpr bool kMma = true;
   static constexpr bool kFp8 = FP8_;
   static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
+  // A stage: the key block, then (at KREGION, 1024-byte aligned for the
+  // swizzled tensor copy) the value block; STAGE_TX bytes land per stage.
+  static constexpr uint32_t KTILE = (uint32_t)D_ * BS * KV_ESZ;
+  static constexpr uint32_t KREGION = kTma ? al1024(KTILE) : KTILE;
+  static constexpr uint32_t STAGE_BYTES = kTma ? al1024(KREGION + KTILE) : KREGION + KTILE;
+  static constexpr uint32_t STAGE_TX = 2 * KTILE;
   // Blocks the producer warp issues together (one per lane): copies of 2 KB
   // or less need more of them in flight than the 4 KB ones.
   static constexpr int kIssueBatch = (KV_ESZ * D * BS <= 2048) ? 32 : 8;
@@ -69,45 +86,16 @@ struct MmaConsumer {
   static constexpr int SCRATCH_FLOATS = 0;
   static constexpr bool kSplitWeights = std::is_same<MT, __nv_bfloat16>::value;
 
-  // Value blocks of 32 tokens.  A dim's row of the page's V layout is then
-  // 64 bytes, so dims d and d + 2 share shared-memory banks, and an ldmatrix
-  // row group of 8 consecutive dims is a 4-way bank conflict.  The block is
-  // staged instead as kVPieces pieces of D / kVPieces dims (one bulk copy
-  // each), piece p placed 16 p bytes past its contiguous position, and the 8
-  // rows of every value fragment matrix take 8 / kVPieces dims from each
-  // piece: 2 pieces leave a 2-way conflict, 4 pieces none.  Every piece is a
-  // copy of its own, and on the long-context batch (32-token blocks, head
-  // size 128) 2 pieces ran fastest: 135 us a call, against 141 us with 4
-  // and 144 us contiguous.  vdim() gives the dim a value-tile row holds: a
-  // fixed permutation of the dims, rotated by kVRot per piece so that
-  // finish()'s stores of the accumulator rows stay spread over the banks
-  // (rotations checked on the CPU for head sizes 64 to 256).  Other block
-  // sizes and fp8 caches stage contiguously.
-  static constexpr int kVPieces = (!FP8_ && BS_ == 32) ? PA_V_PIECES32 : 1;
-  static_assert(kVPieces == 1 || kVPieces == 2 || kVPieces == 4, "1, 2 or 4 value pieces");
-  static constexpr int kVRot = kVPieces == 4 ? 10 : kVPieces == 2 ? 4 : 0;
-  static constexpr int kVDims = D_ / kVPieces;  // dims per piece
-  static constexpr uint32_t kVPieceBytes = (uint32_t)kVDims * BS_ * KV_ESZ;
-  static constexpr uint32_t kVPad = 16u * (kVPieces - 1);  // stage bytes past the contiguous block
-  static_assert(kVPieceBytes % 16 == 0, "pieces are whole 16-byte bulk-copy units");
-
-  // Dim held by row i (0..15) of value tile mt.
-  __device__ __forceinline__ static int vdim(int mt, int i) {
-    if constexpr (kVPieces == 1) {
-      return mt * 16 + i;
+  // Byte offset, in a staged value block, of the 16-byte chunk c (tokens
+  // 8c .. 8c + 7) of dim d's row.  Tensor-copied blocks have rows of
+  // VROW = 2 BS bytes in the VROW-byte swizzle: the chunk index is XORed
+  // with the row's address bits 7 and up (VROW / 16 - 1 of them matter).
+  static constexpr uint32_t VROW = (uint32_t)BS_ * KV_ESZ;
+  __device__ __forceinline__ static uint32_t vchunk(int d, int c) {
+    if constexpr (kTma) {
+      return (uint32_t)d * VROW + ((uint32_t)(c ^ (((uint32_t)d * VROW >> 7) & (VROW / 16u - 1u))) << 4);
     } else {
-      constexpr int R = 8 / kVPieces;  // rows of a fragment matrix per piece
-      const int h = i >> 3, ri = i & 7, p = ri / R;
-      return p * kVDims + (mt * 2 * R + h * R + ri % R + kVRot * p) % kVDims;
-    }
-  }
-  // Byte offset of dim d's row in a staged value block.
-  __device__ __forceinline__ static uint32_t vrow(int d) {
-    if constexpr (kVPieces == 1) {
-      return (uint32_t)d * BS_ * KV_ESZ;
-    } else {
-      const int p = d / kVDims;
-      return (uint32_t)p * (kVPieceBytes + 16u) + (uint32_t)(d - p * kVDims) * BS_ * KV_ESZ;
+      return (uint32_t)d * VROW + (uint32_t)c * 16u;
     }
   }
 
@@ -317,7 +305,7 @@ struct MmaConsumer {
     if (nz < BS) {
       for (int i = lane; i < D * (BS - nz); i += 32) {
         const int d = i / (BS - nz), t = nz + i % (BS - nz);
-        *reinterpret_cast<uint16_t*>(vz + vrow(d) + 2 * t) = 0;
+        *reinterpret_cast<uint16_t*>(vz + vchunk(d, t >> 3) + 2 * (t & 7)) = 0;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -348,7 +336,7 @@ struct MmaConsumer {
       for (int mt = 0; mt < NMT; ++mt) {
         uint32_t a[4];
         const int chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
-        ldmatrix_x4(vcol + vrow(vdim(mt, lane & 15)) + chunk * 16, a);
+        ldmatrix_x4(vcol + vchunk(mt * 16 + (lane & 15), chunk), a);
         if (BS < 16 && !has_b) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -473,9 +461,9 @@ struct MmaConsumer {
     for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        // Accumulator rows r and r + 8 of value tile mt hold dims vdim(mt, r), vdim(mt, r + 8).
+        // Accumulator rows r and r + 8 of value tile mt hold dims mt * 16 + r and + 8.
         float* o = acc_out + (8 * t + hq) * D;
-        const int d_lo = vdim(mt, r), d_hi = vdim(mt, r + 8);
+        const int d_lo = mt * 16 + r, d_hi = d_lo + 8;
         o[d_lo] = acc[mt][t][0];
         o[D + d_lo] = acc[mt][t][1];
         o[d_hi] = acc[mt][t][2];

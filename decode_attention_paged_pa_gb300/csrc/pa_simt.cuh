@@ -23,9 +23,10 @@ struct SimtConsumer {
   static constexpr int kIssueBatch = 8;  // blocks the producer warp issues together
   static constexpr bool kFp8 = false;
   static constexpr int KV_ESZ = (int)sizeof(T_);  // bytes per cached element
-  // A value block is staged contiguously: one piece, no padding.
-  static constexpr int kVPieces = 1;
-  static constexpr uint32_t kVPieceBytes = (uint32_t)D_ * BS_ * sizeof(T_), kVPad = 0;
+  // A ring stage holds one whole block, key then value, each one bulk copy.
+  static constexpr bool kTma = false;
+  static constexpr uint32_t KTILE = (uint32_t)D_ * BS_ * sizeof(T_);
+  static constexpr uint32_t KREGION = KTILE, STAGE_BYTES = 2 * KTILE, STAGE_TX = 2 * KTILE;
   static constexpr int EPC = elems_per_chunk<T_>();  // elements per 16-byte chunk
   // q.k: each lane takes QKD dims of one token; LPT lanes share a token
   // (32 dims for fp32, whose registers hold half as many per byte; half the

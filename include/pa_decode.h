@@ -22,9 +22,13 @@
  *
  * computed in partitions of `partition_size` tokens: partition p holds tokens
  * [p*P, min((p+1)*P, L)) and yields (m_p, l_p, o_p) = (max z, sum e^(z - m_p),
- * normalised weighted V); the partitions are then combined with
- * M = max m_p, w_p = e^(m_p - M) l_p / sum_q e^(m_q - M) l_q, out = sum w_p o_p.
- * A sequence that fits in one partition is written directly (single pass).
+ * normalised weighted V) -- phase 1, one persistent kernel; the partitions
+ * are then combined with M = max m_p, w_p = e^(m_p - M) l_p / sum_q e^(m_q - M)
+ * l_q, out = sum w_p o_p -- phase 2, a second kernel launched as a
+ * programmatic dependent of the first (it starts while the first finishes and
+ * waits for its results).  A sequence that fits in one partition is written
+ * directly by phase 1 (single pass); a call in which no sequence can have two
+ * partitions launches phase 1 only.
  * L = 0 yields zeros (the "flash_attention.metal" page's forward kernel takes
  * 1/l as 0 when l = 0).
  *
@@ -77,14 +81,12 @@ enum {
 };
 
 /*
- * Bytes of device workspace pa_decode_v2 needs for these sizes: a small
- * header (error word, work counter), completion tickets per (sequence, head
- * group) and per chunk of 16 partitions, the phase-1 partition states of the
- * page's launcher -- max_logits [S, H, Pmax] f32, exp_sums [S, H, Pmax] f32
- * and tmp_output [S, H, Pmax, head_size] f32, with
- * Pmax = ceil(max_blocks_per_seq * block_size / partition_size) -- and the
- * same three arrays for the combined state of each chunk of 16 partitions
- * (used by sequences with more than 16 partitions).
+ * Bytes of device workspace pa_decode_v2 needs for these sizes: a 256-byte
+ * header (error word, work counter, where a bounded wait gave up) and the
+ * phase-1 partition states of the page's launcher -- max_logits
+ * [S, H, Pmax] f32, exp_sums [S, H, Pmax] f32 and tmp_output
+ * [S, H, Pmax, head_size] f32, with
+ * Pmax = ceil(max_blocks_per_seq * block_size / partition_size).
  * Returns 0 for invalid sizes.
  */
 size_t pa_decode_v2_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_size,

@@ -41,17 +41,11 @@ def _align(x):
 ])
 def test_workspace_bytes_and_layout(S, H, KH, D, MB, BS, P):
     pmax = -(-(MB * BS) // P)
-    cmax = -(-pmax // 16)
     hdr = 256
-    tickets = hdr
-    ctickets = _align(tickets + S * H * 4)
-    m = _align(ctickets + S * H * cmax * 4)
+    m = hdr
     l = _align(m + S * H * pmax * 4)
     o = _align(l + S * H * pmax * 4)
-    cm = _align(o + S * H * pmax * D * 4)
-    cl = _align(cm + S * H * cmax * 4)
-    co = _align(cl + S * H * cmax * 4)
-    total = _align(co + S * H * cmax * D * 4)
+    total = _align(o + S * H * pmax * D * 4)
     assert binding.workspace_bytes(S, H, KH, D, MB, BS, P) == total
     offs, pm = binding.workspace_layout(S, H, KH, D, MB, BS, P)
     assert offs == (m, l, o, 0, total) and pm == pmax
@@ -126,11 +120,14 @@ def test_mq_entry_rejects_bad_q_len():
 
 
 def test_binding_launch_count_matches_kernel_limit():
-    text = open(os.path.join(ROOT, "decode_attention_paged_pa_gb300", "csrc", "pa_launch.h")).read()
+    text = open(os.path.join(ROOT, "decode_attention_paged_pa_gb300", "csrc", "pa_kernel.cuh")).read()
     limit = int(re.search(r"#define PA_MAX_SEQS_PER_LAUNCH (\d+)", text).group(1))
     assert binding.MAX_ROWS_PER_LAUNCH == limit
-    assert binding.launches_per_call(limit) == 1 and binding.launches_per_call(limit + 1) == 2
-    assert binding.launches_per_call(300, 4) == 1   # multi-query rows share their sequence's launch
+    # phase 1 per `limit` sequences, plus the phase-2 combine
+    assert binding.launches_per_call(limit) == 2 and binding.launches_per_call(limit + 1) == 3
+    assert binding.launches_per_call(300, 4) == 2   # multi-query rows share their sequence's launch
+    # no phase 2 when no sequence can have two partitions
+    assert binding.launches_per_call(300, 1, max_partitions=1) == 1
 
 
 def test_fp8_entry_rejects_bad_scales():

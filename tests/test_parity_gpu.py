@@ -147,6 +147,23 @@ def test_deterministic_across_runs_and_grid_sizes(variant):
         assert torch.equal(out, base), f"max_ctas={ctas}"
 
 
+@pytest.mark.parametrize("variant,BS", [(SIMT, 16), (MMA, 16), (MMA, 32)])
+def test_sequence_output_independent_of_batch(variant, BS):
+    """Units run longest sequence first and each unit's work is split over the
+    warps by its partition and head group only, so a sequence's output does
+    not depend on the rest of the batch: each sequence decoded alone, and the
+    batch in reverse order, give the batch's rows bit for bit."""
+    lens = [700, 1, 3000, 513, 90, 2048, 0, 1500]
+    q, kc, vc, bt, L = random_case(31, S=8, H=16, KH=4, D=128, BS=BS, lens=lens)
+    base, _ = run_gpu(q, kc, vc, bt, L, 0.08, 256, variant)
+    for s in range(len(lens)):
+        one, _ = run_gpu(q[s:s + 1], kc, vc, bt[s:s + 1], L[s:s + 1], 0.08, 256, variant)
+        assert torch.equal(one[0], base[s]), f"sequence {s} alone"
+    rev = torch.arange(len(lens) - 1, -1, -1)
+    r, _ = run_gpu(q[rev].contiguous(), kc, vc, bt[rev].contiguous(), L[rev].contiguous(), 0.08, 256, variant)
+    assert torch.equal(r, base[rev])
+
+
 @pytest.mark.parametrize("variant,KH,G,BS", [(SIMT, 16, 1, 16), (MMA, 16, 1, 16), (MMA, 8, 4, 32),
                                               (SIMT, 8, 1, 32)])
 def test_repeatable_under_load(variant, KH, G, BS):

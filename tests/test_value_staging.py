@@ -1,18 +1,18 @@
-"""CPU checks of how the tensor-core consumer stages a 32-token value block in
-shared memory (no GPU, no attention arithmetic).
+"""CPU checks of how the tensor-core consumer addresses a staged value block
+(no GPU, no attention arithmetic).
 
-The page's value layout [D][BS] gives each dim a row of BS tokens; at 32
-tokens a row is 64 bytes, so an ldmatrix row group of 8 consecutive dims falls
-in 2 of the 8 sixteen-byte bank groups (a 4-way conflict).  The kernel copies
-the block in kVPieces pieces of D / kVPieces dims, piece p placed 16 p bytes
-past its contiguous place, and builds each fragment matrix from 8 / kVPieces
-dims of every piece, rotated by kVRot dims per piece.  These tests restate
-that placement rule and check, for every head size the kernel takes, that the
-tile rows cover each dim once, that every piece stays inside its stage on
-16-byte boundaries, how many ways the fragment loads conflict, and that the
-accumulator hand-over stores are spread no worse than with contiguous rows.
-The piece count and rotations are read from the CUDA source, so a change there
-is checked here.
+A value block is the page's value layout [D][BS] for one kv head: rows of
+R = 2 BS bytes (16-bit elements), copied into shared memory by a tensor copy
+in the R-byte swizzle (32, 64 or 128 bytes for blocks of 16, 32 or 64
+tokens), which XORs the 16-byte chunk index of an address (bits 4..) with
+its bits 7.. (one, two or three of them).  The consumer's ``vchunk(d, c)``
+gives the byte offset of the 16-byte chunk c (tokens 8c .. 8c + 7) of dim d.
+These tests read that expression from the CUDA source and check, for every
+head size and block size the kernel takes, that it is the swizzle rule
+applied to the unswizzled offset, that it maps the block's (dim, chunk)
+pairs one to one onto its 16-byte slots, and that every ldmatrix row group
+(8 consecutive dims, one chunk) falls in 8 distinct bank groups, i.e. is
+free of bank conflicts -- which the unswizzled rows are not.
 """
 import os
 import re
@@ -22,87 +22,61 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 MMA = os.path.join(ROOT, "decode_attention_paged_pa_gb300", "csrc", "pa_mma.cuh")
 HEAD_SIZES = (64, 80, 96, 112, 128, 256)
-ESZ = 2  # 16-bit caches
+BLOCK_SIZES = (16, 32, 64)
+CASES = [(D, BS) for D in HEAD_SIZES for BS in BLOCK_SIZES]
 
 
-def _source_constants():
+def _vchunk_from_source():
     src = open(MMA).read()
-    pieces = int(re.search(r"#define PA_V_PIECES32 (\d+)", src).group(1))
-    m = re.search(r"kVRot = kVPieces == 4 \? (\d+) : kVPieces == 2 \? (\d+) : 0;", src)
-    return pieces, {4: int(m.group(1)), 2: int(m.group(2)), 1: 0}
+    body = src[src.index("static uint32_t vchunk(int d, int c)"):]
+    expr = re.search(r"if constexpr \(kTma\) \{\s*return (.*?);", body, re.S).group(1)
+    py = re.sub(r"\(uint32_t\)", "", expr)
+    py = re.sub(r"(\d+)u\b", r"\1", py)
+    py = py.replace("/", "//")
+    return eval("lambda d, c, VROW: " + py)  # noqa: S307 - an arithmetic expression of the kernel source
 
 
-PIECES, ROT = _source_constants()
+VCHUNK = _vchunk_from_source()
 
 
-def _layout(D, BS, npc):
-    """(vdim, vrow): the dim row i of value tile mt holds, and a dim's byte offset."""
-    per, r = D // npc, 8 // npc
-    piece_bytes = per * BS * ESZ
-
-    def vdim(mt, i):
-        if npc == 1:
-            return mt * 16 + i
-        h, ri = i >> 3, i & 7
-        p = ri // r
-        return p * per + (mt * 2 * r + h * r + ri % r + ROT[npc] * p) % per
-
-    def vrow(d):
-        p = d // per
-        return p * (piece_bytes + 16) + (d - p * per) * BS * ESZ
-
-    return vdim, vrow
+def swizzle(addr: int, row_bytes: int) -> int:
+    """The tensor copy's swizzle of `row_bytes` (32, 64, 128) bytes: the
+    16-byte chunk index XOR address bits 7.. (1, 2 or 3 of them)."""
+    mask = row_bytes // 16 - 1
+    return addr ^ (((addr >> 7) & mask) << 4)
 
 
-def _worst(values):
-    return max(values.count(v) for v in values)
+@pytest.mark.parametrize("D,BS", CASES)
+def test_vchunk_is_the_row_width_swizzle(D, BS):
+    R = 2 * BS
+    for d in range(D):
+        for c in range(BS // 8):
+            assert VCHUNK(d, c, R) == swizzle(d * R + c * 16, R), (d, c)
 
 
-def _check(D, BS, npc):
-    vdim, vrow = _layout(D, BS, npc)
-    kbytes = D * BS * ESZ
-    dims, worst_load, worst_store = [], 0, 0
+@pytest.mark.parametrize("D,BS", CASES)
+def test_vchunk_is_one_to_one_inside_the_block(D, BS):
+    R = 2 * BS
+    slots = sorted(VCHUNK(d, c, R) for d in range(D) for c in range(BS // 8))
+    assert slots == list(range(0, D * R, 16))
+
+
+@pytest.mark.parametrize("D,BS", CASES)
+def test_ldmatrix_row_groups_are_conflict_free(D, BS):
+    # ldmatrix .x4 reads four 8x8 matrices; each is 8 rows of 16 bytes from 8
+    # lanes: dims mt*16 + 8*h + (0..7), one chunk.  32 banks of 4 bytes = 8
+    # groups of 16 bytes; 8 distinct groups means one wavefront.
+    R = 2 * BS
     for mt in range(D // 16):
         for h in range(2):
-            rows = [vdim(mt, 8 * h + ri) for ri in range(8)]
-            dims += rows
-            # One fragment matrix: 8 rows of 16 bytes at token chunk c.
-            for c in range(BS * ESZ // 16):
-                groups = [((vrow(d) + 16 * c) // 16) % 8 for d in rows]
-                worst_load = max(worst_load, _worst(groups))
-                assert all(vrow(d) + 16 * c + 16 <= kbytes + 16 * (npc - 1) for d in rows)
-            # finish(): lane (r, hq) stores float rows hq * D + dim for hq in 0, 2, 4, 6.
-            worst_store = max(worst_store, _worst([(hq * D + d) % 32 for d in rows for hq in (0, 2, 4, 6)]))
-    assert sorted(dims) == list(range(D)), "tile rows must hold every dim exactly once"
-    piece_bytes = kbytes // npc
-    assert piece_bytes % 16 == 0 and all((p * (piece_bytes + 16)) % 16 == 0 for p in range(npc))
-    return worst_load, worst_store
+            for c in range(BS // 8):
+                groups = [(VCHUNK(mt * 16 + 8 * h + i, c, R) // 16) % 8 for i in range(8)]
+                assert len(set(groups)) == 8, (mt, h, c, groups)
 
 
-def test_source_takes_two_pieces_for_32_token_blocks():
-    assert PIECES == 2
-
-
-@pytest.mark.parametrize("D", HEAD_SIZES)
-def test_contiguous_32_token_rows_conflict_four_ways(D):
-    assert _check(D, 32, 1) == (4, 4)
-
-
-@pytest.mark.parametrize("npc", [2, 4])
-@pytest.mark.parametrize("D", HEAD_SIZES)
-def test_pieces_cut_the_load_conflict_and_keep_the_stores_spread(D, npc):
-    worst_load, worst_store = _check(D, 32, npc)
-    assert worst_load == 4 // npc
-    assert worst_store <= 4
-
-
-def test_a_dropped_rotation_is_caught():
-    """Without the per-piece rotation the hand-over stores of head size 128
-    pile onto the same banks: the check above must notice."""
-    saved = dict(ROT)
-    try:
-        ROT[4] = 0
-        assert _check(128, 32, 4)[1] > 4
-    finally:
-        ROT.clear()
-        ROT.update(saved)
+@pytest.mark.parametrize("BS", BLOCK_SIZES)
+def test_unswizzled_rows_would_conflict(BS):
+    # Without the swizzle, 8 rows R bytes apart fill only 8 R / 128 bank groups.
+    R = 2 * BS
+    groups = [((d * R) // 16) % 8 for d in range(8)]
+    assert len(set(groups)) == max(1, 8 * 16 // R) and len(set(groups)) < 8
