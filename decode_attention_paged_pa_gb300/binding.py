@@ -261,7 +261,7 @@ def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, 
 
 # Sequences one phase-1 kernel launch takes (the kernel's order and prefix
 # arrays); a call launches phase 1 once per this many sequences, whatever q_len.
-MAX_ROWS_PER_LAUNCH = 1024
+MAX_ROWS_PER_LAUNCH = 512
 
 
 def launches_per_call(num_seqs: int, q_len: int = 1, max_partitions: int = 2) -> int:

@@ -26,6 +26,14 @@ int device_sm_count() {
   return cache[dev];
 }
 
+// Clears header words [first, first + count) of the workspace before a phase-1
+// launch (the launch is its programmatic dependent, so it may be scheduled as
+// soon as this kernel starts; phase 1 waits for it before it touches the header).
+__global__ void __launch_bounds__(64) pa_clear_header_kernel(int* hdr, int first, int count) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = threadIdx.x; i < count; i += blockDim.x) hdr[first + i] = 0;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -223,13 +231,14 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     own = true;
   }
   int status = PA_OK;
-  // The header (error word, work counter, timeout record) starts at zero.
-  if (cudaMemsetAsync(ws, 0, w.m, st) != cudaSuccess) status = PA_ERR_CUDA;
-
   const size_t esz = elem_bytes(dtype);
   for (int s0 = 0; s0 < S && status == PA_OK; s0 += rows_per_launch) {
     const int n = (S - s0) < rows_per_launch ? (S - s0) : rows_per_launch;
-    if (s0 > 0 && cudaMemsetAsync(ws + sizeof(int) * kHdrWork, 0, sizeof(int), st) != cudaSuccess) {
+    // The header (error word, work counter, timeout record) starts at zero;
+    // a later launch of the same call restarts the work counter only.
+    pa_clear_header_kernel<<<1, 64, 0, st>>>(reinterpret_cast<int*>(ws + w.hdr), s0 == 0 ? 0 : kHdrWork,
+                                             s0 == 0 ? kHdrInts : 1);
+    if (cudaGetLastError() != cudaSuccess) {
       status = PA_ERR_CUDA;
       break;
     }
@@ -294,7 +303,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   }
   // Phase 2 over the whole batch (no sequence has more than one partition if
   // the table holds at most P tokens).  Warps per row: enough that a warp
-  // takes at most 8 partitions, up to 8.
+  // takes at most 16 partitions (one batch of loads), up to 8.
   if (status == PA_OK && w.pmax > 1) {
     CParams cp;
     std::memset(&cp, 0, sizeof cp);
@@ -309,7 +318,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     cp.Pmax = w.pmax;
     cp.P = P;
     cp.max_len = MB * BS;
-    cp.wpr = w.pmax > 32 ? 8 : w.pmax > 16 ? 4 : w.pmax > 8 ? 2 : 1;
+    cp.wpr = w.pmax > 64 ? 8 : w.pmax > 32 ? 4 : w.pmax > 16 ? 2 : 1;
     cp.q_len = q_len;
     cp.Hu = num_heads;
     cp.Gu = num_heads / KH;

@@ -14,7 +14,7 @@
 // Launch: grid (S, ceil(H / RPC)), 8 warps a CTA.  WPR warps share a row
 // (WPR = 8 / RPC, chosen by the host from the largest partition count the
 // table allows): warp sub of a row takes a contiguous range of its
-// partitions, each lane a float4 column of the head, loads in batches of 8
+// partitions, each lane a float4 column of the head, loads in batches of 16
 // partitions; the WPR warp states of a row are then merged in shared memory
 // in warp order, so the result is deterministic.  The kernel is launched as a
 // programmatic dependent of phase 1: it reads the lengths first and waits for
@@ -38,7 +38,7 @@ struct CParams {
 };
 
 constexpr int kCombineWarps = 8;
-constexpr int kCombineBatch = 8;  // partitions whose states are loaded together
+constexpr int kCombineBatch = 16;  // partitions whose states are loaded together
 
 // Output row of row head h of sequence s (as in phase 1).
 __device__ __forceinline__ size_t combine_out_row(const CParams& prm, int s, int h) {
@@ -70,6 +70,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine_kernel(const __
 #pragma unroll
   for (int c = 0; c < CPL; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   const bool row_ok = h < prm.H;
+  // Phase 1 kept the states in L2 (evict-last); they are read once here.
+  const uint64_t pol_once = l2_policy_evict_first();
   if (row_ok) {
     const int per = (np + prm.wpr - 1) / prm.wpr;
     const int p_beg = min(sub * per, np), p_end = min(p_beg + per, np);
@@ -81,12 +83,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine_kernel(const __
 #pragma unroll
       for (int j = 0; j < kCombineBatch; ++j) {
         const bool in = p0 + j < p_end;
-        mv[j] = in ? __ldcg(prm.ws_m + base + p0 + j) : -INFINITY;
-        lv[j] = in ? __ldcg(prm.ws_l + base + p0 + j) : 0.f;
+        mv[j] = in ? ld_f32_policy(prm.ws_m + base + p0 + j, pol_once) : -INFINITY;
+        lv[j] = in ? ld_f32_policy(prm.ws_l + base + p0 + j, pol_once) : 0.f;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           const int col = lane + 32 * c;
-          ov[j][c] = (in && col < D4) ? __ldcg(o4 + (size_t)(p0 + j) * D4 + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+          ov[j][c] = (in && col < D4) ? ld_f4_policy(o4 + (size_t)(p0 + j) * D4 + col, pol_once)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       float gm = mv[0];

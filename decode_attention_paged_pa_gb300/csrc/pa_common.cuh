@@ -134,6 +134,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tma
       : "memory");
 }
 
+// Global stores / loads of fp32 data with an L2 eviction-priority policy.
+__device__ __forceinline__ void st_f4_policy(float4* dst, const float4& v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void st_f32_policy(float* dst, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(policy) : "memory");
+}
+__device__ __forceinline__ float4 ld_f4_policy(const float4* src, uint64_t policy) {
+  float4 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(src), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ float ld_f32_policy(const float* src, uint64_t policy) {
+  float v;
+  asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(src), "l"(policy));
+  return v;
+}
+
 // L2 policy for data read once (K/V pages): evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;

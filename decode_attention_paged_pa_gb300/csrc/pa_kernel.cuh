@@ -44,10 +44,10 @@
 namespace pa {
 
 // Sequences per launch: the kernel keeps the longest-first order and a prefix
-// sum of partitions per sequence in shared memory; longer batches are split
-// into several launches.
+// sum of partitions per sequence in shared memory (6 bytes a sequence, taken
+// from the ring); longer batches are split into several launches.
 #ifndef PA_MAX_SEQS_PER_LAUNCH
-#define PA_MAX_SEQS_PER_LAUNCH 1024
+#define PA_MAX_SEQS_PER_LAUNCH 512
 #endif
 constexpr int kMaxSeqsPerLaunch = PA_MAX_SEQS_PER_LAUNCH;
 static_assert(kMaxSeqsPerLaunch <= 65536, "ranks are kept as 16-bit sequence indices");
@@ -147,8 +147,7 @@ struct Layout {
   static constexpr uint32_t OFF_SCR = al16(OFF_EPI_ML + NC * C::GT * 2 * 4);
   static constexpr uint32_t OFF_RSTAT = al16(OFF_SCR + NC * C::SCRATCH_FLOATS * 4);
   static constexpr uint32_t OFF_EF = al16(OFF_RSTAT + C::GT * 2 * 4);   // NC*GT warp weights + GT sums
-  static constexpr uint32_t OFF_SCAN = al16(OFF_EF + (NC + 1) * C::GT * 4);
-  static constexpr uint32_t OFF_INFO = al16(OFF_SCAN + THREADS * 4);
+  static constexpr uint32_t OFF_INFO = al16(OFF_EF + (NC + 1) * C::GT * 4);
   static constexpr uint32_t OFF_EPI_INFO = al16(OFF_INFO + UQ * sizeof(UnitInfo));
   static constexpr uint32_t OFF_BAR = al16(OFF_EPI_INFO + sizeof(UnitInfo));
   static constexpr uint32_t NBAR = 2 * NSTAGE + 2 * UQ + 2;
@@ -623,6 +622,9 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
   int* err = prm.hdr + kHdrError;
   const int H = prm.H, Pmax = prm.Pmax;
   T* out = static_cast<T*>(prm.out);
+  // Partition states are read back by phase 2 right after this kernel: keep
+  // them in L2 ahead of the streamed K/V (which is marked evict-first).
+  const uint64_t pol_keep = l2_policy_evict_last();
 
   for (uint32_t k = 0;; ++k) {
     // Wait (bounded) for hand-over k.
@@ -680,11 +682,11 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
       if (single) {
         store4<T>(out + out_row_rt(prm, I.s, I.h0 + gh) * D + d4 * 4, val);
       } else {
-        reinterpret_cast<float4*>(prm.ws_o + (sh * Pmax + I.p) * D)[d4] = val;
+        st_f4_policy(reinterpret_cast<float4*>(prm.ws_o + (sh * Pmax + I.p) * D) + d4, val, pol_keep);
       }
       if (d4 == 0) {
-        prm.ws_m[sh * Pmax + I.p] = rstat[gh * 2] * kLn2;
-        prm.ws_l[sh * Pmax + I.p] = ef[NC * GT + gh];
+        st_f32_policy(prm.ws_m + sh * Pmax + I.p, rstat[gh * 2] * kLn2, pol_keep);
+        st_f32_policy(prm.ws_l + sh * Pmax + I.p, ef[NC * GT + gh], pol_keep);
         // A single-partition sequence ends here: its log-sum-exp is the
         // merged maximum (log2 units -> natural) plus the log of the merged sum.
         if (single && prm.lse) prm.lse[out_row_rt(prm, I.s, I.h0 + gh)] = rstat[gh * 2] * kLn2 + logf(ef[NC * GT + gh]);
@@ -705,9 +707,9 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
   const uint32_t sbase = smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_FLAGS);
   volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(smem + LY::OFF_FLAGS + 8);
+  int* bad_len = reinterpret_cast<int*>(smem + LY::OFF_FLAGS + 16);  // a length out of range
   int* pref = reinterpret_cast<int*>(smem + LY::OFF_PREF);
   uint16_t* perm = reinterpret_cast<uint16_t*>(smem + LY::perm_off(prm.S));
-  int* scan = reinterpret_cast<int*>(smem + LY::OFF_SCAN);
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + LY::OFF_INFO);
 
   if (tid == 0) {
@@ -724,6 +726,7 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     mbar_init(bar + 8 * (2 * NS + 2 * UQ + 1), 1);  // hand-over empty: the epilogue warp
     *abort_flag = 0;
     *issued = 0;
+    *bad_len = 0;
     fence_mbarrier_init();
   }
   // Longest-first order.  Every CTA computes the same order from the lengths:
@@ -736,16 +739,17 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     constexpr int NW = LY::THREADS / 32;
     constexpr int NBK = 128;  // sort buckets
     static_assert(LY::THREADS % 32 == 0 && NW <= 32, "whole warps, at most 32");
-    static_assert(LY::RING >= (NBK + kMaxSeqsPerLaunch) * 4, "sort temporaries fit in the ring");
+    static_assert(LY::RING >= (NBK + kMaxSeqsPerLaunch + 2 * NW) * 4, "prologue temporaries fit in the ring");
     const int S = prm.S, nthr = LY::THREADS, max_len = prm.MB * C::BS;
     int* bucket = reinterpret_cast<int*>(smem);       // [NBK] counts, then next free rank
-    int* parts = reinterpret_cast<int*>(smem) + NBK;  // [S] partitions per sequence
+    int* parts = bucket + NBK;                          // [S] partitions per sequence
+    int* scan = parts + kMaxSeqsPerLaunch;              // [2 * NW] warp totals, then warp starts
     for (int i = tid; i < NBK; i += nthr) bucket[i] = 0;
     __syncthreads();
     for (int s = tid; s < S; s += nthr) {
       bool bad = false;
       const int L = seq_tokens<MQ>(prm, s, max_len, &bad);
-      if (bad) atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
+      if (bad) *bad_len = 1;
       const int np = (L + prm.P - 1) / prm.P;
       parts[s] = np;
       atomicAdd(&bucket[NBK - 1 - min(np, NBK - 1)], 1);
@@ -822,6 +826,11 @@ __global__ void __launch_bounds__(Layout<C, NC, NSTAGE>::THREADS, CTAS_PER_SM)
     }
   }
   __syncthreads();
+  // This launch is a programmatic dependent of the kernel that clears the
+  // workspace header: everything above overlaps it, nothing below may touch
+  // the header before it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0 && *bad_len) atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
   if (warp == NC) {
     producer_loop<C, LY, MQ>(prm, smem, pref, perm, info, abort_flag, issued, lane);
   } else if (warp == NC + 1) {

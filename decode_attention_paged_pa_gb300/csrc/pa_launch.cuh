@@ -82,8 +82,18 @@ cudaError_t launch_one(const KParams& prm, int max_ctas, cudaStream_t stream) {
   int grid = device_sm_count() * kCtasPerSm;
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (grid < 1) grid = 1;
-  kern<<<grid, LY::THREADS, LY::bytes(prm.S), stream>>>(prm);
-  return cudaGetLastError();
+  // A programmatic dependent of the header-clearing kernel just before it.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(LY::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = LY::bytes(prm.S);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 }  // namespace pa

@@ -256,14 +256,15 @@ def test_bad_block_id_and_length_are_flagged():
 
 @pytest.mark.parametrize("variant", [SIMT, MMA], ids=["simt", "mma"])
 def test_batch_split_across_launches(variant):
-    """More sequences than one launch takes (1024): the batch is split into
-    launches that share the workspace.  Every sequence matches the oracle,
-    including multi-partition ones on both sides of each split and an empty
-    last sequence."""
+    """More sequences than one launch takes (binding.MAX_ROWS_PER_LAUNCH): the
+    batch is split into launches that share the workspace.  Every sequence
+    matches the oracle, including multi-partition ones on both sides of each
+    split and an empty last sequence."""
     g = torch.Generator().manual_seed(21)
     S = 2100
     lens = torch.randint(1, 700, (S,), generator=g).tolist()
-    lens[1023] = lens[1024] = lens[2047] = lens[2048] = 1500
+    for k in range(binding.MAX_ROWS_PER_LAUNCH, S, binding.MAX_ROWS_PER_LAUNCH):
+        lens[k - 1] = lens[k] = 1500
     lens[S - 1] = 0
     H, KH = (4, 4) if variant == SIMT else (8, 2)
     q, kc, vc, bt, L = random_case(22, S=S, H=H, KH=KH, D=64, BS=16, lens=lens, num_blocks=4096)

@@ -84,13 +84,14 @@ def test_repeat_fp32():
 def _split_lens(seed):
     g = torch.Generator().manual_seed(seed)
     lens = torch.randint(1, 400, (1100,), generator=g).tolist()
-    lens[1023] = lens[1024] = 1300   # multi-partition on both sides of the split
+    for k in range(binding.MAX_ROWS_PER_LAUNCH, len(lens), binding.MAX_ROWS_PER_LAUNCH):
+        lens[k - 1] = lens[k] = 1300   # multi-partition on both sides of each split
     lens[-1] = 0
     return lens
 
 
 def test_fp8_batch_split_across_launches():
-    """More than 1024 sequences over an fp8 cache: split launches, one workspace."""
+    """More sequences than one launch takes, over an fp8 cache: split launches, one workspace."""
     lens = _split_lens(31)
     q, kc, vc, bt, L = fp8_random_case(6101, S=len(lens), H=8, KH=2, D=64, BS=16, lens=lens, num_blocks=2048)
     qd, kd, vd, btd, ld = device(q, kc, vc, bt, L)
