@@ -14,8 +14,8 @@
 // Launch: grid (S, ceil(H / RPC)), 8 warps a CTA.  WPR warps share a row
 // (WPR = 8 / RPC, chosen by the host from the largest partition count the
 // table allows): warp sub of a row takes a contiguous range of its
-// partitions, each lane a float4 column of the head, loads in batches of 16
-// partitions; the WPR warp states of a row are then merged in shared memory
+// partitions, each lane a float4 column of the head (two at head size 256),
+// loads in batches of 16 partitions (8 at head size 256); the WPR warp states of a row are then merged in shared memory
 // in warp order, so the result is deterministic.  The kernel is launched as a
 // programmatic dependent of phase 1: it reads the lengths first and waits for
 // phase 1 to complete (griddepcontrol.wait) before it reads any state.
@@ -37,8 +37,9 @@ struct CParams {
   int q_len, Hu, Gu, G;  // multi-query rows (q_len > 1): row head -> output row
 };
 
+// 8 warps: with 16, CTAs of 512 threads fit one to an SM by registers and a
+// long-context batch's 448 CTAs ran in three waves (phase 2: 7 -> 11 us).
 constexpr int kCombineWarps = 8;
-constexpr int kCombineBatch = 16;  // partitions whose states are loaded together
 
 // Output row of row head h of sequence s (as in phase 1).
 __device__ __forceinline__ size_t combine_out_row(const CParams& prm, int s, int h) {
@@ -51,6 +52,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine_kernel(const __grid_constant__ CParams prm) {
   constexpr int D4 = D / 4;                 // float4 columns of a head
   constexpr int CPL = (D4 + 31) / 32;       // columns per lane
+  // Partitions whose states are loaded together (all in flight at once):
+  // 16, or 8 where a lane takes two columns (registers).
+  constexpr int kCombineBatch = 16 / CPL;
   __shared__ float4 s_acc[kCombineWarps][D4];
   __shared__ float s_m[kCombineWarps], s_t[kCombineWarps];
 

@@ -553,9 +553,10 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     // time.  The grouping depends only on the partition and head group, never
     // on which CTA runs the unit or on the other sequences of the batch, so a
     // sequence's output is bitwise the same in any batch.  An item is one
-    // block, or for the tensor-core consumer over 8-token blocks two
-    // consecutive blocks (one 16-token tile of the products).
-    constexpr int PB = (C::kMma && BS == 8 && !C::kFp8) ? 2 : 1;
+    // block, or for the tensor-core consumer two consecutive blocks: 8-token
+    // blocks of a 16-bit cache (one 16-token tile of the products), 16-token
+    // blocks of an fp8 cache (two tiles, one softmax update).
+    constexpr int PB = (C::kMma && ((BS == 8 && !C::kFp8) || (BS == 16 && C::kFp8))) ? 2 : 1;
     const int u_id = I.p * prm.n_hg + I.hg;
     const int nitem = (I.nb + PB - 1) / PB;
     for (int it = (warp + NC - u_id % NC) % NC; it < nitem; it += NC) {

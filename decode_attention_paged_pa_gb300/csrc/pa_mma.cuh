@@ -203,7 +203,13 @@ struct MmaConsumer {
   __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane, float*,
                                         int tok0) {
     if constexpr (kFp8) {
-      block_fp8(ks, vs, ntok, lane, tok0);
+      uint32_t kb[NTT], vb[NTT];
+#pragma unroll
+      for (int tt = 0; tt < NTT; ++tt) {
+        kb[tt] = smem_addr(ks) + tt * 16 * 16;  // token tt*16 of every 16-byte chunk row
+        vb[tt] = smem_addr(vs) + tt * 16;       // token tt*16 of every dim row
+      }
+      fp8_tiles<NTT>(kb, vb, ntok, lane, tok0);
       return;
     }
     tiles(ks, vs, nullptr, nullptr, ntok, lane, tok0);
@@ -211,10 +217,19 @@ struct MmaConsumer {
 
   // Two consecutive 8-token blocks of a unit as one 16-token tile: block A
   // (tokens 0..7, full) and block B (tokens 8..15, ntok - 8 of them valid).
+  // Over an fp8 cache in 16-token blocks: two consecutive blocks A and B
+  // (ntok tokens of 17..32 valid) as the two tiles of one work item.
   __device__ __forceinline__ void block_pair(const uint8_t* ksA, uint8_t* vsA, const uint8_t* ksB,
                                              uint8_t* vsB, int ntok, int lane, int tok0) {
-    static_assert(BS == 8 && !kFp8, "pairs are 8-token blocks of 16-bit caches");
-    tiles(ksA, vsA, ksB, vsB, ntok, lane, tok0);
+    if constexpr (kFp8) {
+      static_assert(BS == 16, "fp8 pairs are 16-token blocks");
+      const uint32_t kb[2] = {smem_addr(ksA), smem_addr(ksB)};
+      const uint32_t vb[2] = {smem_addr(vsA), smem_addr(vsB)};
+      fp8_tiles<2>(kb, vb, ntok, lane, tok0);
+    } else {
+      static_assert(BS == 8, "16-bit pairs are 8-token blocks");
+      tiles(ksA, vsA, ksB, vsB, ntok, lane, tok0);
+    }
   }
 
   // The 16-bit products over the NTT tiles of one block, or over the tile
@@ -347,21 +362,23 @@ struct MmaConsumer {
     }
   }
 
-  // One staged block of E4M3 codes (see the note above the struct).
-  __device__ __forceinline__ void block_fp8(const uint8_t* ks, const uint8_t* vs, int ntok, int lane,
-                                            int tok0) {
-    const uint32_t kbase = smem_addr(ks), vbase = smem_addr(vs);
+  // NT2 16-token tiles of E4M3 codes (see the note above the struct): tile tt's
+  // key rows at kb[tt] + (chunk * BS + row) * 16 and value rows at
+  // vb[tt] + dim * BS (the tiles of one block, or two consecutive blocks).
+  template <int NT2>
+  __device__ __forceinline__ void fp8_tiles(const uint32_t (&kb)[NT2], const uint32_t (&vb)[NT2], int ntok,
+                                            int lane, int tok0) {
     const int r = lane >> 2, c = lane & 3;
     const int trow_lo = kTok(r), trow_hi = kTok(r + 8);
-    float sc[NTT][4];
+    float sc[NT2][4];
 #pragma unroll
-    for (int tt = 0; tt < NTT; ++tt) {
+    for (int tt = 0; tt < NT2; ++tt) {
       // Chunk kk of the key block holds dims 16kk..16kk+15 of every token in 16 bytes.
       uint32_t wk[NK][2];
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
-        wk[kk][0] = lds32(kbase + (kk * BS + tt * 16 + trow_lo) * 16 + c * 4);
-        wk[kk][1] = lds32(kbase + (kk * BS + tt * 16 + trow_hi) * 16 + c * 4);
+        wk[kk][0] = lds32(kb[tt] + (kk * BS + trow_lo) * 16 + c * 4);
+        wk[kk][1] = lds32(kb[tt] + (kk * BS + trow_hi) * 16 + c * 4);
       }
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -381,20 +398,20 @@ struct MmaConsumer {
     }
     // Value words (dims mt*16 + r and + 8, tokens tt*16 + 4c .. +3) do not
     // depend on the weights: read them before the softmax.
-    uint32_t wv[NTT][NMT][2];
+    uint32_t wv[NT2][NMT][2];
 #pragma unroll
-    for (int tt = 0; tt < NTT; ++tt)
+    for (int tt = 0; tt < NT2; ++tt)
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
-        wv[tt][mt][0] = lds32(vbase + (mt * 16 + r) * BS + tt * 16 + c * 4);
-        wv[tt][mt][1] = lds32(vbase + (mt * 16 + r + 8) * BS + tt * 16 + c * 4);
+        wv[tt][mt][0] = lds32(vb[tt] + (mt * 16 + r) * BS + c * 4);
+        wv[tt][mt][1] = lds32(vb[tt] + (mt * 16 + r + 8) * BS + c * 4);
       }
     float alpha[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       float bm = fmaxf(sc[0][j], sc[0][j + 2]);
 #pragma unroll
-      for (int tt = 1; tt < NTT; ++tt) bm = fmaxf(bm, fmaxf(sc[tt][j], sc[tt][j + 2]));
+      for (int tt = 1; tt < NT2; ++tt) bm = fmaxf(bm, fmaxf(sc[tt][j], sc[tt][j + 2]));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
@@ -404,7 +421,7 @@ struct MmaConsumer {
       m[0][j] = mn;
       float ps = 0.f;
 #pragma unroll
-      for (int tt = 0; tt < NTT; ++tt) {
+      for (int tt = 0; tt < NT2; ++tt) {
         sc[tt][j] = exp2f(sc[tt][j] - ms);
         sc[tt][j + 2] = exp2f(sc[tt][j + 2] - ms);
         ps += sc[tt][j] + sc[tt][j + 2];
@@ -419,7 +436,7 @@ struct MmaConsumer {
       acc[mt][0][3] *= alpha[1];
     }
 #pragma unroll
-    for (int tt = 0; tt < NTT; ++tt) {
+    for (int tt = 0; tt < NT2; ++tt) {
       // Slots past the sequence end hold arbitrary codes (E4M3 has NaNs):
       // clear those bytes so that 0 * NaN cannot reach the accumulator.
       const int keep = ntok - (tt * 16 + c * 4);
