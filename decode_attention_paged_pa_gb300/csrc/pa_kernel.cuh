@@ -181,13 +181,19 @@ enum WaitSite {
   kSiteEpiFull = 9      // epilogue: the consumers' states of a unit
 };
 
+// Longest sleep of the producer warp between polls of the ring.
+constexpr unsigned kMaxBackoffNs = 512;
+
 // Wait (bounded) until the producer has issued at least `target` blocks.
 __device__ __forceinline__ bool wait_issued(const volatile uint32_t* issued, uint32_t target,
                                             volatile int* abort_flag, int* err_word,
                                             long long timeout_ns) {
   if (*issued >= target) return true;
+  // Not issued yet: its copy is at least a memory latency away, so poll
+  // sparingly.
   const uint64_t t0 = global_timer_ns();
   while (true) {
+    __nanosleep(64);
     if (*issued >= target) return true;
     if (*abort_flag) return false;
     if ((long long)(global_timer_ns() - t0) > timeout_ns) {
@@ -363,6 +369,10 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
         bool done = lane >= cnt;
         bool timing = false;
         uint64_t t_start = 0;
+        // Back off while no stage frees up: the polls take issue slots from
+        // the consumer warps of this sub-partition, and the ring holds
+        // microseconds of copies, so a late reissue costs nothing.
+        unsigned backoff = 32, seen = 0;
         while (true) {
           if (!done && mbar_test_wait(bar_empty + 8 * st, ph ^ 1u)) {
             const uint32_t dst = sbase + st * LY::STAGE;
@@ -396,7 +406,10 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
                 record_timeout(abort_flag, err, kSiteStage, (int)g);
                 stop = 1;
               } else {
-                __nanosleep(32);
+                const unsigned n_done = __popc(m);
+                backoff = n_done > seen ? 32u : min(backoff * 2u, kMaxBackoffNs);
+                seen = n_done;
+                __nanosleep(backoff);
               }
             }
           }
@@ -454,16 +467,17 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
 __device__ __forceinline__ bool wait_handover(const KParams& prm, uint32_t bar_eempty, uint32_t k,
                                               volatile int* abort_flag, int* err, int site, int lane) {
   const uint32_t parity = (k & 1u) ^ 1u;
-  if (__all_sync(0xffffffffu, mbar_test_wait(bar_eempty, parity))) return true;
+  // try_wait suspends the warp in hardware (for a bounded time) instead of
+  // spinning on issue slots the other warps of its sub-partition need.
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar_eempty, parity))) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (__all_sync(0xffffffffu, mbar_test_wait(bar_eempty, parity))) return true;
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar_eempty, parity))) return true;
     if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
     if ((long long)(global_timer_ns() - t0) > prm.timeout_ns) {
       if (lane == 0) record_timeout(abort_flag, err, site, (int)k);
       return false;
     }
-    __nanosleep(32);
   }
 }
 
@@ -628,19 +642,18 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
   const uint64_t pol_keep = l2_policy_evict_last();
 
   for (uint32_t k = 0;; ++k) {
-    // Wait (bounded) for hand-over k.
-    bool ok = __all_sync(0xffffffffu, mbar_test_wait(bar_efull, k & 1u));
+    // Wait (bounded) for hand-over k, suspended in hardware between tries.
+    bool ok = __all_sync(0xffffffffu, mbar_try_wait(bar_efull, k & 1u));
     if (!ok) {
       const uint64_t t0 = global_timer_ns();
       while (!ok) {
-        ok = __all_sync(0xffffffffu, mbar_test_wait(bar_efull, k & 1u));
+        ok = __all_sync(0xffffffffu, mbar_try_wait(bar_efull, k & 1u));
         if (ok) break;
         if (__any_sync(0xffffffffu, *abort_flag != 0)) return;
         if ((long long)(global_timer_ns() - t0) > prm.timeout_ns) {
           if (lane == 0) record_timeout(abort_flag, err, kSiteEpiFull, (int)k);
           return;
         }
-        __nanosleep(32);
       }
     }
     const UnitInfo I = *epi_info;
