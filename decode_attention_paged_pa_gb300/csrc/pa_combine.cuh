@@ -18,7 +18,9 @@
 // loads in batches of 16 partitions (8 at head size 256); the WPR warp states of a row are then merged in shared memory
 // in warp order, so the result is deterministic.  The kernel is launched as a
 // programmatic dependent of phase 1: it reads the lengths first and waits for
-// phase 1 to complete (griddepcontrol.wait) before it reads any state.
+// phase 1 to complete (griddepcontrol.wait) before it reads any state.  The
+// maxima and sums of a batch come in one coalesced load each (lane j holds
+// partition j's) and reach the other lanes by shuffles.
 #pragma once
 
 #include "pa_common.cuh"
@@ -82,13 +84,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine_kernel(const __
     const size_t base = ((size_t)s * prm.H + h) * prm.Pmax;
     const float4* o4 = reinterpret_cast<const float4*>(prm.ws_o) + base * D4;
     for (int p0 = p_beg; p0 < p_end; p0 += kCombineBatch) {
-      float mv[kCombineBatch], lv[kCombineBatch];
+      // Lane j < batch holds m and l of partition p0 + j (one coalesced load
+      // each); every lane holds its columns of the batch's outputs.
+      const bool inj = lane < kCombineBatch && p0 + lane < p_end;
+      const float mj = inj ? ld_f32_policy(prm.ws_m + base + p0 + lane, pol_once) : -INFINITY;
+      const float lj = inj ? ld_f32_policy(prm.ws_l + base + p0 + lane, pol_once) : 0.f;
       float4 ov[kCombineBatch][CPL];
 #pragma unroll
       for (int j = 0; j < kCombineBatch; ++j) {
         const bool in = p0 + j < p_end;
-        mv[j] = in ? ld_f32_policy(prm.ws_m + base + p0 + j, pol_once) : -INFINITY;
-        lv[j] = in ? ld_f32_policy(prm.ws_l + base + p0 + j, pol_once) : 0.f;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           const int col = lane + 32 * c;
@@ -96,9 +100,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine_kernel(const __
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      float gm = mv[0];
+      float gm = mj;
 #pragma unroll
-      for (int j = 1; j < kCombineBatch; ++j) gm = fmaxf(gm, mv[j]);
+      for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
       const float Mn = fmaxf(M, gm);
       // States a causal row never reached are (-inf, 0): while every state so
       // far is one, subtract 0 so that they weigh 0 instead of NaN.
@@ -109,9 +113,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) pa_combine_kernel(const __
       for (int c = 0; c < CPL; ++c) {
         acc[c].x *= sc; acc[c].y *= sc; acc[c].z *= sc; acc[c].w *= sc;
       }
+      // Each lane's partition weight, then taken in partition order.
+      const float wj = exp2f((mj - Ms) * kLog2e) * lj;
 #pragma unroll
       for (int j = 0; j < kCombineBatch; ++j) {
-        const float w = exp2f((mv[j] - Ms) * kLog2e) * lv[j];
+        const float w = __shfl_sync(0xffffffffu, wj, j);
         tot += w;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
