@@ -140,10 +140,12 @@ struct Layout {
   static constexpr uint32_t STAGE_TX = C::STAGE_TX;
   static_assert(!C::kTma || (STAGE % 1024 == 0 && VOFF % 1024 == 0), "swizzled value blocks 1024-byte aligned");
   static constexpr uint32_t RING = NSTAGE * STAGE;
-  static constexpr uint32_t QSLOT = C::GT * C::D * (uint32_t)sizeof(typename C::T);
+  static constexpr uint32_t QROW_BYTES = (uint32_t)C::QROW * sizeof(typename C::T);
+  static_assert(QROW_BYTES % 16 == 0, "query rows start on 16-byte boundaries (bulk copies)");
+  static constexpr uint32_t QSLOT = C::GT * QROW_BYTES;
   static constexpr uint32_t OFF_Q = RING;
   static constexpr uint32_t OFF_EPI_ACC = al16(OFF_Q + UQ * QSLOT);
-  static constexpr uint32_t OFF_EPI_ML = al16(OFF_EPI_ACC + NC * C::GT * C::D * 4);
+  static constexpr uint32_t OFF_EPI_ML = al16(OFF_EPI_ACC + NC * C::GT * C::AROW * 4);
   static constexpr uint32_t OFF_SCR = al16(OFF_EPI_ML + NC * C::GT * 2 * 4);
   static constexpr uint32_t OFF_RSTAT = al16(OFF_SCR + NC * C::SCRATCH_FLOATS * 4);
   static constexpr uint32_t OFF_EF = al16(OFF_RSTAT + C::GT * 2 * 4);   // NC*GT warp weights + GT sums
@@ -304,19 +306,20 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
         I.np = Up.np; I.nh = Up.nh; I.h0 = Up.h0; I.L = Up.L;
         const uint32_t qbytes = (uint32_t)(Up.nh * D * sizeof(T));
         mbar_arrive_expect_tx(bar_ufull + 8 * slot, qbytes);
-        if constexpr (!MQ)
+        if constexpr (!MQ && C::QROW == D)
           bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT,
                         static_cast<const T*>(prm.q) + ((size_t)Up.s * prm.H + Up.h0) * D, qbytes,
                         bar_ufull + 8 * slot, pol_keep);
       }
     }
     okp = __shfl_sync(0xffffffffu, (int)okp, 0) != 0;
-    if constexpr (MQ) {
-      // The row heads of a multi-query unit are scattered over the caller's
-      // [S, q_len, H] rows: one row copy per lane.
+    if constexpr (MQ || C::QROW != D) {
+      // One row copy per lane: the row heads of a multi-query unit are
+      // scattered over the caller's [S, q_len, H] rows, and padded rows
+      // (QROW > D) are not contiguous in the slot.
       if (okp && have && lane < Up.nh)
-        bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT + lane * D * (uint32_t)sizeof(T),
-                      static_cast<const T*>(prm.q) + out_row<true>(prm, Up.s, Up.h0 + lane) * D,
+        bulk_copy_g2s(sbase + LY::OFF_Q + slot * LY::QSLOT + lane * LY::QROW_BYTES,
+                      static_cast<const T*>(prm.q) + out_row<MQ>(prm, Up.s, Up.h0 + lane) * D,
                       (uint32_t)(D * sizeof(T)), bar_ufull + 8 * slot, pol_keep);
     }
     if (okp) ++kq;
@@ -612,7 +615,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     // taken unit k-1's.
     if (!wait_handover(prm, bar_eempty, k, abort_flag, err, kSiteHandover, lane)) break;
     ++k;
-    cons.finish(epi_acc + warp * GT * D, epi_ml + warp * GT * 2, lane);
+    cons.finish(epi_acc + warp * GT * C::AROW, epi_ml + warp * GT * 2, lane);
     if (warp == 0 && lane == 0) *epi_info = I;
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_efull);
@@ -685,7 +688,7 @@ __device__ __forceinline__ void epilogue_loop(const KParams& prm, uint8_t* smem,
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
         const float f = ef[w * GT + gh];
-        const float4 v = reinterpret_cast<const float4*>(epi_acc + (w * GT + gh) * D)[d4];
+        const float4 v = reinterpret_cast<const float4*>(epi_acc + (w * GT + gh) * C::AROW)[d4];
         num.x = fmaf(f, v.x, num.x); num.y = fmaf(f, v.y, num.y);
         num.z = fmaf(f, v.z, num.z); num.w = fmaf(f, v.w, num.w);
       }

@@ -84,6 +84,12 @@ struct MmaConsumer {
   static_assert(D % 16 == 0 && (BS == 8 || BS % 16 == 0), "head size a multiple of 16; block 8 or 16k");
   static_assert(!FP8_ || BS % 16 == 0, "fp8 caches take blocks of 16k tokens");
   static constexpr int SCRATCH_FLOATS = 0;
+  // Row strides, in elements, of a staged query row and of a handed-over
+  // state row: 16 bytes past the row, so that the 8 rows a fragment load or
+  // a state store touches (rows a multiple of 128 bytes long otherwise) fall
+  // in distinct shared-memory banks.
+  static constexpr int QROW = D_ + 16 / (int)sizeof(T_);
+  static constexpr int AROW = D_ + 4;
   static constexpr bool kSplitWeights = std::is_same<MT, __nv_bfloat16>::value;
 
   // Byte offset, in a staged value block, of the 16-byte chunk c (tokens
@@ -146,7 +152,7 @@ struct MmaConsumer {
 #pragma unroll
       for (int ks = 0; ks < NK; ++ks) {
         if (n < nh) {
-          const uint2 w = *reinterpret_cast<const uint2*>(q16 + n * D + ks * 16 + 2 * kq);
+          const uint2 w = *reinterpret_cast<const uint2*>(q16 + n * QROW + ks * 16 + 2 * kq);
           const float2 a = F16Traits<T>::to_float2(w.x), b = F16Traits<T>::to_float2(w.y);
           amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))));
         }
@@ -162,7 +168,7 @@ struct MmaConsumer {
       for (int ks = 0; ks < NK; ++ks) {
         uint32_t lo = 0, hi = 0;
         if (n < nh) {
-          const uint2 w = *reinterpret_cast<const uint2*>(q16 + n * D + ks * 16 + 2 * kq);
+          const uint2 w = *reinterpret_cast<const uint2*>(q16 + n * QROW + ks * 16 + 2 * kq);
           const float2 a = F16Traits<T>::to_float2(w.x), b = F16Traits<T>::to_float2(w.y);
           lo = F16Traits<__half>::pack(a.x * up, a.y * up);
           hi = F16Traits<__half>::pack(b.x * up, b.y * up);
@@ -179,8 +185,8 @@ struct MmaConsumer {
           const int h = 8 * t + n;
           uint32_t lo = 0, hi = 0;
           if (h < nh) {
-            lo = *reinterpret_cast<const uint32_t*>(q16 + h * D + ks * 16 + kq);
-            hi = *reinterpret_cast<const uint32_t*>(q16 + h * D + ks * 16 + kq + 8);
+            lo = *reinterpret_cast<const uint32_t*>(q16 + h * QROW + ks * 16 + kq);
+            hi = *reinterpret_cast<const uint32_t*>(q16 + h * QROW + ks * 16 + kq + 8);
           }
           qb[ks][t][0] = lo;
           qb[ks][t][1] = hi;
@@ -479,12 +485,12 @@ struct MmaConsumer {
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         // Accumulator rows r and r + 8 of value tile mt hold dims mt * 16 + r and + 8.
-        float* o = acc_out + (8 * t + hq) * D;
+        float* o = acc_out + (8 * t + hq) * AROW;
         const int d_lo = mt * 16 + r, d_hi = d_lo + 8;
         o[d_lo] = acc[mt][t][0];
-        o[D + d_lo] = acc[mt][t][1];
+        o[AROW + d_lo] = acc[mt][t][1];
         o[d_hi] = acc[mt][t][2];
-        o[D + d_hi] = acc[mt][t][3];
+        o[AROW + d_hi] = acc[mt][t][3];
       }
   }
 };

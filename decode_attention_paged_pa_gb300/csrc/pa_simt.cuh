@@ -52,6 +52,11 @@ struct SimtConsumer {
   float acc[GT][NROW];
 
   // q rows [GT][D] in shared memory; rows >= nh are treated as zero.
+  // Row strides, in elements, of a staged query row and of a handed-over
+  // state row (no padding: a warp's loads and stores here stay in one row).
+  static constexpr int QROW = D;
+  static constexpr int AROW = D;
+
   __device__ __forceinline__ void begin_unit(const T* qs, int nh, float scale_log2, int lane) {
     const int slice = lane / TPP;
 #pragma unroll
@@ -60,7 +65,7 @@ struct SimtConsumer {
       for (int i = 0; i < QCH; ++i) {
         float f[EPC];
         if (g < nh) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(qs + g * D + slice * QKD + i * EPC);
+          const uint4 raw = *reinterpret_cast<const uint4*>(qs + g * QROW + slice * QKD + i * EPC);
           unpack_chunk<T>(raw, f);
         } else {
 #pragma unroll
@@ -195,7 +200,7 @@ struct SimtConsumer {
         float v = acc[g][r];
 #pragma unroll
         for (int off = 1; off < CPR; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (c == 0) acc_out[g * D + r0 + r * RPP] = v;
+        if (c == 0) acc_out[g * AROW + r0 + r * RPP] = v;
       }
       if (lane == 0) {
         ml[g * 2] = m[g];
