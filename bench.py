@@ -379,10 +379,13 @@ def repetitions_needed(first_ms: float, min_seconds: float, cap: int = 2000) -> 
 
 
 class Timer:
-    """Times K calls of ``step`` on ``stream``: one CUDA event per call boundary
-    (back to back), or, with ``flush``, an event pair around each call and an
-    L2-sized write between calls outside them.  Every repetition is bracketed
-    by a barrier and a device synchronise on both sides."""
+    """Times K calls of ``step`` on ``stream``: one CUDA event pair around the K
+    back-to-back calls (an event between calls would stand between one call's
+    last kernel and the next call's first, which otherwise overlap through
+    programmatic dependent launch; the per-call time is the pair's time over
+    K), or, with ``flush``, an event pair around each call and an L2-sized
+    write between calls outside them.  Every repetition is bracketed by a
+    barrier and a device synchronise on both sides."""
 
     def __init__(self, dev, stream, dist, flush: bool):
         self.dev, self.stream, self.dist = dev, stream, dist
@@ -394,14 +397,14 @@ class Timer:
             self.dist.barrier()
         torch.cuda.synchronize(self.dev)
         if self.scrub is None:
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
-            ev[0].record(self.stream)
-            for i in range(k):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            for _ in range(k):
                 step()
-                ev[i + 1].record(self.stream)
+            b.record(self.stream)
             torch.cuda.synchronize(self.dev)
-            per = [ev[i].elapsed_time(ev[i + 1]) for i in range(k)]
-            total = ev[0].elapsed_time(ev[-1])
+            total = a.elapsed_time(b)
+            per = [total / k] * k
         else:
             pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                      for _ in range(k)]

@@ -101,6 +101,8 @@ def _declare(lib):
 def lib() -> ctypes.CDLL:
     """The loaded CUDA library (built on first use if absent)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             path = _build.LIB_PATH
@@ -190,9 +192,9 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, sca
     if block_tables.shape[0] != S or seq_lens.shape[0] != S:
         raise ValueError("block_tables / seq_lens must have num_seqs rows")
     MB = block_tables.shape[1]
-    need = workspace_bytes(S, H, KH, D, MB, BS, partition_size)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+    if workspace is None:  # (a caller's workspace is checked by the library: PA_ERR_WORKSPACE)
+        workspace = torch.empty(max(workspace_bytes(S, H, KH, D, MB, BS, partition_size), 256), dtype=torch.uint8,
+                                device=query.device)
     _check_tensor("workspace", workspace, torch.uint8)
     if lse is not None:
         _check_tensor("lse", lse, torch.float32, 2)
@@ -246,9 +248,9 @@ def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, 
         if tuple(lse.shape) != (S, QL, H):
             raise ValueError("lse must be [num_seqs, q_len, num_heads]")
     MB = block_tables.shape[1]
-    need = workspace_bytes(S * QL, H, KH, D, MB, BS, partition_size)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+    if workspace is None:  # (a caller's workspace is checked by the library: PA_ERR_WORKSPACE)
+        workspace = torch.empty(max(workspace_bytes(S * QL, H, KH, D, MB, BS, partition_size), 256), dtype=torch.uint8,
+                                device=query.device)
     _check_tensor("workspace", workspace, torch.uint8)
     st = lib().pa_decode_v2_mq(
         _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
@@ -302,9 +304,9 @@ def pa_decode_v2_fp8(out, query, key_cache, value_cache, block_tables, seq_lens,
         if tuple(lse.shape) != (S, H):
             raise ValueError("lse must be [num_seqs, num_heads]")
     MB = block_tables.shape[1]
-    need = workspace_bytes(S, H, KH, D, MB, BS, partition_size)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+    if workspace is None:  # (a caller's workspace is checked by the library: PA_ERR_WORKSPACE)
+        workspace = torch.empty(max(workspace_bytes(S, H, KH, D, MB, BS, partition_size), 256), dtype=torch.uint8,
+                                device=query.device)
     _check_tensor("workspace", workspace, torch.uint8)
     st = lib().pa_decode_v2_fp8(
         _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),

@@ -27,11 +27,30 @@ int device_sm_count() {
 }
 
 // Clears header words [first, first + count) of the workspace before a phase-1
-// launch (the launch is its programmatic dependent, so it may be scheduled as
-// soon as this kernel starts; phase 1 waits for it before it touches the header).
+// launch.  It is itself launched as a programmatic dependent of whatever
+// precedes it on the stream, so its launch overlaps that work's end: it first
+// waits for that work to complete (its writes -- the caller's inputs among
+// them -- visible), and only then lets phase 1, its own programmatic
+// dependent, be scheduled; phase 1 waits for this kernel before it touches
+// the header.
 __global__ void __launch_bounds__(64) pa_clear_header_kernel(int* hdr, int first, int count) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = threadIdx.x; i < count; i += blockDim.x) hdr[first + i] = 0;
+}
+
+// The header clear, launched as described above.
+static cudaError_t launch_clear_header(int* hdr, int first, int count, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(64, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa_clear_header_kernel, hdr, first, count);
 }
 
 namespace {
@@ -236,9 +255,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     const int n = (S - s0) < rows_per_launch ? (S - s0) : rows_per_launch;
     // The header (error word, work counter, timeout record) starts at zero;
     // a later launch of the same call restarts the work counter only.
-    pa_clear_header_kernel<<<1, 64, 0, st>>>(reinterpret_cast<int*>(ws + w.hdr), s0 == 0 ? 0 : kHdrWork,
-                                             s0 == 0 ? kHdrInts : 1);
-    if (cudaGetLastError() != cudaSuccess) {
+    if (launch_clear_header(reinterpret_cast<int*>(ws + w.hdr), s0 == 0 ? 0 : kHdrWork,
+                            s0 == 0 ? kHdrInts : 1, st) != cudaSuccess) {
       status = PA_ERR_CUDA;
       break;
     }
