@@ -130,7 +130,8 @@ EncodeTiledFn encode_tiled() {
 // value_cache [NB, KH, D, BS] as a 3-D tensor [NB*KH][D][BS] with a box of one
 // whole block ([1][D][BS]), stored in shared memory in the swizzle of the
 // rows' width (BS * 2 bytes: 32, 64 or 128).
-bool encode_value_map(KParams* prm, const void* value_cache, int num_blocks, int KH, int D, int BS) {
+// kvu: kv heads per box (the unit's consecutive kv heads of one block).
+bool encode_value_map(KParams* prm, const void* value_cache, int num_blocks, int KH, int D, int BS, int kvu) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const CUtensorMapSwizzle sw = BS == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
@@ -139,7 +140,7 @@ bool encode_value_map(KParams* prm, const void* value_cache, int num_blocks, int
   const cuuint32_t unit[3] = {1, 1, 1};
   const cuuint64_t vdim[3] = {(cuuint64_t)BS, (cuuint64_t)D, (cuuint64_t)num_blocks * (cuuint64_t)KH};
   const cuuint64_t vstride[2] = {(cuuint64_t)BS * 2, (cuuint64_t)D * BS * 2};
-  const cuuint32_t vbox[3] = {(cuuint32_t)BS, (cuuint32_t)D, 1};
+  const cuuint32_t vbox[3] = {(cuuint32_t)BS, (cuuint32_t)D, (cuuint32_t)kvu};
   return enc(&prm->tmv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(value_cache), vdim, vstride, vbox,
              unit, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -227,8 +228,14 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   const bool wide = variant == PA_VARIANT_MMA && G > kMmaGroup && !kv_fp8 && D <= 128 &&
                     base_shape(D, BS);
   const int gt = (variant == PA_VARIANT_MMA) ? (wide ? kMmaGroupWide : kMmaGroup) : kSimtGroup;
+  // Four query rows per kv head: a unit's 8 columns take two kv heads (one
+  // block copy each for keys and values covers both), head sizes up to 128
+  // and blocks of 8, 16 or 32 tokens.
+  const bool pairs = variant == PA_VARIANT_MMA && !kv_fp8 && !wide && q_len == 1 && G * 2 == kMmaGroup &&
+                     KH % 2 == 0 && D <= 128 && (BS == 8 || BS == 16 || BS == 32);
+  const int kvu = pairs ? 2 : 1;
   const int hg_per_kv = (G + gt - 1) / gt;
-  const int n_hg = KH * hg_per_kv;
+  const int n_hg = KH * hg_per_kv / kvu;
   const int rows_per_launch = kMaxSeqsPerLaunch;  // sequences per launch
   const int chunk = S < rows_per_launch ? S : rows_per_launch;
   if ((long long)chunk * w.pmax * n_hg > INT_MAX / 2) return PA_ERR_UNSUPPORTED;
@@ -239,7 +246,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   std::memset(&maps, 0, sizeof maps);
   if (tma_values) {
     if ((long long)num_blocks * KH > INT_MAX) return PA_ERR_UNSUPPORTED;
-    if (!encode_value_map(&maps, value_cache, num_blocks, KH, D, BS)) return PA_ERR_CUDA;
+    if (!encode_value_map(&maps, value_cache, num_blocks, KH, D, BS, kvu)) return PA_ERR_CUDA;
   }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -297,6 +304,12 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     else if (wide)
       e = dtype == PA_DTYPE_FP16 ? launch_mma16_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma16_bf16(prm, D, BS, max_ctas, st);
+    else if (pairs && BS == 8)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma_g8_f16(prm, D, max_ctas, st) : launch_mma_g8_bf16(prm, D, max_ctas, st);
+    else if (pairs && BS == 16)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma_g16_f16(prm, D, max_ctas, st) : launch_mma_g16_bf16(prm, D, max_ctas, st);
+    else if (pairs)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma_g32_f16(prm, D, max_ctas, st) : launch_mma_g32_bf16(prm, D, max_ctas, st);
     else if (variant == PA_VARIANT_MMA && BS == 8)
       e = dtype == PA_DTYPE_FP16 ? launch_mma_b8_f16(prm, D, max_ctas, st)
                                  : launch_mma_b8_bf16(prm, D, max_ctas, st);

@@ -134,7 +134,7 @@ struct Layout {
   static constexpr int THREADS = NCT + 64;     // + producer warp + epilogue warp
   // A stage holds one block of one kv head: the K block, then at VOFF the V
   // block; its copies deliver STAGE_TX bytes.
-  static constexpr uint32_t KBYTES = C::KTILE;
+  static constexpr uint32_t KBYTES = C::KBLK;
   static constexpr uint32_t VOFF = C::KREGION;
   static constexpr uint32_t STAGE = C::STAGE_BYTES;
   static constexpr uint32_t STAGE_TX = C::STAGE_TX;
@@ -235,10 +235,17 @@ __device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pre
   U.t0 = U.p * prm.P;
   U.t1 = min(U.t0 + prm.P, L);
   U.nb = (U.t1 - U.t0 + BS - 1) / BS;
-  U.kv = U.hg / prm.hg_per_kv;
-  const int hgk = U.hg - U.kv * prm.hg_per_kv;
-  U.h0 = U.kv * prm.G + hgk * GT;
-  U.nh = min(GT, prm.G - hgk * GT);
+  if constexpr (C::KVU > 1) {
+    // Head group hg: kv heads KVU hg .. KVU hg + KVU - 1, their G * KVU query heads.
+    U.kv = U.hg * C::KVU;
+    U.h0 = U.kv * prm.G;
+    U.nh = min(GT, prm.G * C::KVU);
+  } else {
+    U.kv = U.hg / prm.hg_per_kv;
+    const int hgk = U.hg - U.kv * prm.hg_per_kv;
+    U.h0 = U.kv * prm.G + hgk * GT;
+    U.nh = min(GT, prm.G - hgk * GT);
+  }
   return U;
 }
 
@@ -557,7 +564,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
       break;
     }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
-                    prm.scale_log2, lane);
+                    prm.scale_log2, lane, prm.G);
     if constexpr (C::kMma)
       cons.set_limits([&](int h) { return row_limit<MQ>(prm, I.L, I.h0 + h); }, lane);
     fence_proxy_async_smem();  // the query slot is refilled by a bulk copy: same ordering as a stage

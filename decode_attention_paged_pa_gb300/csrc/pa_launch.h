@@ -35,6 +35,14 @@ cudaError_t launch_mma_b8_f16(const KParams& prm, int D, int max_ctas, cudaStrea
 cudaError_t launch_mma_b8_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_b64_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_b64_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+// Tensor-core instances over pairs of kv heads (4 query heads per kv head,
+// head sizes up to 128), in 8-, 16- and 32-token blocks.
+cudaError_t launch_mma_g8_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_g8_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_g16_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_g16_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_g32_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma_g32_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
 // The same over an fp8 (E4M3) KV cache, queries and output fp16 / bf16.
 cudaError_t launch_mma8_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma8_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);

@@ -55,7 +55,15 @@ constexpr uint32_t al1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 // row i of a 16-token tile holds token kTok(i) below: a lane's value word
 // then covers four consecutive tokens of one dim, and the eight token rows a
 // lane quad reads fall in distinct shared-memory banks.
-template <typename T_, int D_, int BS_, bool FP8_ = false, int NT_ = 1>
+// KVU_: kv heads per unit.  With fewer than 8 query heads per kv head (G),
+// the 8 columns of a tile hold the query heads of KVU = 8 / G consecutive kv
+// heads: a stage then holds one block of each of them (the cache keeps the kv
+// heads of a block contiguous, so still one copy for the keys and one for the
+// values), and each product runs once per kv head with the query (scores) or
+// weight (values) columns of the other kv heads zeroed, into the same
+// accumulators.  The softmax, the weights and the stage's waits then serve
+// KVU kv heads at once, and the copies are KVU times larger.
+template <typename T_, int D_, int BS_, bool FP8_ = false, int NT_ = 1, int KVU_ = 1>
 struct MmaConsumer {
   using T = T_;
   using MT = typename std::conditional<FP8_, __half, T_>::type;  // operand type of the products
@@ -64,18 +72,24 @@ struct MmaConsumer {
   static constexpr bool kTma = !FP8_ && BS_ >= 16;
   static constexpr int D = D_, BS = BS_, GT = 8 * NT_;
   static_assert(NT_ == 1 || (NT_ == 2 && !FP8_), "one or two column tiles (one over fp8 caches)");
+  static constexpr int KVU = KVU_;
+  static_assert(KVU_ == 1 || (NT_ == 1 && !FP8_ && 8 % KVU_ == 0), "kv-head groups: one 8-column tile, 16-bit caches");
   static constexpr bool kMma = true;
   static constexpr bool kFp8 = FP8_;
   static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
-  // A stage: the key block, then (at KREGION, 1024-byte aligned for the
-  // swizzled tensor copy) the value block; STAGE_TX bytes land per stage.
+  // A stage: the key blocks of the unit's KVU kv heads (KTILE bytes each,
+  // contiguous), then (at KREGION, 1024-byte aligned for the swizzled tensor
+  // copy) their value blocks; STAGE_TX bytes land per stage.  A kv head's
+  // value block starts KTILE bytes after the previous one's: a multiple of the
+  // swizzle's repeat (8 rows), as every head size is a multiple of 8.
   static constexpr uint32_t KTILE = (uint32_t)D_ * BS * KV_ESZ;
-  static constexpr uint32_t KREGION = kTma ? al1024(KTILE) : KTILE;
-  static constexpr uint32_t STAGE_BYTES = kTma ? al1024(KREGION + KTILE) : KREGION + KTILE;
-  static constexpr uint32_t STAGE_TX = 2 * KTILE;
+  static constexpr uint32_t KBLK = (uint32_t)KVU_ * KTILE;
+  static constexpr uint32_t KREGION = kTma ? al1024(KBLK) : KBLK;
+  static constexpr uint32_t STAGE_BYTES = kTma ? al1024(KREGION + KBLK) : KREGION + KBLK;
+  static constexpr uint32_t STAGE_TX = 2 * KBLK;
   // Blocks the producer warp issues together (one per lane): copies of 2 KB
   // or less need more of them in flight than the 4 KB ones.
-  static constexpr int kIssueBatch = (KV_ESZ * D * BS <= 2048) ? 32 : 8;
+  static constexpr int kIssueBatch = (KBLK <= 2048) ? 32 : 8;
   static constexpr int NK = D / 16;    // k-steps of the score product
   static constexpr int NMT = D / 16;   // 16-dim tiles of the value product
   // 16-token tiles per block.  An 8-token block fills half of one tile: the
@@ -105,7 +119,10 @@ struct MmaConsumer {
     }
   }
 
-  uint32_t qb[NK][NT][2];  // Q^T fragments (B operand) per column tile, packed element pairs
+  // Q^T fragments (B operand) per column tile and kv head of the unit, packed
+  // element pairs (with KVU > 1, the columns of the other kv heads zero).
+  uint32_t qb[NK][NT * KVU_][2];
+  int ub;  // KVU > 1: the kv head (0 .. KVU - 1) of this lane's weight column
   float m[NT][2], l[NT][2];  // heads 8t + 2*(lane%4) and 8t + 2*(lane%4) + 1 of tile t
   float acc[NMT][NT][4];
   float scale_log2;
@@ -142,8 +159,11 @@ struct MmaConsumer {
       for (int j = 0; j < 2; ++j) lim[t][j] = limit_of(8 * t + (lane & 3) * 2 + j);
   }
 
-  __device__ __forceinline__ void begin_unit(const T* qs, int nh, float sl2, int lane) {
+  // G: query heads per kv head (columns n of a KVU > 1 unit belong to kv
+  // head n / G of the unit).
+  __device__ __forceinline__ void begin_unit(const T* qs, int nh, float sl2, int lane, int G) {
     const int n = lane >> 2, kq = (lane & 3) * 2;
+    ub = KVU_ > 1 ? n / G : 0;
     const uint16_t* q16 = reinterpret_cast<const uint16_t*>(qs);
     if constexpr (kFp8) {
       // Dims 16ks + 4c .. +3 of head n, scaled by 2^s so that the unit's
@@ -188,8 +208,12 @@ struct MmaConsumer {
             lo = *reinterpret_cast<const uint32_t*>(q16 + h * QROW + ks * 16 + kq);
             hi = *reinterpret_cast<const uint32_t*>(q16 + h * QROW + ks * 16 + kq + 8);
           }
-          qb[ks][t][0] = lo;
-          qb[ks][t][1] = hi;
+#pragma unroll
+          for (int u = 0; u < KVU_; ++u) {
+            const bool mine = KVU_ == 1 || ub == u;
+            qb[ks][t * KVU_ + u][0] = mine ? lo : 0u;
+            qb[ks][t * KVU_ + u][1] = mine ? hi : 0u;
+          }
         }
     }
 #pragma unroll
@@ -262,14 +286,17 @@ struct MmaConsumer {
         for (int i = 0; i < 4; ++i) c[t][i] = c2[t][i] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
-        uint32_t a[4];
         // (An 8-token block: rows 8..15 are block B's, or repeat rows 0..7 and are masked below.)
         const int tok = tt * 16 + (lane & (BS >= 16 ? 15 : 7)), chunk = 2 * kk + (lane >> 4);
-        ldmatrix_x4(krow + (chunk * BS + tok) * 16, a);
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (kk & 1) Mma<T>::run(c2[t], a, qb[kk][t][0], qb[kk][t][1]);
-          else Mma<T>::run(c[t], a, qb[kk][t][0], qb[kk][t][1]);
+        for (int u = 0; u < KVU; ++u) {
+          uint32_t a[4];
+          ldmatrix_x4(krow + u * KTILE + (chunk * BS + tok) * 16, a);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if ((kk * KVU + u) & 1) Mma<T>::run(c2[t], a, qb[kk][t * KVU + u][0], qb[kk][t * KVU + u][1]);
+            else Mma<T>::run(c[t], a, qb[kk][t * KVU + u][0], qb[kk][t * KVU + u][1]);
+          }
         }
       }
       const int t_lo = tt * 16 + r, t_hi = t_lo + 8;
@@ -324,10 +351,12 @@ struct MmaConsumer {
     uint8_t* vz = has_b ? vsB : vs;
     const int nz = has_b ? ntok - 8 : ntok;
     if (nz < BS) {
-      for (int i = lane; i < D * (BS - nz); i += 32) {
-        const int d = i / (BS - nz), t = nz + i % (BS - nz);
-        *reinterpret_cast<uint16_t*>(vz + vchunk(d, t >> 3) + 2 * (t & 7)) = 0;
-      }
+#pragma unroll
+      for (int u = 0; u < KVU; ++u)
+        for (int i = lane; i < D * (BS - nz); i += 32) {
+          const int d = i / (BS - nz), t = nz + i % (BS - nz);
+          *reinterpret_cast<uint16_t*>(vz + u * KTILE + vchunk(d, t >> 3) + 2 * (t & 7)) = 0;
+        }
       fence_proxy_async_smem();
       __syncwarp();
     }
@@ -354,15 +383,20 @@ struct MmaConsumer {
         }
       }
 #pragma unroll
-      for (int mt = 0; mt < NMT; ++mt) {
-        uint32_t a[4];
-        const int chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
-        ldmatrix_x4(vcol + vchunk(mt * 16 + (lane & 15), chunk), a);
-        if (BS < 16 && !has_b) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
+      for (int u = 0; u < KVU; ++u) {
+        // kv head u's value product takes the weight columns of its own query heads.
+        const bool mine = KVU == 1 || ub == u;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          Mma<T>::run(acc[mt][t], a, b0[t], b1[t]);
-          if constexpr (kSplitWeights) Mma<T>::run(acc[mt][t], a, r0[t], r1[t]);
+        for (int mt = 0; mt < NMT; ++mt) {
+          uint32_t a[4];
+          const int chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
+          ldmatrix_x4(vcol + u * KTILE + vchunk(mt * 16 + (lane & 15), chunk), a);
+          if (BS < 16 && !has_b) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            Mma<T>::run(acc[mt][t], a, mine ? b0[t] : 0u, mine ? b1[t] : 0u);
+            if constexpr (kSplitWeights) Mma<T>::run(acc[mt][t], a, mine ? r0[t] : 0u, mine ? r1[t] : 0u);
+          }
         }
       }
     }

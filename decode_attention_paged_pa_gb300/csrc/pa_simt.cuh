@@ -27,6 +27,8 @@ struct SimtConsumer {
   static constexpr bool kTma = false;
   static constexpr uint32_t KTILE = (uint32_t)D_ * BS_ * sizeof(T_);
   static constexpr uint32_t KREGION = KTILE, STAGE_BYTES = 2 * KTILE, STAGE_TX = 2 * KTILE;
+  static constexpr int KVU = 1;  // kv heads per unit
+  static constexpr uint32_t KBLK = KTILE;
   static constexpr int EPC = elems_per_chunk<T_>();  // elements per 16-byte chunk
   // q.k: each lane takes QKD dims of one token; LPT lanes share a token
   // (32 dims for fp32, whose registers hold half as many per byte; half the
@@ -57,7 +59,7 @@ struct SimtConsumer {
   static constexpr int QROW = D;
   static constexpr int AROW = D;
 
-  __device__ __forceinline__ void begin_unit(const T* qs, int nh, float scale_log2, int lane) {
+  __device__ __forceinline__ void begin_unit(const T* qs, int nh, float scale_log2, int lane, int /*G*/) {
     const int slice = lane / TPP;
 #pragma unroll
     for (int g = 0; g < GT; ++g) {
