@@ -231,8 +231,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   // Four query rows per kv head: a unit's 8 columns take two kv heads (one
   // block copy each for keys and values covers both), head sizes up to 128
   // and blocks of 8, 16 or 32 tokens.
-  const bool pairs = variant == PA_VARIANT_MMA && !kv_fp8 && !wide && q_len == 1 && G * 2 == kMmaGroup &&
-                     KH % 2 == 0 && D <= 128 && (BS == 8 || BS == 16 || BS == 32);
+  const bool pairs = variant == PA_VARIANT_MMA && !wide && q_len == 1 && G * 2 == kMmaGroup && KH % 2 == 0 &&
+                     D <= 128 && (BS == 8 || BS == 16 || BS == 32);
   const int kvu = pairs ? 2 : 1;
   const int hg_per_kv = (G + gt - 1) / gt;
   const int n_hg = KH * hg_per_kv / kvu;
@@ -298,7 +298,10 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     prm.n_hg = n_hg;
     prm.timeout_ns = timeout_ns > 0 ? timeout_ns : (1LL << 31);
     cudaError_t e;
-    if (kv_fp8)
+    if (kv_fp8 && pairs)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma8_g_f16(prm, D, BS, max_ctas, st)
+                                 : launch_mma8_g_bf16(prm, D, BS, max_ctas, st);
+    else if (kv_fp8)
       e = dtype == PA_DTYPE_FP16 ? launch_mma8_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma8_bf16(prm, D, BS, max_ctas, st);
     else if (wide)

@@ -46,6 +46,9 @@ cudaError_t launch_mma_g32_bf16(const KParams& prm, int D, int max_ctas, cudaStr
 // The same over an fp8 (E4M3) KV cache, queries and output fp16 / bf16.
 cudaError_t launch_mma8_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma8_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+// ... and over pairs of kv heads (4 query heads per kv head, head sizes 64 and 128).
+cudaError_t launch_mma8_g_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_g_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 
 // Phase 2: the cross-partition combine of every multi-partition row, launched
 // as a programmatic dependent of the phase-1 launch before it on `st`.

@@ -73,7 +73,7 @@ struct MmaConsumer {
   static constexpr int D = D_, BS = BS_, GT = 8 * NT_;
   static_assert(NT_ == 1 || (NT_ == 2 && !FP8_), "one or two column tiles (one over fp8 caches)");
   static constexpr int KVU = KVU_;
-  static_assert(KVU_ == 1 || (NT_ == 1 && !FP8_ && 8 % KVU_ == 0), "kv-head groups: one 8-column tile, 16-bit caches");
+  static_assert(KVU_ == 1 || (NT_ == 1 && 8 % KVU_ == 0), "kv-head groups: one 8-column tile");
   static constexpr bool kMma = true;
   static constexpr bool kFp8 = FP8_;
   static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
@@ -193,8 +193,12 @@ struct MmaConsumer {
           lo = F16Traits<__half>::pack(a.x * up, a.y * up);
           hi = F16Traits<__half>::pack(b.x * up, b.y * up);
         }
-        qb[ks][0][0] = lo;
-        qb[ks][0][1] = hi;
+#pragma unroll
+        for (int u = 0; u < KVU_; ++u) {
+          const bool mine = KVU_ == 1 || ub == u;
+          qb[ks][u][0] = mine ? lo : 0u;
+          qb[ks][u][1] = mine ? hi : 0u;
+        }
       }
       sl2 *= down;
     } else {
@@ -413,20 +417,23 @@ struct MmaConsumer {
     float sc[NT2][4];
 #pragma unroll
     for (int tt = 0; tt < NT2; ++tt) {
-      // Chunk kk of the key block holds dims 16kk..16kk+15 of every token in 16 bytes.
-      uint32_t wk[NK][2];
-#pragma unroll
-      for (int kk = 0; kk < NK; ++kk) {
-        wk[kk][0] = lds32(kb[tt] + (kk * BS + trow_lo) * 16 + c * 4);
-        wk[kk][1] = lds32(kb[tt] + (kk * BS + trow_hi) * 16 + c * 4);
-      }
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kk = 0; kk < NK; ++kk) {
-        const uint32_t a[4] = {e4m3x2(wk[kk][0]), e4m3x2(wk[kk][1]), e4m3x2(wk[kk][0] >> 16),
-                               e4m3x2(wk[kk][1] >> 16)};
-        if (kk & 1) Mma<__half>::run(c1, a, qb[kk][0][0], qb[kk][0][1]);
-        else Mma<__half>::run(c0, a, qb[kk][0][0], qb[kk][0][1]);
+      for (int u = 0; u < KVU; ++u) {
+        // Chunk kk of a key block holds dims 16kk..16kk+15 of every token in 16 bytes.
+        uint32_t wk[NK][2];
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+          wk[kk][0] = lds32(kb[tt] + u * KTILE + (kk * BS + trow_lo) * 16 + c * 4);
+          wk[kk][1] = lds32(kb[tt] + u * KTILE + (kk * BS + trow_hi) * 16 + c * 4);
+        }
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+          const uint32_t a[4] = {e4m3x2(wk[kk][0]), e4m3x2(wk[kk][1]), e4m3x2(wk[kk][0] >> 16),
+                                 e4m3x2(wk[kk][1] >> 16)};
+          if ((kk * KVU + u) & 1) Mma<__half>::run(c1, a, qb[kk][u][0], qb[kk][u][1]);
+          else Mma<__half>::run(c0, a, qb[kk][u][0], qb[kk][u][1]);
+        }
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) c0[i] += c1[i];
@@ -438,6 +445,7 @@ struct MmaConsumer {
     }
     // Value words (dims mt*16 + r and + 8, tokens tt*16 + 4c .. +3) do not
     // depend on the weights: read them before the softmax.
+    // (Those of the unit's first kv head; the others' are read in their turn.)
     uint32_t wv[NT2][NMT][2];
 #pragma unroll
     for (int tt = 0; tt < NT2; ++tt)
@@ -475,26 +483,43 @@ struct MmaConsumer {
       acc[mt][0][2] *= alpha[0];
       acc[mt][0][3] *= alpha[1];
     }
+    // The weights' B fragments per tile (quads c >= 2 find their tokens 4c,
+    // 4c+1 in score rows 2c+8, 2c+9), and the value bytes each tile keeps:
+    // slots past the sequence end hold arbitrary codes (E4M3 has NaNs), which
+    // are cleared so that 0 * NaN cannot reach the accumulator.
+    uint32_t bw[NT2][2], vmask[NT2];
 #pragma unroll
     for (int tt = 0; tt < NT2; ++tt) {
-      // Slots past the sequence end hold arbitrary codes (E4M3 has NaNs):
-      // clear those bytes so that 0 * NaN cannot reach the accumulator.
       const int keep = ntok - (tt * 16 + c * 4);
-      const uint32_t vmask = keep >= 4 ? 0xffffffffu : (keep <= 0 ? 0u : (1u << (8 * keep)) - 1u);
+      vmask[tt] = keep >= 4 ? 0xffffffffu : (keep <= 0 ? 0u : (1u << (8 * keep)) - 1u);
       const uint32_t p0 = F16Traits<__half>::pack(sc[tt][0], sc[tt][1]);
       const uint32_t p1 = F16Traits<__half>::pack(sc[tt][2], sc[tt][3]);
-      uint32_t b0 = movmatrix_trans(p0), b1 = movmatrix_trans(p1);
-      // Quads c >= 2 find their tokens 4c, 4c+1 in score rows 2c+8, 2c+9.
-      if (c >= 2) {
-        const uint32_t t = b0;
-        b0 = b1;
-        b1 = t;
-      }
+      const uint32_t b0 = movmatrix_trans(p0), b1 = movmatrix_trans(p1);
+      bw[tt][0] = c >= 2 ? b1 : b0;
+      bw[tt][1] = c >= 2 ? b0 : b1;
+    }
 #pragma unroll
-      for (int mt = 0; mt < NMT; ++mt) {
-        const uint32_t v0 = wv[tt][mt][0] & vmask, v1 = wv[tt][mt][1] & vmask;
-        const uint32_t a[4] = {e4m3x2(v0), e4m3x2(v1), e4m3x2(v0 >> 16), e4m3x2(v1 >> 16)};
-        Mma<__half>::run(acc[mt][0], a, b0, b1);
+    for (int u = 0; u < KVU; ++u) {
+      if (u > 0) {
+#pragma unroll
+        for (int tt = 0; tt < NT2; ++tt)
+#pragma unroll
+          for (int mt = 0; mt < NMT; ++mt) {
+            wv[tt][mt][0] = lds32(vb[tt] + u * KTILE + (mt * 16 + r) * BS + c * 4);
+            wv[tt][mt][1] = lds32(vb[tt] + u * KTILE + (mt * 16 + r + 8) * BS + c * 4);
+          }
+      }
+      // kv head u's value product takes the weight columns of its own query heads.
+      const bool mine = KVU == 1 || ub == u;
+#pragma unroll
+      for (int tt = 0; tt < NT2; ++tt) {
+        const uint32_t b0 = mine ? bw[tt][0] : 0u, b1 = mine ? bw[tt][1] : 0u;
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+          const uint32_t v0 = wv[tt][mt][0] & vmask[tt], v1 = wv[tt][mt][1] & vmask[tt];
+          const uint32_t a[4] = {e4m3x2(v0), e4m3x2(v1), e4m3x2(v0 >> 16), e4m3x2(v1 >> 16)};
+          Mma<__half>::run(acc[mt][0], a, b0, b1);
+        }
       }
     }
   }

@@ -30,7 +30,7 @@ def run_fp8(q, kc, vc, bt, lens, scale, k_scale, v_scale, P):
 CASES = [  # (H, KH, D, BS, qdtype)
     (4, 4, 128, 16, torch.float16), (8, 2, 128, 16, torch.bfloat16), (16, 2, 128, 32, torch.float16),
     (8, 2, 64, 16, torch.float16), (8, 2, 64, 32, torch.bfloat16), (4, 2, 256, 16, torch.bfloat16),
-    (8, 8, 256, 32, torch.float16),
+    (8, 8, 256, 32, torch.float16), (12, 3, 128, 16, torch.bfloat16), (16, 4, 64, 32, torch.float16),
 ]
 
 
