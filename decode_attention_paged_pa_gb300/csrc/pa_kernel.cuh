@@ -577,11 +577,10 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     // time.  The grouping depends only on the partition and head group, never
     // on which CTA runs the unit or on the other sequences of the batch, so a
     // sequence's output is bitwise the same in any batch.  An item is one
-    // block, or for the tensor-core consumer two consecutive blocks: 8-token
-    // blocks of a 16-bit cache (one 16-token tile of the products), 16-token
-    // blocks of an fp8 cache with one kv head per unit (two tiles, one softmax
-    // update; with two kv heads a block is already twice the work).
-    constexpr int PB = (C::kMma && ((BS == 8 && !C::kFp8) || (BS == 16 && C::kFp8 && C::KVU == 1))) ? 2 : 1;
+    // block, or two consecutive blocks where the consumer says so
+    // (kItemBlocks: one 16-token tile of 8-token blocks, or one softmax update
+    // over two 16-token tiles).
+    constexpr int PB = C::kItemBlocks;
     const int u_id = I.p * prm.n_hg + I.hg;
     const int nitem = (I.nb + PB - 1) / PB;
     for (int it = (warp + NC - u_id % NC) % NC; it < nitem; it += NC) {

@@ -95,6 +95,12 @@ struct MmaConsumer {
   // 16-token tiles per block.  An 8-token block fills half of one tile: the
   // score rows of tokens 8..15 are masked and their value columns are zero.
   static constexpr int NTT = BS >= 16 ? BS / 16 : 1;
+  // Blocks per work item: a pair for 8-token 16-bit blocks (one 16-token
+  // tile), for 16-token blocks of 16 query rows (two column tiles: the
+  // softmax and rescale then serve 32 tokens) and for 16-token fp8 blocks of
+  // one kv head (one softmax update over two tiles); one otherwise.
+  static constexpr int kItemBlocks = (BS == 8 && !FP8_) ? 2
+                                     : (BS == 16 && ((FP8_ && KVU_ == 1) || (!FP8_ && NT_ == 2))) ? 2 : 1;
   static_assert(D % 16 == 0 && (BS == 8 || BS % 16 == 0), "head size a multiple of 16; block 8 or 16k");
   static_assert(!FP8_ || BS % 16 == 0, "fp8 caches take blocks of 16k tokens");
   static constexpr int SCRATCH_FLOATS = 0;
@@ -246,7 +252,18 @@ struct MmaConsumer {
       fp8_tiles<NTT>(kb, vb, ntok, lane, tok0);
       return;
     }
-    tiles(ks, vs, nullptr, nullptr, ntok, lane, tok0);
+    if constexpr (!kFp8) {
+      // The NTT tiles of one block (an 8-token block: half a tile).
+      uint32_t kt[NTT], vt[NTT];
+      int vc[NTT];
+#pragma unroll
+      for (int tt = 0; tt < NTT; ++tt) {
+        kt[tt] = smem_addr(ks) + tt * 16 * 16;
+        vt[tt] = smem_addr(vs);
+        vc[tt] = 2 * tt;
+      }
+      tiles<NTT>(kt, vt, vc, false, vs, ntok, ntok, lane, tok0);
+    }
   }
 
   // Two consecutive 8-token blocks of a unit as one 16-token tile: block A
@@ -260,27 +277,37 @@ struct MmaConsumer {
       const uint32_t kb[2] = {smem_addr(ksA), smem_addr(ksB)};
       const uint32_t vb[2] = {smem_addr(vsA), smem_addr(vsB)};
       fp8_tiles<2>(kb, vb, ntok, lane, tok0);
+    } else if constexpr (BS == 8) {
+      // One tile: K fragment rows 8..15 (lanes 8..15, 24..31) and V fragment
+      // token columns 8..15 (lanes 16..31) come from block B.
+      const uint32_t kt[1] = {smem_addr((lane & 8) ? ksB : ksA)};
+      const uint32_t vt[1] = {smem_addr((lane >> 4) ? vsB : vsA)};
+      const int vc[1] = {0};
+      tiles<1>(kt, vt, vc, true, vsB, ntok - 8, ntok, lane, tok0);
     } else {
-      static_assert(BS == 8, "16-bit pairs are 8-token blocks");
-      tiles(ksA, vsA, ksB, vsB, ntok, lane, tok0);
+      static_assert(BS == 16, "16-bit pairs are 8- or 16-token blocks");
+      const uint32_t kt[2] = {smem_addr(ksA), smem_addr(ksB)};
+      const uint32_t vt[2] = {smem_addr(vsA), smem_addr(vsB)};
+      const int vc[2] = {0, 0};
+      tiles<2>(kt, vt, vc, false, vsB, ntok - 16, ntok, lane, tok0);
     }
   }
 
-  // The 16-bit products over the NTT tiles of one block, or over the tile
-  // made of 8-token blocks A and B (ksB == nullptr: B absent, rows 8..15 of
-  // the tile repeat A's and are masked, their value columns are zero).
-  __device__ __forceinline__ void tiles(const uint8_t* ks, uint8_t* vs, const uint8_t* ksB, uint8_t* vsB,
-                                        int ntok, int lane, int tok0) {
-    const uint32_t kbase = smem_addr(ks), vbase = smem_addr(vs);
-    const bool has_b = BS < 16 && ksB != nullptr;
-    // 8-token blocks: the K fragment rows 8..15 (lanes 8..15, 24..31) and the
-    // V fragment token columns 8..15 (lanes 16..31) come from block B.
-    const uint32_t krow = (BS < 16 && has_b && (lane & 8)) ? smem_addr(ksB) : kbase;
-    const uint32_t vcol = (BS < 16 && has_b && (lane >> 4)) ? smem_addr(vsB) : vbase;
+  // The 16-bit products over the NTI 16-token tiles of one work item (tokens
+  // 16 tt .. 16 tt + 15 of the item in tile tt): this lane's ldmatrix rows of
+  // tile tt's keys at kt[tt] + (chunk * BS + row) * 16, its value columns in
+  // the 16-byte chunk vc[tt] + (lane >> 4) of the dim rows at vt[tt].  8-token
+  // blocks (NTI = 1) fill one tile from two blocks through the lanes'
+  // addresses; without block B (has_b false) rows 8..15 repeat A's and are
+  // masked, their value columns are zero.  vz: the value block whose tokens
+  // nz .. BS - 1 lie past the sequence end (none if nz >= BS).
+  template <int NTI>
+  __device__ __forceinline__ void tiles(const uint32_t (&kt)[NTI], const uint32_t (&vt)[NTI], const int (&vc)[NTI],
+                                        bool has_b, uint8_t* vz, int nz, int ntok, int lane, int tok0) {
     const int r = lane >> 2;
-    float sc[NTT][NT][4];
+    float sc[NTI][NT][4];
 #pragma unroll
-    for (int tt = 0; tt < NTT; ++tt) {
+    for (int tt = 0; tt < NTI; ++tt) {
       // Two accumulators (even / odd k-steps) per column tile halve the
       // dependent mma chain.
       float c[NT][4], c2[NT][4];
@@ -291,11 +318,11 @@ struct MmaConsumer {
 #pragma unroll
       for (int kk = 0; kk < NK; ++kk) {
         // (An 8-token block: rows 8..15 are block B's, or repeat rows 0..7 and are masked below.)
-        const int tok = tt * 16 + (lane & (BS >= 16 ? 15 : 7)), chunk = 2 * kk + (lane >> 4);
+        const int tok = lane & (BS >= 16 ? 15 : 7), chunk = 2 * kk + (lane >> 4);
 #pragma unroll
         for (int u = 0; u < KVU; ++u) {
           uint32_t a[4];
-          ldmatrix_x4(krow + u * KTILE + (chunk * BS + tok) * 16, a);
+          ldmatrix_x4(kt[tt] + u * KTILE + (chunk * BS + tok) * 16, a);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             if ((kk * KVU + u) & 1) Mma<T>::run(c2[t], a, qb[kk][t * KVU + u][0], qb[kk][t * KVU + u][1]);
@@ -321,7 +348,7 @@ struct MmaConsumer {
       for (int j = 0; j < 2; ++j) {
         float bm = fmaxf(sc[0][t][j], sc[0][t][j + 2]);
 #pragma unroll
-        for (int tt = 1; tt < NTT; ++tt) bm = fmaxf(bm, fmaxf(sc[tt][t][j], sc[tt][t][j + 2]));
+        for (int tt = 1; tt < NTI; ++tt) bm = fmaxf(bm, fmaxf(sc[tt][t][j], sc[tt][t][j + 2]));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
@@ -333,7 +360,7 @@ struct MmaConsumer {
         m[t][j] = mn;
         float ps = 0.f;
 #pragma unroll
-        for (int tt = 0; tt < NTT; ++tt) {
+        for (int tt = 0; tt < NTI; ++tt) {
           sc[tt][t][j] = exp2f(sc[tt][t][j] - ms);
           sc[tt][t][j + 2] = exp2f(sc[tt][t][j + 2] - ms);
           ps += sc[tt][t][j] + sc[tt][t][j + 2];
@@ -352,8 +379,6 @@ struct MmaConsumer {
     // Slots past the sequence end hold arbitrary cache contents; zero them
     // so that 0 * (NaN or Inf) cannot reach the accumulator (for a pair, in
     // block B, the one that can be partial).
-    uint8_t* vz = has_b ? vsB : vs;
-    const int nz = has_b ? ntok - 8 : ntok;
     if (nz < BS) {
 #pragma unroll
       for (int u = 0; u < KVU; ++u)
@@ -365,7 +390,7 @@ struct MmaConsumer {
       __syncwarp();
     }
 #pragma unroll
-    for (int tt = 0; tt < NTT; ++tt) {
+    for (int tt = 0; tt < NTI; ++tt) {
       // P fragment rows = tokens, cols = heads; transpose to the B operand.
       // bf16 keeps 8 significant bits, so a weight rounded once can be off by
       // 2^-9 of itself: enough, over a handful of tokens, to miss the parity
@@ -393,8 +418,8 @@ struct MmaConsumer {
 #pragma unroll
         for (int mt = 0; mt < NMT; ++mt) {
           uint32_t a[4];
-          const int chunk = tt * 2 + (BS >= 16 ? (lane >> 4) : 0);
-          ldmatrix_x4(vcol + u * KTILE + vchunk(mt * 16 + (lane & 15), chunk), a);
+          const int chunk = vc[tt] + (BS >= 16 ? (lane >> 4) : 0);
+          ldmatrix_x4(vt[tt] + u * KTILE + vchunk(mt * 16 + (lane & 15), chunk), a);
           if (BS < 16 && !has_b) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
 #pragma unroll
           for (int t = 0; t < NT; ++t) {

@@ -28,6 +28,7 @@ struct SimtConsumer {
   static constexpr uint32_t KTILE = (uint32_t)D_ * BS_ * sizeof(T_);
   static constexpr uint32_t KREGION = KTILE, STAGE_BYTES = 2 * KTILE, STAGE_TX = 2 * KTILE;
   static constexpr int KVU = 1;  // kv heads per unit
+  static constexpr int kItemBlocks = 1;  // blocks per work item
   static constexpr uint32_t KBLK = KTILE;
   static constexpr int EPC = elems_per_chunk<T_>();  // elements per 16-byte chunk
   // q.k: each lane takes QKD dims of one token; LPT lanes share a token
