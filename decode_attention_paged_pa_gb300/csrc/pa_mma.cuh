@@ -96,11 +96,10 @@ struct MmaConsumer {
   // score rows of tokens 8..15 are masked and their value columns are zero.
   static constexpr int NTT = BS >= 16 ? BS / 16 : 1;
   // Blocks per work item: a pair for 8-token 16-bit blocks (one 16-token
-  // tile), for 16-token blocks of 16 query rows (two column tiles: the
-  // softmax and rescale then serve 32 tokens) and for 16-token fp8 blocks of
-  // one kv head (one softmax update over two tiles); one otherwise.
-  static constexpr int kItemBlocks = (BS == 8 && !FP8_) ? 2
-                                     : (BS == 16 && ((FP8_ && KVU_ == 1) || (!FP8_ && NT_ == 2))) ? 2 : 1;
+  // tile) and for 16-token fp8 blocks of one kv head (one softmax update over
+  // two tiles); one otherwise.  (Pairs of 16-token blocks for units of 16
+  // query rows, two column tiles, were 4% slower on the multi-query batch.)
+  static constexpr int kItemBlocks = (BS == 8 && !FP8_) ? 2 : (BS == 16 && FP8_ && KVU_ == 1) ? 2 : 1;
   static_assert(D % 16 == 0 && (BS == 8 || BS % 16 == 0), "head size a multiple of 16; block 8 or 16k");
   static_assert(!FP8_ || BS % 16 == 0, "fp8 caches take blocks of 16k tokens");
   static constexpr int SCRATCH_FLOATS = 0;
