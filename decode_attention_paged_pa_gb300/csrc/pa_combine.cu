@@ -9,10 +9,7 @@ namespace {
 
 template <typename T, int D>
 cudaError_t go(const CParams& prm, cudaStream_t st) {
-  const int rpc = kCombineWarps / prm.wpr;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)prm.S, (unsigned)((prm.H + rpc - 1) / rpc), 1);
-  cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   // A programmatic dependent of the phase-1 launch just before it on the
@@ -23,6 +20,20 @@ cudaError_t go(const CParams& prm, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (prm.S <= kRowsMaxSeqs && prm.Pmax > 16) {
+    // Rows that a single warp would take in two batches or more: one
+    // persistent CTA per SM (no more than the batch's rows could need).  With
+    // short rows only, the per-sequence grid is as good (its CTAs, 8 rows of
+    // one warp each, are short) and the persistent one lost 0.2-0.9%.
+    const long long rows = (long long)prm.S * prm.H;
+    const int sms = device_sm_count();
+    cfg.gridDim = dim3((unsigned)(rows < sms ? rows : sms), 1, 1);
+    cfg.blockDim = dim3(kRowsWarps * 32, 1, 1);
+    return cudaLaunchKernelEx(&cfg, pa_combine_rows_kernel<T, D>, prm);
+  }
+  const int rpc = kCombineWarps / prm.wpr;
+  cfg.gridDim = dim3((unsigned)prm.S, (unsigned)((prm.H + rpc - 1) / rpc), 1);
+  cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
   return cudaLaunchKernelEx(&cfg, pa_combine_kernel<T, D>, prm);
 }
 
