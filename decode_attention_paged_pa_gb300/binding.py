@@ -268,10 +268,10 @@ MAX_ROWS_PER_LAUNCH = 512
 
 def launches_per_call(num_seqs: int, q_len: int = 1, max_partitions: int = 2) -> int:
     """Kernel launches one call makes (for launch counts in measurements):
-    phase 1 once per MAX_ROWS_PER_LAUNCH sequences, and the phase-2 combine
-    once if a sequence can have more than one partition (``max_partitions`` =
-    ceil(max_blocks_per_seq * block_size / partition_size))."""
-    return max(1, -(-num_seqs // MAX_ROWS_PER_LAUNCH)) + (1 if max_partitions > 1 else 0)
+    the header clear and phase 1 once per MAX_ROWS_PER_LAUNCH sequences, and
+    the phase-2 combine once if a sequence can have more than one partition
+    (``max_partitions`` = ceil(max_blocks_per_seq * block_size / partition_size))."""
+    return 2 * max(1, -(-num_seqs // MAX_ROWS_PER_LAUNCH)) + (1 if max_partitions > 1 else 0)
 
 
 def pa_decode_v2_fp8(out, query, key_cache, value_cache, block_tables, seq_lens, scale: float,

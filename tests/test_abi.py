@@ -123,11 +123,11 @@ def test_binding_launch_count_matches_kernel_limit():
     text = open(os.path.join(ROOT, "decode_attention_paged_pa_gb300", "csrc", "pa_kernel.cuh")).read()
     limit = int(re.search(r"#define PA_MAX_SEQS_PER_LAUNCH (\d+)", text).group(1))
     assert binding.MAX_ROWS_PER_LAUNCH == limit
-    # phase 1 per `limit` sequences, plus the phase-2 combine
-    assert binding.launches_per_call(limit) == 2 and binding.launches_per_call(limit + 1) == 3
-    assert binding.launches_per_call(300, 4) == 2   # multi-query rows share their sequence's launch
+    # the header clear and phase 1 per `limit` sequences, plus the phase-2 combine
+    assert binding.launches_per_call(limit) == 3 and binding.launches_per_call(limit + 1) == 5
+    assert binding.launches_per_call(300, 4) == 3   # multi-query rows share their sequence's launch
     # no phase 2 when no sequence can have two partitions
-    assert binding.launches_per_call(300, 1, max_partitions=1) == 1
+    assert binding.launches_per_call(300, 1, max_partitions=1) == 2
 
 
 def test_fp8_entry_rejects_bad_scales():
