@@ -333,13 +333,16 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     return okp;
   };
 
-  // The work counter is read one unit ahead: the next unit is claimed when
-  // unit k starts streaming, and planned and published once k's first batch
-  // of copies is issued (the atomic has returned by then).  A CTA thus holds
-  // at most the unit it streams and the next one, which keeps the end of the
-  // work even across CTAs.  CTA i's first unit is unit i, without an atomic
-  // (all CTAs start at once, and their first claims would queue on one
-  // word); the counter hands out units gridDim.x, gridDim.x + 1, ...
+  // The work counter is read as late as the ring allows: the next unit is
+  // claimed when unit k's last batch of copies starts, and planned and
+  // published once that batch is issued (the atomic has returned by then,
+  // and the ring still holds up to NSTAGE blocks for the consumers).  A CTA
+  // thus commits to a unit only when it is about to stream it, which keeps
+  // the end of the work even across CTAs (claiming at the start of unit k
+  // left up to two units to a CTA when the counter ran out).  CTA i's first
+  // unit is unit i, without an atomic (all CTAs start at once, and their
+  // first claims would queue on one word); the counter hands out units
+  // gridDim.x, gridDim.x + 1, ...
   int u_cur = blockIdx.x;
   UnitPlan U{};
   bool have = plan_next(u_cur, U);
@@ -348,7 +351,11 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
   ok = publish(U, have);
   while (have && ok) {
     int u_req = 0;
-    if (lane == 0) u_req = atomicAdd(prm.hdr + kHdrWork, 1) + (int)gridDim.x;
+    bool claimed = false;
+    auto claim_next = [&]() {
+      if (lane == 0) u_req = atomicAdd(prm.hdr + kHdrWork, 1) + (int)gridDim.x;
+      claimed = true;
+    };
     bool have_next = false, published_next = false;
     UnitPlan Un{};
     int bids_next = 0;
@@ -363,10 +370,7 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
       const int b32 = (c0 == 0) ? bids : load_block_id<C, MQ>(prm, U, c0, lane);
       const int cend = min(c0 + 32, U.nb);
       for (int jb = c0; jb < cend && ok; jb += BATCH) {
-        if (jb > 0 && !published_next) {
-          publish_next();
-          if (!ok) break;
-        }
+        if (!claimed && jb + BATCH >= U.nb) claim_next();  // the unit's last batch
         if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) {
           ok = false;
           break;
@@ -439,6 +443,7 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
         g += cnt;
       }
     }
+    if (ok && !claimed) claim_next();
     if (ok && !published_next) publish_next();
     U = Un;
     bids = bids_next;
