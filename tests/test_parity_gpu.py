@@ -271,6 +271,21 @@ def test_batch_split_across_launches(variant):
     check_parity(q, kc, vc, bt, L, 0.125, 256, variant, what=f"{S} sequences")
 
 
+@pytest.mark.parametrize("S", [2000, 2100], ids=["rows-2000", "per-sequence-2100"])
+def test_many_sequences_with_long_tables(S):
+    """More than 16 partitions in the table: up to 2048 sequences the combine
+    runs as persistent row groups (each sequence's warps per row from its own
+    partition count, the row-group prefix over all sequences in shared
+    memory), past that as a grid over sequences.  Both match the oracle."""
+    g = torch.Generator().manual_seed(23 + S)
+    lens = torch.randint(1, 300, (S,), generator=g).tolist()
+    for k in range(0, S, 97):
+        lens[k] = 1500  # 24 partitions of 64
+    lens[S - 1] = 0
+    q, kc, vc, bt, L = random_case(24, S=S, H=8, KH=2, D=64, BS=16, lens=lens, num_blocks=4096)
+    check_parity(q, kc, vc, bt, L, 0.125, 64, MMA, what=f"{S} sequences, P = 64")
+
+
 def test_more_than_1024_partitions():
     """600,000 tokens at P = 512 is 1172 partitions; all of them are combined."""
     L, BS, D = 600_000, 16, 64
