@@ -2,7 +2,9 @@
 // (phase 1).
 //
 // Work unit = (sequence s, partition p, head group hg): the tokens
-// [p*P, min((p+1)*P, L)) of s against GT query heads that share one kv head.
+// [p*P, min((p+1)*P, L)) of s against GT query heads that share one kv head
+// (or, for consumers with KVU > 1, the query heads of KVU consecutive kv
+// heads: one block of each of them per ring stage).
 // This is the phase-1 program of the page "paged_attention_v2_triton.py --
 // Triton PagedAttention V2 for BI-V100" (`_paged_attn_v2_partition_kernel`,
 // grid (seq, head, partition)), except that only used partitions become units
@@ -17,9 +19,10 @@
 //     on mbarriers: the key block by a 1-D bulk async copy, the value block by
 //     a 1-D bulk copy or (tensor-core consumer over 16-bit caches, C::kTma) a
 //     3-D tensor copy that lays its rows out in the swizzle of their width;
-//   * warps 0..NC-1 (consumers): block j of unit (p, hg) goes to warp
-//     (j + p * n_hg + hg) % NC (a fixed grouping, so results do not depend on
-//     scheduling), which folds it into its private online-softmax state
+//   * warps 0..NC-1 (consumers): work item j of unit (p, hg) (a block, or two
+//     consecutive blocks: C::kItemBlocks) goes to warp (j + p * n_hg + hg) % NC
+//     (a fixed grouping, so results do not depend on scheduling), which folds
+//     it into its private online-softmax state
 //     (SimtConsumer or MmaConsumer).  The CTA's g-th block (counted over all
 //     its units) lives in ring stage g % NSTAGE.  Warps run at different
 //     speeds, so a fast warp could reach stage g % NSTAGE while the stage's
@@ -54,8 +57,9 @@ static_assert(kMaxSeqsPerLaunch <= 65536, "ranks are kept as 16-bit sequence ind
 
 struct KParams {
   // Tensor map of the value cache (C::kTma consumers only): [NB * KH][D][BS]
-  // elements, box [1][D][BS], shared-memory rows in the swizzle of their
-  // width (BS * 2 bytes: 32, 64 or 128).
+  // elements, box [C::KVU][D][BS] (the unit's kv heads of one block),
+  // shared-memory rows in the swizzle of their width (BS * 2 bytes: 32, 64
+  // or 128).
   CUtensorMap tmv;
   void* out;
   const void* q;
@@ -75,7 +79,7 @@ struct KParams {
   float v_scale;      // multiplies every output: 1, or an fp8 cache's v_scale
   int S, H, KH, G, MB, num_blocks, P, Pmax;
   int hg_per_kv;  // ceil(G / GT)
-  int n_hg;       // KH * hg_per_kv
+  int n_hg;       // head groups per partition: KH * hg_per_kv, or KH / KVU
   long long timeout_ns;
 };
 
