@@ -261,7 +261,7 @@ struct MmaConsumer {
         vt[tt] = smem_addr(vs);
         vc[tt] = 2 * tt;
       }
-      tiles<NTT>(kt, vt, vc, false, vs, ntok, ntok, lane, tok0);
+      tiles<NTT>(kt, vt, vc, false, ntok, lane, tok0);
     }
   }
 
@@ -282,13 +282,13 @@ struct MmaConsumer {
       const uint32_t kt[1] = {smem_addr((lane & 8) ? ksB : ksA)};
       const uint32_t vt[1] = {smem_addr((lane >> 4) ? vsB : vsA)};
       const int vc[1] = {0};
-      tiles<1>(kt, vt, vc, true, vsB, ntok - 8, ntok, lane, tok0);
+      tiles<1>(kt, vt, vc, true, ntok, lane, tok0);
     } else {
       static_assert(BS == 16, "16-bit pairs are 8- or 16-token blocks");
       const uint32_t kt[2] = {smem_addr(ksA), smem_addr(ksB)};
       const uint32_t vt[2] = {smem_addr(vsA), smem_addr(vsB)};
       const int vc[2] = {0, 0};
-      tiles<2>(kt, vt, vc, false, vsB, ntok - 16, ntok, lane, tok0);
+      tiles<2>(kt, vt, vc, false, ntok, lane, tok0);
     }
   }
 
@@ -298,11 +298,11 @@ struct MmaConsumer {
   // the 16-byte chunk vc[tt] + (lane >> 4) of the dim rows at vt[tt].  8-token
   // blocks (NTI = 1) fill one tile from two blocks through the lanes'
   // addresses; without block B (has_b false) rows 8..15 repeat A's and are
-  // masked, their value columns are zero.  vz: the value block whose tokens
-  // nz .. BS - 1 lie past the sequence end (none if nz >= BS).
+  // masked, their value columns are zero.  ntok: the item's tokens that lie
+  // before the sequence end.
   template <int NTI>
   __device__ __forceinline__ void tiles(const uint32_t (&kt)[NTI], const uint32_t (&vt)[NTI], const int (&vc)[NTI],
-                                        bool has_b, uint8_t* vz, int nz, int ntok, int lane, int tok0) {
+                                        bool has_b, int ntok, int lane, int tok0) {
     const int r = lane >> 2;
     float sc[NTI][NT][4];
 #pragma unroll
@@ -375,19 +375,13 @@ struct MmaConsumer {
         acc[mt][t][2] *= alpha[t][0];
         acc[mt][t][3] *= alpha[t][1];
       }
-    // Slots past the sequence end hold arbitrary cache contents; zero them
-    // so that 0 * (NaN or Inf) cannot reach the accumulator (for a pair, in
-    // block B, the one that can be partial).
-    if (nz < BS) {
-#pragma unroll
-      for (int u = 0; u < KVU; ++u)
-        for (int i = lane; i < D * (BS - nz); i += 32) {
-          const int d = i / (BS - nz), t = nz + i % (BS - nz);
-          *reinterpret_cast<uint16_t*>(vz + u * KTILE + vchunk(d, t >> 3) + 2 * (t & 7)) = 0;
-        }
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
+    // Slots past the sequence end hold arbitrary cache contents: the value
+    // fragments' elements of those tokens are zeroed in registers, so that
+    // 0 * (NaN or Inf) cannot reach the accumulator.  A lane's value fragment
+    // covers tokens 2c, 2c + 1 (registers 0, 1) and 2c + 8, 2c + 9
+    // (registers 2, 3) of each tile, c = lane % 4; low halves first.
+    const bool ragged = ntok < 16 * NTI;
+    const int tq = 2 * (lane & 3);
 #pragma unroll
     for (int tt = 0; tt < NTI; ++tt) {
       // P fragment rows = tokens, cols = heads; transpose to the B operand.
@@ -420,6 +414,12 @@ struct MmaConsumer {
           const int chunk = vc[tt] + (BS >= 16 ? (lane >> 4) : 0);
           ldmatrix_x4(vt[tt] + u * KTILE + vchunk(mt * 16 + (lane & 15), chunk), a);
           if (BS < 16 && !has_b) a[2] = a[3] = 0u;  // tokens 8..15 of the tile do not exist
+          if (ragged) {
+            const int t = tt * 16 + tq;
+            const uint32_t k0 = (t < ntok ? 0xffffu : 0u) | (t + 1 < ntok ? 0xffff0000u : 0u);
+            const uint32_t k1 = (t + 8 < ntok ? 0xffffu : 0u) | (t + 9 < ntok ? 0xffff0000u : 0u);
+            a[0] &= k0; a[1] &= k0; a[2] &= k1; a[3] &= k1;
+          }
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             Mma<T>::run(acc[mt][t], a, mine ? b0[t] : 0u, mine ? b1[t] : 0u);
