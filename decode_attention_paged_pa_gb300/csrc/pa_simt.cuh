@@ -156,12 +156,29 @@ struct SimtConsumer {
         for (int ps = 0; ps < NPASS; ++ps) pw[g * BS + ps * TPP + tl] = sc[ps][g];
       }
     }
+    if (ntok < BS) {
+      // Slots past the sequence end hold arbitrary cache contents; zero them
+      // so that 0 * (NaN or Inf) cannot reach the accumulator.  Rows of up to
+      // 32 tokens: a lane clears its dims' tails (no index division; the
+      // head-size-256 batch +0.7%); longer rows: consecutive slots over the
+      // lanes (a lane a row would put every lane's stores in one bank).
+      if constexpr (BS <= 32) {
+        for (int d = lane; d < D; d += 32)
+          for (int t = ntok; t < BS; ++t) {
+            if constexpr (sizeof(T) == 4) reinterpret_cast<uint32_t*>(vs)[d * BS + t] = 0u;
+            else reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+          }
+      } else {
+        for (int i = lane; i < D * (BS - ntok); i += 32) {
+          const int d = i / (BS - ntok), t = ntok + i % (BS - ntok);
+          if constexpr (sizeof(T) == 4) reinterpret_cast<uint32_t*>(vs)[d * BS + t] = 0u;
+          else reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+        }
+      }
+      fence_proxy_async_smem();
+    }
     __syncwarp();
     const int r0 = lane / CPR, c = lane % CPR;
-    // Slots past the sequence end hold arbitrary cache contents: their value
-    // elements are cleared after unpacking, so that 0 * (NaN or Inf) cannot
-    // reach the accumulator (this lane's chunk: tokens c * EPC .. + EPC - 1).
-    const bool ragged = ntok < BS;
     float pv[GT][EPC];
 #pragma unroll
     for (int g = 0; g < GT; ++g)
@@ -176,10 +193,6 @@ struct SimtConsumer {
       const uint4 raw = *reinterpret_cast<const uint4*>(vs + (d * BS + c * EPC) * KV_ESZ);
       float f[EPC];
       unpack_chunk<T>(raw, f);
-      if (ragged) {
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) f[e] = (c * EPC + e < ntok) ? f[e] : 0.f;
-      }
 #pragma unroll
       for (int g = 0; g < GT; ++g)
 #pragma unroll
