@@ -141,8 +141,17 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
-def _stream_handle(stream) -> int | None:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream, like: torch.Tensor | None = None) -> int | None:
+    """The CUDA stream handle to launch on: ``stream`` (a torch stream or a raw
+    handle), else PyTorch's current stream on ``like``'s device (looked up
+    through the raw-stream accessor where PyTorch has one: the public
+    ``torch.cuda.current_stream()`` costs about 3 us a call)."""
     if stream is None:
+        if _raw_stream is not None and like is not None:
+            return _raw_stream(like.get_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -205,14 +214,14 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, seq_lens, sca
         st = lib().pa_decode_v2_lse(
             _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
             _ptr(seq_lens), float(scale), S, H, KH, D, BS, int(partition_size), _DTYPE_CODE_F32[dt],
-            _stream_handle(stream), MB, NB, _ptr(workspace), workspace.numel())
+            _stream_handle(stream, query), MB, NB, _ptr(workspace), workspace.numel())
         if st != PA_OK:
             raise PaError(st, "pa_decode_v2_lse")
         return workspace
     st = lib().pa_decode_v2_ex(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         _ptr(seq_lens), float(scale), S, H, KH, D, BS, int(partition_size), _DTYPE_CODE_F32[dt],
-        _stream_handle(stream), MB, NB, _ptr(workspace), workspace.numel(), int(variant),
+        _stream_handle(stream, query), MB, NB, _ptr(workspace), workspace.numel(), int(variant),
         int(max_ctas), int(timeout_ns))
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2")
@@ -255,7 +264,7 @@ def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, 
     st = lib().pa_decode_v2_mq(
         _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         _ptr(seq_lens), float(scale), S, QL, H, KH, D, BS, int(partition_size), _DTYPE_CODE[dt],
-        _stream_handle(stream), MB, NB, _ptr(workspace), workspace.numel())
+        _stream_handle(stream, query), MB, NB, _ptr(workspace), workspace.numel())
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2_mq")
     return workspace
@@ -311,7 +320,7 @@ def pa_decode_v2_fp8(out, query, key_cache, value_cache, block_tables, seq_lens,
     st = lib().pa_decode_v2_fp8(
         _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         _ptr(seq_lens), float(scale), float(k_scale), float(v_scale), S, H, KH, D, BS,
-        int(partition_size), _DTYPE_CODE[dt], _stream_handle(stream), MB, NB, _ptr(workspace),
+        int(partition_size), _DTYPE_CODE[dt], _stream_handle(stream, query), MB, NB, _ptr(workspace),
         workspace.numel())
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2_fp8")
@@ -348,7 +357,7 @@ def pa_decode_v2_host_io(out_host, query_host, key_cache, value_cache, block_tab
     st = lib().pa_decode_v2_host_io(
         _ptr(out_host), _ptr(query_host), _ptr(key_cache), _ptr(value_cache),
         _ptr(block_tables_host), _ptr(seq_lens_host), float(scale), S, H, KH, D, BS,
-        int(partition_size), _DTYPE_CODE_F32[query_host.dtype], _stream_handle(stream), MB, NB,
+        int(partition_size), _DTYPE_CODE_F32[query_host.dtype], _stream_handle(stream, key_cache), MB, NB,
         _ptr(workspace), workspace.numel())
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2_host_io")
@@ -357,7 +366,7 @@ def pa_decode_v2_host_io(out_host, query_host, key_cache, value_cache, block_tab
 def device_status(workspace: torch.Tensor, stream=None) -> int:
     """Device-side error word of the last call on ``workspace`` (synchronises the stream)."""
     v = ctypes.c_int(0)
-    st = lib().pa_decode_v2_device_status(_ptr(workspace), _stream_handle(stream), ctypes.byref(v))
+    st = lib().pa_decode_v2_device_status(_ptr(workspace), _stream_handle(stream, workspace), ctypes.byref(v))
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2_device_status")
     return int(v.value)
