@@ -141,7 +141,9 @@ int pa_decode_v2(void* out, const void* query, const void* key_cache, const void
  * pa_decode_v2 with tuning controls, for tests and measurement.
  *   variant     PA_VARIANT_*; SIMT takes one query head per pass over the
  *               kv head's blocks (a group of G query heads takes G passes),
- *               MMA up to 8 query heads per pass.  SIMT handles head sizes
+ *               MMA up to 8 query heads per pass (with G = 4, those of two kv
+ *               heads, one block of each per pass; head sizes up to 128,
+ *               blocks of 8, 16 or 32 tokens, an even kv-head count).  SIMT handles head sizes
  *               64/128/256 with blocks of 16 or 32 tokens (other shapes:
  *               PA_ERR_UNSUPPORTED); MMA every supported shape.  AUTO picks
  *               SIMT for G = 1 where it applies, MMA otherwise.
