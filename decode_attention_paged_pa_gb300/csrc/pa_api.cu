@@ -228,10 +228,10 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   const bool wide = variant == PA_VARIANT_MMA && G > kMmaGroup && !kv_fp8 && D <= 128 &&
                     base_shape(D, BS);
   const int gt = (variant == PA_VARIANT_MMA) ? (wide ? kMmaGroupWide : kMmaGroup) : kSimtGroup;
-  // Four query rows per kv head: a unit's 8 columns take two kv heads (one
-  // block copy each for keys and values covers both), head sizes up to 128
-  // and blocks of 8, 16 or 32 tokens.
-  const bool pairs = variant == PA_VARIANT_MMA && !wide && q_len == 1 && G * 2 == kMmaGroup && KH % 2 == 0 &&
+  // Four query rows per kv head (query heads, or multi-query row heads): a
+  // unit's 8 columns take two kv heads (one block copy each for keys and
+  // values covers both), head sizes up to 128 and blocks of 8, 16 or 32 tokens.
+  const bool pairs = variant == PA_VARIANT_MMA && !wide && G * 2 == kMmaGroup && KH % 2 == 0 &&
                      D <= 128 && (BS == 8 || BS == 16 || BS == 32);
   const int kvu = pairs ? 2 : 1;
   const int hg_per_kv = (G + gt - 1) / gt;

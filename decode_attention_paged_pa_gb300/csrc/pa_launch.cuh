@@ -62,7 +62,7 @@ cudaError_t launch_one(const KParams& prm, int max_ctas, cudaStream_t stream) {
   // Multi-query rows run on the tensor-core consumer only (the API routes
   // them there), so the CUDA-core consumer has no multi-query instance.
   auto kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, false>;
-  if constexpr (C::kMma && C::KVU == 1) {
+  if constexpr (C::kMma) {
     if (prm.q_len > 1) kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, true>;
   } else {
     if (prm.q_len > 1) return cudaErrorInvalidValue;

@@ -57,3 +57,24 @@ def test_kv_head_pairs_ignore_garbage_past_the_end(BS):
     out, _ = run(q, kc2, vc2, bt, L, 0.1, 64)
     assert torch.isfinite(out.float()).all()
     assert torch.equal(out, ref_out)
+
+
+MQ_CASES = [(dt, q_len, G, KH, BS) for dt in (torch.float16, torch.bfloat16) for q_len, G in ((2, 2), (4, 1))
+            for KH in (2, 3) for BS in (8, 16, 32)]
+
+
+@pytest.mark.parametrize("dt,q_len,G,KH,BS", MQ_CASES,
+                         ids=[f"{str(c[0])[6:]}-q{c[1]}-G{c[2]}-KH{c[3]}-BS{c[4]}" for c in MQ_CASES])
+def test_kv_head_pairs_multi_query(dt, q_len, G, KH, BS):
+    """Multi-query decode with four row heads per kv head (q_len x G = 4): the
+    unit's 8 columns hold two kv heads' row heads, each masked to its causal
+    limit (an odd kv-head count runs one kv head a unit)."""
+    from test_mq_gpu import mq_case, run_mq
+    lens = [q_len, q_len + 1, 64, 64 + q_len - 1, 65, 700, 1500]
+    q, kc, vc, bt, L = mq_case(9300 + q_len + G + KH + BS, S=len(lens), q_len=q_len, H=G * KH, KH=KH, D=128,
+                               BS=BS, lens=lens, dtype=dt)
+    out, lse = run_mq(q, kc, vc, bt, L, 0.09, 64)
+    ref, ref_lse = oracle.decode_mq(q, kc, vc, bt, L, 0.09, DT_CODE[dt])
+    ok, worst = within_tolerance(out.double().numpy(), ref)
+    assert ok, f"worst excess {worst:.3e}"
+    lse_close(lse.numpy(), ref_lse)
