@@ -28,6 +28,9 @@ definition in ``pa_oracle.c``:
 * :func:`decode_fp8kv` -- decode over an E4M3 (fp8) KV cache with per-tensor
                          k_scale / v_scale (key layout x = 16), and
   :func:`e4m3_decode`   the code -> value map it uses;
+* :func:`decode_mq_fp8kv` -- multi-query decode (the causal rows of
+                         :func:`decode_mq`) over an E4M3 cache (the keys and
+                         values of :func:`decode_fp8kv`);
 * :func:`decode_fp32` -- decode with fp32 query and caches (key layout x = 4).
 
 Inputs are the raw 16-bit patterns of fp16 / bf16 tensors (numpy ``uint16``)
@@ -90,6 +93,9 @@ def _declare(lib):
     lib.pa_oracle_e4m3_decode.restype = c_int
     lib.pa_oracle_decode_fp8kv.argtypes = [dp, dp, up, u8p, u8p, ip, ip, c_double, c_double, c_double] + [c_int] * 8
     lib.pa_oracle_decode_fp8kv.restype = c_int
+    lib.pa_oracle_decode_mq_fp8kv.argtypes = ([dp, dp, up, u8p, u8p, ip, ip, c_double, c_double, c_double]
+                                              + [c_int] * 9)
+    lib.pa_oracle_decode_mq_fp8kv.restype = c_int
     fp = ctypes.POINTER(ctypes.c_float)
     lib.pa_oracle_decode_fp32.argtypes = [dp, dp, fp, fp, fp, ip, ip, c_double] + [c_int] * 7
     lib.pa_oracle_decode_fp32.restype = c_int
@@ -326,6 +332,31 @@ class Oracle:
         return out, lse
 
 
+    def decode_mq_fp8kv(self, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                        k_scale: float, v_scale: float, qdtype: int, nthreads: int = 0):
+        """Multi-query decode (query [S, q_len, H, D]) over E4M3 caches laid out as for
+        decode_fp8kv; returns (out [S, q_len, H, D], lse [S, q_len, H]) in float64."""
+        q = _u16(query)
+        kc, vc = _u8(key_cache), _u8(value_cache)
+        bt, lens = _i32(block_tables), _i32(seq_lens)
+        S, q_len, H, D = q.shape
+        nb, KH, dx, BS, x = kc.shape
+        if x != 16 or dx * x != D or tuple(vc.shape) != (nb, KH, D, BS):
+            raise ValueError("fp8 caches must be [NB, KH, D/16, BS, 16] and [NB, KH, D, BS]")
+        if bt.shape[0] != S or lens.shape[0] != S:
+            raise ValueError("block_tables and seq_lens need one row per sequence")
+        MB = bt.shape[1]
+        out = np.zeros((S, q_len, H, D), dtype=np.float64)
+        lse = np.zeros((S, q_len, H), dtype=np.float64)
+        rc = self.lib.pa_oracle_decode_mq_fp8kv(
+            _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), _ptr(q, ctypes.c_uint16),
+            _ptr(kc, ctypes.c_uint8), _ptr(vc, ctypes.c_uint8), _ptr(bt, ctypes.c_int32),
+            _ptr(lens, ctypes.c_int32), float(np.float32(scale)), float(np.float32(k_scale)),
+            float(np.float32(v_scale)), S, q_len, H, KH, D, BS, MB, qdtype, nthreads)
+        if rc != 0:
+            raise ValueError("oracle decode_mq_fp8kv rejected its arguments")
+        return out, lse
+
     def decode_fp32(self, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
                         nthreads: int = 0):
         """Decode with fp32 query and caches (key_cache [NB, KH, D/4, BS, 4], value_cache
@@ -387,6 +418,10 @@ def e4m3_decode(*args, **kwargs) -> np.ndarray:
 
 def decode_fp8kv(*args, **kwargs):
     return default().decode_fp8kv(*args, **kwargs)
+
+
+def decode_mq_fp8kv(*args, **kwargs):
+    return default().decode_mq_fp8kv(*args, **kwargs)
 
 
 def decode_fp32(*args, **kwargs):

@@ -440,6 +440,61 @@ int pa_oracle_decode_fp8kv(double* out, double* lse, const uint16_t* q, const ui
     return bad ? -1 : 0;
 }
 
+/* Multi-query decode over an fp8 (E4M3) KV cache: the q_len causal rows of
+ * pa_oracle_decode_mq (row i of a sequence of L tokens sees positions
+ * 0 .. L - q_len + i) with the keys and values of pa_oracle_decode_fp8kv
+ * (k_scale * E4M3(K), v_scale * E4M3(V), key layout x = 16).  query, out
+ * [S, q_len, H, D], lse [S, q_len, H] (may be NULL); L < q_len is an error. */
+int pa_oracle_decode_mq_fp8kv(double* out, double* lse, const uint16_t* q, const uint8_t* kc,
+                              const uint8_t* vc, const int32_t* bt, const int32_t* lens,
+                              double scale, double k_scale, double v_scale, int S, int q_len,
+                              int H, int KH, int D, int BS, int MB, int qdtype, int nthreads) {
+    if (S < 0 || q_len <= 0 || H <= 0 || KH <= 0 || H % KH || D <= 0 || D % 16 || BS <= 0 || MB < 0)
+        return -1;
+    int bad = 0;
+    if (nthreads <= 0) nthreads = pa_oracle_max_threads();
+    const long rows = (long)S * q_len * H;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : bad)
+    for (long r = 0; r < rows; ++r) {
+        const int h = (int)(r % H);
+        const int i = (int)((r / H) % q_len);
+        const int s = (int)(r / ((long)H * q_len));
+        double* o_r = out + (size_t)r * D;
+        for (int d = 0; d < D; ++d) o_r[d] = 0.0;
+        if (lse) lse[r] = -INFINITY;
+        const int L = lens[s];
+        if (L < q_len || L > MB * BS) { bad = 1; continue; }
+        const int seen = L - q_len + i + 1;             /* positions 0 .. L - q_len + i */
+        double* z = (double*)malloc(sizeof(double) * (size_t)seen);
+        if (!z) { bad = 1; continue; }
+        const int kh = h / (H / KH);
+        const uint16_t* qrow = q + ((size_t)(s * q_len + i) * H + h) * D;
+        for (int t = 0; t < seen; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += to_double(qrow[d], qdtype) *
+                       (k_scale * e4m3_to_double(kc[key_index_x16(b, kh, d, o, KH, D, BS)]));
+            z[t] = scale * acc;
+        }
+        double mu = -INFINITY;
+        for (int t = 0; t < seen; ++t) if (z[t] > mu) mu = z[t];
+        double den = 0.0;
+        for (int t = 0; t < seen; ++t) { z[t] = exp(z[t] - mu); den += z[t]; }
+        for (int t = 0; t < seen; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            for (int d = 0; d < D; ++d)
+                o_r[d] += z[t] * (v_scale * e4m3_to_double(vc[value_index(b, kh, d, o, KH, D, BS)]));
+        }
+        for (int d = 0; d < D; ++d) o_r[d] /= den;
+        if (lse) lse[r] = mu + log(den);
+        free(z);
+    }
+    return bad ? -1 : 0;
+}
+
 /* key_cache[b, kh, d / x, o, d % x] with x = 16 / sizeof(element) = 4 for
  * four-byte (fp32) elements ([PA-V2]: the launcher's x = 16 / sizeof(dtype)). */
 static size_t key_index_x4(long b, int kh, int d, int o, int KH, int D, int BS) {

@@ -416,6 +416,59 @@ def pin_fp8kv_scales(orc):
     assert np.max(np.abs(c - a)) > 1e-6, "k_scale must matter"
 
 
+
+def _mq_fp8_case(seed, S, q_len, H, KH, D, BS, lens, qdtype=torch.float16):
+    """Random multi-query inputs over E4M3 code caches: query [S, q_len, H, D]."""
+    from pa_testutil import fp8_random_case
+    q, kc, vc, bt, L = fp8_random_case(seed, S=S * q_len, H=H, KH=KH, D=D, BS=BS, lens=list(lens) * q_len,
+                                       qdtype=qdtype)
+    return q.view(S, q_len, H, D).contiguous(), kc, vc, bt[:S].contiguous(), L[:S].contiguous()
+
+
+def pin_mq_fp8kv_textbook(orc):
+    """Special case = textbook: numpy softmax(scale q (k_scale K)^T + causal mask)
+    (v_scale V) per query row, K and V decoded by torch's float8_e4m3fn from
+    token-major views of the caches; row i of L tokens sees positions <= L - q_len + i."""
+    for dt in (FP16, BF16):
+        q, kc, vc, bt, lens = _mq_fp8_case(171 + dt, S=2, q_len=3, H=4, KH=2, D=32, BS=4, lens=[3, 13],
+                                           qdtype=TORCH_DT[dt])
+        out, lse = orc.decode_mq_fp8kv(q, kc, vc, bt, lens, 0.3, 0.5, 2.0, dt)
+        nb, KH, dx, BS, x = kc.shape
+        k_tok = kc.view(torch.float8_e4m3fn).to(torch.float64).permute(0, 3, 1, 2, 4).reshape(nb, BS, KH, dx * x)
+        v_tok = vc.view(torch.float8_e4m3fn).to(torch.float64).permute(0, 3, 1, 2)
+        sc = float(np.float32(0.3))
+        for s in range(2):
+            L = int(lens[s])
+            t = torch.arange(L)
+            b = bt[s].long()[t // BS]
+            K, V = (0.5 * k_tok[b, t % BS]).numpy(), (2.0 * v_tok[b, t % BS]).numpy()
+            for i in range(3):
+                n = L - 3 + i + 1
+                for h in range(4):
+                    z = sc * (K[:n, h // 2, :] @ q[s, i, h].to(torch.float64).numpy())
+                    w = np.exp(z - z.max())
+                    _close(out[s, i, h], (w / w.sum()) @ V[:n, h // 2, :], 1e-13, "fp8 causal textbook")
+                    _close(lse[s, i, h], z.max() + math.log(w.sum()), 1e-13, "fp8 causal lse")
+
+
+def pin_mq_fp8kv_reductions(orc):
+    """Reductions to pinned functions, bitwise: one query row is decode_fp8kv; with
+    unit scales the E4M3 values, exact in fp16, stored in fp16 caches of the x = 8
+    layout give decode_mq's result."""
+    q, kc, vc, bt, lens = _mq_fp8_case(181, S=3, q_len=1, H=6, KH=3, D=32, BS=8, lens=[1, 9, 30])
+    out, lse = orc.decode_mq_fp8kv(q, kc, vc, bt, lens, 0.2, 1.5, 0.75, FP16)
+    ref, ref_lse = orc.decode_fp8kv(q[:, 0], kc, vc, bt, lens, 0.2, 1.5, 0.75, FP16)
+    assert np.array_equal(out[:, 0], ref) and np.array_equal(lse[:, 0], ref_lse), "q_len 1 is decode_fp8kv"
+    q, kc, vc, bt, lens = _mq_fp8_case(191, S=2, q_len=4, H=4, KH=2, D=32, BS=4, lens=[4, 11])
+    out, lse = orc.decode_mq_fp8kv(q, kc, vc, bt, lens, 0.3, 1.0, 1.0, FP16)
+    nb, KH, dx, BS, x = kc.shape
+    k_tok = kc.view(torch.float8_e4m3fn).permute(0, 3, 1, 2, 4).reshape(nb, BS, KH, dx * x).to(torch.float16)
+    v_tok = vc.view(torch.float8_e4m3fn).permute(0, 3, 1, 2).to(torch.float16)
+    kc16, vc16 = caches_from_tokens(k_tok.contiguous(), v_tok.contiguous())
+    ref, ref_lse = orc.decode_mq(q, kc16, vc16, bt, lens, 0.3, FP16)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse), "unit scales are decode_mq on the values"
+
+
 def pin_fp32_textbook(orc):
     """Special case = textbook: numpy softmax(scale q K^T) V (and max + log sum
     of the scores) on fp32 caches whose token-major views come from permuting
@@ -503,5 +556,6 @@ ALL_PINS = [
     pin_lse_golden_two_token, pin_lse_closed_forms, pin_lse_library, pin_lse_partition_identity,
     pin_mq_textbook_causal, pin_mq_uniform_causal_bounds,
     pin_e4m3_library, pin_e4m3_golden, pin_fp8kv_textbook, pin_fp8kv_scales,
+    pin_mq_fp8kv_textbook, pin_mq_fp8kv_reductions,
     pin_fp32_textbook, pin_fp32_equals_16bit,
 ]

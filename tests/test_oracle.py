@@ -56,6 +56,15 @@ MUTANTS = [
     ("fp8_k_scale_dropped", "(k_scale * e4m3_to_double(", "(1.0 * e4m3_to_double(", 1),
     ("fp8_v_scale_dropped", "(v_scale * e4m3_to_double(", "(1.0 * e4m3_to_double(", 1),
     ("fp8_key_x8", "    const int x = 16;\n    return", "    const int x = 8;\n    return", 1),
+    ("mq_fp8_not_causal", "const int seen = L - q_len + i + 1;", "const int seen = L;", 1),
+    ("mq_fp8_causal_off_by_one", "const int seen = L - q_len + i + 1;", "const int seen = L - q_len + i;", 1),
+    ("mq_fp8_first_query_row_only", "const uint16_t* qrow = q + ((size_t)(s * q_len + i) * H + h) * D;",
+     "const uint16_t* qrow = q + ((size_t)(s * q_len) * H + h) * D;", 1),
+    ("mq_fp8_k_scale_dropped", "acc += to_double(qrow[d], qdtype) *\n                       (k_scale *",
+     "acc += to_double(qrow[d], qdtype) *\n                       (1.0 *", 1),
+    ("mq_fp8_v_scale_dropped", "o_r[d] += z[t] * (v_scale *", "o_r[d] += z[t] * (1.0 *", 1),
+    ("mq_fp8_value_read_with_key_layout", "o_r[d] += z[t] * (v_scale * e4m3_to_double(vc[value_index(",
+     "o_r[d] += z[t] * (v_scale * e4m3_to_double(vc[key_index_x16(", 1),
     ("fp32_key_x8", "    const int x = 4;\n    return", "    const int x = 8;\n    return", 1),
     ("fp32_key_read_as_value", "(double)kc[key_index_x4(b, kh, d, o, KH, D, BS)]",
      "(double)kc[value_index(b, kh, d, o, KH, D, BS)]", 1),
