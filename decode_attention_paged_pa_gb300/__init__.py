@@ -9,4 +9,5 @@ from .binding import (  # noqa: F401
     PA_DTYPE_BF16, PA_DTYPE_FP16, PA_DTYPE_FP32, PA_ERR_CUDA, PA_ERR_DEVICE_BOUNDS, PA_ERR_INVALID_ARG,
     PA_ERR_TIMEOUT, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_OK, PA_VARIANT_AUTO, PA_VARIANT_MMA,
     PA_VARIANT_SIMT, PaError, device_status, host_io_workspace_bytes, pa_decode_v2,
-    pa_decode_v2_fp8, pa_decode_v2_host_io, pa_decode_v2_mq, status_string, workspace_bytes, workspace_layout)
+    pa_decode_v2_fp8, pa_decode_v2_host_io, pa_decode_v2_mq, pa_decode_v2_mq_fp8, status_string,
+    workspace_bytes, workspace_layout)

@@ -44,6 +44,7 @@ EXPORTED_SYMBOLS = (
     "pa_decode_v2_lse",
     "pa_decode_v2_mq",
     "pa_decode_v2_fp8",
+    "pa_decode_v2_mq_fp8",
     "pa_decode_v2_workspace_bytes",
     "pa_decode_v2_workspace_layout",
     "pa_decode_v2_host_io",
@@ -87,6 +88,9 @@ def _declare(lib):
     # out, lse, query .. seq_lens, scale, k_scale, v_scale, then pa_decode_v2's from num_seqs on
     lib.pa_decode_v2_fp8.argtypes = [vp, vp] + base[1:7] + [cf, cf] + base[7:]
     lib.pa_decode_v2_fp8.restype = ci
+    # pa_decode_v2_fp8's arguments with q_len after num_seqs
+    lib.pa_decode_v2_mq_fp8.argtypes = [vp, vp] + base[1:7] + [cf, cf, ci, ci] + base[8:]
+    lib.pa_decode_v2_mq_fp8.restype = ci
     lib.pa_decode_v2_host_io.argtypes = base
     lib.pa_decode_v2_host_io.restype = ci
     lib.pa_decode_v2_host_io_workspace_bytes.argtypes = [ci] * 7
@@ -324,6 +328,50 @@ def pa_decode_v2_fp8(out, query, key_cache, value_cache, block_tables, seq_lens,
         workspace.numel())
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2_fp8")
+    return workspace
+
+
+def pa_decode_v2_mq_fp8(out, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                        k_scale: float = 1.0, v_scale: float = 1.0, partition_size: int = 512,
+                        workspace: torch.Tensor | None = None, stream=None, lse: torch.Tensor | None = None):
+    """Multi-query decode over an fp8 (E4M3) KV cache (see include/pa_decode.h):
+    query/out [S, q_len, H, D] fp16 or bf16, each query row i of sequence s
+    attending to positions 0 .. seq_lens[s] - q_len + i; the caches hold E4M3
+    codes as for :func:`pa_decode_v2_fp8`.  ``lse`` (float32 [S, q_len, H]) is
+    optional.  Returns the workspace used."""
+    _check_tensor("query", query, ndim=4)
+    dt = query.dtype
+    if dt not in _DTYPE_CODE:
+        raise TypeError("query must be float16 or bfloat16")
+    _check_tensor("out", out, dt, 4)
+    _check_tensor("key_cache", key_cache, torch.uint8, 5)
+    _check_tensor("value_cache", value_cache, torch.uint8, 4)
+    _check_tensor("block_tables", block_tables, torch.int32, 2)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    S, QL, H, D = query.shape
+    NB, KH, DX, BS, X = key_cache.shape
+    if tuple(out.shape) != (S, QL, H, D) or X != 16 or DX * X != D:
+        raise ValueError("inconsistent query / out / key_cache shapes (fp8 key_cache is [NB, KH, D/16, BS, 16])")
+    if tuple(value_cache.shape) != (NB, KH, D, BS):
+        raise ValueError("value_cache must be [num_blocks, KH, D, BS]")
+    if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables / seq_lens must have num_seqs rows")
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, 3)
+        if tuple(lse.shape) != (S, QL, H):
+            raise ValueError("lse must be [num_seqs, q_len, num_heads]")
+    MB = block_tables.shape[1]
+    if workspace is None:  # (a caller's workspace is checked by the library: PA_ERR_WORKSPACE)
+        workspace = torch.empty(max(workspace_bytes(S * QL, H, KH, D, MB, BS, partition_size), 256), dtype=torch.uint8,
+                                device=query.device)
+    _check_tensor("workspace", workspace, torch.uint8)
+    st = lib().pa_decode_v2_mq_fp8(
+        _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        _ptr(seq_lens), float(scale), float(k_scale), float(v_scale), S, QL, H, KH, D, BS,
+        int(partition_size), _DTYPE_CODE[dt], _stream_handle(stream, query), MB, NB, _ptr(workspace),
+        workspace.numel())
+    if st != PA_OK:
+        raise PaError(st, "pa_decode_v2_mq_fp8")
     return workspace
 
 

@@ -203,7 +203,7 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   if (!supported(D, BS, P)) return PA_ERR_UNSUPPORTED;
   if (kv_fp8 && variant == PA_VARIANT_SIMT) return PA_ERR_UNSUPPORTED;  // fp8 runs on tensor cores
   const bool simt_ok = base_shape(D, BS) || (dtype != PA_DTYPE_FP32 && simt_extra_shape(D, BS));
-  if ((!base_shape(D, BS) && kv_fp8) || (variant == PA_VARIANT_SIMT && !simt_ok)) return PA_ERR_UNSUPPORTED;
+  if (variant == PA_VARIANT_SIMT && !simt_ok) return PA_ERR_UNSUPPORTED;
   // fp32 runs on the CUDA-core family only (single-query, its shapes).
   if (dtype == PA_DTYPE_FP32 &&
       (kv_fp8 || q_len > 1 || variant == PA_VARIANT_MMA || !base_shape(D, BS)))
@@ -298,12 +298,27 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     prm.n_hg = n_hg;
     prm.timeout_ns = timeout_ns > 0 ? timeout_ns : (1LL << 31);
     cudaError_t e;
-    if (kv_fp8 && pairs)
+    if (kv_fp8 && pairs && BS == 8)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma8_gb8_f16(prm, D, max_ctas, st)
+                                 : launch_mma8_gb8_bf16(prm, D, max_ctas, st);
+    else if (kv_fp8 && pairs && (D == 64 || D == 128))
       e = dtype == PA_DTYPE_FP16 ? launch_mma8_g_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma8_g_bf16(prm, D, BS, max_ctas, st);
-    else if (kv_fp8)
+    else if (kv_fp8 && pairs)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma8_gx_f16(prm, D, BS, max_ctas, st)
+                                 : launch_mma8_gx_bf16(prm, D, BS, max_ctas, st);
+    else if (kv_fp8 && BS == 8)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma8_b8_f16(prm, D, max_ctas, st)
+                                 : launch_mma8_b8_bf16(prm, D, max_ctas, st);
+    else if (kv_fp8 && BS == 64)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma8_b64_f16(prm, D, max_ctas, st)
+                                 : launch_mma8_b64_bf16(prm, D, max_ctas, st);
+    else if (kv_fp8 && base_shape(D, BS))
       e = dtype == PA_DTYPE_FP16 ? launch_mma8_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma8_bf16(prm, D, BS, max_ctas, st);
+    else if (kv_fp8)
+      e = dtype == PA_DTYPE_FP16 ? launch_mma8_x_f16(prm, D, BS, max_ctas, st)
+                                 : launch_mma8_x_bf16(prm, D, BS, max_ctas, st);
     else if (wide)
       e = dtype == PA_DTYPE_FP16 ? launch_mma16_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma16_bf16(prm, D, BS, max_ctas, st);
@@ -413,6 +428,19 @@ extern "C" int pa_decode_v2_mq(void* out, float* lse, const void* query, const v
                      num_seqs, q_len, num_heads, num_kv_heads, head_size, block_size,
                      partition_size, dtype, stream, max_blocks_per_seq, num_blocks, workspace,
                      workspace_bytes, PA_VARIANT_AUTO, 0, 0);
+}
+
+extern "C" int pa_decode_v2_mq_fp8(void* out, float* lse, const void* query, const void* key_cache,
+                                   const void* value_cache, const int32_t* block_tables,
+                                   const int32_t* seq_lens, float scale, float k_scale, float v_scale,
+                                   int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_size,
+                                   int block_size, int partition_size, int dtype, void* stream,
+                                   int max_blocks_per_seq, int num_blocks, void* workspace,
+                                   size_t workspace_bytes) {
+  return decode_impl(out, lse, query, key_cache, value_cache, block_tables, seq_lens, scale,
+                     num_seqs, q_len, num_heads, num_kv_heads, head_size, block_size,
+                     partition_size, dtype, stream, max_blocks_per_seq, num_blocks, workspace,
+                     workspace_bytes, PA_VARIANT_AUTO, 0, 0, true, k_scale, v_scale);
 }
 
 extern "C" int pa_decode_v2(void* out, const void* query, const void* key_cache, const void* value_cache,

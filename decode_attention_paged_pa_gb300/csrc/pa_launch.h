@@ -46,9 +46,23 @@ cudaError_t launch_mma_g32_bf16(const KParams& prm, int D, int max_ctas, cudaStr
 // The same over an fp8 (E4M3) KV cache, queries and output fp16 / bf16.
 cudaError_t launch_mma8_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma8_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
-// ... and over pairs of kv heads (4 query heads per kv head, head sizes 64 and 128).
+// (head sizes 64, 128, 256 with 16- or 32-token blocks), at head sizes 80, 96,
+// 112 with 16- or 32-token blocks (_x), and in 8- or 64-token blocks (_b8, _b64).
+cudaError_t launch_mma8_x_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_x_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_b8_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_b8_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_b64_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_b64_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+// ... and over pairs of kv heads (4 query heads per kv head): head sizes 64
+// and 128 with 16- or 32-token blocks, 80, 96, 112 with 16- or 32-token
+// blocks (_gx), and every head size up to 128 in 8-token blocks (_gb8).
 cudaError_t launch_mma8_g_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma8_g_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_gx_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_gx_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_gb8_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
+cudaError_t launch_mma8_gb8_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st);
 
 // Phase 2: the cross-partition combine of every multi-partition row, launched
 // as a programmatic dependent of the phase-1 launch before it on `st`.

@@ -54,7 +54,9 @@ constexpr uint32_t al1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 // 2c+1 and 2c+8, 2c+9; the query fragments use the same assignment), and MMA
 // row i of a 16-token tile holds token kTok(i) below: a lane's value word
 // then covers four consecutive tokens of one dim, and the eight token rows a
-// lane quad reads fall in distinct shared-memory banks.
+// lane quad reads fall in distinct shared-memory banks.  Two 8-token blocks
+// fill one tile (its tokens 0..7 from the first), and a 64-token block runs
+// as two softmax updates of two tiles each.
 // KVU_: kv heads per unit.  With fewer than 8 query heads per kv head (G),
 // the 8 columns of a tile hold the query heads of KVU = 8 / G consecutive kv
 // heads: a stage then holds one block of each of them (the cache keeps the kv
@@ -95,13 +97,12 @@ struct MmaConsumer {
   // 16-token tiles per block.  An 8-token block fills half of one tile: the
   // score rows of tokens 8..15 are masked and their value columns are zero.
   static constexpr int NTT = BS >= 16 ? BS / 16 : 1;
-  // Blocks per work item: a pair for 8-token 16-bit blocks (one 16-token
-  // tile) and for 16-token fp8 blocks of one kv head (one softmax update over
-  // two tiles); one otherwise.  (Pairs of 16-token blocks for units of 16
-  // query rows, two column tiles, were 4% slower on the multi-query batch.)
-  static constexpr int kItemBlocks = (BS == 8 && !FP8_) ? 2 : (BS == 16 && FP8_ && KVU_ == 1) ? 2 : 1;
+  // Blocks per work item: a pair for 8-token blocks (one 16-token tile) and
+  // for 16-token fp8 blocks of one kv head (one softmax update over two
+  // tiles); one otherwise.  (Pairs of 16-token blocks for units of 16 query
+  // rows, two column tiles, were 4% slower on the multi-query batch.)
+  static constexpr int kItemBlocks = (BS == 8) ? 2 : (BS == 16 && FP8_ && KVU_ == 1) ? 2 : 1;
   static_assert(D % 16 == 0 && (BS == 8 || BS % 16 == 0), "head size a multiple of 16; block 8 or 16k");
-  static_assert(!FP8_ || BS % 16 == 0, "fp8 caches take blocks of 16k tokens");
   static constexpr int SCRATCH_FLOATS = 0;
   // Row strides, in elements, of a staged query row and of a handed-over
   // state row: 16 bytes past the row, so that the 8 rows a fragment load or
@@ -242,13 +243,25 @@ struct MmaConsumer {
   __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane, float*,
                                         int tok0) {
     if constexpr (kFp8) {
-      uint32_t kb[NTT], vb[NTT];
+      if constexpr (BS == 8) {
+        // Half a tile: the rows of tokens 8..15 read block A again (masked).
+        fp8_pair8(ks, vs, ks, vs, ntok, lane, tok0);
+      } else {
+        // At most two tiles per softmax update (a 64-token block takes two
+        // updates): the value words of a whole update stay in registers.
+        constexpr int NTU = NTT < 2 ? NTT : 2;
 #pragma unroll
-      for (int tt = 0; tt < NTT; ++tt) {
-        kb[tt] = smem_addr(ks) + tt * 16 * 16;  // token tt*16 of every 16-byte chunk row
-        vb[tt] = smem_addr(vs) + tt * 16;       // token tt*16 of every dim row
+        for (int h = 0; h < NTT / NTU; ++h) {
+          if (h > 0 && ntok <= h * 16 * NTU) break;
+          uint32_t klo[NTU], khi[NTU], vv[NTU];
+#pragma unroll
+          for (int tt = 0; tt < NTU; ++tt) {
+            const int tile = h * NTU + tt;
+            fp8_rows(smem_addr(ks) + tile * 16 * 16, smem_addr(vs) + tile * 16, lane, klo[tt], khi[tt], vv[tt]);
+          }
+          fp8_tiles<NTU>(klo, khi, vv, ntok - h * 16 * NTU, lane, tok0 + h * 16 * NTU);
+        }
       }
-      fp8_tiles<NTT>(kb, vb, ntok, lane, tok0);
       return;
     }
     if constexpr (!kFp8) {
@@ -271,11 +284,14 @@ struct MmaConsumer {
   // (ntok tokens of 17..32 valid) as the two tiles of one work item.
   __device__ __forceinline__ void block_pair(const uint8_t* ksA, uint8_t* vsA, const uint8_t* ksB,
                                              uint8_t* vsB, int ntok, int lane, int tok0) {
-    if constexpr (kFp8) {
-      static_assert(BS == 16, "fp8 pairs are 16-token blocks");
-      const uint32_t kb[2] = {smem_addr(ksA), smem_addr(ksB)};
-      const uint32_t vb[2] = {smem_addr(vsA), smem_addr(vsB)};
-      fp8_tiles<2>(kb, vb, ntok, lane, tok0);
+    if constexpr (kFp8 && BS == 8) {
+      fp8_pair8(ksA, vsA, ksB, vsB, ntok, lane, tok0);
+    } else if constexpr (kFp8) {
+      static_assert(BS == 16, "fp8 pairs are 8- or 16-token blocks");
+      uint32_t klo[2], khi[2], vv[2];
+      fp8_rows(smem_addr(ksA), smem_addr(vsA), lane, klo[0], khi[0], vv[0]);
+      fp8_rows(smem_addr(ksB), smem_addr(vsB), lane, klo[1], khi[1], vv[1]);
+      fp8_tiles<2>(klo, khi, vv, ntok, lane, tok0);
     } else if constexpr (BS == 8) {
       // One tile: K fragment rows 8..15 (lanes 8..15, 24..31) and V fragment
       // token columns 8..15 (lanes 16..31) come from block B.
@@ -430,12 +446,36 @@ struct MmaConsumer {
     }
   }
 
-  // NT2 16-token tiles of E4M3 codes (see the note above the struct): tile tt's
-  // key rows at kb[tt] + (chunk * BS + row) * 16 and value rows at
-  // vb[tt] + dim * BS (the tiles of one block, or two consecutive blocks).
+  // This lane's fragment addresses in a 16-token fp8 tile whose key rows start
+  // at kb (token row t of chunk kk at kb + (kk * BS + t) * 16) and whose value
+  // rows start at vb (dim d at vb + d * BS): its two key rows (MMA rows
+  // lane / 4 and lane / 4 + 8) in chunk 0, and its four tokens in dim row 0.
+  __device__ __forceinline__ static void fp8_rows(uint32_t kb, uint32_t vb, int lane, uint32_t& klo,
+                                                  uint32_t& khi, uint32_t& vv) {
+    const int r = lane >> 2, c = lane & 3;
+    klo = kb + kTok(r) * 16 + c * 4;
+    khi = kb + kTok(r + 8) * 16 + c * 4;
+    vv = vb + c * 4;
+  }
+
+  // One 16-token tile of two 8-token fp8 blocks: tokens 0..7 from block A,
+  // 8..15 from block B (ntok of the 16 before the sequence end).
+  __device__ __forceinline__ void fp8_pair8(const uint8_t* ksA, const uint8_t* vsA, const uint8_t* ksB,
+                                            const uint8_t* vsB, int ntok, int lane, int tok0) {
+    const int r = lane >> 2, c = lane & 3;
+    const int tl = kTok(r), th = kTok(r + 8);
+    const uint32_t klo[1] = {smem_addr(tl < 8 ? ksA : ksB) + (tl & 7) * 16 + c * 4};
+    const uint32_t khi[1] = {smem_addr(th < 8 ? ksA : ksB) + (th & 7) * 16 + c * 4};
+    const uint32_t vv[1] = {smem_addr(c < 2 ? vsA : vsB) + (c & 1) * 4};
+    fp8_tiles<1>(klo, khi, vv, ntok, lane, tok0);
+  }
+
+  // NT2 16-token tiles of E4M3 codes (see the note above the struct), by this
+  // lane's fragment addresses (fp8_rows): its key words of chunk kk at
+  // klo[tt] / khi[tt] + kk * BS * 16, its value word of dim d at vv[tt] + d * BS.
   template <int NT2>
-  __device__ __forceinline__ void fp8_tiles(const uint32_t (&kb)[NT2], const uint32_t (&vb)[NT2], int ntok,
-                                            int lane, int tok0) {
+  __device__ __forceinline__ void fp8_tiles(const uint32_t (&klo)[NT2], const uint32_t (&khi)[NT2],
+                                            const uint32_t (&vv)[NT2], int ntok, int lane, int tok0) {
     const int r = lane >> 2, c = lane & 3;
     const int trow_lo = kTok(r), trow_hi = kTok(r + 8);
     float sc[NT2][4];
@@ -448,8 +488,8 @@ struct MmaConsumer {
         uint32_t wk[NK][2];
 #pragma unroll
         for (int kk = 0; kk < NK; ++kk) {
-          wk[kk][0] = lds32(kb[tt] + u * KTILE + (kk * BS + trow_lo) * 16 + c * 4);
-          wk[kk][1] = lds32(kb[tt] + u * KTILE + (kk * BS + trow_hi) * 16 + c * 4);
+          wk[kk][0] = lds32(klo[tt] + u * KTILE + kk * BS * 16);
+          wk[kk][1] = lds32(khi[tt] + u * KTILE + kk * BS * 16);
         }
 #pragma unroll
         for (int kk = 0; kk < NK; ++kk) {
@@ -475,8 +515,8 @@ struct MmaConsumer {
     for (int tt = 0; tt < NT2; ++tt)
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
-        wv[tt][mt][0] = lds32(vb[tt] + (mt * 16 + r) * BS + c * 4);
-        wv[tt][mt][1] = lds32(vb[tt] + (mt * 16 + r + 8) * BS + c * 4);
+        wv[tt][mt][0] = lds32(vv[tt] + (mt * 16 + r) * BS);
+        wv[tt][mt][1] = lds32(vv[tt] + (mt * 16 + r + 8) * BS);
       }
     float alpha[2];
 #pragma unroll
@@ -529,8 +569,8 @@ struct MmaConsumer {
         for (int tt = 0; tt < NT2; ++tt)
 #pragma unroll
           for (int mt = 0; mt < NMT; ++mt) {
-            wv[tt][mt][0] = lds32(vb[tt] + u * KTILE + (mt * 16 + r) * BS + c * 4);
-            wv[tt][mt][1] = lds32(vb[tt] + u * KTILE + (mt * 16 + r + 8) * BS + c * 4);
+            wv[tt][mt][0] = lds32(vv[tt] + u * KTILE + (mt * 16 + r) * BS);
+            wv[tt][mt][1] = lds32(vv[tt] + u * KTILE + (mt * 16 + r + 8) * BS);
           }
       }
       // kv head u's value product takes the weight columns of its own query heads.

@@ -1,0 +1,25 @@
+// pa_mma8gb8_f16.cu -- instances of the paged decode kernel with the tensor-core
+// (mma.sync) consumer over an fp8 (E4M3) KV cache in 8-token blocks and pairs
+// of kv heads (4 query heads per kv head; head sizes up to 128), queries and
+// output __half.
+#include "pa_launch.cuh"
+#include "pa_mma.cuh"
+
+namespace pa {
+
+template <int D>
+static cudaError_t go(const KParams& prm, int max_ctas, cudaStream_t st) {
+  return launch_one<MmaConsumer<__half, D, 8, true, 1, 2>, mma8_consumer_warps<D>()>(prm, max_ctas, st);
+}
+
+cudaError_t launch_mma8_gb8_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st) {
+  switch (D) {
+    case 64: return go<64>(prm, max_ctas, st);
+    case 80: return go<80>(prm, max_ctas, st);
+    case 96: return go<96>(prm, max_ctas, st);
+    case 112: return go<112>(prm, max_ctas, st);
+    default: return go<128>(prm, max_ctas, st);
+  }
+}
+
+}  // namespace pa

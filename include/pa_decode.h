@@ -198,9 +198,9 @@ int pa_decode_v2_lse(void* out, float* lse, const void* query, const void* key_c
  *   query, out   [num_seqs, num_heads, head_size]   dtype (fp16 or bf16)
  *   k_scale, v_scale   finite fp32 multipliers (PA_ERR_INVALID_ARG otherwise)
  * Every other argument, the workspace, ownership and errors are those of
- * pa_decode_v2_lse.  The tensor-core kernel family runs every group size;
- * head_size must be 64, 128 or 256 and block_size 16 or 32
- * (PA_ERR_UNSUPPORTED otherwise).
+ * pa_decode_v2_lse.  The tensor-core kernel family runs every group size
+ * and every shape pa_decode_v2 takes: head_size 64, 80, 96, 112, 128 or 256,
+ * block_size 8, 16, 32 or 64 (PA_ERR_UNSUPPORTED otherwise).
  */
 int pa_decode_v2_fp8(void* out, float* lse, const void* query, const void* key_cache,
                      const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,
@@ -237,6 +237,30 @@ int pa_decode_v2_mq(void* out, float* lse, const void* query, const void* key_ca
                     float scale, int num_seqs, int q_len, int num_heads, int num_kv_heads,
                     int head_size, int block_size, int partition_size, int dtype, void* stream,
                     int max_blocks_per_seq, int num_blocks, void* workspace, size_t workspace_bytes);
+
+/*
+ * Multi-query decode over an fp8 (E4M3) KV cache: the q_len causal query rows
+ * of pa_decode_v2_mq (row i of sequence s sits at position L - q_len + i and
+ * sees positions 0 .. L - q_len + i) with the caches, scales and element
+ * reading of pa_decode_v2_fp8 (the launcher of "paged_attention_v2_triton.py
+ * -- Triton PagedAttention V2 for BI-V100" takes kv_cache_dtype, k_scale and
+ * v_scale whatever the query rows).
+ *   query, out   [num_seqs, q_len, num_heads, head_size]   dtype (fp16 or bf16)
+ *   key_cache    [num_blocks, num_kv_heads, head_size/16, block_size, 16] uint8
+ *   value_cache  [num_blocks, num_kv_heads, head_size, block_size]        uint8
+ *   lse          NULL, or DEVICE [num_seqs, q_len, num_heads] fp32, written
+ *   k_scale, v_scale   finite fp32 multipliers (PA_ERR_INVALID_ARG otherwise)
+ *   seq_lens     each in [q_len, max_blocks_per_seq*block_size]
+ *   workspace    >= pa_decode_v2_workspace_bytes(num_seqs * q_len, ...) bytes, or NULL
+ * Shapes as for pa_decode_v2_fp8 (PA_ERR_UNSUPPORTED otherwise); every other
+ * argument, the ownership and the errors are those of pa_decode_v2_mq.
+ */
+int pa_decode_v2_mq_fp8(void* out, float* lse, const void* query, const void* key_cache,
+                        const void* value_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                        float scale, float k_scale, float v_scale, int num_seqs, int q_len,
+                        int num_heads, int num_kv_heads, int head_size, int block_size,
+                        int partition_size, int dtype, void* stream, int max_blocks_per_seq,
+                        int num_blocks, void* workspace, size_t workspace_bytes);
 
 /*
  * Bytes of device workspace pa_decode_v2_host_io needs: the workspace of

@@ -137,13 +137,26 @@ def test_fp8_entry_rejects_bad_scales():
                                   ctypes.c_float(ks), ctypes.c_float(vs), 2, 4, 2, 128, 16, 512, 0, None,
                                   4, 8, FAKE, 1 << 30)
         assert st == binding.PA_ERR_INVALID_ARG
+        st = lib.pa_decode_v2_mq_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
+                                     ctypes.c_float(ks), ctypes.c_float(vs), 2, 2, 4, 2, 128, 16, 512, 0, None,
+                                     4, 8, FAKE, 1 << 30)
+        assert st == binding.PA_ERR_INVALID_ARG
+    for q_len in (0, 1025):
+        st = lib.pa_decode_v2_mq_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
+                                     ctypes.c_float(1.0), ctypes.c_float(1.0), 2, q_len, 4, 2, 128, 16, 512, 0,
+                                     None, 4, 8, FAKE, 1 << 30)
+        assert st == binding.PA_ERR_INVALID_ARG, q_len
+    st = lib.pa_decode_v2_mq_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
+                                 ctypes.c_float(1.0), ctypes.c_float(1.0), 2, 2, 4, 2, 128, 16, 512,
+                                 binding.PA_DTYPE_FP32, None, 4, 8, FAKE, 1 << 30)
+    assert st == binding.PA_ERR_UNSUPPORTED
 
 
 def test_shapes_outside_a_family_are_rejected():
     """The tensor-core family takes every shape; the CUDA-core family head sizes
     80/96/112 with 16/32/64-token blocks and 64-token blocks at 64/128 next to
-    its base shapes, never 8-token blocks; fp8 caches take head sizes
-    64/128/256 and blocks of 16 or 32."""
+    its base shapes, never 8-token blocks; fp8 caches take every supported
+    head size and block size, on tensor cores only."""
     lib = binding.lib()
 
     def ex(D, BS, variant):
@@ -157,9 +170,18 @@ def test_shapes_outside_a_family_are_rejected():
         assert ex(D, BS, binding.PA_VARIANT_SIMT) == binding.PA_ERR_UNSUPPORTED, (D, BS)
         assert ex(D, BS, binding.PA_VARIANT_MMA) == binding.PA_OK, (D, BS)
         assert ex(D, BS, binding.PA_VARIANT_AUTO) == binding.PA_OK, (D, BS)
-    for D, BS in ((80, 16), (128, 8), (128, 64)):
+    for D, BS in ((80, 16), (128, 8), (128, 64), (256, 8), (112, 64), (96, 32)):
         st = lib.pa_decode_v2_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
-                                  ctypes.c_float(1.0), ctypes.c_float(1.0), 2, 4, 2, D, BS, 512, 0, None,
+                                  ctypes.c_float(1.0), ctypes.c_float(1.0), 0, 4, 2, D, BS, 512, 0, None,
+                                  4, 8, FAKE, 1 << 30)
+        assert st == binding.PA_OK, (D, BS)
+        st = lib.pa_decode_v2_mq_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
+                                     ctypes.c_float(1.0), ctypes.c_float(1.0), 0, 2, 4, 2, D, BS, 512, 0, None,
+                                     4, 8, FAKE, 1 << 30)
+        assert st == binding.PA_OK, (D, BS)
+    for D, BS in ((48, 16), (128, 24)):
+        st = lib.pa_decode_v2_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
+                                  ctypes.c_float(1.0), ctypes.c_float(1.0), 2, 4, 2, D, BS, 528, 0, None,
                                   4, 8, FAKE, 1 << 30)
         assert st == binding.PA_ERR_UNSUPPORTED, (D, BS)
 
