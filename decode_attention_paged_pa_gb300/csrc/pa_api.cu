@@ -222,9 +222,10 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
   const int G = H / KH;
   if (variant == PA_VARIANT_AUTO)
     variant = ((G == 1 || dtype == PA_DTYPE_FP32) && !kv_fp8 && simt_ok) ? PA_VARIANT_SIMT : PA_VARIANT_MMA;
-  // More than 8 query rows per kv head: the tensor-core instances with two
-  // column tiles (16 rows per unit) read each K/V block once for 16 rows
-  // (head sizes 64 and 128, blocks of 16 or 32 tokens, 16-bit caches).
+  // More than 8 query rows per kv head: the tensor-core instances for units
+  // of 16 rows (the rows on the M side of the products) read each K/V block
+  // once for 16 rows (head sizes 64 and 128, blocks of 16 or 32 tokens,
+  // 16-bit caches).
   const bool wide = variant == PA_VARIANT_MMA && G > kMmaGroup && !kv_fp8 && D <= 128 &&
                     base_shape(D, BS);
   const int gt = (variant == PA_VARIANT_MMA) ? (wide ? kMmaGroupWide : kMmaGroup) : kSimtGroup;

@@ -253,20 +253,26 @@ __device__ __forceinline__ UnitPlan plan_unit(const KParams& prm, const int* pre
   return U;
 }
 
-// This lane's block-table entry among blocks [c0, c0 + 32) of unit U (0 past
-// the unit's end).  An id outside the pool is recorded and replaced by 0, so
-// nothing is read out of bounds.
-template <class C, bool MQ>
-__device__ __forceinline__ int load_block_id(const KParams& prm, const UnitPlan& U, int c0, int lane) {
-  int b = 0;
-  if (c0 + lane < U.nb) {
-    b = __ldg(prm.bt + (size_t)U.s * prm.MB + U.t0 / C::BS + c0 + lane);
-    if ((unsigned)b >= (unsigned)prm.num_blocks) {
-      atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
-      b = 0;
-    }
+// This lane's block-table entry among blocks [c0, c0 + 32) of unit U, as
+// loaded (0 past the unit's end): issuing the load and checking the entry
+// (check_block_id) are split so that the load's latency can overlap other
+// work.
+template <class C>
+__device__ __forceinline__ int fetch_block_id(const KParams& prm, const UnitPlan& U, int c0, int lane) {
+  return (c0 + lane < U.nb) ? __ldg(prm.bt + (size_t)U.s * prm.MB + U.t0 / C::BS + c0 + lane) : 0;
+}
+// An id outside the pool is recorded and replaced by 0, so nothing is read
+// out of bounds.
+__device__ __forceinline__ int check_block_id(const KParams& prm, int b) {
+  if ((unsigned)b >= (unsigned)prm.num_blocks) {
+    atomicCAS(prm.hdr + kHdrError, 0, kErrDeviceBounds);
+    b = 0;
   }
   return b;
+}
+template <class C>
+__device__ __forceinline__ int load_block_id(const KParams& prm, const UnitPlan& U, int c0, int lane) {
+  return check_block_id(prm, fetch_block_id<C>(prm, U, c0, lane));
 }
 
 template <class C, class LY, bool MQ>
@@ -337,21 +343,23 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
     return okp;
   };
 
-  // The work counter is read as late as the ring allows: the next unit is
-  // claimed when unit k's last batch of copies starts, and planned and
-  // published once that batch is issued (the atomic has returned by then,
-  // and the ring still holds up to NSTAGE blocks for the consumers).  A CTA
-  // thus commits to a unit only when it is about to stream it, which keeps
-  // the end of the work even across CTAs (claiming at the start of unit k
-  // left up to two units to a CTA when the counter ran out).  CTA i's first
-  // unit is unit i, without an atomic (all CTAs start at once, and their
-  // first claims would queue on one word); the counter hands out units
-  // gridDim.x, gridDim.x + 1, ...
+  // The work counter is read late: the next unit is claimed when unit k's
+  // second-to-last batch of copies starts (its last, for a unit of one
+  // batch), planned when the last batch starts, with the load of its first
+  // block ids in flight while that batch issues, and published once the
+  // batch is issued.  A CTA thus commits to a unit only shortly before it
+  // streams it, which keeps the end of the work even across CTAs (claiming
+  // at the start of unit k left up to two units to a CTA when the counter
+  // ran out), and the two round trips (the atomic, the block-table load)
+  // stay off the gap between the units' copies.  CTA i's first unit is unit
+  // i, without an atomic (all CTAs start at once, and their first claims
+  // would queue on one word); the counter hands out units gridDim.x,
+  // gridDim.x + 1, ...
   int u_cur = blockIdx.x;
   UnitPlan U{};
   bool have = plan_next(u_cur, U);
   int bids = 0;  // this lane's block id among the unit's first 32 blocks
-  if (have) bids = load_block_id<C, MQ>(prm, U, 0, lane);
+  if (have) bids = load_block_id<C>(prm, U, 0, lane);
   ok = publish(U, have);
   while (have && ok) {
     int u_req = 0;
@@ -360,21 +368,27 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
       if (lane == 0) u_req = atomicAdd(prm.hdr + kHdrWork, 1) + (int)gridDim.x;
       claimed = true;
     };
-    bool have_next = false, published_next = false;
+    bool have_next = false, planned_next = false;
     UnitPlan Un{};
-    int bids_next = 0;
-    auto publish_next = [&]() {
+    int bids_next = 0;  // as fetched: checked when the unit is published
+    auto plan_fetch_next = [&]() {
       const int u_nx = __shfl_sync(0xffffffffu, u_req, 0);
       have_next = plan_next(u_nx, Un);
-      if (have_next) bids_next = load_block_id<C, MQ>(prm, Un, 0, lane);
-      ok = publish(Un, have_next);
-      published_next = true;
+      if (have_next) bids_next = fetch_block_id<C>(prm, Un, 0, lane);
+      planned_next = true;
     };
+    // Batches of the unit: those of its 32-block chunks (a batch never crosses one).
+    const int nbatch = (U.nb / 32) * ((32 + BATCH - 1) / BATCH) + (U.nb % 32 + BATCH - 1) / BATCH;
+    int ib = 0;
     for (int c0 = 0; c0 < U.nb && ok; c0 += 32) {
-      const int b32 = (c0 == 0) ? bids : load_block_id<C, MQ>(prm, U, c0, lane);
+      const int b32 = (c0 == 0) ? bids : load_block_id<C>(prm, U, c0, lane);
       const int cend = min(c0 + 32, U.nb);
-      for (int jb = c0; jb < cend && ok; jb += BATCH) {
-        if (!claimed && jb + BATCH >= U.nb) claim_next();  // the unit's last batch
+      for (int jb = c0; jb < cend && ok; jb += BATCH, ++ib) {
+        if (!claimed && ib + 2 >= nbatch) {
+          claim_next();  // the unit's second-to-last batch (its only one)
+        } else if (claimed && !planned_next && ib + 1 == nbatch) {
+          plan_fetch_next();  // the last batch: the claim issued a batch ago has returned
+        }
         if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) {
           ok = false;
           break;
@@ -448,7 +462,11 @@ __device__ __forceinline__ void producer_loop(const KParams& prm, uint8_t* smem,
       }
     }
     if (ok && !claimed) claim_next();
-    if (ok && !published_next) publish_next();
+    if (ok && !planned_next) plan_fetch_next();
+    if (ok) {
+      if (have_next) bids_next = check_block_id(prm, bids_next);
+      ok = publish(Un, have_next);
+    }
     U = Un;
     bids = bids_next;
     have = have_next;

@@ -10,7 +10,7 @@
 namespace pa {
 
 // Query heads per work unit of each kernel family (the tensor-core family
-// takes 16, two column tiles, where a kv head has more than 8 query rows).
+// takes 16 where a kv head has more than 8 query rows).
 constexpr int kSimtGroup = 1;
 constexpr int kMmaGroup = 8;
 constexpr int kMmaGroupWide = 16;

@@ -5,8 +5,8 @@
 //   S[tokens x heads]  = K[tokens x D] . Q^T[D x heads]       (mma m16n8k16, M = 16 tokens)
 //   O^T[D x heads]    += V^T[D x tokens] . P^T[tokens x heads] (mma m16n8k16, M = 16 dims)
 //
-// with 8 query heads as the N = 8 side of the instruction (NT_ = 2: two such
-// column tiles, 16 heads, share every K and V fragment).  Both cache layouts
+// with 8 query heads as the N = 8 side of the instruction (units of 16 query
+// rows of one kv head take MmaRowConsumer, pa_mma_rows.cuh).  Both cache layouts
 // of the page "paged_attention_v2_triton.py -- Triton PagedAttention V2 for
 // BI-V100" already are the operands ldmatrix wants: a K block [D/8][BS][8]
 // stores 16 bytes (8 dims) of one token contiguously, i.e. one ldmatrix row of
@@ -65,17 +65,16 @@ constexpr uint32_t al1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 // weight (values) columns of the other kv heads zeroed, into the same
 // accumulators.  The softmax, the weights and the stage's waits then serve
 // KVU kv heads at once, and the copies are KVU times larger.
-template <typename T_, int D_, int BS_, bool FP8_ = false, int NT_ = 1, int KVU_ = 1>
+template <typename T_, int D_, int BS_, bool FP8_ = false, int KVU_ = 1>
 struct MmaConsumer {
   using T = T_;
   using MT = typename std::conditional<FP8_, __half, T_>::type;  // operand type of the products
-  static constexpr int NT = NT_;  // 8-head column tiles per unit
+  static constexpr int NT = 1;  // 8-head column tiles per unit
   // kTma: the value block is staged by a swizzled tensor copy.
   static constexpr bool kTma = !FP8_ && BS_ >= 16;
-  static constexpr int D = D_, BS = BS_, GT = 8 * NT_;
-  static_assert(NT_ == 1 || (NT_ == 2 && !FP8_), "one or two column tiles (one over fp8 caches)");
+  static constexpr int D = D_, BS = BS_, GT = 8 * NT;
   static constexpr int KVU = KVU_;
-  static_assert(KVU_ == 1 || (NT_ == 1 && 8 % KVU_ == 0), "kv-head groups: one 8-column tile");
+  static_assert(KVU_ == 1 || 8 % KVU_ == 0, "kv-head groups share one 8-column tile");
   static constexpr bool kMma = true;
   static constexpr bool kFp8 = FP8_;
   static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
@@ -99,8 +98,7 @@ struct MmaConsumer {
   static constexpr int NTT = BS >= 16 ? BS / 16 : 1;
   // Blocks per work item: a pair for 8-token blocks (one 16-token tile) and
   // for 16-token fp8 blocks of one kv head (one softmax update over two
-  // tiles); one otherwise.  (Pairs of 16-token blocks for units of 16 query
-  // rows, two column tiles, were 4% slower on the multi-query batch.)
+  // tiles); one otherwise.
   static constexpr int kItemBlocks = (BS == 8) ? 2 : (BS == 16 && FP8_ && KVU_ == 1) ? 2 : 1;
   static_assert(D % 16 == 0 && (BS == 8 || BS % 16 == 0), "head size a multiple of 16; block 8 or 16k");
   static constexpr int SCRATCH_FLOATS = 0;

@@ -1,15 +1,16 @@
 // pa_mma16_bf16.cu -- instances of the paged decode kernel with the tensor-core
-// (mma.sync) consumer taking 16 query heads (two 8-head column tiles) per unit,
-// for groups of more than 8 query rows per kv head (head sizes 64 and 128: at
-// 256 the accumulators no longer fit the registers), element type __nv_bfloat16.
+// (mma.sync) consumer for units of 16 query rows of one kv head (the rows in
+// the M = 16 side of the products), for groups of more than 8 query rows per
+// kv head (head sizes 64 and 128: at 256 the accumulators no longer fit the
+// registers), element type __nv_bfloat16.
 #include "pa_launch.cuh"
-#include "pa_mma.cuh"
+#include "pa_mma_rows.cuh"
 
 namespace pa {
 
 template <int D, int BS>
 static cudaError_t go(const KParams& prm, int max_ctas, cudaStream_t st) {
-  return launch_one<MmaConsumer<__nv_bfloat16, D, BS, false, 2>, kMmaConsumerWarps>(prm, max_ctas, st);
+  return launch_one<MmaRowConsumer<__nv_bfloat16, D, BS>, kMmaConsumerWarps>(prm, max_ctas, st);
 }
 
 cudaError_t launch_mma16_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st) {

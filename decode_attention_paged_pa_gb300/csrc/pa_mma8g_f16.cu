@@ -9,7 +9,7 @@ namespace pa {
 
 template <int D, int BS>
 static cudaError_t go(const KParams& prm, int max_ctas, cudaStream_t st) {
-  return launch_one<MmaConsumer<__half, D, BS, true, 1, 2>, mma8_consumer_warps<D>()>(prm, max_ctas, st);
+  return launch_one<MmaConsumer<__half, D, BS, true, 2>, mma8_consumer_warps<D>()>(prm, max_ctas, st);
 }
 
 cudaError_t launch_mma8_g_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st) {

@@ -9,7 +9,7 @@ namespace pa {
 
 template <int D>
 static cudaError_t go(const KParams& prm, int max_ctas, cudaStream_t st) {
-  return launch_one<MmaConsumer<__nv_bfloat16, D, 16, false, 1, 2>, kMmaConsumerWarps>(prm, max_ctas, st);
+  return launch_one<MmaConsumer<__nv_bfloat16, D, 16, false, 2>, kMmaConsumerWarps>(prm, max_ctas, st);
 }
 
 cudaError_t launch_mma_g16_bf16(const KParams& prm, int D, int max_ctas, cudaStream_t st) {

@@ -9,7 +9,7 @@ namespace pa {
 
 template <int D>
 static cudaError_t go(const KParams& prm, int max_ctas, cudaStream_t st) {
-  return launch_one<MmaConsumer<__half, D, 32, false, 1, 2>, kMmaConsumerWarps>(prm, max_ctas, st);
+  return launch_one<MmaConsumer<__half, D, 32, false, 2>, kMmaConsumerWarps>(prm, max_ctas, st);
 }
 
 cudaError_t launch_mma_g32_f16(const KParams& prm, int D, int max_ctas, cudaStream_t st) {
