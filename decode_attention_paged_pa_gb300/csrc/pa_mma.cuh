@@ -88,9 +88,12 @@ struct MmaConsumer {
   static constexpr uint32_t KREGION = kTma ? al1024(KBLK) : KBLK;
   static constexpr uint32_t STAGE_BYTES = kTma ? al1024(KREGION + KBLK) : KREGION + KBLK;
   static constexpr uint32_t STAGE_TX = 2 * KBLK;
-  // Blocks the producer warp issues together (one per lane): copies of 2 KB
-  // or less need more of them in flight than the 4 KB ones.
-  static constexpr int kIssueBatch = (KBLK <= 2048) ? 32 : 8;
+  // Blocks the producer warp issues together (one per lane, as their stages
+  // free up): 16, or 32 for copies of 2 KB or less.  (Batches of 4 / 8 / 16
+  // blocks: the multi-query GQA batch 558 / 464 / 459 us, the fp8 one
+  // 298 / 259 / 257 us; the producer re-polls a batch's stages with a
+  // growing back-off, which small batches hit more often.)
+  static constexpr int kIssueBatch = (KBLK <= 2048) ? 32 : 16;
   static constexpr int NK = D / 16;    // k-steps of the score product
   static constexpr int NMT = D / 16;   // 16-dim tiles of the value product
   // 16-token tiles per block.  An 8-token block fills half of one tile: the

@@ -46,7 +46,7 @@ struct MmaRowConsumer {
   static constexpr uint32_t KREGION = al1024(KBLK);
   static constexpr uint32_t STAGE_BYTES = al1024(KREGION + KBLK);
   static constexpr uint32_t STAGE_TX = 2 * KBLK;
-  static constexpr int kIssueBatch = (KBLK <= 2048) ? 32 : 8;
+  static constexpr int kIssueBatch = (KBLK <= 2048) ? 32 : 16;  // as MmaConsumer
   static constexpr int kItemBlocks = 1;
   static constexpr int NK = D / 16;   // k-steps (16 dims) of the score product
   static constexpr int NN = D / 8;    // 8-dim column tiles of the value product
