@@ -31,10 +31,14 @@ cudaError_t go(const CParams& prm, cudaStream_t st) {
     cfg.blockDim = dim3(kRowsWarps * 32, 1, 1);
     return cudaLaunchKernelEx(&cfg, pa_combine_rows_kernel<T, D>, prm);
   }
-  const int rpc = kCombineWarps / prm.wpr;
+  // CTAs of 4 warps where a row takes at most 4 (five CTAs of a 98-register
+  // kernel fit an SM where two of 8 warps did: 20 warps in flight, not 16).
+  const int nw = prm.wpr <= 4 ? 4 : kCombineWarps;
+  const int rpc = nw / prm.wpr;
   cfg.gridDim = dim3((unsigned)prm.S, (unsigned)((prm.H + rpc - 1) / rpc), 1);
-  cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
-  return cudaLaunchKernelEx(&cfg, pa_combine_kernel<T, D>, prm);
+  cfg.blockDim = dim3(nw * 32, 1, 1);
+  if (nw == 4) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<T, D, 4>, prm);
+  return cudaLaunchKernelEx(&cfg, pa_combine_kernel<T, D, kCombineWarps>, prm);
 }
 
 template <typename T>

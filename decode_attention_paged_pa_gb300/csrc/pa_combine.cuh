@@ -49,8 +49,9 @@ struct CParams {
   int q_len, Hu, Gu, G;  // multi-query rows (q_len > 1): row head -> output row
 };
 
-// pa_combine_kernel: 8 warps (with 16, CTAs of 512 threads fit one to an SM
-// by registers and a long-context batch's 448 CTAs ran in three waves).
+// pa_combine_kernel: 8 warps where a row takes 8 of them, 4 otherwise (with
+// 16, CTAs of 512 threads fit one to an SM by registers and a long-context
+// batch's 448 CTAs ran in three waves).
 constexpr int kCombineWarps = 8;
 // pa_combine_rows_kernel: 16 warps, one CTA per SM; batches of up to this many
 // sequences (their row-group prefix is kept in shared memory).
@@ -185,18 +186,18 @@ __device__ __forceinline__ void combine_rows(const CParams& prm, int s, int np, 
   if (lane == 0 && prm.lse) prm.lse[orow] = Mr + logf(total);
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kCombineWarps * 32) pa_combine_kernel(const __grid_constant__ CParams prm) {
-  __shared__ float4 s_acc[kCombineWarps][D / 4];
-  __shared__ float s_m[kCombineWarps], s_t[kCombineWarps];
+template <typename T, int D, int NW>
+__global__ void __launch_bounds__(NW * 32) pa_combine_kernel(const __grid_constant__ CParams prm) {
+  __shared__ float4 s_acc[NW][D / 4];
+  __shared__ float s_m[NW], s_t[NW];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.x;
   const int np = seq_partitions(prm, s);
   if (np <= 1) return;  // finished by phase 1 (or empty: zeros written there)
   // Partition states are phase 1's output.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int rpc = kCombineWarps / prm.wpr;
-  combine_rows<T, D, kCombineWarps>(prm, s, np, prm.wpr, blockIdx.y * rpc, warp, lane, s_acc, s_m, s_t);
+  const int rpc = NW / prm.wpr;
+  combine_rows<T, D, NW>(prm, s, np, prm.wpr, blockIdx.y * rpc, warp, lane, s_acc, s_m, s_t);
 }
 
 // Warps per row of a sequence with np partitions (pa_combine_rows_kernel).
