@@ -31,7 +31,9 @@ definition in ``pa_oracle.c``:
 * :func:`decode_mq_fp8kv` -- multi-query decode (the causal rows of
                          :func:`decode_mq`) over an E4M3 cache (the keys and
                          values of :func:`decode_fp8kv`);
-* :func:`decode_fp32` -- decode with fp32 query and caches (key layout x = 4).
+* :func:`decode_fp32` -- decode with fp32 query and caches (key layout x = 4);
+* :func:`decode_mq_fp32` -- multi-query decode (the causal rows of
+                         :func:`decode_mq`) with fp32 query and caches.
 
 Inputs are the raw 16-bit patterns of fp16 / bf16 tensors (numpy ``uint16``)
 in the page's layouts; the fp32 ``scale`` is widened to double exactly.
@@ -99,6 +101,8 @@ def _declare(lib):
     fp = ctypes.POINTER(ctypes.c_float)
     lib.pa_oracle_decode_fp32.argtypes = [dp, dp, fp, fp, fp, ip, ip, c_double] + [c_int] * 7
     lib.pa_oracle_decode_fp32.restype = c_int
+    lib.pa_oracle_decode_mq_fp32.argtypes = [dp, dp, fp, fp, fp, ip, ip, c_double] + [c_int] * 8
+    lib.pa_oracle_decode_mq_fp32.restype = c_int
     lib.pa_oracle_max_threads.argtypes = []
     lib.pa_oracle_max_threads.restype = c_int
     return lib
@@ -378,6 +382,29 @@ class Oracle:
             raise ValueError("oracle decode_fp32 rejected its arguments")
         return out, lse
 
+    def decode_mq_fp32(self, query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                       nthreads: int = 0):
+        """Multi-query decode (query [S, q_len, H, D]) with fp32 query and caches laid
+        out as for decode_fp32; returns (out [S, q_len, H, D], lse [S, q_len, H]) in float64."""
+        q, kc, vc = _f32(query), _f32(key_cache), _f32(value_cache)
+        bt, lens = _i32(block_tables), _i32(seq_lens)
+        S, q_len, H, D = q.shape
+        nb, KH, dx, BS, x = kc.shape
+        if x != 4 or dx * x != D or tuple(vc.shape) != (nb, KH, D, BS):
+            raise ValueError("fp32 caches must be [NB, KH, D/4, BS, 4] and [NB, KH, D, BS]")
+        if bt.shape[0] != S or lens.shape[0] != S:
+            raise ValueError("block_tables and seq_lens need one row per sequence")
+        MB = bt.shape[1]
+        out = np.zeros((S, q_len, H, D), dtype=np.float64)
+        lse = np.zeros((S, q_len, H), dtype=np.float64)
+        rc = self.lib.pa_oracle_decode_mq_fp32(
+            _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), _ptr(q, ctypes.c_float),
+            _ptr(kc, ctypes.c_float), _ptr(vc, ctypes.c_float), _ptr(bt, ctypes.c_int32),
+            _ptr(lens, ctypes.c_int32), float(np.float32(scale)), S, q_len, H, KH, D, BS, MB, nthreads)
+        if rc != 0:
+            raise ValueError("oracle decode_mq_fp32 rejected its arguments")
+        return out, lse
+
 _default = None
 
 
@@ -426,3 +453,7 @@ def decode_mq_fp8kv(*args, **kwargs):
 
 def decode_fp32(*args, **kwargs):
     return default().decode_fp32(*args, **kwargs)
+
+
+def decode_mq_fp32(*args, **kwargs):
+    return default().decode_mq_fp32(*args, **kwargs)

@@ -552,3 +552,56 @@ int pa_oracle_decode_fp32(double* out, double* lse, const float* q, const float*
     }
     return bad ? -1 : 0;
 }
+
+/* Multi-query decode with fp32 query, caches and result: the q_len causal
+ * rows of pa_oracle_decode_mq (row i of a sequence of L tokens sees positions
+ * 0 .. L - q_len + i) over the fp32 caches of pa_oracle_decode_fp32 (key
+ * layout x = 4).  query, out [S, q_len, H, D], lse [S, q_len, H] (may be
+ * NULL); L < q_len is an error. */
+int pa_oracle_decode_mq_fp32(double* out, double* lse, const float* q, const float* kc, const float* vc,
+                             const int32_t* bt, const int32_t* lens, double scale, int S, int q_len,
+                             int H, int KH, int D, int BS, int MB, int nthreads) {
+    if (S < 0 || q_len <= 0 || H <= 0 || KH <= 0 || H % KH || D <= 0 || D % 4 || BS <= 0 || MB < 0)
+        return -1;
+    int bad = 0;
+    if (nthreads <= 0) nthreads = pa_oracle_max_threads();
+    const long rows = (long)S * q_len * H;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : bad)
+    for (long r = 0; r < rows; ++r) {
+        const int h = (int)(r % H);
+        const int i = (int)((r / H) % q_len);
+        const int s = (int)(r / ((long)H * q_len));
+        double* o_r = out + (size_t)r * D;
+        for (int d = 0; d < D; ++d) o_r[d] = 0.0;
+        if (lse) lse[r] = -INFINITY;
+        const int L = lens[s];
+        if (L < q_len || L > MB * BS) { bad = 1; continue; }
+        const int upto = L - q_len + i + 1;             /* positions 0 .. L - q_len + i */
+        double* z = (double*)malloc(sizeof(double) * (size_t)upto);
+        if (!z) { bad = 1; continue; }
+        const int kh = h / (H / KH);
+        const float* qr = q + ((size_t)(s * q_len + i) * H + h) * D;
+        for (int t = 0; t < upto; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += (double)qr[d] * (double)kc[key_index_x4(b, kh, d, o, KH, D, BS)];
+            z[t] = scale * acc;
+        }
+        double mu = -INFINITY;
+        for (int t = 0; t < upto; ++t) if (z[t] > mu) mu = z[t];
+        double den = 0.0;
+        for (int t = 0; t < upto; ++t) { z[t] = exp(z[t] - mu); den += z[t]; }
+        for (int t = 0; t < upto; ++t) {
+            long b = bt[(size_t)s * MB + t / BS];
+            int o = t % BS;
+            for (int d = 0; d < D; ++d)
+                o_r[d] += z[t] * (double)vc[value_index(b, kh, d, o, KH, D, BS)];
+        }
+        for (int d = 0; d < D; ++d) o_r[d] /= den;
+        if (lse) lse[r] = mu + log(den);
+        free(z);
+    }
+    return bad ? -1 : 0;
+}

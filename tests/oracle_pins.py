@@ -503,6 +503,54 @@ def pin_fp32_equals_16bit(orc):
     assert np.array_equal(lse, orc.lse(q, kc, vc, bt, lens, 0.3, FP16))
 
 
+
+def _mq_f32_case(seed, S, q_len, H, KH, D, BS, lens):
+    """Random multi-query fp32 inputs: query [S, q_len, H, D], caches in the x = 4 layout."""
+    from pa_testutil import f32_random_case
+    q, kc, vc, bt, L = f32_random_case(seed, S=S * q_len, H=H, KH=KH, D=D, BS=BS, lens=list(lens) * q_len)
+    return q.view(S, q_len, H, D).contiguous(), kc, vc, bt[:S].contiguous(), L[:S].contiguous()
+
+
+def pin_mq_fp32_textbook(orc):
+    """Special case = textbook: numpy softmax(scale q K^T + causal mask) V per
+    query row on fp32 caches whose token-major views come from permuting the
+    axes of the x = 4 layout; row i of L tokens sees positions <= L - q_len + i."""
+    q, kc, vc, bt, lens = _mq_f32_case(201, S=2, q_len=3, H=4, KH=2, D=24, BS=4, lens=[3, 14])
+    out, lse = orc.decode_mq_fp32(q, kc, vc, bt, lens, 0.3)
+    nb, KH, dx, BS, x = kc.shape
+    k_tok = kc.to(torch.float64).permute(0, 3, 1, 2, 4).reshape(nb, BS, KH, dx * x)
+    v_tok = vc.to(torch.float64).permute(0, 3, 1, 2)
+    sc = float(np.float32(0.3))
+    for s in range(2):
+        L = int(lens[s])
+        t = torch.arange(L)
+        b = bt[s].long()[t // BS]
+        K, V = k_tok[b, t % BS].numpy(), v_tok[b, t % BS].numpy()
+        for i in range(3):
+            n = L - 3 + i + 1
+            for h in range(4):
+                z = sc * (K[:n, h // 2, :] @ q[s, i, h].to(torch.float64).numpy())
+                w = np.exp(z - z.max())
+                _close(out[s, i, h], (w / w.sum()) @ V[:n, h // 2, :], 1e-13, "fp32 causal textbook")
+                _close(lse[s, i, h], z.max() + math.log(w.sum()), 1e-13, "fp32 causal lse")
+
+
+def pin_mq_fp32_reductions(orc):
+    """Reductions to pinned functions, bitwise: one query row is decode_fp32; fp16
+    values widened to fp32 (exactly) in the x = 4 layout give decode_mq's result
+    on the x = 8 layout."""
+    from pa_testutil import f32_caches_from_tokens
+    q, kc, vc, bt, lens = _mq_f32_case(211, S=3, q_len=1, H=6, KH=3, D=24, BS=8, lens=[1, 9, 30])
+    out, lse = orc.decode_mq_fp32(q, kc, vc, bt, lens, 0.2)
+    ref, ref_lse = orc.decode_fp32(q[:, 0], kc, vc, bt, lens, 0.2)
+    assert np.array_equal(out[:, 0], ref) and np.array_equal(lse[:, 0], ref_lse), "q_len 1 is decode_fp32"
+    q, kc, vc, bt, lens = _mq_case(221, S=2, q_len=4, H=4, KH=2, D=32, BS=4, lens=[4, 11])
+    k_tok, v_tok = token_views(kc, vc)
+    kc4, vc4 = f32_caches_from_tokens(k_tok.float(), v_tok.float())
+    out, lse = orc.decode_mq_fp32(q.float(), kc4, vc4, bt, lens, 0.3)
+    ref, ref_lse = orc.decode_mq(q, kc, vc, bt, lens, 0.3, FP16)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse), "fp16 values in fp32 are decode_mq"
+
 def _tiled_online_forward(q, K, V, scale, tile):
     """softmax(scale q K^T) V by the tiled online softmax of the forward kernel
     of the page "flash_attention.metal -- Flash Attention Metal Shaders" (one
@@ -557,5 +605,5 @@ ALL_PINS = [
     pin_mq_textbook_causal, pin_mq_uniform_causal_bounds,
     pin_e4m3_library, pin_e4m3_golden, pin_fp8kv_textbook, pin_fp8kv_scales,
     pin_mq_fp8kv_textbook, pin_mq_fp8kv_reductions,
-    pin_fp32_textbook, pin_fp32_equals_16bit,
+    pin_fp32_textbook, pin_fp32_equals_16bit, pin_mq_fp32_textbook, pin_mq_fp32_reductions,
 ]

@@ -69,6 +69,13 @@ MUTANTS = [
     ("fp32_key_read_as_value", "(double)kc[key_index_x4(b, kh, d, o, KH, D, BS)]",
      "(double)kc[value_index(b, kh, d, o, KH, D, BS)]", 1),
     ("fp32_weights_dropped", "o_sh[d] += z[t] * (double)vc[", "o_sh[d] += (double)vc[", 1),
+    ("mq_fp32_not_causal", "const int upto = L - q_len + i + 1;", "const int upto = L;", 1),
+    ("mq_fp32_causal_off_by_one", "const int upto = L - q_len + i + 1;", "const int upto = L - q_len + i;", 1),
+    ("mq_fp32_first_query_row_only", "const float* qr = q + ((size_t)(s * q_len + i) * H + h) * D;",
+     "const float* qr = q + ((size_t)(s * q_len) * H + h) * D;", 1),
+    ("mq_fp32_key_read_as_value", "(double)qr[d] * (double)kc[key_index_x4(",
+     "(double)qr[d] * (double)kc[value_index(", 1),
+    ("mq_fp32_weights_dropped", "o_r[d] += z[t] * (double)vc[", "o_r[d] += (double)vc[", 1),
     ("empty_sequence_not_zero", "if (L <= 0) continue;\n        if (L > MB * BS) { bad = 1; continue; }\n        double* z",
      "if (L > MB * BS) { bad = 1; continue; }\n        double* z", 1),
 ]
