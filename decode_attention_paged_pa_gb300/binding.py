@@ -236,13 +236,14 @@ def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, 
                     partition_size: int = 512, workspace: torch.Tensor | None = None, stream=None,
                     lse: torch.Tensor | None = None):
     """Multi-query decode into ``out`` (see include/pa_decode.h): query/out
-    [S, q_len, H, D]; each query row i of sequence s attends to positions
+    [S, q_len, H, D] (fp16, bf16 or fp32, key layout as for
+    :func:`pa_decode_v2`); each query row i of sequence s attends to positions
     0 .. seq_lens[s] - q_len + i.  ``lse`` (float32 [S, q_len, H]) is optional.
     Returns the workspace used."""
     _check_tensor("query", query, ndim=4)
     dt = query.dtype
-    if dt not in _DTYPE_CODE:
-        raise TypeError("query must be float16 or bfloat16")
+    if dt not in _DTYPE_CODE_F32:
+        raise TypeError("query must be float16, bfloat16 or float32")
     _check_tensor("out", out, dt, 4)
     _check_tensor("key_cache", key_cache, dt, 5)
     _check_tensor("value_cache", value_cache, dt, 4)
@@ -250,7 +251,7 @@ def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, 
     _check_tensor("seq_lens", seq_lens, torch.int32, 1)
     S, QL, H, D = query.shape
     NB, KH, DX, BS, X = key_cache.shape
-    if tuple(out.shape) != (S, QL, H, D) or X != 8 or DX * X != D:
+    if tuple(out.shape) != (S, QL, H, D) or X != 16 // query.element_size() or DX * X != D:
         raise ValueError("inconsistent query / out / key_cache shapes")
     if tuple(value_cache.shape) != (NB, KH, D, BS):
         raise ValueError("value_cache must be [num_blocks, KH, D, BS]")
@@ -267,7 +268,7 @@ def pa_decode_v2_mq(out, query, key_cache, value_cache, block_tables, seq_lens, 
     _check_tensor("workspace", workspace, torch.uint8)
     st = lib().pa_decode_v2_mq(
         _ptr(out), _ptr(lse), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
-        _ptr(seq_lens), float(scale), S, QL, H, KH, D, BS, int(partition_size), _DTYPE_CODE[dt],
+        _ptr(seq_lens), float(scale), S, QL, H, KH, D, BS, int(partition_size), _DTYPE_CODE_F32[dt],
         _stream_handle(stream, query), MB, NB, _ptr(workspace), workspace.numel())
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2_mq")

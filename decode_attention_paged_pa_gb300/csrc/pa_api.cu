@@ -77,7 +77,7 @@ bool base_shape(int D, int BS) {
   return (D == 64 || D == 128 || D == 256) && (BS == 16 || BS == 32);
 }
 
-// The CUDA-core family's further 16-bit shapes: head sizes 80, 96, 112 with
+// The CUDA-core family's further shapes: head sizes 80, 96, 112 with
 // blocks of 16, 32 or 64 tokens, and 64-token blocks at head sizes 64, 128.
 bool simt_extra_shape(int D, int BS) {
   return ((D == 80 || D == 96 || D == 112) && (BS == 16 || BS == 32 || BS == 64)) ||
@@ -202,11 +202,11 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     return PA_ERR_INVALID_ARG;
   if (!supported(D, BS, P)) return PA_ERR_UNSUPPORTED;
   if (kv_fp8 && variant == PA_VARIANT_SIMT) return PA_ERR_UNSUPPORTED;  // fp8 runs on tensor cores
-  const bool simt_ok = base_shape(D, BS) || (dtype != PA_DTYPE_FP32 && simt_extra_shape(D, BS));
+  const bool simt_ok = base_shape(D, BS) || simt_extra_shape(D, BS);
   if (variant == PA_VARIANT_SIMT && !simt_ok) return PA_ERR_UNSUPPORTED;
-  // fp32 runs on the CUDA-core family only (single-query, its shapes).
-  if (dtype == PA_DTYPE_FP32 &&
-      (kv_fp8 || q_len > 1 || variant == PA_VARIANT_MMA || !base_shape(D, BS)))
+  // fp32 runs on the CUDA-core family only (its shapes; multi-query rows on
+  // its causal instances).
+  if (dtype == PA_DTYPE_FP32 && (kv_fp8 || variant == PA_VARIANT_MMA || !simt_ok))
     return PA_ERR_UNSUPPORTED;
   if (S == 0) return PA_OK;
   if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens)
@@ -341,8 +341,12 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     else if (variant == PA_VARIANT_MMA)
       e = dtype == PA_DTYPE_FP16 ? launch_mma_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma_bf16(prm, D, BS, max_ctas, st);
+    else if (dtype == PA_DTYPE_FP32 && q_len > 1)
+      e = base_shape(D, BS) ? launch_simt_mq_f32(prm, D, BS, max_ctas, st)
+                            : launch_simtx_mq_f32(prm, D, BS, max_ctas, st);
     else if (dtype == PA_DTYPE_FP32)
-      e = launch_simt_f32(prm, D, BS, max_ctas, st);
+      e = base_shape(D, BS) ? launch_simt_f32(prm, D, BS, max_ctas, st)
+                            : launch_simtx_f32(prm, D, BS, max_ctas, st);
     else if (!base_shape(D, BS))
       e = dtype == PA_DTYPE_FP16 ? launch_simtx_f16(prm, D, BS, max_ctas, st)
                                  : launch_simtx_bf16(prm, D, BS, max_ctas, st);

@@ -592,7 +592,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& prm, uint8_t* smem,
     }
     cons.begin_unit(reinterpret_cast<const T*>(smem + LY::OFF_Q + slot * LY::QSLOT), I.nh,
                     prm.scale_log2, lane, prm.G);
-    if constexpr (C::kMma)
+    if constexpr (C::kMma || MQ)
       cons.set_limits([&](int h) { return row_limit<MQ>(prm, I.L, I.h0 + h); }, lane);
     fence_proxy_async_smem();  // the query slot is refilled by a bulk copy: same ordering as a stage
     __syncwarp();

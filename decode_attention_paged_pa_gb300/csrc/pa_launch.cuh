@@ -59,13 +59,18 @@ template <class C, int NC>
 cudaError_t launch_one(const KParams& prm, int max_ctas, cudaStream_t stream) {
   using SZ = Sizing<C, NC>;
   using LY = typename SZ::LY;
-  // Multi-query rows run on the tensor-core consumer only (the API routes
-  // them there), so the CUDA-core consumer has no multi-query instance.
-  auto kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, false>;
+  // Multi-query rows run on the tensor-core consumer, and on the CUDA-core
+  // consumer's causal instances (fp32); those have no single-query kernel.
+  void (*kern)(KParams) = nullptr;
   if constexpr (C::kMma) {
-    if (prm.q_len > 1) kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, true>;
+    kern = prm.q_len > 1 ? pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, true>
+                         : pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, false>;
+  } else if constexpr (C::kCausal) {
+    if (prm.q_len <= 1) return cudaErrorInvalidValue;
+    kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, true>;
   } else {
     if (prm.q_len > 1) return cudaErrorInvalidValue;
+    kern = pa_decode_kernel<C, NC, SZ::NS, kCtasPerSm, false>;
   }
   // The shared-memory opt-in is set once per kernel instance and device.
   static std::atomic<uint64_t> opted_in[2] = {};

@@ -23,6 +23,10 @@ cudaError_t launch_simt_f32(const KParams& prm, int D, int BS, int max_ctas, cud
 // 64-token blocks at head sizes 64, 128 (fp16 / bf16).
 cudaError_t launch_simtx_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_simtx_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_simtx_f32(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+// Multi-query rows with fp32 elements: the causal instances, base and further shapes.
+cudaError_t launch_simt_mq_f32(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+cudaError_t launch_simtx_mq_f32(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma16_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);

@@ -76,6 +76,7 @@ struct MmaConsumer {
   static constexpr int KVU = KVU_;
   static_assert(KVU_ == 1 || 8 % KVU_ == 0, "kv-head groups share one 8-column tile");
   static constexpr bool kMma = true;
+  static constexpr bool kCausal = false;  // (every unit is masked by its limits)
   static constexpr bool kFp8 = FP8_;
   static constexpr int KV_ESZ = FP8_ ? 1 : 2;  // bytes per cached element
   // A stage: the key blocks of the unit's KVU kv heads (KTILE bytes each,

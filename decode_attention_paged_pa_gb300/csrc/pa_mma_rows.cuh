@@ -38,6 +38,7 @@ struct MmaRowConsumer {
   static_assert((D_ == 64 || D_ == 128) && (BS_ == 16 || BS_ == 32), "head sizes 64/128, blocks of 16/32");
   static constexpr bool kTma = true;
   static constexpr bool kMma = true;
+  static constexpr bool kCausal = false;  // (every unit is masked by its limits)
   static constexpr bool kFp8 = false;
   static constexpr int KVU = 1;
   static constexpr int KV_ESZ = 2;

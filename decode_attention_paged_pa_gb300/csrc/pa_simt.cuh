@@ -15,11 +15,15 @@
 
 namespace pa {
 
-template <typename T_, int D_, int BS_, int GT_>
+// CAUSAL_: the instance for the causal rows of multi-query decode (each
+// head masked to the positions it may see; used for fp32 elements, whose
+// multi-query rows run on this family).
+template <typename T_, int D_, int BS_, int GT_, bool CAUSAL_ = false>
 struct SimtConsumer {
   using T = T_;
   static constexpr int D = D_, BS = BS_, GT = GT_;
   static constexpr bool kMma = false;
+  static constexpr bool kCausal = CAUSAL_;
   // Blocks the producer warp issues together (MHA batch: 8 / 24 / 32 blocks
   // 363.5 / 355.3 / 359.4 us).
   static constexpr int kIssueBatch = 24;
@@ -55,6 +59,7 @@ struct SimtConsumer {
   float qf[GT][QKD];
   float m[GT], l[GT];
   float acc[GT][NROW];
+  int lim[GT];  // causal instances: positions [0, lim) each head sees
 
   // q rows [GT][D] in shared memory; rows >= nh are treated as zero.
   // Row strides, in elements, of a staged query row and of a handed-over
@@ -86,14 +91,20 @@ struct SimtConsumer {
     }
   }
 
-  // One staged block: ks = K block, vs = V block (shared memory), ntok valid
-  // tokens (1..BS).  pw = this warp's scratch (SCRATCH_FLOATS floats).
-  // Causal rows are multi-query only, which runs on the tensor-core consumer.
+  // Positions each head of the unit may see (causal instances only).
   template <class F>
-  __device__ __forceinline__ void set_limits(F, int) {}
+  __device__ __forceinline__ void set_limits(F limit_of, int) {
+    if constexpr (kCausal) {
+#pragma unroll
+      for (int g = 0; g < GT; ++g) lim[g] = limit_of(g);
+    }
+  }
 
+  // One staged block: ks = K block, vs = V block (shared memory), ntok valid
+  // tokens (1..BS) starting at position tok0.  pw = this warp's scratch
+  // (SCRATCH_FLOATS floats).
   __device__ __forceinline__ void block(const uint8_t* ks, uint8_t* vs, int ntok, int lane,
-                                        float* pw, int /*tok0*/) {
+                                        float* pw, int tok0) {
     const int tl = lane % TPP, slice = lane / TPP;
     float sc[NPASS][GT];
 #pragma unroll
@@ -130,6 +141,9 @@ struct SimtConsumer {
 #pragma unroll
         for (int off = TPP; off < 32; off <<= 1) sc[ps][g] += __shfl_xor_sync(0xffffffffu, sc[ps][g], off);
         if (t >= ntok) sc[ps][g] = -INFINITY;
+        if constexpr (kCausal) {
+          if (tok0 + t >= lim[g]) sc[ps][g] = -INFINITY;
+        }
       }
     }
     // Online softmax update (log2 domain: q carries scale * log2(e)).
@@ -141,12 +155,15 @@ struct SimtConsumer {
 #pragma unroll
       for (int off = 1; off < TPP; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
       const float mn = fmaxf(m[g], bm);
-      const float alpha = exp2f(m[g] - mn);
+      // A causal row that has seen no position yet keeps m = -inf: subtract
+      // 0 instead, so its weights and rescale come out 0, not NaN.
+      const float ms = (kCausal && mn == -INFINITY) ? 0.f : mn;
+      const float alpha = exp2f(m[g] - ms);
       m[g] = mn;
       float psum = 0.f;
 #pragma unroll
       for (int ps = 0; ps < NPASS; ++ps) {
-        const float p = exp2f(sc[ps][g] - mn);
+        const float p = exp2f(sc[ps][g] - ms);
         sc[ps][g] = p;
         psum += p;
       }

@@ -187,7 +187,8 @@ def test_shapes_outside_a_family_are_rejected():
 
 
 def test_fp32_only_on_the_cuda_core_family():
-    """fp32 (dtype 2) runs single-query on the CUDA-core family, its shapes only."""
+    """fp32 (dtype 2) runs on the CUDA-core family, its shapes only (single- and
+    multi-query), never over an fp8 cache."""
     lib = binding.lib()
 
     def ex(D, BS, variant, dtype=binding.PA_DTYPE_FP32):
@@ -197,12 +198,15 @@ def test_fp32_only_on_the_cuda_core_family():
     assert ex(128, 16, binding.PA_VARIANT_AUTO) == binding.PA_OK
     assert ex(128, 16, binding.PA_VARIANT_SIMT) == binding.PA_OK
     assert ex(128, 16, binding.PA_VARIANT_MMA) == binding.PA_ERR_UNSUPPORTED
-    assert ex(96, 16, binding.PA_VARIANT_AUTO) == binding.PA_ERR_UNSUPPORTED
+    assert ex(96, 16, binding.PA_VARIANT_AUTO) == binding.PA_OK
+    assert ex(112, 64, binding.PA_VARIANT_AUTO) == binding.PA_OK
     assert ex(128, 8, binding.PA_VARIANT_AUTO) == binding.PA_ERR_UNSUPPORTED
+    assert ex(96, 16, binding.PA_VARIANT_MMA) == binding.PA_ERR_UNSUPPORTED
     assert ex(128, 16, binding.PA_VARIANT_AUTO, dtype=3) == binding.PA_ERR_INVALID_ARG
-    st = lib.pa_decode_v2_mq(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 2, 4,
-                             4, 2, 128, 16, 512, binding.PA_DTYPE_FP32, None, 4, 8, FAKE, 1 << 30)
-    assert st == binding.PA_ERR_UNSUPPORTED
+    for D, BS, want in ((128, 16, binding.PA_OK), (80, 64, binding.PA_OK), (128, 8, binding.PA_ERR_UNSUPPORTED)):
+        st = lib.pa_decode_v2_mq(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 0, 4,
+                                 4, 2, D, BS, 512, binding.PA_DTYPE_FP32, None, 4, 8, FAKE, 1 << 30)
+        assert st == want, (D, BS)
     st = lib.pa_decode_v2_fp8(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125),
                               ctypes.c_float(1.0), ctypes.c_float(1.0), 2, 4, 2, 128, 16, 512,
                               binding.PA_DTYPE_FP32, None, 4, 8, FAKE, 1 << 30)

@@ -106,3 +106,53 @@ def test_fp32_rejected_outside_its_family():
         binding.pa_decode_v2(out, q.to(dev), kc.to(dev), vc.to(dev), bt.to(dev), L.to(dev), 0.1,
                              variant=binding.PA_VARIANT_MMA)
     assert e.value.status == binding.PA_ERR_UNSUPPORTED
+
+
+# The CUDA-core family's further shapes with fp32 elements.
+XCASES = [(D, BS, G) for D, BS in ((80, 16), (96, 32), (112, 64), (64, 64), (128, 64), (80, 64)) for G in (1, 2)]
+
+
+@pytest.mark.parametrize("D,BS,G", XCASES, ids=[f"D{c[0]}-BS{c[1]}-G{c[2]}" for c in XCASES])
+def test_fp32_more_shapes(D, BS, G):
+    P = 128
+    lens = [1, BS - 1, BS + 1, 2 * P - 1, 3 * P + 5, 17 * P + 3, 0]
+    KH = 2
+    q, kc, vc, bt, L = f32_random_case(4200 + D + BS + G, S=len(lens), H=KH * G, KH=KH, D=D, BS=BS, lens=lens)
+    out, lse = run(q, kc, vc, bt, L, 1.0 / math.sqrt(D), P, lse=True)
+    ref, ref_lse = oracle.decode_fp32(q, kc, vc, bt, L, 1.0 / math.sqrt(D))
+    ok, worst = within_tolerance(out.double().numpy(), ref, ATOL32, RTOL32)
+    assert ok, f"worst excess {worst:.3e}"
+    assert torch.all(out[-1] == 0)
+    lse_close(lse.numpy(), ref_lse)
+
+
+def run_mq32(q, kc, vc, bt, lens, scale, P):
+    dev = torch.device("cuda")
+    q, kc, vc, bt, lens = (t.to(dev) for t in (q, kc, vc, bt, lens))
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), device=dev)
+    ws = binding.pa_decode_v2_mq(out, q, kc, vc, bt, lens, scale, partition_size=P, lse=lse)
+    assert binding.device_status(ws) == binding.PA_OK
+    return out.cpu(), lse.cpu()
+
+
+MQ32_CASES = [(q_len, G, D, BS) for q_len, G in ((2, 1), (4, 2), (3, 4)) for D, BS in ((128, 16), (64, 32), (96, 64))]
+
+
+@pytest.mark.parametrize("q_len,G,D,BS", MQ32_CASES, ids=[f"q{c[0]}-G{c[1]}-D{c[2]}-BS{c[3]}" for c in MQ32_CASES])
+def test_fp32_multi_query(q_len, G, D, BS):
+    """Multi-query decode with fp32 elements (the CUDA-core family's causal
+    instances): every row masked to its causal limit (L = q_len leaves row 0
+    one token), partition edges inside the causal band, two-level combine."""
+    KH, P = 2, 64
+    lens = [q_len, q_len + 1, P, P + q_len - 1, P + 1, 700, 1500]
+    S = len(lens)
+    q, kc, vc, bt, L = f32_random_case(4300 + q_len + G + D + BS, S=S * q_len, H=KH * G, KH=KH, D=D, BS=BS,
+                                       lens=lens * q_len)
+    q = q.view(S, q_len, KH * G, D).contiguous()
+    bt, L = bt[:S].contiguous(), L[:S].contiguous()
+    out, lse = run_mq32(q, kc, vc, bt, L, 0.09, P)
+    ref, ref_lse = oracle.decode_mq_fp32(q, kc, vc, bt, L, 0.09)
+    ok, worst = within_tolerance(out.double().numpy(), ref, ATOL32, RTOL32)
+    assert ok, f"worst excess {worst:.3e}"
+    lse_close(lse.numpy(), ref_lse)
