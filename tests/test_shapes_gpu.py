@@ -134,8 +134,9 @@ WIDE = [(dt, D, BS, G) for dt in (torch.float16, torch.bfloat16) for D in (64, 1
 
 @pytest.mark.parametrize("dt,D,BS,G", WIDE, ids=[f"{str(c[0])[6:]}-D{c[1]}-BS{c[2]}-G{c[3]}" for c in WIDE])
 def test_parity_wide_groups(dt, D, BS, G):
-    """More than 8 query heads per kv head: units of 16 heads (two column tiles;
-    head size 256 keeps units of 8), partly filled when G is not a multiple of 16."""
+    """More than 8 query heads per kv head: units of 16 heads (the rows on the M
+    side of the products; head size 256 keeps units of 8), partly filled when G
+    is not a multiple of 16."""
     P = 64
     lens = [1, BS + 1, 2 * P - 1, 17 * P + 3]
     KH = 2
@@ -159,6 +160,35 @@ def test_multi_query_wide_units(q_len, G):
     ok, worst = within_tolerance(out.double().numpy(), ref)
     assert ok, f"worst excess {worst:.3e}"
     lse_close(lse.numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("D,BS", [(64, 16), (128, 32), (128, 16)])
+def test_wide_units_ignore_garbage_past_the_end(D, BS):
+    """NaN in every slot past each sequence's end and in unused blocks, under
+    units of 16 query rows: the result is bitwise that of finite contents."""
+    S, KH = 4, 2
+    lens = [3, BS, BS + 5, 200]
+    q, kc, vc, bt, L = random_case(131 + D + BS, S=S, H=16 * KH, KH=KH, D=D, BS=BS, lens=lens)
+    ref_out, _ = run(q, kc, vc, bt, L, 0.1, 64)
+    k_tok, v_tok = token_views(kc, vc)
+    k2, v2 = k_tok.clone(), v_tok.clone()
+    used = set()
+    for s in range(S):
+        for j in range(-(-lens[s] // BS)):
+            b = int(bt[s, j])
+            used.add(b)
+            last = lens[s] - j * BS
+            if last < BS:
+                k2[b, last:] = float("nan")
+                v2[b, last:] = float("nan")
+    for b in range(kc.shape[0]):
+        if b not in used:
+            k2[b] = float("nan")
+            v2[b] = float("nan")
+    kc2, vc2 = caches_from_tokens(k2, v2)
+    out, _ = run(q, kc2, vc2, bt, L, 0.1, 64)
+    assert torch.isfinite(out.float()).all()
+    assert torch.equal(out, ref_out)
 
 
 def test_wide_units_deterministic_across_grid_sizes():
