@@ -80,3 +80,15 @@ def test_unswizzled_rows_would_conflict(BS):
     R = 2 * BS
     groups = [((d * R) // 16) % 8 for d in range(8)]
     assert len(set(groups)) == max(1, 8 * 16 // R) and len(set(groups)) < 8
+
+
+def test_row_consumer_uses_the_same_value_addressing():
+    """The 16-row consumer (pa_mma_rows.cuh) addresses a staged value block by
+    the same expression, so every check above holds for it too."""
+    rows = open(os.path.join(ROOT, "decode_attention_paged_pa_gb300", "csrc", "pa_mma_rows.cuh")).read()
+    body = rows[rows.index("static uint32_t vchunk(int d, int c)"):]
+    expr = re.search(r"\{\s*return (.*?);", body, re.S).group(1)
+    src = open(MMA).read()
+    mma_body = src[src.index("static uint32_t vchunk(int d, int c)"):]
+    mma_expr = re.search(r"if constexpr \(kTma\) \{\s*return (.*?);", mma_body, re.S).group(1)
+    assert " ".join(expr.split()) == " ".join(mma_expr.split())
