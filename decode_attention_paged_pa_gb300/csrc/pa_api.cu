@@ -202,7 +202,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     return PA_ERR_INVALID_ARG;
   if (!supported(D, BS, P)) return PA_ERR_UNSUPPORTED;
   if (kv_fp8 && variant == PA_VARIANT_SIMT) return PA_ERR_UNSUPPORTED;  // fp8 runs on tensor cores
-  const bool simt_ok = base_shape(D, BS) || simt_extra_shape(D, BS);
+  // (8-token blocks on the CUDA cores: fp32 only; the 16-bit types take the tensor cores there.)
+  const bool simt_ok = base_shape(D, BS) || simt_extra_shape(D, BS) || (dtype == PA_DTYPE_FP32 && BS == 8);
   if (variant == PA_VARIANT_SIMT && !simt_ok) return PA_ERR_UNSUPPORTED;
   // fp32 runs on the CUDA-core family only (its shapes; multi-query rows on
   // its causal instances).
@@ -341,6 +342,8 @@ int decode_impl(void* out, float* lse, const void* query, const void* key_cache,
     else if (variant == PA_VARIANT_MMA)
       e = dtype == PA_DTYPE_FP16 ? launch_mma_f16(prm, D, BS, max_ctas, st)
                                  : launch_mma_bf16(prm, D, BS, max_ctas, st);
+    else if (dtype == PA_DTYPE_FP32 && BS == 8)
+      e = launch_simt_b8_f32(prm, D, max_ctas, st);
     else if (dtype == PA_DTYPE_FP32 && q_len > 1)
       e = base_shape(D, BS) ? launch_simt_mq_f32(prm, D, BS, max_ctas, st)
                             : launch_simtx_mq_f32(prm, D, BS, max_ctas, st);

@@ -12,7 +12,8 @@
 //
 // One CTA per SM runs until the units run out:
 //   * warp NC (producer): takes units from a global counter (dynamic
-//     scheduling balances skewed sequence lengths), publishes each unit's
+//     scheduling balances skewed sequence lengths; the next unit is claimed
+//     and planned during the current unit's last batches), publishes each unit's
 //     description and query rows through a 2-slot unit queue, and streams the
 //     unit's physical K and V blocks -- each a contiguous D*BS*(element
 //     size)-byte run in the page's layouts -- into shared memory, completing
@@ -23,7 +24,7 @@
 //     consecutive blocks: C::kItemBlocks) goes to warp (j + p * n_hg + hg) % NC
 //     (a fixed grouping, so results do not depend on scheduling), which folds
 //     it into its private online-softmax state
-//     (SimtConsumer or MmaConsumer).  The CTA's g-th block (counted over all
+//     (SimtConsumer, MmaConsumer or MmaRowConsumer).  The CTA's g-th block (counted over all
 //     its units) lives in ring stage g % NSTAGE.  Warps run at different
 //     speeds, so a fast warp could reach stage g % NSTAGE while the stage's
 //     previous copy (block g - NSTAGE) is still in flight, and an mbarrier

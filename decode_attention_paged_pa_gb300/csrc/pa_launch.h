@@ -27,6 +27,8 @@ cudaError_t launch_simtx_f32(const KParams& prm, int D, int BS, int max_ctas, cu
 // Multi-query rows with fp32 elements: the causal instances, base and further shapes.
 cudaError_t launch_simt_mq_f32(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_simtx_mq_f32(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
+// fp32 caches in 8-token blocks, single- and multi-query.
+cudaError_t launch_simt_b8_f32(const KParams& prm, int D, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma_bf16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);
 cudaError_t launch_mma16_f16(const KParams& prm, int D, int BS, int max_ctas, cudaStream_t st);

@@ -41,7 +41,11 @@ struct SimtConsumer {
   // (32 dims for fp32, whose registers hold half as many per byte; half the
   // head for head sizes 80, 96, 112).
   static constexpr bool kPow2D = (D & (D - 1)) == 0;
-  static constexpr int QKD = !kPow2D ? D / 2 : (D >= 128 && KV_ESZ == 2) ? 64 : 32;
+  // 8-token fp32 blocks: a quarter of the head a lane (8 tokens a pass: the
+  // block is one pass), 32 dims at head size 256 (two passes).
+  static constexpr bool kB8 = BS_ == 8 && KV_ESZ == 4;
+  static constexpr int QKD = kB8 ? (D == 256 ? 32 : D / 4)
+                                 : !kPow2D ? D / 2 : (D >= 128 && KV_ESZ == 2) ? 64 : 32;
   static constexpr int LPT = D / QKD;
   static constexpr int TPP = 32 / LPT;        // tokens per pass over the warp
   static constexpr int NPASS = BS / TPP;

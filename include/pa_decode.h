@@ -117,10 +117,9 @@ int pa_decode_v2_workspace_layout(int num_seqs, int num_heads, int num_kv_heads,
  *   seq_lens     [num_seqs] int32, each in [0, max_blocks_per_seq*block_size]
  *   scale        softmax scale applied to q.k (fp32)
  *   dtype        PA_DTYPE_FP16, PA_DTYPE_BF16 or PA_DTYPE_FP32 (fp32 runs on the
- *                CUDA-core family, one query head per pass, at that family's
- *                shapes -- see pa_decode_v2_ex -- single- and multi-query;
- *                PA_ERR_UNSUPPORTED for the tensor-core variant, 8-token
- *                blocks and fp8 caches)
+ *                CUDA-core family, one query head per pass, every head size
+ *                and block size, single- and multi-query; PA_ERR_UNSUPPORTED
+ *                for the tensor-core variant and fp8 caches)
  *   stream       cudaStream_t to enqueue on
  *   max_blocks_per_seq  row stride of block_tables (the page's launcher reads
  *                it from the tensor's shape; a C ABI has to be told)
@@ -146,9 +145,10 @@ int pa_decode_v2(void* out, const void* query, const void* key_cache, const void
  *               heads, one block of each per pass; head sizes up to 128,
  *               blocks of 8, 16 or 32 tokens, an even kv-head count).  SIMT handles head sizes
  *               64/128/256 with blocks of 16 or 32 tokens, 80/96/112 with
- *               blocks of 16, 32 or 64, and 64/128 with blocks of 64 (8-token
- *               blocks: PA_ERR_UNSUPPORTED); MMA every supported shape of the
- *               16-bit types.  AUTO picks SIMT for G = 1 or fp32 where it
+ *               blocks of 16, 32 or 64, and 64/128 with blocks of 64, and
+ *               fp32 in 8-token blocks at every head size (16-bit types in
+ *               8-token blocks: PA_ERR_UNSUPPORTED); MMA every supported
+ *               shape of the 16-bit types.  AUTO picks SIMT for G = 1 or fp32 where it
  *               applies, MMA otherwise.
  *   max_ctas    upper bound on the persistent grid (0 = one CTA per SM).
  *   timeout_ns  bound on every device-side wait (0 = 2^31 ns).

@@ -187,8 +187,9 @@ def test_shapes_outside_a_family_are_rejected():
 
 
 def test_fp32_only_on_the_cuda_core_family():
-    """fp32 (dtype 2) runs on the CUDA-core family, its shapes only (single- and
-    multi-query), never over an fp8 cache."""
+    """fp32 (dtype 2) runs on the CUDA-core family, every shape (single- and
+    multi-query, 8-token blocks included), never on tensor cores or over an fp8
+    cache; 16-bit 8-token blocks stay off the CUDA-core family."""
     lib = binding.lib()
 
     def ex(D, BS, variant, dtype=binding.PA_DTYPE_FP32):
@@ -200,10 +201,14 @@ def test_fp32_only_on_the_cuda_core_family():
     assert ex(128, 16, binding.PA_VARIANT_MMA) == binding.PA_ERR_UNSUPPORTED
     assert ex(96, 16, binding.PA_VARIANT_AUTO) == binding.PA_OK
     assert ex(112, 64, binding.PA_VARIANT_AUTO) == binding.PA_OK
-    assert ex(128, 8, binding.PA_VARIANT_AUTO) == binding.PA_ERR_UNSUPPORTED
+    assert ex(128, 8, binding.PA_VARIANT_AUTO) == binding.PA_OK
+    assert ex(80, 8, binding.PA_VARIANT_SIMT) == binding.PA_OK
+    assert ex(128, 8, binding.PA_VARIANT_AUTO, dtype=binding.PA_DTYPE_FP16) == binding.PA_OK
+    assert ex(128, 8, binding.PA_VARIANT_SIMT, dtype=binding.PA_DTYPE_FP16) == binding.PA_ERR_UNSUPPORTED
     assert ex(96, 16, binding.PA_VARIANT_MMA) == binding.PA_ERR_UNSUPPORTED
     assert ex(128, 16, binding.PA_VARIANT_AUTO, dtype=3) == binding.PA_ERR_INVALID_ARG
-    for D, BS, want in ((128, 16, binding.PA_OK), (80, 64, binding.PA_OK), (128, 8, binding.PA_ERR_UNSUPPORTED)):
+    for D, BS, want in ((128, 16, binding.PA_OK), (80, 64, binding.PA_OK), (112, 8, binding.PA_OK),
+                        (128, 24, binding.PA_ERR_UNSUPPORTED)):
         st = lib.pa_decode_v2_mq(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.125), 0, 4,
                                  4, 2, D, BS, 512, binding.PA_DTYPE_FP32, None, 4, 8, FAKE, 1 << 30)
         assert st == want, (D, BS)

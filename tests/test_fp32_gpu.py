@@ -108,8 +108,9 @@ def test_fp32_rejected_outside_its_family():
     assert e.value.status == binding.PA_ERR_UNSUPPORTED
 
 
-# The CUDA-core family's further shapes with fp32 elements.
-XCASES = [(D, BS, G) for D, BS in ((80, 16), (96, 32), (112, 64), (64, 64), (128, 64), (80, 64)) for G in (1, 2)]
+# The CUDA-core family's further shapes with fp32 elements, 8-token blocks included.
+XCASES = [(D, BS, G) for D, BS in ((80, 16), (96, 32), (112, 64), (64, 64), (128, 64), (80, 64),
+                                    (64, 8), (80, 8), (96, 8), (112, 8), (128, 8), (256, 8)) for G in (1, 2)]
 
 
 @pytest.mark.parametrize("D,BS,G", XCASES, ids=[f"D{c[0]}-BS{c[1]}-G{c[2]}" for c in XCASES])
@@ -136,7 +137,8 @@ def run_mq32(q, kc, vc, bt, lens, scale, P):
     return out.cpu(), lse.cpu()
 
 
-MQ32_CASES = [(q_len, G, D, BS) for q_len, G in ((2, 1), (4, 2), (3, 4)) for D, BS in ((128, 16), (64, 32), (96, 64))]
+MQ32_CASES = [(q_len, G, D, BS) for q_len, G in ((2, 1), (4, 2), (3, 4))
+              for D, BS in ((128, 16), (64, 32), (96, 64), (112, 8), (256, 8))]
 
 
 @pytest.mark.parametrize("q_len,G,D,BS", MQ32_CASES, ids=[f"q{c[0]}-G{c[1]}-D{c[2]}-BS{c[3]}" for c in MQ32_CASES])
