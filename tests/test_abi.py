@@ -153,9 +153,10 @@ def test_fp8_entry_rejects_bad_scales():
 
 
 def test_shapes_outside_a_family_are_rejected():
-    """The tensor-core family takes every shape; the CUDA-core family head sizes
-    80/96/112 with 16/32/64-token blocks and 64-token blocks at 64/128 next to
-    its base shapes, never 8-token blocks; fp8 caches take every supported
+    """With 16-bit elements the tensor-core family takes every shape; the
+    CUDA-core family head sizes 80/96/112 with 16/32/64-token blocks and
+    64-token blocks at 64/128 next to its base shapes, never 8-token blocks
+    (fp32 takes those: see the fp32 test); fp8 caches take every supported
     head size and block size, on tensor cores only."""
     lib = binding.lib()
 
