@@ -130,6 +130,10 @@ int pa_decode_v2_workspace_layout(int num_seqs, int num_heads, int num_kv_heads,
  *                contents on entry do not matter: the call writes every byte
  *                of it that it reads.
  * out, query and the caches must be 16-byte aligned; tables 4-byte aligned.
+ * With a workspace given, a call only enqueues kernels on `stream` (no
+ * allocation, no synchronisation), so it can be captured into a CUDA graph
+ * and replayed with new contents in its buffers (lengths up to the table's
+ * capacity); the first call for a given shape should come before the capture.
  */
 int pa_decode_v2(void* out, const void* query, const void* key_cache, const void* value_cache,
                  const int32_t* block_tables, const int32_t* seq_lens, float scale,
